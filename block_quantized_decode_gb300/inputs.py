@@ -1,0 +1,121 @@
+"""Seeded synthetic inputs shared by the tests and the bench.
+
+This module holds no arithmetic of the method itself: it only draws raw
+quant bytes, scales and float activations with numpy's ``default_rng`` and
+describes the workload shapes.  Both the CUDA path and the CPU oracle are
+fed the same host bytes from here.
+
+Value distributions (stated for every workload):
+  * Q4_0 weights: every nibble uniform in 0..15 (so every byte uniform in
+    0..255), block scales float32 uniform in [1e-3, 1e-2];
+  * Q8_0 weights: int8 uniform in [-127, 127], scales uniform in [1e-4, 1e-3];
+  * activations: float32 standard normal.
+Shapes follow the pages' workloads (TinyLlama-1.1B layer, Llama-7B FFN
+stack, Qwen2.5-0.5B lm_head; see the ONNX Runtime page, "Results first" and
+"Synthetic FFN (context)").  No trained weights or datasets are used.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+QK = 32
+Q8_0 = 0
+Q4_0 = 1
+
+
+def q4_weights(rows: int, cols: int, seed: int, lo: float = 1e-3, hi: float = 1e-2):
+    """(q uint8 [rows, cols/2], d float32 [rows, cols/32]) with random nibbles."""
+    assert cols % QK == 0
+    rng = np.random.default_rng(seed)
+    q = rng.integers(0, 256, size=(rows, cols // 2), dtype=np.uint8)
+    d = rng.uniform(lo, hi, size=(rows, cols // QK)).astype(np.float32)
+    return q, d
+
+
+def q8_weights(rows: int, cols: int, seed: int, lo: float = 1e-4, hi: float = 1e-3):
+    """(q int8 [rows, cols], d float32 [rows, cols/32]); q uniform in [-127, 127]."""
+    assert cols % QK == 0
+    rng = np.random.default_rng(seed)
+    q = rng.integers(-127, 128, size=(rows, cols), dtype=np.int8)
+    d = rng.uniform(lo, hi, size=(rows, cols // QK)).astype(np.float32)
+    return q, d
+
+
+def weights(wtype: int, rows: int, cols: int, seed: int):
+    return q4_weights(rows, cols, seed) if wtype == Q4_0 else q8_weights(rows, cols, seed)
+
+
+def activations(m: int, k: int, seed: int) -> np.ndarray:
+    """float32 [m, k] ~ N(0, 1)."""
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal(size=(m, k)).astype(np.float32)
+
+
+# --------------------------------------------------------------------------
+# Workload shapes.  ``seed`` of tensor i is base_seed + i (the pages give no
+# seeds; the tiny case uses seed 0 as stated).
+# --------------------------------------------------------------------------
+@dataclass
+class Matvec:
+    name: str
+    wtype: int
+    rows: int
+    cols: int
+    input_of: str = "x"      # which vector feeds it: "x" or the name of a prior output
+
+
+@dataclass
+class Workload:
+    name: str
+    m: int
+    mats: list = field(default_factory=list)
+    chained: bool = False
+    description: str = ""
+
+
+def tiny_q4() -> Workload:
+    return Workload("tiny_q4_256x512", 1, [Matvec("w", Q4_0, 256, 512)],
+                    description="Q4_0 256x512, M=1, seed 0")
+
+
+def tinyllama_layer() -> Workload:
+    """One TinyLlama-1.1B-shaped decode layer, Q4_0, M=1.
+
+    Data flow (steps outside the matvec path are identity): q, k, v all
+    read Q8_0(x); Wo reads Q8_0(q); gate and up read Q8_0(o); down reads
+    Q8_0(gate)."""
+    d, kv, ff = 2048, 256, 5632
+    return Workload("tinyllama1.1b_layer_q4_0", 1, [
+        Matvec("wq", Q4_0, d, d, "x"),
+        Matvec("wk", Q4_0, kv, d, "x"),
+        Matvec("wv", Q4_0, kv, d, "x"),
+        Matvec("wo", Q4_0, d, d, "wq"),
+        Matvec("w_gate", Q4_0, ff, d, "wo"),
+        Matvec("w_up", Q4_0, ff, d, "wo"),
+        Matvec("w_down", Q4_0, d, ff, "w_gate"),
+    ], chained=True, description="TinyLlama-1.1B-shaped layer, Q4_0, M=1")
+
+
+def llama7b_ffn(wtype: int = Q4_0, layers: int = 8) -> Workload:
+    mats = []
+    prev = "x"
+    for i in range(layers):
+        mats.append(Matvec(f"up{i}", wtype, 11008, 4096, prev))
+        mats.append(Matvec(f"down{i}", wtype, 4096, 11008, f"up{i}"))
+        prev = f"down{i}"
+    tag = "q4_0" if wtype == Q4_0 else "q8_0"
+    return Workload(f"llama7b_ffn8_{tag}", 1, mats, chained=True,
+                    description=f"8-layer Llama-7B FFN stack, {tag.upper()}, M=1, chained")
+
+
+def qwen_lm_head() -> Workload:
+    return Workload("qwen2.5-0.5b_lm_head_q8_0", 1, [Matvec("lm_head", Q8_0, 151936, 896)],
+                    description="Qwen2.5-0.5B-shaped lm_head, Q8_0, M=1")
+
+
+def small_m(m: int) -> Workload:
+    return Workload(f"gemm_q4_0_m{m}", m, [Matvec("up", Q4_0, 11008, 4096, "x"),
+                                            Matvec("down", Q4_0, 4096, 11008, "x")],
+                    description=f"Q4_0 small-M GEMM, M={m}, 11008x4096 and 4096x11008")

@@ -1,0 +1,52 @@
+"""Plant plausible mistakes in copies of the oracle (on the CPU) and check
+that at least one pin fails for each: a dropped term, a wrong sign, a
+wrong index, a swapped nibble, a wrong constant.  This shows that the pins
+in tests/oracle_pins.py constrain every step of the oracle."""
+import os
+
+import pytest
+
+import oracle
+from tests import oracle_pins as P
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "mlq_oracle.c")
+
+# (name, original text, mutated text); every mutant stays in bounds.
+MUTANTS = [
+    ("high_nibble_as_low", "(bytes16[j] >> 4) - 8", "(bytes16[j] & 0x0F) - 8"),
+    ("offset_7_not_8", "(int)(bytes16[j] & 0x0F) - 8", "(int)(bytes16[j] & 0x0F) - 7"),
+    ("nibble_halves_swapped", "w[j + 16] = (int8_t)((int)(bytes16[j] >> 4) - 8);",
+     "w[j + 16] = (int8_t)((int)(bytes16[j] & 0x0F) - 8); w[j] = (int8_t)((int)(bytes16[j] >> 4) - 8);"),
+    ("dropped_dx", "t = t * xd[b];", "t = t;"),
+    ("wrong_dw_index", "wd[(size_t)r * nb + b]", "wd[b]"),
+    ("wrong_x_block", "int32_t sumi = block_dot(w, xq + (size_t)b * ORACLE_QK);", "int32_t sumi = block_dot(w, xq);"),
+    ("no_accumulate", "sum = sum + t;", "sum = t;"),
+    ("id_128", "127.0f / amax", "128.0f / amax"),
+    ("d_128", "amax / 127.0f", "amax / 128.0f"),
+    ("round_not_signed", "copysignf(0.5f, x[j])", "0.5f"),
+    ("clamp_126", "if (v >= 127.0f)       qq = 127;", "if (v >= 127.0f)       qq = 126;"),
+    ("nan_not_zero", "else if (v != v)       qq = 0;", "else if (v != v)       qq = 1;"),
+    ("fused_round", "float v = x[j] * id;                         /* one rounded multiply  */\n        v = v + copysignf(0.5f, x[j]);",
+     "float v = fmaf(x[j], id, copysignf(0.5f, x[j]));"),
+    ("round_half_even", "v = truncf(v);", "v = rintf(v - copysignf(0.5f, x[j]));"),
+    ("dot_drops_last", "for (int j = 0; j < ORACLE_QK; ++j) s +=", "for (int j = 0; j < ORACLE_QK - 1; ++j) s +="),
+    ("row_range_from_zero", "for (int r = r0; r < r1; ++r) {\n        float sum", "for (int r = 0; r < r1; ++r) {\n        float sum"),
+    ("small_m_row_stride", "Y + (size_t)m * ldy", "Y + (size_t)m * rows"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique/found"
+    mpath = tmp_path / f"{name}.c"
+    mpath.write_text(src.replace(old, new))
+    lib = oracle.compile_c(str(mpath), str(tmp_path / f"lib_{name}.so"))
+    O = oracle.Oracle(lib)
+    failed = []
+    for pin in P.ALL_PINS:
+        try:
+            pin(O)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"mutant {name} passed every pin"
