@@ -1,0 +1,448 @@
+"""Benchmark of the block-quantized decode hot path on GB300.
+
+One step = one pass of the workload's hot path through the C ABI: Q8_0
+quantisation of each input vector, then every Q4_0 / Q8_0 product.  The
+default workload is one TinyLlama-1.1B-shaped decode layer (Q4_0, M = 1:
+q, k, v, o, gate, up, down; 27.5 MB of weights); --workload picks another.
+
+Timing: W untimed warm-up steps, then K steps bracketed by a barrier and a
+device synchronize, timed with CUDA events on the launching stream; the
+steps replay one CUDA graph per weight copy, and consecutive steps read
+different copies (together more than 3x the L2 size), so every step streams
+its weights from HBM.  Rank 0 prints one JSON line.
+
+Also measured in the same run: the dominant kernel's per-launch duration
+(CUDA events captured into an instrumented copy of the graphs), the same
+metric end to end (pinned host input -> device, step, outputs -> host),
+SM clocks during the timed region, and the CPU oracle on the host cores
+(cpu_baseline).  ``--impl reference`` times the oracle alone as the
+reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "M=1 Q4_0/Q8_0 matvec weight GB/s and GOP/s; % of GB300 HBM roofline"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="tinyllama_layer")
+    p.add_argument("--copies", type=int, default=0, help="weight copies (0 = auto, > 3x L2)")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-graph", action="store_true")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; no data-path collective)
+# ----------------------------------------------------------------------------
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg, device=None):
+    if pg is not None:
+        if device is not None:
+            pg.barrier(device_ids=[device])
+        else:
+            pg.barrier()
+
+
+def max_over_ranks(pg, v: float, device=None) -> float:
+    if pg is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=device if device is not None else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# host-side helpers
+# ----------------------------------------------------------------------------
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def ncu_traffic(kernel_file: str, workload: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"matvec_q4_{workload}.md")
+    src = os.path.join(ROOT, "block_quantized_decode_gb300", "csrc", kernel_file)
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    m_sha = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_tr or m_sha.group(1) != sha:
+        return None
+    return float(m_tr.group(1))
+
+
+# ----------------------------------------------------------------------------
+# the CPU oracle on the host cores (cpu_baseline and the reference arm)
+# ----------------------------------------------------------------------------
+class OraclePass:
+    """One pass of the workload with the oracle: quantise each input, then
+    every product with rows split statically over `threads` host threads
+    (the oracle's own [r0, r1) interface; ctypes releases the GIL)."""
+
+    def __init__(self, wl, threads: int):
+        import numpy as np
+        from concurrent.futures import ThreadPoolExecutor
+
+        import oracle
+        from block_quantized_decode_gb300 import inputs as I
+        self.np = np
+        self.O = oracle
+        self.wl = wl
+        self.threads = threads
+        self.pool = ThreadPoolExecutor(max_workers=threads)
+        self.mats = []
+        self.x = {}
+        for i, mv in enumerate(wl.mats):
+            src = f"x{mv.cols}" if mv.input_of == "x" else mv.input_of
+            if mv.input_of == "x" and src not in self.x:
+                self.x[src] = I.activations(wl.m, mv.cols, seed=1000 + len(self.x))
+            q, d = I.weights(mv.wtype, mv.rows, mv.cols, seed=i)
+            self.mats.append((mv, src, q, d))
+        self.weight_bytes = sum(q.nbytes + d.nbytes for _, _, q, d in self.mats)
+        self.ops = sum(2 * wl.m * mv.rows * mv.cols for mv, _, _, _ in self.mats)
+
+    def run(self):
+        np, O = self.np, self.O
+        fp = dict(self.x)
+        qa = {}
+        for mv, src, q, d in self.mats:
+            if src not in qa:
+                qa[src] = O.quantize_q8(fp[src].reshape(self.wl.m, -1))
+            xq, xd = qa[src]
+            Y = np.zeros((self.wl.m, mv.rows), dtype=np.float32)
+            cuts = [mv.rows * t // self.threads for t in range(self.threads + 1)]
+            futs = []
+            for t in range(self.threads):
+                a, b = cuts[t], cuts[t + 1]
+                if b > a:
+                    futs.append(self.pool.submit(O.gemm_small_m, mv.wtype, q, d, mv.rows, mv.cols,
+                                                 xq, xd, self.wl.m, a, b, None, Y))
+            for f in futs:
+                f.result()
+            fp[mv.name] = Y
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def time_oracle(wl, seconds: float, threads: int, max_steps: int | None = None):
+    op = OraclePass(wl, threads)
+    op.run()  # warm (page-in, thread start)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        op.run()
+        n += 1
+        el = time.perf_counter() - t0
+        if (max_steps is not None and n >= max_steps) or (max_steps is None and el >= seconds):
+            break
+    return op, n, el
+
+
+# ----------------------------------------------------------------------------
+# the reference arm: the oracle as it stands
+# ----------------------------------------------------------------------------
+def run_reference(args, wl, world, rank):
+    if rank != 0:
+        return 0
+    threads = host_cores()
+    op = OraclePass(wl, threads)
+    for _ in range(max(0, args.warmup)):
+        op.run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        op.run()
+    el = time.perf_counter() - t0
+    v = op.weight_bytes * args.steps / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 dot -> int32, f32 accumulate (CPU oracle)", "data": "synthetic",
+        "config": {"workload": wl.name, "M": wl.m, "weight_bytes_per_step": op.weight_bytes},
+        "gops": op.ops * args.steps / el / 1e9,
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{args.steps} full passes of {wl.name} after {args.warmup} warm-up"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def run_ours(args, wl, world, rank, local, pg):
+    import torch
+
+    import block_quantized_decode_gb300 as M
+    from block_quantized_decode_gb300.runner import WorkloadRunner
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    M.mlq_init()
+    props = torch.cuda.get_device_properties(local)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
+    from block_quantized_decode_gb300 import inputs as I
+    wbytes = sum((mv.rows * mv.cols // 2 if mv.wtype == I.Q4_0 else mv.rows * mv.cols)
+                 + mv.rows * mv.cols // 32 * 4 for mv in wl.mats)
+    copies = args.copies or max(2, math.ceil(3 * l2 / wbytes))
+    r = WorkloadRunner(wl, copies=copies, device=f"cuda:{local}")
+    assert r.weight_bytes() == wbytes
+    stream = torch.cuda.Stream(device=dev)
+
+    # ---- graphs: one per weight copy (plain), one per copy instrumented
+    q4_idx = [i for i, m in enumerate(r.mats) if m.spec.wtype == I.Q4_0] or list(range(len(r.mats)))
+    dominant = "matvec_m1_kernel<Q4_0>" if r.m == 1 and any(
+        m.spec.wtype == I.Q4_0 for m in r.mats) else (
+        "matvec_m1_kernel<Q8_0>" if r.m == 1 else "gemm_q4_small_m")
+    ev_ok = True
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        ev_ok = False
+    with torch.cuda.stream(stream):
+        for c in range(copies):  # eager warm-up of every copy (kernel attributes, caches)
+            r.step(copy=c)
+    stream.synchronize()
+    graphs, igraphs, ievents = [], [], []
+    if not args.no_graph:
+        for c in range(copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                r.step(copy=c)
+            graphs.append(g)
+        if ev_ok:
+            for c in range(copies):
+                evs = {i: (torch.cuda.Event(enable_timing=True, external=True),
+                           torch.cuda.Event(enable_timing=True, external=True)) for i in q4_idx}
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    r.step(copy=c, before_mat=lambda i: evs[i][0].record() if i in evs else None,
+                           after_mat=lambda i: evs[i][1].record() if i in evs else None)
+                igraphs.append(g)
+                ievents.append(evs)
+
+    def do_step(i):
+        if graphs:
+            graphs[i % copies].replay()
+        else:
+            r.step(copy=i % copies)
+
+    # ---- headline timed region
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            do_step(i)
+    stream.synchronize()
+    barrier(pg, local)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(args.steps):
+            do_step(args.warmup + i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg, local)
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    ms_max = max_over_ranks(pg, ms, dev)
+    steps = args.steps
+    value = world * wbytes * steps / (ms_max / 1e3) / 1e9
+    gops = world * r.ops() * steps / (ms_max / 1e3) / 1e9
+
+    # ---- dominant-kernel launch durations (instrumented graphs)
+    peaks, peak_src = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    roofline = None
+    if igraphs:
+        tot_ms, tot_bytes, launches = 0.0, 0, 0
+        nrep = min(steps, 4 * copies)
+        with torch.cuda.stream(stream):
+            for i in range(nrep):
+                c = i % copies
+                igraphs[c].replay()
+                stream.synchronize()
+                for mi, (a, b) in ievents[c].items():
+                    tot_ms += a.elapsed_time(b)
+                    m = r.mats[mi]
+                    tot_bytes += m.host_q.nbytes + m.host_d.nbytes
+                    launches += 1
+        per_launch_bytes = tot_bytes / launches
+        per_launch_s = tot_ms / launches / 1e3
+        ach = per_launch_bytes / per_launch_s / 1e9
+        roofline = {"kernel": dominant, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                    "frac": ach / hbm, "peak_source": peak_src,
+                    "traffic": ncu_traffic("matvec.cu", wl.name),
+                    "bytes_per_launch": per_launch_bytes, "us_per_launch": per_launch_s * 1e6,
+                    "launches_timed": launches}
+
+    # ---- end to end: pinned host input -> step -> outputs to pinned host
+    host_out = r.outputs_to_host()
+    torch.cuda.synchronize()
+    e2e_steps = min(steps, 100)
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        with torch.cuda.stream(stream):
+            r.upload_inputs(stream)
+            do_step(i)
+            r.outputs_to_host(host_out)
+        stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e_s = max_over_ranks(pg, e2e_s, dev)
+    e2e = {"value": world * wbytes * e2e_steps / e2e_s / 1e9, "unit": UNIT,
+           "h2d_bytes_per_step": r.h2d_bytes(), "d2h_bytes_per_step": r.d2h_bytes(),
+           "steps": e2e_steps, "how": "wall clock; per step: pinned H2D of inputs, graph replay "
+                                      "of the C-ABI calls, D2H of every output, stream sync"}
+
+    assert M.mlq_last_device_error(stream) == M.MLQ_OK
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        threads = host_cores()
+        op, n, el = time_oracle(wl, args.cpu_seconds, threads)
+        cpu = {"value": op.weight_bytes * n / el / 1e9, "unit": UNIT, "cores": threads,
+               "kind": "oracle",
+               "sample": f"{n} full passes of {wl.name} in {el:.1f} s, rows split over {threads} threads"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": ms_max / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "q4_0/q8_0: int8 dot -> int32, f32 accumulate", "data": "synthetic",
+            "config": {"workload": wl.name, "M": r.m,
+                       "matrices": [f"{m.spec.name}:{m.spec.rows}x{m.spec.cols}:"
+                                    f"{'q4_0' if m.spec.wtype == I.Q4_0 else 'q8_0'}" for m in r.mats],
+                       "weight_bytes_per_step": wbytes,
+                       "l2": f"inputs larger than L2: {copies} rotating weight copies "
+                             f"({copies * wbytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
+                       "graphs": bool(graphs), "parallelism": f"replicas x{world} (independent decode streams)"},
+            "gops": gops, "hbm_frac": value / world / hbm,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": r.kernels_per_step * steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    from block_quantized_decode_gb300 import inputs as I
+    if args.workload not in I.WORKLOADS:
+        raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(I.WORKLOADS)}")
+    wl = I.WORKLOADS[args.workload]()
+    world, rank, local, pg = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, wl, world, rank)
+        return run_ours(args, wl, world, rank, local, pg)
+    finally:
+        if pg is not None:
+            pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,14 @@
+"""GB300 (sm_103a) block-quantized decode: Q8_0 activation quantiser,
+M = 1 Q4_0 / Q8_0 matrix-vector products and the small-M batched product,
+behind the C ABI of libmlq.so (include/mlq.h).
+
+The Python names below are the C entry points of the same names; they only
+marshal arguments (see binding.py).
+"""
+from .binding import (  # noqa: F401
+    EXPORTS, LIB_PATH, MLQ_E_ALIGN, MLQ_E_ARCH, MLQ_E_CUDA, MLQ_E_NULL, MLQ_E_SHAPE,
+    MLQ_E_TIMEOUT, MLQ_E_TYPE, MLQ_MAX_COLS, MLQ_MAX_M, MLQ_OK, MLQ_Q4_0, MLQ_Q8_0, MLQ_QK,
+    MlqError, QAct, QTensor, lib, mlq_block_sumi, mlq_debug_set_wait_limit_ns,
+    mlq_gemm_q4_small_m, mlq_init, mlq_last_device_error, mlq_matvec_q4, mlq_matvec_q8,
+    mlq_quantize_q8, mlq_status_str,
+)

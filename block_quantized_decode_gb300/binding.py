@@ -1,0 +1,190 @@
+"""Thin Python binding of libmlq's C ABI (include/mlq.h).
+
+Argument marshalling only: every function here fills the C structs from
+torch tensors (or raw integer device addresses) and calls the entry point of
+the same name in libmlq.so.  All arithmetic runs in the library's CUDA
+kernels; there is no Python or CPU fallback.  A non-MLQ_OK status raises
+``MlqError``.  If libmlq.so has not been built, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+MLQ_OK, MLQ_E_SHAPE, MLQ_E_ALIGN, MLQ_E_TYPE, MLQ_E_NULL, MLQ_E_ARCH, MLQ_E_CUDA, MLQ_E_TIMEOUT = range(8)
+MLQ_Q8_0 = 0
+MLQ_Q4_0 = 1
+MLQ_QK = 32
+MLQ_MAX_COLS = 65536
+MLQ_MAX_M = 16
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmlq.so")
+
+# every symbol include/mlq.h declares
+EXPORTS = (
+    "mlq_init", "mlq_quantize_q8", "mlq_matvec_q4", "mlq_matvec_q8",
+    "mlq_gemm_q4_small_m", "mlq_block_sumi", "mlq_last_device_error",
+    "mlq_debug_set_wait_limit_ns", "mlq_status_str",
+)
+
+
+class MlqError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_name(status)} ({status})")
+
+
+class _QTensor(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("d", ctypes.c_void_p), ("rows", ctypes.c_int),
+                ("cols", ctypes.c_int), ("type", ctypes.c_uint8)]
+
+
+class _QAct(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("d", ctypes.c_void_p), ("n", ctypes.c_int),
+                ("m", ctypes.c_int)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmlq.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_int
+        QT, QA = ctypes.POINTER(_QTensor), ctypes.POINTER(_QAct)
+        L.mlq_init.argtypes = []
+        L.mlq_quantize_q8.argtypes = [QA, P, I, P]
+        L.mlq_matvec_q4.argtypes = [P, QT, QA, I, I, P]
+        L.mlq_matvec_q8.argtypes = [P, QT, QA, I, I, P]
+        L.mlq_gemm_q4_small_m.argtypes = [P, I, QT, QA, I, I, I, P]
+        L.mlq_block_sumi.argtypes = [P, QT, QA, I, I, P]
+        L.mlq_last_device_error.argtypes = [P]
+        L.mlq_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        L.mlq_status_str.argtypes = [S]
+        L.mlq_status_str.restype = ctypes.c_char_p
+        for name in EXPORTS:
+            if name != "mlq_status_str":
+                getattr(L, name).restype = S
+        _lib = L
+    return _lib
+
+
+def status_name(s: int) -> str:
+    try:
+        return lib().mlq_status_str(s).decode()
+    except Exception:  # library not loadable: still name the code
+        names = ["MLQ_OK", "MLQ_E_SHAPE", "MLQ_E_ALIGN", "MLQ_E_TYPE", "MLQ_E_NULL",
+                 "MLQ_E_ARCH", "MLQ_E_CUDA", "MLQ_E_TIMEOUT"]
+        return names[s] if 0 <= s < len(names) else "MLQ_E_UNKNOWN"
+
+
+def _addr(t) -> int | None:
+    """Device address of a torch tensor, or an integer passed through."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        try:
+            import torch
+            if torch.cuda.is_available():
+                return torch.cuda.current_stream().cuda_stream
+        except Exception:
+            pass
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+@dataclass
+class QTensor:
+    """Weight tensor: q (raw quant bytes) and d (float32 scales) on the device."""
+    q: object
+    d: object
+    rows: int
+    cols: int
+    type: int
+
+    def c(self) -> _QTensor:
+        return _QTensor(_addr(self.q), _addr(self.d), self.rows, self.cols, self.type)
+
+
+@dataclass
+class QAct:
+    """Q8_0 activations: m rows of n (q int8, d float32) on the device."""
+    q: object
+    d: object
+    n: int
+    m: int = 1
+
+    def c(self) -> _QAct:
+        return _QAct(_addr(self.q), _addr(self.d), self.n, self.m)
+
+
+def _check(s: int, where: str) -> None:
+    if s != MLQ_OK:
+        raise MlqError(s, where)
+
+
+def mlq_init() -> None:
+    _check(lib().mlq_init(), "mlq_init")
+
+
+def mlq_quantize_q8(out: QAct, x, k: int, stream=None) -> None:
+    co = out.c()
+    _check(lib().mlq_quantize_q8(ctypes.byref(co), _addr(x), k, _stream(stream)), "mlq_quantize_q8")
+
+
+def mlq_matvec_q4(y, W: QTensor, x: QAct, r0: int, r1: int, stream=None) -> None:
+    cw, cx = W.c(), x.c()
+    _check(lib().mlq_matvec_q4(_addr(y), ctypes.byref(cw), ctypes.byref(cx), r0, r1,
+                               _stream(stream)), "mlq_matvec_q4")
+
+
+def mlq_matvec_q8(y, W: QTensor, x: QAct, r0: int, r1: int, stream=None) -> None:
+    cw, cx = W.c(), x.c()
+    _check(lib().mlq_matvec_q8(_addr(y), ctypes.byref(cw), ctypes.byref(cx), r0, r1,
+                               _stream(stream)), "mlq_matvec_q8")
+
+
+def mlq_gemm_q4_small_m(Y, ldy: int, W: QTensor, X: QAct, M: int, r0: int, r1: int,
+                        stream=None) -> None:
+    cw, cx = W.c(), X.c()
+    _check(lib().mlq_gemm_q4_small_m(_addr(Y), ldy, ctypes.byref(cw), ctypes.byref(cx), M, r0, r1,
+                                     _stream(stream)), "mlq_gemm_q4_small_m")
+
+
+def mlq_block_sumi(sumi, W: QTensor, x: QAct, r0: int, r1: int, stream=None) -> None:
+    cw, cx = W.c(), x.c()
+    _check(lib().mlq_block_sumi(_addr(sumi), ctypes.byref(cw), ctypes.byref(cx), r0, r1,
+                                _stream(stream)), "mlq_block_sumi")
+
+
+def mlq_last_device_error(stream=None) -> int:
+    """Synchronise the stream and return (not raise) the device status."""
+    return lib().mlq_last_device_error(_stream(stream))
+
+
+def mlq_debug_set_wait_limit_ns(limit_ns: int) -> None:
+    _check(lib().mlq_debug_set_wait_limit_ns(limit_ns), "mlq_debug_set_wait_limit_ns")
+
+
+def mlq_status_str(s: int) -> str:
+    return lib().mlq_status_str(s).decode()
+
+
+def raw_call(name: str, *args) -> int:
+    """Call an entry point with already-marshalled arguments and return its
+    status (host-side validation tests use this with fake addresses)."""
+    return getattr(lib(), name)(*args)

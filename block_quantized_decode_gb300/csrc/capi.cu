@@ -1,0 +1,236 @@
+// capi.cu -- the extern "C" boundary of libmlq (declared in include/mlq.h).
+//
+// Every entry point validates its arguments on the host first (status codes
+// as in the page "Legacy-ISA ML Inference Runtime -- Design Spec", Sec. 6
+// "Error handling": return a status, never abort), then checks the device
+// (compute capability 10.3, cached per device), then queues one kernel on
+// the caller's stream.  Nothing here allocates device memory.
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "mlq.h"
+#include "mlq_launch.h"
+
+namespace {
+
+// Device status word: kernels record MLQ_E_TIMEOUT here when a bounded wait
+// gives up.  One instance per device (a __device__ variable lives in every
+// context that loads the module); its address is looked up once per device.
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DevInfo {
+  std::atomic<int> state{0};  // 0 = unknown, 1 = usable, 2 = unusable
+  int num_sms = 0;
+  int *status = nullptr;
+};
+
+DevInfo g_dev[kMaxDevices];
+std::mutex g_init_mu;
+std::atomic<unsigned long long> g_wait_ns{1000000000ull};
+std::atomic<int> g_pdl{-1};
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool pdl_enabled() {
+  int v = g_pdl.load(std::memory_order_relaxed);
+  if (v < 0) {
+    const char *e = std::getenv("MLQ_PDL");
+    v = (e != nullptr && std::strcmp(e, "0") == 0) ? 0 : 1;
+    g_pdl.store(v, std::memory_order_relaxed);
+  }
+  return v == 1;
+}
+
+// Compute capability of `dev`; MLQ_FAKE_CC="major.minor" overrides it (a
+// host-side test hook for the architecture guard).
+bool query_cc(int dev, int *major, int *minor) {
+  const char *fake = std::getenv("MLQ_FAKE_CC");
+  if (fake != nullptr) {
+    char *end = nullptr;
+    *major = static_cast<int>(std::strtol(fake, &end, 10));
+    *minor = (end != nullptr && *end == '.') ? static_cast<int>(std::strtol(end + 1, nullptr, 10)) : 0;
+    return true;
+  }
+  if (cudaDeviceGetAttribute(major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return false;
+  return true;
+}
+
+mlq_status device_info(DevInfo **out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return MLQ_E_ARCH;
+  }
+  DevInfo &d = g_dev[dev];
+  int st = d.state.load(std::memory_order_acquire);
+  if (st == 0) {
+    std::lock_guard<std::mutex> lk(g_init_mu);
+    st = d.state.load(std::memory_order_acquire);
+    if (st == 0) {
+      int major = 0, minor = 0, sms = 0;
+      bool ok = query_cc(dev, &major, &minor) && major == 10 && minor == 3;
+      ok = ok && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
+      int *status = nullptr;
+      ok = ok && cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_device_status) == cudaSuccess;
+      if (!ok) cudaGetLastError();
+      d.num_sms = sms;
+      d.status = status;
+      st = ok ? 1 : 2;
+      d.state.store(st, std::memory_order_release);
+    }
+  }
+  if (st != 1) return MLQ_E_ARCH;
+  *out = &d;
+  return MLQ_OK;
+}
+
+mlq_status make_ctx(mlq::LaunchCtx *ctx, void *stream) {
+  DevInfo *d = nullptr;
+  mlq_status s = device_info(&d);
+  if (s != MLQ_OK) return s;
+  ctx->stream = static_cast<cudaStream_t>(stream);
+  ctx->pdl = pdl_enabled();
+  ctx->num_sms = d->num_sms;
+  ctx->status = d->status;
+  ctx->wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  return MLQ_OK;
+}
+
+mlq_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return MLQ_OK;
+  cudaGetLastError();
+  return MLQ_E_CUDA;
+}
+
+bool cols_ok(int cols) { return cols > 0 && cols % MLQ_QK == 0 && cols <= MLQ_MAX_COLS; }
+
+// Checks common to every product with a weight tensor.
+mlq_status check_weights(const mlq_qtensor *W, const mlq_qact *x, int r0, int r1) {
+  if (W == nullptr || x == nullptr) return MLQ_E_NULL;
+  if (W->q == nullptr || W->d == nullptr || x->q == nullptr || x->d == nullptr) return MLQ_E_NULL;
+  if (W->type != MLQ_Q4_0 && W->type != MLQ_Q8_0) return MLQ_E_TYPE;
+  if (!cols_ok(W->cols) || W->rows < 0 || x->n != W->cols) return MLQ_E_SHAPE;
+  if (r0 < 0 || r1 < r0 || r1 > W->rows) return MLQ_E_SHAPE;
+  if (!aligned(W->q, 16) || !aligned(W->d, 16) || !aligned(x->q, 16) || !aligned(x->d, 16))
+    return MLQ_E_ALIGN;
+  return MLQ_OK;
+}
+
+mlq_status matvec_common(float *y, int32_t *sumi, const mlq_qtensor *W, const mlq_qact *x,
+                         int r0, int r1, void *stream, int want_type) {
+  if (y == nullptr && sumi == nullptr) return MLQ_E_NULL;
+  mlq_status s = check_weights(W, x, r0, r1);
+  if (s != MLQ_OK) return s;
+  if (want_type >= 0 && W->type != want_type) return MLQ_E_TYPE;
+  if (x->m != 1) return MLQ_E_SHAPE;
+  if (!aligned(y != nullptr ? static_cast<const void *>(y) : static_cast<const void *>(sumi), 4))
+    return MLQ_E_ALIGN;
+  mlq::LaunchCtx ctx;
+  s = make_ctx(&ctx, stream);
+  if (s != MLQ_OK) return s;
+  return from_cuda(mlq::launch_matvec_m1(ctx, W->type, W->q, W->d, W->cols / MLQ_QK, x->q, x->d,
+                                         y, sumi, r0, r1));
+}
+
+}  // namespace
+
+extern "C" {
+
+mlq_status mlq_init(void) {
+  DevInfo *d = nullptr;
+  return device_info(&d);
+}
+
+mlq_status mlq_quantize_q8(mlq_qact *out, const float *x, int k, void *stream) {
+  if (out == nullptr || x == nullptr || out->q == nullptr || out->d == nullptr) return MLQ_E_NULL;
+  if (!cols_ok(k) || out->n != k || out->m < 1) return MLQ_E_SHAPE;
+  if (!aligned(x, 16) || !aligned(out->q, 16) || !aligned(out->d, 16)) return MLQ_E_ALIGN;
+  mlq::LaunchCtx ctx;
+  mlq_status s = make_ctx(&ctx, stream);
+  if (s != MLQ_OK) return s;
+  return from_cuda(mlq::launch_quantize_q8(ctx, x, out->q, out->d, out->m, k));
+}
+
+mlq_status mlq_matvec_q4(float *y, const mlq_qtensor *W, const mlq_qact *x, int r0, int r1,
+                         void *stream) {
+  if (y == nullptr) return MLQ_E_NULL;
+  return matvec_common(y, nullptr, W, x, r0, r1, stream, MLQ_Q4_0);
+}
+
+mlq_status mlq_matvec_q8(float *y, const mlq_qtensor *W, const mlq_qact *x, int r0, int r1,
+                         void *stream) {
+  if (y == nullptr) return MLQ_E_NULL;
+  return matvec_common(y, nullptr, W, x, r0, r1, stream, MLQ_Q8_0);
+}
+
+mlq_status mlq_block_sumi(int32_t *sumi, const mlq_qtensor *W, const mlq_qact *x, int r0, int r1,
+                          void *stream) {
+  if (sumi == nullptr) return MLQ_E_NULL;
+  return matvec_common(nullptr, sumi, W, x, r0, r1, stream, -1);
+}
+
+mlq_status mlq_gemm_q4_small_m(float *Y, int ldy, const mlq_qtensor *W, const mlq_qact *X, int M,
+                               int r0, int r1, void *stream) {
+  if (Y == nullptr) return MLQ_E_NULL;
+  mlq_status s = check_weights(W, X, r0, r1);
+  if (s != MLQ_OK) return s;
+  if (W->type != MLQ_Q4_0) return MLQ_E_TYPE;
+  if (M < 1 || M > MLQ_MAX_M || X->m != M || ldy < r1 || ldy < 1) return MLQ_E_SHAPE;
+  if (!aligned(Y, 4)) return MLQ_E_ALIGN;
+  mlq::LaunchCtx ctx;
+  s = make_ctx(&ctx, stream);
+  if (s != MLQ_OK) return s;
+  return from_cuda(mlq::launch_gemm_q4_small_m(ctx, W->q, W->d, W->cols / MLQ_QK, X->q, X->d, M,
+                                               Y, ldy, r0, r1));
+}
+
+mlq_status mlq_last_device_error(void *stream) {
+  DevInfo *d = nullptr;
+  mlq_status s = device_info(&d);
+  if (s != MLQ_OK) return s;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return MLQ_E_CUDA;
+  }
+  int v = 0;
+  if (cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return MLQ_E_CUDA;
+  }
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaGetLastError();
+      return MLQ_E_CUDA;
+    }
+    return static_cast<mlq_status>(v);
+  }
+  return MLQ_OK;
+}
+
+mlq_status mlq_debug_set_wait_limit_ns(uint64_t limit_ns) {
+  g_wait_ns.store(limit_ns, std::memory_order_relaxed);
+  return MLQ_OK;
+}
+
+const char *mlq_status_str(mlq_status s) {
+  switch (s) {
+    case MLQ_OK: return "MLQ_OK";
+    case MLQ_E_SHAPE: return "MLQ_E_SHAPE";
+    case MLQ_E_ALIGN: return "MLQ_E_ALIGN";
+    case MLQ_E_TYPE: return "MLQ_E_TYPE";
+    case MLQ_E_NULL: return "MLQ_E_NULL";
+    case MLQ_E_ARCH: return "MLQ_E_ARCH";
+    case MLQ_E_CUDA: return "MLQ_E_CUDA";
+    case MLQ_E_TIMEOUT: return "MLQ_E_TIMEOUT";
+  }
+  return "MLQ_E_UNKNOWN";
+}
+
+}  // extern "C"

@@ -1,0 +1,52 @@
+// mlq_launch.h -- host-side declarations shared by the C-ABI shim and the
+// kernel translation units of libmlq (not part of the public ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mlq {
+
+// Everything a launcher needs besides the operands.
+struct LaunchCtx {
+  cudaStream_t stream;
+  bool pdl;                     // launch with programmatic stream serialization
+  int num_sms;                  // SMs of the current device
+  int *status;                  // device status word (MLQ_E_TIMEOUT on a bounded-wait give-up)
+  unsigned long long wait_ns;   // limit of every device-side wait
+};
+
+// Launch `kern` with cudaLaunchKernelEx, optionally with programmatic
+// dependent launch, on ctx.stream.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          const LaunchCtx &ctx, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = ctx.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = ctx.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// quantize.cu: m rows of k floats -> Q8_0 (q, d).
+cudaError_t launch_quantize_q8(const LaunchCtx &ctx, const float *x, int8_t *q, float *d, int m,
+                               int k);
+
+// matvec.cu: M = 1 product over rows [r0, r1).  qtype 0 = Q8_0, 1 = Q4_0.
+// Exactly one of y / sumi is non-null (sumi = per-block int32 test hook).
+cudaError_t launch_matvec_m1(const LaunchCtx &ctx, int qtype, const void *wq, const float *wd,
+                             int nb, const int8_t *xq, const float *xd, float *y, int32_t *sumi,
+                             int r0, int r1);
+
+// gemm_small_m.cu: M activation rows (1..16) against a Q4_0 matrix.
+cudaError_t launch_gemm_q4_small_m(const LaunchCtx &ctx, const void *wq, const float *wd, int nb,
+                                   const int8_t *xq, const float *xd, int M, float *Y, int ldy,
+                                   int r0, int r1);
+
+}  // namespace mlq

@@ -119,3 +119,22 @@ def small_m(m: int) -> Workload:
     return Workload(f"gemm_q4_0_m{m}", m, [Matvec("up", Q4_0, 11008, 4096, "x"),
                                             Matvec("down", Q4_0, 4096, 11008, "x")],
                     description=f"Q4_0 small-M GEMM, M={m}, 11008x4096 and 4096x11008")
+
+
+def llama7b_ffn_q8_lm_head() -> Workload:
+    wl = llama7b_ffn(Q8_0)
+    wl.mats.append(Matvec("lm_head", Q8_0, 151936, 896, "x"))
+    wl.name = "llama7b_ffn8_q8_0+qwen2.5-0.5b_lm_head"
+    wl.description = "8-layer Llama-7B FFN stack Q8_0 (chained) + Qwen2.5-0.5B lm_head Q8_0, M=1"
+    return wl
+
+
+WORKLOADS = {
+    "tiny_q4": tiny_q4,
+    "tinyllama_layer": tinyllama_layer,
+    "llama7b_ffn_q4": lambda: llama7b_ffn(Q4_0),
+    "llama7b_ffn_q8_lm_head": llama7b_ffn_q8_lm_head,
+    "qwen_lm_head": qwen_lm_head,
+    "small_m4": lambda: small_m(4),
+    "small_m16": lambda: small_m(16),
+}

@@ -1,0 +1,126 @@
+"""Device-resident workloads driven through the C ABI.
+
+A ``WorkloadRunner`` owns the device buffers of one workload (weights,
+activations, Q8_0 activation buffers, outputs) and issues one pass of the
+hot path -- quantize each input once, then the Q4_0/Q8_0 products -- as C-ABI
+calls on a stream.  torch supplies device memory, pinned host memory, streams
+and CUDA graphs; every arithmetic step runs in libmlq's kernels.
+
+Weights can be replicated ``copies`` times so that consecutive passes read
+different bytes (inputs larger than L2 between timed passes).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import binding as B
+from . import inputs as I
+
+
+@dataclass
+class _Mat:
+    spec: I.Matvec
+    src: str               # input buffer name
+    q: list                # per copy: device quant bytes
+    d: list                # per copy: device scales
+    y: torch.Tensor        # output [m, rows] float32
+    host_q: np.ndarray
+    host_d: np.ndarray
+
+
+class WorkloadRunner:
+    def __init__(self, wl: I.Workload, copies: int = 1, device: str = "cuda:0",
+                 seed_base: int = 0, x_seed_base: int = 1000):
+        self.wl = wl
+        self.m = wl.m
+        self.copies = copies
+        self.dev = torch.device(device)
+        self.mats: list[_Mat] = []
+        self.sources: dict[str, int] = {}   # input name -> length K
+        self.x_host: dict[str, np.ndarray] = {}
+        self.x_pinned: dict[str, torch.Tensor] = {}
+        self.fp32: dict[str, torch.Tensor] = {}   # float32 vectors feeding a quantize
+        self.qbuf: dict[str, B.QAct] = {}
+        for i, mv in enumerate(wl.mats):
+            src = f"x{mv.cols}" if mv.input_of == "x" else mv.input_of
+            if mv.input_of == "x" and src not in self.x_host:
+                xs = I.activations(self.m, mv.cols, seed=x_seed_base + len(self.x_host))
+                self.x_host[src] = xs
+                self.x_pinned[src] = torch.from_numpy(xs).pin_memory()
+                self.fp32[src] = torch.from_numpy(xs).to(self.dev)
+            self.sources.setdefault(src, mv.cols)
+            hq, hd = I.weights(mv.wtype, mv.rows, mv.cols, seed=seed_base + i)
+            qs, ds = [], []
+            for _ in range(copies):
+                qs.append(torch.from_numpy(hq.reshape(-1)).to(self.dev))
+                ds.append(torch.from_numpy(hd.reshape(-1)).to(self.dev))
+            y = torch.zeros((self.m, mv.rows), dtype=torch.float32, device=self.dev)
+            self.mats.append(_Mat(mv, src, qs, ds, y, hq, hd))
+        for m in self.mats:
+            self.fp32.setdefault(m.spec.name, m.y)
+        for src, k in self.sources.items():
+            q = torch.empty((self.m, k), dtype=torch.int8, device=self.dev)
+            d = torch.empty((self.m, k // I.QK), dtype=torch.float32, device=self.dev)
+            self.qbuf[src] = B.QAct(q, d, k, self.m)
+        self.kernels_per_step = len(self.sources) + len(self.mats)
+
+    # ---- sizes ---------------------------------------------------------------
+    def weight_bytes(self) -> int:
+        return sum(m.host_q.nbytes + m.host_d.nbytes for m in self.mats)
+
+    def ops(self) -> int:
+        return sum(2 * self.m * m.spec.rows * m.spec.cols for m in self.mats)
+
+    def h2d_bytes(self) -> int:
+        return sum(t.numel() * 4 for t in self.x_pinned.values())
+
+    def d2h_bytes(self) -> int:
+        return sum(m.y.numel() * 4 for m in self.mats)
+
+    # ---- one pass --------------------------------------------------------------
+    def step(self, copy: int = 0, stream=None, before_mat=None, after_mat=None) -> None:
+        """Issue one pass on `stream`: each input is quantised right before
+        its first consumer, then each product runs.  before_mat/after_mat
+        (optional callables taking the matrix index) let the bench record
+        events around the products."""
+        done = set()
+        for i, m in enumerate(self.mats):
+            if m.src not in done:
+                B.mlq_quantize_q8(self.qbuf[m.src], self.fp32[m.src], self.sources[m.src], stream)
+                done.add(m.src)
+            W = B.QTensor(m.q[copy], m.d[copy], m.spec.rows, m.spec.cols, m.spec.wtype)
+            if before_mat is not None:
+                before_mat(i)
+            if self.m == 1:
+                f = B.mlq_matvec_q4 if m.spec.wtype == I.Q4_0 else B.mlq_matvec_q8
+                f(m.y, W, self.qbuf[m.src], 0, m.spec.rows, stream)
+            else:
+                B.mlq_gemm_q4_small_m(m.y, m.spec.rows, W, self.qbuf[m.src], self.m, 0,
+                                      m.spec.rows, stream)
+            if after_mat is not None:
+                after_mat(i)
+
+    def upload_inputs(self, stream=None) -> None:
+        """Host -> device copy of every external input (pinned, async)."""
+        with torch.cuda.stream(stream) if stream is not None else _null():
+            for src, t in self.x_pinned.items():
+                self.fp32[src].copy_(t, non_blocking=True)
+
+    def outputs_to_host(self, host: dict | None = None) -> dict:
+        host = {} if host is None else host
+        for m in self.mats:
+            if m.spec.name not in host:
+                host[m.spec.name] = torch.empty(m.y.shape, dtype=torch.float32).pin_memory()
+            host[m.spec.name].copy_(m.y, non_blocking=True)
+        return host
+
+
+class _null:
+    def __enter__(self):
+        return None
+
+    def __exit__(self, *a):
+        return False

@@ -1,0 +1,160 @@
+/*
+ * mlq.h -- C ABI of the GB300 (sm_103a) block-quantized decode library.
+ *
+ * The operations follow the page "Legacy-ISA ML Inference Runtime -- Design
+ * Spec":
+ *   Sec. 4 (Quantization Formats) fixes the data: blocks of QK = 32
+ *     elements; Q8_0 = int8 quants clamped to [-127, 127] plus one float32
+ *     scale per block; Q4_0 = 16 bytes per block (low nibble = element
+ *     0..15, high nibble = element 16..31, value = nibble - 8) plus one
+ *     float32 scale; quants and scales of a tensor are two separate arrays;
+ *     per block sumi = sum(qw*qx) is an int32 and the output accumulates
+ *     (float)sumi * dw * dx in float32.
+ *   Sec. 5 (Kernel Interface) fixes the calls: matvec over a row range
+ *     [r0, r1) of W, and quantize_q8 with
+ *     q = trunc(x*id + copysign(0.5, x)), id = 127/amax, d = amax/127.
+ *   Sec. 6 (Error handling) fixes the convention: every call returns a
+ *     status, nothing aborts.
+ * The small-M product (M independent activation rows against one weight
+ * matrix) is the batched-decode case of the page "ONNX Runtime", section
+ * "6. Panel loop (pre-TCM)" (M = 4 rows of 4096 x 11008).
+ *
+ * Memory and layout (all pointers inside the structs are DEVICE pointers;
+ * the structs themselves may live in host memory and are read during the
+ * call only):
+ *   W->q  Q4_0: rows * cols/2 bytes; block b of row r is the 16 bytes at
+ *              offset (r*nb + b)*16, nb = cols/32.
+ *         Q8_0: rows * cols int8; block b of row r at offset (r*nb + b)*32.
+ *   W->d  rows * nb float32; scale of block (r, b) at index r*nb + b.
+ *   x->q  m rows of n int8 (row i at x->q + i*n); x->d m rows of n/32 floats.
+ *   y     float32 indexed by absolute row: y[r] for r in [r0, r1).  Entries
+ *         outside [r0, r1) are never written.
+ * Every q and d pointer must be 16-byte aligned (torch allocations are).
+ * n (= cols) must be a positive multiple of 32 and at most MLQ_MAX_COLS.
+ *
+ * Ownership: the caller owns every buffer.  No call allocates device memory
+ * or keeps a pointer after it returns.
+ *
+ * Launch: every compute call is asynchronous on `stream` (a cudaStream_t
+ * passed as void*; NULL = the legacy default stream) and returns as soon
+ * as the work is queued.  A status other than MLQ_OK means nothing was
+ * queued.  Device-side problems (a bounded wait that gave up) are reported
+ * by mlq_last_device_error() after the work has finished.
+ *
+ * Kernels are launched with programmatic dependent launch: a kernel may
+ * start while the previous kernel on the stream is finishing and prefetch
+ * weight bytes into L2 (always safe: L2 is the point of coherence), but it
+ * reads and writes nothing through the caches before that previous kernel
+ * has completed.  Set the environment variable MLQ_PDL=0 to launch plainly.
+ */
+#ifndef MLQ_H
+#define MLQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLQ_QK 32
+#define MLQ_MAX_COLS 65536
+#define MLQ_MAX_M 16
+
+typedef enum {
+    MLQ_OK = 0,
+    MLQ_E_SHAPE = 1,   /* cols % 32 != 0, cols > MLQ_MAX_COLS, r0/r1 outside
+                          0 <= r0 <= r1 <= rows, x->n != W->cols, M outside
+                          1..16, x->m != M, ldy < r1, k != out->n           */
+    MLQ_E_ALIGN = 2,   /* a q or d pointer is not 16-byte aligned          */
+    MLQ_E_TYPE = 3,    /* W->type does not match the entry point           */
+    MLQ_E_NULL = 4,    /* a required pointer is NULL                       */
+    MLQ_E_ARCH = 5,    /* no CUDA device, or it is not compute capability
+                          10.3 (the library is built for sm_103a only)     */
+    MLQ_E_CUDA = 6,    /* a CUDA runtime call (launch, copy) failed        */
+    MLQ_E_TIMEOUT = 7  /* a bounded device-side wait gave up; results of
+                          that work are undefined                          */
+} mlq_status;
+
+enum { MLQ_Q8_0 = 0, MLQ_Q4_0 = 1 };
+
+/* Weight tensor (Design Spec Sec. 4, ml_qtensor).  type is MLQ_Q8_0 or
+ * MLQ_Q4_0; q holds raw bytes (int8 for Q8_0, packed nibbles for Q4_0). */
+typedef struct {
+    void *q;
+    float *d;
+    int rows, cols;
+    uint8_t type;
+} mlq_qtensor;
+
+/* Q8_0 activations (Design Spec Sec. 4, ml_qact) extended to m rows of n. */
+typedef struct {
+    int8_t *q;
+    float *d;
+    int n;
+    int m;
+} mlq_qact;
+
+/* Check that device 0.. the current device is compute capability 10.3 and
+ * cache its SM count.  Called implicitly by every entry point; returns
+ * MLQ_E_ARCH without a suitable device.  Idempotent, thread-safe. */
+mlq_status mlq_init(void);
+
+/* Design Spec Sec. 4 "Q8 quantization" and Sec. 5 quantize_q8: quantise
+ * out->m rows of k float32 (x, device, row-major m x k) into out->q
+ * (m x k int8) and out->d (m x k/32 float32).  Per block of 32:
+ * amax = max|x|, d = amax/127 (IEEE division), id = 127/amax (0 when
+ * amax = 0), q = trunc(x*id + copysign(0.5, x)) with the product and the
+ * sum each rounded to float32 (no fused multiply-add), clamped to
+ * [-127, 127]; a NaN (0 * inf when 127/amax overflows) stores 0.  Results
+ * are bit-identical to that definition.  Requires out->n == k and
+ * out->m >= 1. */
+mlq_status mlq_quantize_q8(mlq_qact *out, const float *x, int k, void *stream);
+
+/* Design Spec Sec. 5 matvec_q4: for r in [r0, r1)
+ *   y[r] = sum_b (float)sumi(r, b) * W->d[r*nb + b] * x->d[b],
+ *   sumi(r, b) = sum_j (nibble(r, b, j) - 8) * x->q[32b + j]   (exact int32).
+ * W->type must be MLQ_Q4_0; x->m must be 1.  The float32 sum is taken in
+ * an order other than b = 0, 1, ...; it agrees with the in-order sum within
+ * 1e-5 * sum_b |term_b| per row. */
+mlq_status mlq_matvec_q4(float *y, const mlq_qtensor *W, const mlq_qact *x,
+                         int r0, int r1, void *stream);
+
+/* Design Spec Sec. 5 matvec_q8: as mlq_matvec_q4 with int8 weights
+ * (W->type == MLQ_Q8_0). */
+mlq_status mlq_matvec_q8(float *y, const mlq_qtensor *W, const mlq_qact *X,
+                         int r0, int r1, void *stream);
+
+/* Batched small-M decode (ONNX Runtime page, "6. Panel loop"): M activation
+ * rows X (X->m == M, each quantised per row) against one Q4_0 matrix:
+ *   Y[m*ldy + r] = sum_b (float)sumi(m, r, b) * W->d[r*nb + b] * X->d[m*nb + b]
+ * for m < M, r in [r0, r1).  1 <= M <= 16; ldy >= r1.  Same tolerance as
+ * the M = 1 calls, per (m, r). */
+mlq_status mlq_gemm_q4_small_m(float *Y, int ldy, const mlq_qtensor *W, const mlq_qact *X,
+                               int M, int r0, int r1, void *stream);
+
+/* Test hook (Design Spec Sec. 7: per-block int32 sums are checked exactly):
+ * sumi[(r - r0)*nb + b] for r in [r0, r1), b < nb, computed by the same
+ * block-dot code as the matvec of W->type (Q4_0 or Q8_0); x->m must be 1. */
+mlq_status mlq_block_sumi(int32_t *sumi, const mlq_qtensor *W, const mlq_qact *x,
+                          int r0, int r1, void *stream);
+
+/* Synchronise `stream`, then report and clear the library's device status
+ * word: MLQ_E_TIMEOUT if any kernel since the last call gave up a bounded
+ * wait, MLQ_E_CUDA if the stream reported an error, else MLQ_OK. */
+mlq_status mlq_last_device_error(void *stream);
+
+/* Test hook: limit, in nanoseconds, of every device-side wait (default
+ * 1e9 = one second).  0 makes every wait give up at once, which exercises
+ * the timeout path without any real hang: the kernel then records
+ * MLQ_E_TIMEOUT, drains its own copies in flight with the default limit
+ * and returns.  Affects launches made after the call. */
+mlq_status mlq_debug_set_wait_limit_ns(uint64_t limit_ns);
+
+/* Human-readable name of a status. Never NULL. */
+const char *mlq_status_str(mlq_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLQ_H */

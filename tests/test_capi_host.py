@@ -1,0 +1,154 @@
+"""The C-ABI library on the host (no GPU needed): it builds for sm_103a,
+loads, exports every symbol include/mlq.h declares, and rejects bad
+arguments with the documented status before touching the device
+(page "Legacy-ISA ML Inference Runtime -- Design Spec", Sec. 6 "Error
+handling": a status, never an abort; loader checks K % 32 == 0)."""
+import ctypes
+import os
+import re
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def M():
+    from block_quantized_decode_gb300 import build as B
+    B.build()
+    import block_quantized_decode_gb300 as pkg
+    pkg.lib()
+    return pkg
+
+
+def header_symbols():
+    src = open(os.path.join(ROOT, "include", "mlq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mlq_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(M):
+    declared = header_symbols()
+    assert len(declared) >= 9
+    out = subprocess.run(["nm", "-D", "--defined-only", M.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (mlq_[a-z0-9_]+)$", out, flags=re.M))
+    missing = [s for s in declared if s not in exported]
+    assert not missing, missing
+    assert sorted(M.EXPORTS) == declared
+    for s in declared:
+        getattr(M.lib(), s)
+
+
+def test_status_strings(M):
+    names = ["MLQ_OK", "MLQ_E_SHAPE", "MLQ_E_ALIGN", "MLQ_E_TYPE", "MLQ_E_NULL", "MLQ_E_ARCH",
+             "MLQ_E_CUDA", "MLQ_E_TIMEOUT"]
+    for i, n in enumerate(names):
+        assert M.mlq_status_str(i) == n
+    assert M.mlq_status_str(99) == "MLQ_E_UNKNOWN"
+
+
+# fake, 256-byte aligned "device" addresses: validation never dereferences them
+A = 1 << 20
+
+
+def qt(q=A, d=2 * A, rows=64, cols=128, t=1):
+    from block_quantized_decode_gb300.binding import _QTensor
+    return _QTensor(q, d, rows, cols, t)
+
+
+def qa(q=3 * A, d=4 * A, n=128, m=1):
+    from block_quantized_decode_gb300.binding import _QAct
+    return _QAct(q, d, n, m)
+
+
+def call(M, name, *args):
+    return M.binding.raw_call(name, *args)
+
+
+def mv(M, name="mlq_matvec_q4", y=5 * A, W=None, x=None, r0=0, r1=64):
+    W = qt() if W is None else W
+    x = qa() if x is None else x
+    return call(M, name, y, ctypes.byref(W), ctypes.byref(x), r0, r1, None)
+
+
+def test_validation_matvec(M):
+    assert mv(M, y=None) == M.MLQ_E_NULL
+    assert call(M, "mlq_matvec_q4", 5 * A, None, ctypes.byref(qa()), 0, 1, None) == M.MLQ_E_NULL
+    assert mv(M, W=qt(q=0)) == M.MLQ_E_NULL
+    assert mv(M, x=qa(d=0)) == M.MLQ_E_NULL
+    assert mv(M, W=qt(t=0)) == M.MLQ_E_TYPE            # Q8_0 tensor to the Q4_0 entry
+    assert mv(M, "mlq_matvec_q8") == M.MLQ_E_TYPE      # Q4_0 tensor to the Q8_0 entry
+    assert mv(M, W=qt(t=7)) == M.MLQ_E_TYPE
+    assert mv(M, W=qt(cols=100), x=qa(n=100)) == M.MLQ_E_SHAPE   # K % 32 != 0
+    assert mv(M, W=qt(cols=0), x=qa(n=0)) == M.MLQ_E_SHAPE
+    assert mv(M, W=qt(cols=65568), x=qa(n=65568)) == M.MLQ_E_SHAPE  # > MLQ_MAX_COLS
+    assert mv(M, x=qa(n=96)) == M.MLQ_E_SHAPE          # x->n != W->cols
+    assert mv(M, x=qa(m=2)) == M.MLQ_E_SHAPE           # M = 1 entry
+    assert mv(M, r0=-1) == M.MLQ_E_SHAPE
+    assert mv(M, r0=5, r1=4) == M.MLQ_E_SHAPE
+    assert mv(M, r1=65) == M.MLQ_E_SHAPE
+    assert mv(M, W=qt(q=A + 8)) == M.MLQ_E_ALIGN
+    assert mv(M, W=qt(d=2 * A + 4)) == M.MLQ_E_ALIGN
+    assert mv(M, x=qa(q=3 * A + 1)) == M.MLQ_E_ALIGN
+    assert mv(M, y=5 * A + 2) == M.MLQ_E_ALIGN
+
+
+def test_validation_quantize(M):
+    q = lambda out, x=6 * A, k=128: call(M, "mlq_quantize_q8", ctypes.byref(out), x, k, None)
+    assert q(qa(), x=None) == M.MLQ_E_NULL
+    assert q(qa(q=0)) == M.MLQ_E_NULL
+    assert q(qa(n=96), k=96 + 1) == M.MLQ_E_SHAPE
+    assert q(qa(n=128), k=96) == M.MLQ_E_SHAPE
+    assert q(qa(m=0)) == M.MLQ_E_SHAPE
+    assert q(qa(), x=6 * A + 4) == M.MLQ_E_ALIGN
+    assert q(qa(d=4 * A + 8)) == M.MLQ_E_ALIGN
+
+
+def test_validation_gemm_and_sumi(M):
+    def g(Y=5 * A, ldy=64, W=None, X=None, Mrows=4, r0=0, r1=64):
+        W = qt() if W is None else W
+        X = qa(m=4) if X is None else X
+        return call(M, "mlq_gemm_q4_small_m", Y, ldy, ctypes.byref(W), ctypes.byref(X), Mrows,
+                    r0, r1, None)
+    assert g(Y=None) == M.MLQ_E_NULL
+    assert g(W=qt(t=0)) == M.MLQ_E_TYPE
+    assert g(Mrows=0, X=qa(m=0)) == M.MLQ_E_SHAPE
+    assert g(Mrows=17, X=qa(m=17)) == M.MLQ_E_SHAPE
+    assert g(Mrows=4, X=qa(m=3)) == M.MLQ_E_SHAPE
+    assert g(ldy=63) == M.MLQ_E_SHAPE
+    assert g(Y=5 * A + 1) == M.MLQ_E_ALIGN
+    s = lambda **k: call(M, "mlq_block_sumi", k.get("out", 5 * A), ctypes.byref(k.get("W", qt())),
+                         ctypes.byref(qa()), 0, 64, None)
+    assert s(out=None) == M.MLQ_E_NULL
+    assert s(W=qt(t=9)) == M.MLQ_E_TYPE
+
+
+def _cuda_available():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+@pytest.mark.skipif(_cuda_available(), reason="checks the no-device path")
+def test_valid_call_without_device_is_arch_error(M):
+    assert M.binding.raw_call("mlq_init") == M.MLQ_E_ARCH
+    assert mv(M) == M.MLQ_E_ARCH
+
+
+def test_arch_guard_with_faked_capability():
+    """A device that reports another compute capability is refused with
+    MLQ_E_ARCH (the library is built for sm_103a only)."""
+    code = ("import block_quantized_decode_gb300 as M; import sys; "
+            "sys.exit(M.binding.raw_call('mlq_init'))")
+    env = dict(os.environ, MLQ_FAKE_CC="9.0", PYTHONPATH=ROOT)
+    r = subprocess.run([sys.executable, "-c", code], env=env, cwd=ROOT, timeout=300)
+    assert r.returncode == 5  # MLQ_E_ARCH
+
+
+def test_debug_wait_limit_hook(M):
+    M.mlq_debug_set_wait_limit_ns(10 ** 9)
