@@ -43,14 +43,19 @@ FALLBACK_HBM_GBS = 6800.0
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
-    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--steps", type=int, default=0,
+                   help="timed steps (0 = as many as fill about --seconds of the timed region)")
+    p.add_argument("--seconds", type=float, default=1.5)
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="tinyllama_layer")
     p.add_argument("--copies", type=int, default=0, help="weight copies (0 = auto, > 3x L2)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--prefetch", choices=["none", "all", "next"], default="none",
+                   help="L2 prefetch of weights through mlq_prefetch_l2: all (whole pass "
+                        "first) or next (one product ahead); measured slower in-chain, so off")
     return p.parse_args()
 
 
@@ -101,7 +106,7 @@ def measured_peaks():
 
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -118,7 +123,9 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0: float | None = None, t1: float | None = None):
+        """Median clocks of the samples taken between host times t0 and t1
+        (the timed region); if none fell inside it, of all samples taken."""
         if self.proc is None:
             return None
         time.sleep(0.25)
@@ -128,41 +135,49 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
+        import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        samples = []
         for line in out.splitlines():
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                samples.append((ts, float(parts[1]), float(parts[2]),
+                                {n for n, v in zip(names, parts[5:9]) if v.lower() == "active"}))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        if not samples:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        inside = [x for x in samples if t0 is not None and t0 <= x[0] <= t1]
+        use = inside or samples
+        return {"sm_mhz": statistics.median(x[1] for x in use),
+                "sm_max_mhz": max(x[2] for x in use),
+                "samples": len(use), "window": "timed region" if inside else "whole run",
+                "reasons": sorted(set().union(*[x[3] for x in use]))}
 
 
-def ncu_traffic(kernel_file: str, workload: str):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, if it was taken on the current kernel source; else None."""
+def ncu_traffic(workload: str, bytes_per_launch: float):
+    """DRAM bytes per launch of the dominant kernel: the DRAM/algorithmic
+    ratio of the committed ncu summary times the algorithmic bytes per
+    launch, if the summary was taken on the current kernel source; else
+    None."""
     path = os.path.join(ROOT, "profiles", f"matvec_q4_{workload}.md")
-    src = os.path.join(ROOT, "block_quantized_decode_gb300", "csrc", kernel_file)
+    csrc = os.path.join(ROOT, "block_quantized_decode_gb300", "csrc")
     try:
         text = open(path).read()
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        h = hashlib.sha256()
+        for f in ("matvec.cu", "mlq_device.cuh"):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+        sha = h.hexdigest()[:16]
     except OSError:
         return None
     m_sha = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
-    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_sha or not m_tr or m_sha.group(1) != sha:
+    m_r = re.search(r"dram_over_algorithmic:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_r or m_sha.group(1) != sha:
         return None
-    return float(m_tr.group(1))
+    return float(m_r.group(1)) * bytes_per_launch
 
 
 # ----------------------------------------------------------------------------
@@ -244,22 +259,23 @@ def run_reference(args, wl, world, rank):
         return 0
     threads = host_cores()
     op = OraclePass(wl, threads)
-    for _ in range(max(0, args.warmup)):
+    for _ in range(min(max(0, args.warmup), 3)):
         op.run()
     t0 = time.perf_counter()
-    for _ in range(args.steps):
+    steps = args.steps if args.steps > 0 else max(3, int(args.seconds / 0.1))
+    for _ in range(steps):
         op.run()
     el = time.perf_counter() - t0
-    v = op.weight_bytes * args.steps / el / 1e9
+    v = op.weight_bytes * steps / el / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": el / steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8 dot -> int32, f32 accumulate (CPU oracle)", "data": "synthetic",
         "config": {"workload": wl.name, "M": wl.m, "weight_bytes_per_step": op.weight_bytes},
         "gops": op.ops * args.steps / el / 1e9,
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"{args.steps} full passes of {wl.name} after {args.warmup} warm-up"},
+                         "sample": f"{steps} full passes of {wl.name} after {args.warmup} warm-up"},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -285,103 +301,123 @@ def run_ours(args, wl, world, rank, local, pg):
                  + mv.rows * mv.cols // 32 * 4 for mv in wl.mats)
     copies = args.copies or max(2, math.ceil(3 * l2 / wbytes))
     r = WorkloadRunner(wl, copies=copies, device=f"cuda:{local}")
+    pf = args.prefetch
+    if pf == "none":
+        pf = None
     assert r.weight_bytes() == wbytes
     stream = torch.cuda.Stream(device=dev)
 
     # ---- graphs: one per weight copy (plain), one per copy instrumented
-    q4_idx = [i for i, m in enumerate(r.mats) if m.spec.wtype == I.Q4_0] or list(range(len(r.mats)))
     dominant = "matvec_m1_kernel<Q4_0>" if r.m == 1 and any(
         m.spec.wtype == I.Q4_0 for m in r.mats) else (
         "matvec_m1_kernel<Q8_0>" if r.m == 1 else "gemm_q4_small_m")
-    ev_ok = True
-    try:
-        torch.cuda.Event(enable_timing=True, external=True)
-    except TypeError:
-        ev_ok = False
     with torch.cuda.stream(stream):
         for c in range(copies):  # eager warm-up of every copy (kernel attributes, caches)
-            r.step(copy=c)
+            r.step(copy=c, prefetch=pf)
     stream.synchronize()
-    graphs, igraphs, ievents = [], [], []
+    graphs = []
     if not args.no_graph:
         for c in range(copies):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                r.step(copy=c)
+                r.step(copy=c, prefetch=pf)
             graphs.append(g)
-        if ev_ok:
-            for c in range(copies):
-                evs = {i: (torch.cuda.Event(enable_timing=True, external=True),
-                           torch.cuda.Event(enable_timing=True, external=True)) for i in q4_idx}
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    r.step(copy=c, before_mat=lambda i: evs[i][0].record() if i in evs else None,
-                           after_mat=lambda i: evs[i][1].record() if i in evs else None)
-                igraphs.append(g)
-                ievents.append(evs)
 
     def do_step(i):
         if graphs:
             graphs[i % copies].replay()
         else:
-            r.step(copy=i % copies)
+            r.step(copy=i % copies, prefetch=pf)
 
     # ---- headline timed region
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            do_step(i)
-    stream.synchronize()
-    barrier(pg, local)
-    torch.cuda.synchronize()
     clocks = ClockSampler(local)
     clocks.start()
-    time.sleep(0.3)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a0.record(stream)
+        for i in range(args.warmup):
+            do_step(i)
+        a1.record(stream)
+    stream.synchronize()
+    steps = args.steps
+    if steps <= 0:  # fill about args.seconds, same count on every rank
+        per = a0.elapsed_time(a1) / 1e3 / max(1, args.warmup)
+        steps = max(10, int(args.seconds / max(per, 1e-7)))
+        steps = int(max_over_ranks(pg, float(steps), dev))
+    barrier(pg, local)
+    torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    t_host0 = time.time()
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for i in range(args.steps):
+        for i in range(steps):
             do_step(args.warmup + i)
         e1.record(stream)
     torch.cuda.synchronize()
+    t_host1 = time.time()
     barrier(pg, local)
-    clk = clocks.stop()
+    clk = clocks.stop(t_host0, t_host1)
     ms = e0.elapsed_time(e1)
     ms_max = max_over_ranks(pg, ms, dev)
-    steps = args.steps
     value = world * wbytes * steps / (ms_max / 1e3) / 1e9
     gops = world * r.ops() * steps / (ms_max / 1e3) / 1e9
 
-    # ---- dominant-kernel launch durations (instrumented graphs)
+    # ---- dominant-kernel launch durations: every distinct product shape of
+    # the step replayed back to back in its own graph (rotating weight
+    # copies, so every launch streams from HBM), CUDA events on the launching
+    # stream; achieved = algorithmic weight bytes per launch / mean duration,
+    # weighted by how often the shape occurs in the step.
     peaks, peak_src = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     roofline = None
-    if igraphs:
-        tot_ms, tot_bytes, launches = 0.0, 0, 0
-        nrep = min(steps, 4 * copies)
-        with torch.cuda.stream(stream):
-            for i in range(nrep):
-                c = i % copies
-                igraphs[c].replay()
+    if graphs:
+        shapes = {}
+        for i, m in enumerate(r.mats):
+            shapes.setdefault((m.spec.wtype, m.spec.rows, m.spec.cols), []).append(i)
+        per_shape, tot_bytes, tot_s = [], 0.0, 0.0
+        launches = 2 * copies
+        for (wt, rows, cols), idx in shapes.items():
+            i0 = idx[0]
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for j in range(launches):
+                    r.product(i0, copy=j % copies)
+            with torch.cuda.stream(stream):
+                g.replay()
+            stream.synchronize()
+            best = None
+            for _ in range(3):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    a.record(stream)
+                    g.replay()
+                    b.record(stream)
                 stream.synchronize()
-                for mi, (a, b) in ievents[c].items():
-                    tot_ms += a.elapsed_time(b)
-                    m = r.mats[mi]
-                    tot_bytes += m.host_q.nbytes + m.host_d.nbytes
-                    launches += 1
-        per_launch_bytes = tot_bytes / launches
-        per_launch_s = tot_ms / launches / 1e3
-        ach = per_launch_bytes / per_launch_s / 1e9
+                t = a.elapsed_time(b) / 1e3 / launches
+                best = t if best is None else min(best, t)
+            m = r.mats[i0]
+            nbytes = m.host_q.nbytes + m.host_d.nbytes
+            per_shape.append({"shape": f"{rows}x{cols}:{'q4_0' if wt == I.Q4_0 else 'q8_0'}",
+                              "per_step": len(idx), "us_per_launch": best * 1e6,
+                              "GBps": nbytes / best / 1e9})
+            tot_bytes += nbytes * len(idx)
+            tot_s += best * len(idx)
+            del g
+        ach = tot_bytes / tot_s / 1e9
         roofline = {"kernel": dominant, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
                     "frac": ach / hbm, "peak_source": peak_src,
-                    "traffic": ncu_traffic("matvec.cu", wl.name),
-                    "bytes_per_launch": per_launch_bytes, "us_per_launch": per_launch_s * 1e6,
-                    "launches_timed": launches}
+                    "traffic": ncu_traffic(wl.name, tot_bytes / sum(p["per_step"] for p in per_shape)),
+                    "bytes_per_launch": tot_bytes / sum(p["per_step"] for p in per_shape),
+                    "us_per_launch": tot_s / sum(p["per_step"] for p in per_shape) * 1e6,
+                    "method": f"{launches} back-to-back launches per shape in one CUDA graph, "
+                              "best of 3 replays, CUDA events on the launching stream",
+                    "per_shape": per_shape}
 
     # ---- end to end: pinned host input -> step -> outputs to pinned host
     host_out = r.outputs_to_host()
     torch.cuda.synchronize()
-    e2e_steps = min(steps, 100)
+    e2e_steps = min(steps, 500)
     t0 = time.perf_counter()
     for i in range(e2e_steps):
         with torch.cuda.stream(stream):
@@ -418,10 +454,10 @@ def run_ours(args, wl, world, rank, local, pg):
                        "weight_bytes_per_step": wbytes,
                        "l2": f"inputs larger than L2: {copies} rotating weight copies "
                              f"({copies * wbytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
-                       "graphs": bool(graphs), "parallelism": f"replicas x{world} (independent decode streams)"},
+                       "graphs": bool(graphs), "l2_prefetch": pf or "none", "parallelism": f"replicas x{world} (independent decode streams)"},
             "gops": gops, "hbm_frac": value / world / hbm,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": r.kernels_per_step * steps,
+            "gpu_launches": (r.kernels_per_step + {None: 0, "all": 1, "next": len(r.mats)}[pf]) * steps,
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)

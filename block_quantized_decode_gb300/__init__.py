@@ -10,5 +10,5 @@ from .binding import (  # noqa: F401
     MLQ_E_TIMEOUT, MLQ_E_TYPE, MLQ_MAX_COLS, MLQ_MAX_M, MLQ_OK, MLQ_Q4_0, MLQ_Q8_0, MLQ_QK,
     MlqError, QAct, QTensor, lib, mlq_block_sumi, mlq_debug_set_wait_limit_ns,
     mlq_gemm_q4_small_m, mlq_init, mlq_last_device_error, mlq_matvec_q4, mlq_matvec_q8,
-    mlq_quantize_q8, mlq_status_str,
+    mlq_prefetch_l2, mlq_quantize_q8, mlq_status_str,
 )

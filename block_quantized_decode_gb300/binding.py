@@ -25,7 +25,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmlq.so")
 EXPORTS = (
     "mlq_init", "mlq_quantize_q8", "mlq_matvec_q4", "mlq_matvec_q8",
     "mlq_gemm_q4_small_m", "mlq_block_sumi", "mlq_last_device_error",
-    "mlq_debug_set_wait_limit_ns", "mlq_status_str",
+    "mlq_debug_set_wait_limit_ns", "mlq_status_str", "mlq_prefetch_l2",
 )
 
 
@@ -66,6 +66,7 @@ def lib() -> ctypes.CDLL:
         L.mlq_block_sumi.argtypes = [P, QT, QA, I, I, P]
         L.mlq_last_device_error.argtypes = [P]
         L.mlq_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        L.mlq_prefetch_l2.argtypes = [P, P, I, P]
         L.mlq_status_str.argtypes = [S]
         L.mlq_status_str.restype = ctypes.c_char_p
         for name in EXPORTS:
@@ -169,6 +170,14 @@ def mlq_block_sumi(sumi, W: QTensor, x: QAct, r0: int, r1: int, stream=None) -> 
     cw, cx = W.c(), x.c()
     _check(lib().mlq_block_sumi(_addr(sumi), ctypes.byref(cw), ctypes.byref(cx), r0, r1,
                                 _stream(stream)), "mlq_block_sumi")
+
+
+def mlq_prefetch_l2(ranges, stream=None) -> None:
+    """ranges: sequence of (tensor or device address, byte count)."""
+    n = len(ranges)
+    ptrs = (ctypes.c_void_p * max(n, 1))(*[_addr(p) for p, _ in ranges])
+    sizes = (ctypes.c_size_t * max(n, 1))(*[int(b) for _, b in ranges])
+    _check(lib().mlq_prefetch_l2(ptrs, sizes, n, _stream(stream)), "mlq_prefetch_l2")
 
 
 def mlq_last_device_error(stream=None) -> int:

@@ -190,6 +190,22 @@ mlq_status mlq_gemm_q4_small_m(float *Y, int ldy, const mlq_qtensor *W, const ml
                                                Y, ldy, r0, r1));
 }
 
+mlq_status mlq_prefetch_l2(const void *const *ptrs, const size_t *bytes, int n, void *stream) {
+  if (n < 0 || n > MLQ_MAX_PREFETCH_RANGES) return MLQ_E_SHAPE;
+  if (n > 0 && (ptrs == nullptr || bytes == nullptr)) return MLQ_E_NULL;
+  mlq::PrefetchList list;
+  list.n = n;
+  for (int i = 0; i < n; ++i) {
+    if (ptrs[i] == nullptr && bytes[i] != 0) return MLQ_E_NULL;
+    list.ptr[i] = ptrs[i];
+    list.bytes[i] = bytes[i];
+  }
+  mlq::LaunchCtx ctx;
+  mlq_status s = make_ctx(&ctx, stream);
+  if (s != MLQ_OK) return s;
+  return from_cuda(mlq::launch_prefetch_l2(ctx, list));
+}
+
 mlq_status mlq_last_device_error(void *stream) {
   DevInfo *d = nullptr;
   mlq_status s = device_info(&d);

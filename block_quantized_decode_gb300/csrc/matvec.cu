@@ -36,6 +36,8 @@
 //  * Reduction: per-lane float partials, a warp-shuffle tree per task, and
 //    (when a row spans several chunks) a fixed-order sum of the per-chunk
 //    partials in shared memory: deterministic, no atomics.
+#include <cstdlib>
+
 #include "mlq_device.cuh"
 #include "mlq_launch.h"
 
@@ -312,10 +314,37 @@ static cudaError_t launch_qt(const LaunchCtx &ctx, MatvecArgs a, int upr) {
   return launch_variant<QT, 4, SUMI>(ctx, a);
 }
 
+// Kernel choice.  Measured on GB300 (graph replays, programmatic dependent
+// launch): the register-pipelined kernel above is faster for rows of 2048
+// or more elements (the Llama-7B FFN and TinyLlama shapes), the bulk-copy
+// ring kernel for very many short rows (a 151936 x 896 Q8_0 lm_head: 29.5 us
+// vs 54 us), where per-task overheads dominate the register kernel.
+// MLQ_MATVEC_KERNEL=ldg|tma overrides the choice (A/B timing).
+static int kernel_override() {
+  static const int v = [] {
+    const char *e = std::getenv("MLQ_MATVEC_KERNEL");
+    if (e == nullptr) return 0;
+    if (e[0] == 'l') return 1;
+    if (e[0] == 't') return 2;
+    return 0;
+  }();
+  return v;
+}
+
+static bool prefer_tma(int nb, int rows, int num_sms) {
+  const int o = kernel_override();
+  if (o != 0) return o == 2;
+  return nb <= 32 && rows >= 64 * num_sms;
+}
+
 cudaError_t launch_matvec_m1(const LaunchCtx &ctx, int qtype, const void *wq, const float *wd,
                              int nb, const int8_t *xq, const float *xd, float *y, int32_t *sumi,
                              int r0, int r1) {
   if (r1 <= r0) return cudaSuccess;
+  if (prefer_tma(nb, r1 - r0, ctx.num_sms)) {
+    const cudaError_t e = launch_matvec_m1_tma(ctx, qtype, wq, wd, nb, xq, xd, y, sumi, r0, r1);
+    if (e != cudaErrorNotSupported) return e;
+  }
   MatvecArgs a;
   a.wq = static_cast<const uint8_t *>(wq);
   a.wd = wd;

@@ -51,22 +51,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
+// SM cycle counter: cheap to read, so polling it does not slow the wait
+// loop.  Wait limits are given in nanoseconds and converted at 2 cycles per
+// ns (about the 2.07 GHz maximum SM clock), so a limit is "about" that long.
+__device__ __forceinline__ uint64_t sm_cycles() { return static_cast<uint64_t>(clock64()); }
+__device__ __forceinline__ uint64_t limit_cycles(unsigned long long limit_ns) {
+  return static_cast<uint64_t>(limit_ns) * 2u;
 }
-// Wait for phase `parity` of the mbarrier, giving up after limit_ns
+// Wait for phase `parity` of the mbarrier, giving up after about limit_ns
 // nanoseconds.  limit_ns == 0 gives up at once (test hook: exercises the
 // timeout path with no real hang).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   unsigned long long limit_ns) {
   if (limit_ns == 0) return false;
-  const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > limit_ns) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = sm_cycles(), lim = limit_cycles(limit_ns);
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (sm_cycles() - t0 > lim) return false;
   }
-  return true;
 }
 
 // ---- bulk asynchronous copies (TMA, non-tensor) -----------------------------

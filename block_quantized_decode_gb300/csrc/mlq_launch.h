@@ -34,6 +34,15 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+// prefetch.cu: up to kMaxPrefetchRanges byte ranges to hint into L2.
+constexpr int kMaxPrefetchRanges = 32;
+struct PrefetchList {
+  const void *ptr[kMaxPrefetchRanges];
+  size_t bytes[kMaxPrefetchRanges];
+  int n;
+};
+cudaError_t launch_prefetch_l2(const LaunchCtx &ctx, const PrefetchList &list);
+
 // quantize.cu: m rows of k floats -> Q8_0 (q, d).
 cudaError_t launch_quantize_q8(const LaunchCtx &ctx, const float *x, int8_t *q, float *d, int m,
                                int k);
@@ -43,6 +52,12 @@ cudaError_t launch_quantize_q8(const LaunchCtx &ctx, const float *x, int8_t *q, 
 cudaError_t launch_matvec_m1(const LaunchCtx &ctx, int qtype, const void *wq, const float *wd,
                              int nb, const int8_t *xq, const float *xd, float *y, int32_t *sumi,
                              int r0, int r1);
+
+// matvec_tma.cu: the bulk-copy ring version of launch_matvec_m1; returns
+// cudaErrorNotSupported without launching when the shape does not suit it.
+cudaError_t launch_matvec_m1_tma(const LaunchCtx &ctx, int qtype, const void *wq, const float *wd,
+                                 int nb, const int8_t *xq, const float *xd, float *y,
+                                 int32_t *sumi, int r0, int r1);
 
 // gemm_small_m.cu: M activation rows (1..16) against a Q4_0 matrix.
 cudaError_t launch_gemm_q4_small_m(const LaunchCtx &ctx, const void *wq, const float *wd, int nb,

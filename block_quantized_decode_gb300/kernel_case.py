@@ -1,0 +1,105 @@
+"""Run one libmlq entry point on one shape, for timing and for profilers.
+
+    python -m block_quantized_decode_gb300.kernel_case --op matvec_q4 --rows 4096 --cols 11008
+
+Weights are random device bytes, replicated over enough copies that the
+copies together exceed 3x L2; the call is captured ITERS times in one CUDA
+graph (one copy per launch) and replayed.  Prints the mean time per launch
+from CUDA events and the weight bytes per launch over that time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+
+import torch
+
+from . import binding as B
+
+
+def main():
+    p = argparse.ArgumentParser()
+    p.add_argument("--op", default="matvec_q4",
+                   choices=["matvec_q4", "matvec_q8", "gemm_q4", "quantize"])
+    p.add_argument("--rows", type=int, default=4096)
+    p.add_argument("--cols", type=int, default=11008)
+    p.add_argument("--m", type=int, default=1)
+    p.add_argument("--iters", type=int, default=50)
+    p.add_argument("--reps", type=int, default=5)
+    p.add_argument("--copies", type=int, default=0)
+    p.add_argument("--no-graph", action="store_true")
+    a = p.parse_args()
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(0)
+    B.mlq_init()
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    rows, cols, m = a.rows, a.cols, a.m
+    nb = cols // 32
+    q8 = a.op == "matvec_q8"
+    qbytes = rows * cols if q8 else rows * cols // 2
+    wbytes = qbytes + rows * nb * 4
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    copies = a.copies or max(1, math.ceil(3 * l2 / max(wbytes, 1)))
+    copies = min(copies, a.iters)
+    Ws = []
+    if a.op != "quantize":
+        for _ in range(copies):
+            q = torch.randint(-128, 128, (qbytes,), dtype=torch.int8, device=dev, generator=g)
+            if q8:
+                q.clamp_(-127, 127)
+            d = torch.rand((rows * nb,), device=dev, generator=g) * 9e-3 + 1e-3
+            Ws.append(B.QTensor(q, d, rows, cols, B.MLQ_Q8_0 if q8 else B.MLQ_Q4_0))
+    x = torch.randn((m, cols), device=dev, generator=g)
+    xa = B.QAct(torch.empty((m, cols), dtype=torch.int8, device=dev),
+                torch.empty((m, nb), dtype=torch.float32, device=dev), cols, m)
+    B.mlq_quantize_q8(xa, x, cols)
+    y = torch.empty((m, rows), dtype=torch.float32, device=dev)
+
+    def call(i):
+        if a.op == "quantize":
+            B.mlq_quantize_q8(xa, x, cols)
+        elif a.op == "gemm_q4":
+            B.mlq_gemm_q4_small_m(y, rows, Ws[i % copies], xa, m, 0, rows)
+        elif q8:
+            B.mlq_matvec_q8(y, Ws[i % copies], xa, 0, rows)
+        else:
+            B.mlq_matvec_q4(y, Ws[i % copies], xa, 0, rows)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for i in range(copies):
+            call(i)
+    s.synchronize()
+    graph = None
+    if not a.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            for i in range(a.iters):
+                call(i)
+    times = []
+    for _ in range(a.reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            if graph is not None:
+                graph.replay()
+            else:
+                for i in range(a.iters):
+                    call(i)
+            e1.record(s)
+        s.synchronize()
+        times.append(e0.elapsed_time(e1) / a.iters * 1e3)
+    assert B.mlq_last_device_error(s) == B.MLQ_OK
+    us = min(times)
+    moved = wbytes if a.op != "quantize" else m * cols * (4 + 1) + m * nb * 4
+    print(json.dumps({"op": a.op, "rows": rows, "cols": cols, "m": m, "copies": copies,
+                      "us_per_launch": us, "us_all": times, "bytes_per_launch": moved,
+                      "GBps": moved / (us * 1e-6) / 1e9,
+                      "gops": 2.0 * m * rows * cols / (us * 1e-6) / 1e9 if a.op != "quantize" else 0.0}))
+
+
+if __name__ == "__main__":
+    main()

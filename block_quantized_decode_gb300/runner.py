@@ -81,13 +81,29 @@ class WorkloadRunner:
         return sum(m.y.numel() * 4 for m in self.mats)
 
     # ---- one pass --------------------------------------------------------------
-    def step(self, copy: int = 0, stream=None, before_mat=None, after_mat=None) -> None:
+    def weight_ranges(self, i: int, copy: int = 0):
+        m = self.mats[i]
+        return [(m.q[copy], m.host_q.nbytes), (m.d[copy], m.host_d.nbytes)]
+
+    def step(self, copy: int = 0, stream=None, before_mat=None, after_mat=None,
+             prefetch: str | None = None) -> None:
         """Issue one pass on `stream`: each input is quantised right before
         its first consumer, then each product runs.  before_mat/after_mat
         (optional callables taking the matrix index) let the bench record
-        events around the products."""
+        events around the products.  prefetch: None, "all" (hint every
+        weight of the pass into L2 first) or "next" (hint the next
+        product's weights into L2 before each product)."""
         done = set()
+        if prefetch == "all":
+            ranges = []
+            for i in range(len(self.mats)):
+                ranges += self.weight_ranges(i, copy)
+            B.mlq_prefetch_l2(ranges, stream)
+        elif prefetch == "next" and self.mats:
+            B.mlq_prefetch_l2(self.weight_ranges(0, copy), stream)
         for i, m in enumerate(self.mats):
+            if prefetch == "next" and i + 1 < len(self.mats):
+                B.mlq_prefetch_l2(self.weight_ranges(i + 1, copy), stream)
             if m.src not in done:
                 B.mlq_quantize_q8(self.qbuf[m.src], self.fp32[m.src], self.sources[m.src], stream)
                 done.add(m.src)
@@ -102,6 +118,17 @@ class WorkloadRunner:
                                       m.spec.rows, stream)
             if after_mat is not None:
                 after_mat(i)
+
+    def product(self, i: int, copy: int = 0, stream=None) -> None:
+        """Only the i-th product (its input must already be quantised)."""
+        m = self.mats[i]
+        W = B.QTensor(m.q[copy], m.d[copy], m.spec.rows, m.spec.cols, m.spec.wtype)
+        if self.m == 1:
+            f = B.mlq_matvec_q4 if m.spec.wtype == I.Q4_0 else B.mlq_matvec_q8
+            f(m.y, W, self.qbuf[m.src], 0, m.spec.rows, stream)
+        else:
+            B.mlq_gemm_q4_small_m(m.y, m.spec.rows, W, self.qbuf[m.src], self.m, 0, m.spec.rows,
+                                  stream)
 
     def upload_inputs(self, stream=None) -> None:
         """Host -> device copy of every external input (pinned, async)."""

@@ -59,6 +59,7 @@ extern "C" {
 #define MLQ_QK 32
 #define MLQ_MAX_COLS 65536
 #define MLQ_MAX_M 16
+#define MLQ_MAX_PREFETCH_RANGES 32
 
 typedef enum {
     MLQ_OK = 0,
@@ -137,6 +138,18 @@ mlq_status mlq_gemm_q4_small_m(float *Y, int ldy, const mlq_qtensor *W, const ml
  * block-dot code as the matvec of W->type (Q4_0 or Q8_0); x->m must be 1. */
 mlq_status mlq_block_sumi(int32_t *sumi, const mlq_qtensor *W, const mlq_qact *x,
                           int r0, int r1, void *stream);
+
+/* Hint n byte ranges (device pointers ptrs[i], lengths bytes[i]; the two
+ * arrays live in host memory and are read during the call) into L2, e.g.
+ * the weights of the next products of a decode step, so that their HBM
+ * reads overlap earlier work.  Queues one short kernel that issues bulk L2
+ * prefetches and exits; the data keeps arriving after it finishes.  Pure
+ * hint: it changes no memory, never waits for earlier work on the stream
+ * and never makes later work read stale data (L2 is the device's point of
+ * coherence).  Unaligned range ends are trimmed to 16-byte boundaries.
+ * 0 <= n <= MLQ_MAX_PREFETCH_RANGES.  No counterpart on the pages: an
+ * addition for GPU decode chains. */
+mlq_status mlq_prefetch_l2(const void *const *ptrs, const size_t *bytes, int n, void *stream);
 
 /* Synchronise `stream`, then report and clear the library's device status
  * word: MLQ_E_TIMEOUT if any kernel since the last call gave up a bounded

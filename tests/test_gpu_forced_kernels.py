@@ -1,0 +1,26 @@
+"""The M = 1 products have two kernels (register-pipelined loads, and a
+bulk-copy ring); the dispatcher picks one per shape.  Re-run the per-block
+sum and product parity tests with each kernel forced, in child processes
+(the choice is read once per process from MLQ_MATVEC_KERNEL)."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.mark.skipif(os.environ.get("MLQ_MATVEC_KERNEL") is not None,
+                    reason="already inside a forced-kernel run")
+@pytest.mark.parametrize("kernel", ["ldg", "tma"])
+def test_parity_with_forced_kernel(kernel):
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    env = dict(os.environ, MLQ_MATVEC_KERNEL=kernel, PYTHONPATH=ROOT)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        "tests/test_gpu_parity.py", "-k", "sumi or matvec or timeout"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=1200)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
