@@ -53,6 +53,11 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--path", choices=["auto", "fused", "chain", "calls"], default="auto",
+                   help="fused: one mlq_matvec_fused launch per phase; chain: one "
+                        "mlq_decode_chain launch per step; calls: one C-ABI call per quantize "
+                        "and product; auto: fused for M = 1 steps under 64 MB of weights "
+                        "(latency-bound, fewer launches win), else calls")
     p.add_argument("--prefetch", choices=["none", "all", "next"], default="none",
                    help="L2 prefetch of weights through mlq_prefetch_l2: all (whole pass "
                         "first) or next (one product ahead); measured slower in-chain, so off")
@@ -158,17 +163,17 @@ class ClockSampler:
                 "reasons": sorted(set().union(*[x[3] for x in use]))}
 
 
-def ncu_traffic(workload: str, bytes_per_launch: float):
+def ncu_traffic(profile: str, sources, bytes_per_launch: float):
     """DRAM bytes per launch of the dominant kernel: the DRAM/algorithmic
-    ratio of the committed ncu summary times the algorithmic bytes per
-    launch, if the summary was taken on the current kernel source; else
-    None."""
-    path = os.path.join(ROOT, "profiles", f"matvec_q4_{workload}.md")
+    ratio of the committed ncu summary profiles/<profile>.md times the
+    algorithmic bytes per launch, if the summary was taken on the current
+    kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"{profile}.md")
     csrc = os.path.join(ROOT, "block_quantized_decode_gb300", "csrc")
     try:
         text = open(path).read()
         h = hashlib.sha256()
-        for f in ("matvec.cu", "mlq_device.cuh"):
+        for f in sources:
             h.update(open(os.path.join(csrc, f), "rb").read())
         sha = h.hexdigest()[:16]
     except OSError:
@@ -304,6 +309,16 @@ def run_ours(args, wl, world, rank, local, pg):
     pf = args.prefetch
     if pf == "none":
         pf = None
+    path = args.path if args.path != "auto" else (
+        "fused" if r.m == 1 and wbytes < 64 * 2 ** 20 else "calls")
+
+    def one_pass(c):
+        if path == "chain":
+            r.step_chain(copy=c)
+        elif path == "fused":
+            r.step_fused(copy=c)
+        else:
+            r.step(copy=c, prefetch=pf)
     assert r.weight_bytes() == wbytes
     stream = torch.cuda.Stream(device=dev)
 
@@ -313,21 +328,21 @@ def run_ours(args, wl, world, rank, local, pg):
         "matvec_m1_kernel<Q8_0>" if r.m == 1 else "gemm_q4_small_m")
     with torch.cuda.stream(stream):
         for c in range(copies):  # eager warm-up of every copy (kernel attributes, caches)
-            r.step(copy=c, prefetch=pf)
+            one_pass(c)
     stream.synchronize()
     graphs = []
     if not args.no_graph:
         for c in range(copies):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                r.step(copy=c, prefetch=pf)
+                one_pass(c)
             graphs.append(g)
 
     def do_step(i):
         if graphs:
             graphs[i % copies].replay()
         else:
-            r.step(copy=i % copies, prefetch=pf)
+            one_pass(i % copies)
 
     # ---- headline timed region
     clocks = ClockSampler(local)
@@ -371,7 +386,35 @@ def run_ours(args, wl, world, rank, local, pg):
     peaks, peak_src = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     roofline = None
-    if graphs:
+    if graphs and path == "chain":
+        launches = 2 * copies
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(launches):
+                r.step_chain(copy=j % copies)
+        with torch.cuda.stream(stream):
+            g.replay()
+        stream.synchronize()
+        best = None
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+            stream.synchronize()
+            t = a.elapsed_time(b) / 1e3 / launches
+            best = t if best is None else min(best, t)
+        del g
+        ach = wbytes / best / 1e9
+        qt = "Q4_0" if r.mats[0].spec.wtype == I.Q4_0 else "Q8_0"
+        roofline = {"kernel": f"decode_chain_kernel<{qt}>", "bound": "hbm", "achieved": ach,
+                    "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_source": peak_src,
+                    "traffic": ncu_traffic(f"chain_{wl.name}", ("chain.cu", "mlq_device.cuh"), wbytes),
+                    "bytes_per_launch": wbytes, "us_per_launch": best * 1e6,
+                    "method": f"{launches} back-to-back chain launches (one per step) in one CUDA "
+                              "graph, best of 3 replays, CUDA events on the launching stream"}
+    elif graphs:
         shapes = {}
         for i, m in enumerate(r.mats):
             shapes.setdefault((m.spec.wtype, m.spec.rows, m.spec.cols), []).append(i)
@@ -407,7 +450,8 @@ def run_ours(args, wl, world, rank, local, pg):
         ach = tot_bytes / tot_s / 1e9
         roofline = {"kernel": dominant, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
                     "frac": ach / hbm, "peak_source": peak_src,
-                    "traffic": ncu_traffic(wl.name, tot_bytes / sum(p["per_step"] for p in per_shape)),
+                    "traffic": ncu_traffic(f"matvec_q4_{wl.name}", ("matvec.cu", "mlq_device.cuh"),
+                                           tot_bytes / sum(p["per_step"] for p in per_shape)),
                     "bytes_per_launch": tot_bytes / sum(p["per_step"] for p in per_shape),
                     "us_per_launch": tot_s / sum(p["per_step"] for p in per_shape) * 1e6,
                     "method": f"{launches} back-to-back launches per shape in one CUDA graph, "
@@ -454,10 +498,11 @@ def run_ours(args, wl, world, rank, local, pg):
                        "weight_bytes_per_step": wbytes,
                        "l2": f"inputs larger than L2: {copies} rotating weight copies "
                              f"({copies * wbytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
-                       "graphs": bool(graphs), "l2_prefetch": pf or "none", "parallelism": f"replicas x{world} (independent decode streams)"},
+                       "graphs": bool(graphs), "path": path, "l2_prefetch": pf or "none", "parallelism": f"replicas x{world} (independent decode streams)"},
             "gops": gops, "hbm_frac": value / world / hbm,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": (r.kernels_per_step + {None: 0, "all": 1, "next": len(r.mats)}[pf]) * steps,
+            "gpu_launches": (1 if path == "chain" else len(r.chain_phases()) if path == "fused" else
+                             r.kernels_per_step + {None: 0, "all": 1, "next": len(r.mats)}[pf]) * steps,
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)

@@ -26,7 +26,11 @@ EXPORTS = (
     "mlq_init", "mlq_quantize_q8", "mlq_matvec_q4", "mlq_matvec_q8",
     "mlq_gemm_q4_small_m", "mlq_block_sumi", "mlq_last_device_error",
     "mlq_debug_set_wait_limit_ns", "mlq_status_str", "mlq_prefetch_l2",
+    "mlq_chain_workspace_bytes", "mlq_decode_chain", "mlq_matvec_fused",
 )
+MLQ_FUSED_MAX_PRODUCTS = 8
+MLQ_CHAIN_MAX_PRODUCTS = 32
+MLQ_CHAIN_MAX_PHASES = 24
 
 
 class MlqError(RuntimeError):
@@ -43,6 +47,15 @@ class _QTensor(ctypes.Structure):
 class _QAct(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("d", ctypes.c_void_p), ("n", ctypes.c_int),
                 ("m", ctypes.c_int)]
+
+
+class _ChainProduct(ctypes.Structure):
+    _fields_ = [("W", _QTensor), ("y", ctypes.c_void_p)]
+
+
+class _ChainPhase(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("n", ctypes.c_int), ("first", ctypes.c_int),
+                ("count", ctypes.c_int), ("xq_out", ctypes.c_void_p), ("xd_out", ctypes.c_void_p)]
 
 
 _lib = None
@@ -67,10 +80,15 @@ def lib() -> ctypes.CDLL:
         L.mlq_last_device_error.argtypes = [P]
         L.mlq_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
         L.mlq_prefetch_l2.argtypes = [P, P, I, P]
+        L.mlq_chain_workspace_bytes.argtypes = [I]
+        L.mlq_chain_workspace_bytes.restype = ctypes.c_size_t
+        L.mlq_decode_chain.argtypes = [ctypes.POINTER(_ChainPhase), I, ctypes.POINTER(_ChainProduct),
+                                       I, P, ctypes.c_size_t, P]
+        L.mlq_matvec_fused.argtypes = [P, I, ctypes.POINTER(_ChainProduct), I, P, P, P]
         L.mlq_status_str.argtypes = [S]
         L.mlq_status_str.restype = ctypes.c_char_p
         for name in EXPORTS:
-            if name != "mlq_status_str":
+            if name not in ("mlq_status_str", "mlq_chain_workspace_bytes"):
                 getattr(L, name).restype = S
         _lib = L
     return _lib
@@ -178,6 +196,70 @@ def mlq_prefetch_l2(ranges, stream=None) -> None:
     ptrs = (ctypes.c_void_p * max(n, 1))(*[_addr(p) for p, _ in ranges])
     sizes = (ctypes.c_size_t * max(n, 1))(*[int(b) for _, b in ranges])
     _check(lib().mlq_prefetch_l2(ptrs, sizes, n, _stream(stream)), "mlq_prefetch_l2")
+
+
+@dataclass
+class ChainProduct:
+    """One product of a chain: y = W x (x = its phase's quantised input)."""
+    W: QTensor
+    y: object
+
+
+@dataclass
+class ChainPhase:
+    """Quantise x (n float32) and run products[first:first+count]."""
+    x: object
+    n: int
+    first: int
+    count: int
+    xq_out: object = None
+    xd_out: object = None
+
+
+def mlq_chain_workspace_bytes(nphases: int) -> int:
+    return lib().mlq_chain_workspace_bytes(nphases)
+
+
+class ChainCall:
+    """Marshalled arguments of one mlq_decode_chain call (built once, so
+    that repeated calls cost one ctypes call each)."""
+
+    def __init__(self, phases, products, workspace, workspace_bytes=None):
+        self.ph = (_ChainPhase * len(phases))(*[
+            _ChainPhase(_addr(p.x), p.n, p.first, p.count, _addr(p.xq_out), _addr(p.xd_out))
+            for p in phases])
+        self.pr = (_ChainProduct * len(products))(*[_ChainProduct(p.W.c(), _addr(p.y)) for p in products])
+        self.nph, self.npr = len(phases), len(products)
+        self.ws = _addr(workspace)
+        self.wsb = (workspace.numel() * workspace.element_size() if workspace_bytes is None
+                    else workspace_bytes)
+
+    def __call__(self, stream=None) -> None:
+        _check(lib().mlq_decode_chain(self.ph, self.nph, self.pr, self.npr, self.ws, self.wsb,
+                                      _stream(stream)), "mlq_decode_chain")
+
+
+class FusedCall:
+    """Marshalled arguments of one mlq_matvec_fused call."""
+
+    def __init__(self, x, n, products, xq_out=None, xd_out=None):
+        self.x, self.n = _addr(x), n
+        self.pr = (_ChainProduct * len(products))(*[_ChainProduct(p.W.c(), _addr(p.y)) for p in products])
+        self.npr = len(products)
+        self.xq, self.xd = _addr(xq_out), _addr(xd_out)
+
+    def __call__(self, stream=None) -> None:
+        _check(lib().mlq_matvec_fused(self.x, self.n, self.pr, self.npr, self.xq, self.xd,
+                                      _stream(stream)), "mlq_matvec_fused")
+
+
+def mlq_matvec_fused(x, n, products, xq_out=None, xd_out=None, stream=None) -> None:
+    """Quantise x (n float32) and run every product (ChainProduct) of width n."""
+    FusedCall(x, n, products, xq_out, xd_out)(stream)
+
+
+def mlq_decode_chain(phases, products, workspace, workspace_bytes=None, stream=None) -> None:
+    ChainCall(phases, products, workspace, workspace_bytes)(stream)
 
 
 def mlq_last_device_error(stream=None) -> int:

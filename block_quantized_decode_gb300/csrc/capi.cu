@@ -33,6 +33,7 @@ DevInfo g_dev[kMaxDevices];
 std::mutex g_init_mu;
 std::atomic<unsigned long long> g_wait_ns{1000000000ull};
 std::atomic<int> g_pdl{-1};
+std::atomic<int> g_early{-1};
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -42,6 +43,16 @@ bool pdl_enabled() {
     const char *e = std::getenv("MLQ_PDL");
     v = (e != nullptr && std::strcmp(e, "0") == 0) ? 0 : 1;
     g_pdl.store(v, std::memory_order_relaxed);
+  }
+  return v == 1;
+}
+
+bool early_enabled() {
+  int v = g_early.load(std::memory_order_relaxed);
+  if (v < 0) {
+    const char *e = std::getenv("MLQ_STATIC_WEIGHTS");
+    v = (e != nullptr && std::strcmp(e, "1") == 0) ? 1 : 0;
+    g_early.store(v, std::memory_order_relaxed);
   }
   return v == 1;
 }
@@ -99,6 +110,7 @@ mlq_status make_ctx(mlq::LaunchCtx *ctx, void *stream) {
   ctx->num_sms = d->num_sms;
   ctx->status = d->status;
   ctx->wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  ctx->early_weights = ctx->pdl && early_enabled();
   return MLQ_OK;
 }
 
@@ -136,6 +148,50 @@ mlq_status matvec_common(float *y, int32_t *sumi, const mlq_qtensor *W, const ml
   if (s != MLQ_OK) return s;
   return from_cuda(mlq::launch_matvec_m1(ctx, W->type, W->q, W->d, W->cols / MLQ_QK, x->q, x->d,
                                          y, sumi, r0, r1));
+}
+
+// Host-side checks and marshalling of a chain (everything but the workspace).
+mlq_status build_chain_args(const mlq_chain_phase *phases, int nphases,
+                            const mlq_chain_product *products, int nproducts,
+                            mlq::ChainArgs *a) {
+  if (phases == nullptr || products == nullptr) return MLQ_E_NULL;
+  if (nphases < 1 || nphases > MLQ_CHAIN_MAX_PHASES) return MLQ_E_SHAPE;
+  if (nproducts < 1 || nproducts > MLQ_CHAIN_MAX_PRODUCTS) return MLQ_E_SHAPE;
+  const uint8_t type = products[0].W.type;
+  for (int j = 0; j < nproducts; ++j) {
+    const mlq_chain_product &p = products[j];
+    if (p.W.rows > 0 && (p.W.q == nullptr || p.W.d == nullptr || p.y == nullptr)) return MLQ_E_NULL;
+    if (p.W.type != MLQ_Q4_0 && p.W.type != MLQ_Q8_0) return MLQ_E_TYPE;
+    if (p.W.type != type) return MLQ_E_TYPE;
+    if (!cols_ok(p.W.cols) || p.W.cols % 128 != 0 || p.W.rows < 0) return MLQ_E_SHAPE;
+    if (!aligned(p.W.q, 16) || !aligned(p.W.d, 16) || !aligned(p.y, 4)) return MLQ_E_ALIGN;
+    a->prod[j].wq = static_cast<const uint8_t *>(p.W.q);
+    a->prod[j].wd = p.W.d;
+    a->prod[j].y = p.y;
+    a->prod[j].rows = p.W.rows;
+  }
+  int kmax = 0;
+  for (int i = 0; i < nphases; ++i) {
+    const mlq_chain_phase &ph = phases[i];
+    if (ph.x == nullptr) return MLQ_E_NULL;
+    if ((ph.xq_out == nullptr) != (ph.xd_out == nullptr)) return MLQ_E_NULL;
+    if (ph.count < 1 || ph.first < 0 || ph.first > nproducts - ph.count) return MLQ_E_SHAPE;
+    if (!cols_ok(ph.n) || ph.n % 128 != 0) return MLQ_E_SHAPE;
+    for (int j = ph.first; j < ph.first + ph.count; ++j)
+      if (products[j].W.cols != ph.n) return MLQ_E_SHAPE;
+    if (!aligned(ph.x, 16) || !aligned(ph.xq_out, 16) || !aligned(ph.xd_out, 16))
+      return MLQ_E_ALIGN;
+    a->phase[i].x = ph.x;
+    a->phase[i].xq_out = ph.xq_out;
+    a->phase[i].xd_out = ph.xd_out;
+    a->phase[i].nb = ph.n / MLQ_QK;
+    a->phase[i].first = ph.first;
+    a->phase[i].count = ph.count;
+    if (ph.n > kmax) kmax = ph.n;
+  }
+  a->nphases = nphases;
+  a->kmax = kmax;
+  return MLQ_OK;
 }
 
 }  // namespace
@@ -188,6 +244,59 @@ mlq_status mlq_gemm_q4_small_m(float *Y, int ldy, const mlq_qtensor *W, const ml
   if (s != MLQ_OK) return s;
   return from_cuda(mlq::launch_gemm_q4_small_m(ctx, W->q, W->d, W->cols / MLQ_QK, X->q, X->d, M,
                                                Y, ldy, r0, r1));
+}
+
+mlq_status mlq_matvec_fused(const float *x, int n, const mlq_chain_product *products,
+                            int nproducts, int8_t *xq_out, float *xd_out, void *stream) {
+  if (x == nullptr || products == nullptr) return MLQ_E_NULL;
+  if ((xq_out == nullptr) != (xd_out == nullptr)) return MLQ_E_NULL;
+  if (nproducts < 1 || nproducts > MLQ_FUSED_MAX_PRODUCTS || !cols_ok(n)) return MLQ_E_SHAPE;
+  if (!aligned(x, 16) || !aligned(xq_out, 16) || !aligned(xd_out, 16)) return MLQ_E_ALIGN;
+  mlq::FusedArgs a;
+  const uint8_t type = products[0].W.type;
+  for (int j = 0; j < nproducts; ++j) {
+    const mlq_chain_product &p = products[j];
+    if (p.W.rows > 0 && (p.W.q == nullptr || p.W.d == nullptr || p.y == nullptr)) return MLQ_E_NULL;
+    if (p.W.type != MLQ_Q4_0 && p.W.type != MLQ_Q8_0) return MLQ_E_TYPE;
+    if (p.W.type != type) return MLQ_E_TYPE;
+    if (p.W.cols != n || p.W.rows < 0) return MLQ_E_SHAPE;
+    if (!aligned(p.W.q, 16) || !aligned(p.W.d, 16) || !aligned(p.y, 4)) return MLQ_E_ALIGN;
+    a.prod[j].wq = static_cast<const uint8_t *>(p.W.q);
+    a.prod[j].wd = p.W.d;
+    a.prod[j].y = p.y;
+    a.prod[j].rows = p.W.rows;
+  }
+  a.nproducts = nproducts;
+  a.x = x;
+  a.nb = n / MLQ_QK;
+  a.xq_out = xq_out;
+  a.xd_out = xd_out;
+  a.total_rows = 0;
+  a.nchunks = 1;
+  mlq::LaunchCtx ctx;
+  mlq_status s = make_ctx(&ctx, stream);
+  if (s != MLQ_OK) return s;
+  return from_cuda(mlq::launch_matvec_fused(ctx, type, a));
+}
+
+size_t mlq_chain_workspace_bytes(int nphases) {
+  return nphases < 0 ? 0 : static_cast<size_t>(nphases + 1) * sizeof(unsigned);
+}
+
+mlq_status mlq_decode_chain(const mlq_chain_phase *phases, int nphases,
+                            const mlq_chain_product *products, int nproducts, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+  mlq::ChainArgs a;
+  mlq_status s = build_chain_args(phases, nphases, products, nproducts, &a);
+  if (s != MLQ_OK) return s;
+  if (workspace == nullptr) return MLQ_E_NULL;
+  if (!aligned(workspace, 4)) return MLQ_E_ALIGN;
+  if (workspace_bytes < mlq_chain_workspace_bytes(nphases)) return MLQ_E_SHAPE;
+  a.counters = static_cast<unsigned *>(workspace);
+  mlq::LaunchCtx ctx;
+  s = make_ctx(&ctx, stream);
+  if (s != MLQ_OK) return s;
+  return from_cuda(mlq::launch_decode_chain(ctx, products[0].W.type, a));
 }
 
 mlq_status mlq_prefetch_l2(const void *const *ptrs, const size_t *bytes, int n, void *stream) {

@@ -134,6 +134,19 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// ---- Q8_0 quantisation of one element ---------------------------------------
+// Design Spec Sec. 5 rounding: q = trunc(x*id + copysign(0.5, x)) with the
+// multiply and the add each rounded to float32 (__fmul_rn / __fadd_rn are
+// never contracted into an FMA), clamped to [-127, 127]; NaN (0 * inf when
+// 127/amax overflows) stores 0.  Shared by every kernel that quantises, so
+// their bytes are identical by construction.
+__device__ __forceinline__ int quant_one(float x, float id) {
+  float v = __fmul_rn(x, id);
+  v = __fadd_rn(v, copysignf(0.5f, x));
+  v = truncf(v);
+  return v >= 127.0f ? 127 : (v <= -127.0f ? -127 : (v == v ? static_cast<int>(v) : 0));
+}
+
 // Record a device-side status (first writer wins).
 __device__ __forceinline__ void set_status(int *status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);

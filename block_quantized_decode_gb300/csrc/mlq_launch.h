@@ -14,6 +14,8 @@ struct LaunchCtx {
   int num_sms;                  // SMs of the current device
   int *status;                  // device status word (MLQ_E_TIMEOUT on a bounded-wait give-up)
   unsigned long long wait_ns;   // limit of every device-side wait
+  bool early_weights;           // weights are not written by earlier queued work:
+                                // their first loads may precede the dependency wait
 };
 
 // Launch `kern` with cudaLaunchKernelEx, optionally with programmatic
@@ -58,6 +60,56 @@ cudaError_t launch_matvec_m1(const LaunchCtx &ctx, int qtype, const void *wq, co
 cudaError_t launch_matvec_m1_tma(const LaunchCtx &ctx, int qtype, const void *wq, const float *wd,
                                  int nb, const int8_t *xq, const float *xd, float *y,
                                  int32_t *sumi, int r0, int r1);
+
+// chain.cu: a decode step of dependent products in one persistent launch.
+constexpr int kChainMaxProducts = 32;
+constexpr int kChainMaxPhases = 24;
+struct ChainProductDev {
+  const uint8_t *wq;
+  const float *wd;
+  float *y;
+  int rows;
+};
+struct ChainPhaseDev {
+  const float *x;
+  int8_t *xq_out;
+  float *xd_out;
+  int nb;
+  int first, count;
+};
+struct ChainArgs {
+  ChainProductDev prod[kChainMaxProducts];
+  ChainPhaseDev phase[kChainMaxPhases];
+  int nphases;
+  int kmax;             // largest phase width
+  unsigned *counters;   // nphases + 1 words of caller workspace, zero on entry and exit
+  int *status;
+  unsigned long long wait_ns;
+  int ns, stage_bytes, xbuf_bytes;  // ring geometry (set by the launcher)
+};
+cudaError_t launch_decode_chain(const LaunchCtx &ctx, int qtype, const ChainArgs &a);
+
+// fused.cu: quantise x and run up to kFusedMaxProducts products of its width.
+constexpr int kFusedMaxProducts = 8;
+struct FusedProduct {
+  const uint8_t *wq;
+  const float *wd;
+  float *y;
+  int rows;
+};
+struct FusedArgs {
+  FusedProduct prod[kFusedMaxProducts];
+  int nproducts;
+  const float *x;
+  int nb;
+  int8_t *xq_out;   // optional copy of the quantised x (written by CTA 0)
+  float *xd_out;
+  int total_rows;   // set by the launcher
+  int nchunks;      // set by the launcher
+  int early;        // set by the launcher: first weight loads before the dependency wait
+  int prefetch;     // set by the launcher: hint the CTA's weights into L2 first
+};
+cudaError_t launch_matvec_fused(const LaunchCtx &ctx, int qtype, const FusedArgs &a);
 
 // gemm_small_m.cu: M activation rows (1..16) against a Q4_0 matrix.
 cudaError_t launch_gemm_q4_small_m(const LaunchCtx &ctx, const void *wq, const float *wd, int nb,

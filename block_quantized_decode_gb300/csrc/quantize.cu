@@ -18,20 +18,15 @@
 
 namespace mlq {
 
-__device__ __forceinline__ int quant_one(float x, float id) {
-  float v = __fmul_rn(x, id);
-  v = __fadd_rn(v, copysignf(0.5f, x));
-  v = truncf(v);
-  return v >= 127.0f ? 127 : (v <= -127.0f ? -127 : (v == v ? static_cast<int>(v) : 0));
-}
-
 __global__ void __launch_bounds__(256) quantize_q8_kernel(const float *__restrict__ x,
                                                           int8_t *__restrict__ q,
                                                           float *__restrict__ d,
                                                           long long nblocks) {
-  // x may be the output of the previous kernel on the stream.
-  griddep_wait();
+  // Let the next kernel start its prologue now (it still waits for this
+  // grid before reading our output); then wait for x, which may be the
+  // output of the previous kernel on the stream.
   griddep_launch_dependents();
+  griddep_wait();
   const int lane = threadIdx.x & 31;
   const int sub = lane >> 3;   // which of the warp's four blocks
   const int part = lane & 7;   // which four elements of the block

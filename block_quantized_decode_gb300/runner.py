@@ -66,6 +66,58 @@ class WorkloadRunner:
             d = torch.empty((self.m, k // I.QK), dtype=torch.float32, device=self.dev)
             self.qbuf[src] = B.QAct(q, d, k, self.m)
         self.kernels_per_step = len(self.sources) + len(self.mats)
+        self._chain_calls = {}
+        self.chain_ws = None
+
+    # ---- the whole pass as one chain launch ------------------------------------
+    def chain_phases(self):
+        """Runs of consecutive products that read the same input."""
+        phases = []
+        for i, m in enumerate(self.mats):
+            if phases and phases[-1][0] == m.src:
+                phases[-1][2] += 1
+            else:
+                phases.append([m.src, i, 1])
+        return phases
+
+    def chain_call(self, copy: int = 0):
+        if copy not in self._chain_calls:
+            if self.m != 1:
+                raise ValueError("decode chains are M = 1")
+            phases = self.chain_phases()
+            if self.chain_ws is None:
+                nbytes = B.mlq_chain_workspace_bytes(len(phases))
+                self.chain_ws = torch.zeros((nbytes + 3) // 4, dtype=torch.int32, device=self.dev)
+            cp = [B.ChainPhase(self.fp32[src], self.sources[src], first, count,
+                               self.qbuf[src].q, self.qbuf[src].d) for src, first, count in phases]
+            pr = [B.ChainProduct(B.QTensor(m.q[copy], m.d[copy], m.spec.rows, m.spec.cols,
+                                           m.spec.wtype), m.y) for m in self.mats]
+            self._chain_calls[copy] = B.ChainCall(cp, pr, self.chain_ws)
+        return self._chain_calls[copy]
+
+    def fused_calls(self, copy: int = 0):
+        key = ("fused", copy)
+        if key not in self._chain_calls:
+            if self.m != 1:
+                raise ValueError("fused phases are M = 1")
+            calls = []
+            for src, first, count in self.chain_phases():
+                pr = [B.ChainProduct(B.QTensor(m.q[copy], m.d[copy], m.spec.rows, m.spec.cols,
+                                               m.spec.wtype), m.y)
+                      for m in self.mats[first:first + count]]
+                calls.append(B.FusedCall(self.fp32[src], self.sources[src], pr,
+                                         self.qbuf[src].q, self.qbuf[src].d))
+            self._chain_calls[key] = calls
+        return self._chain_calls[key]
+
+    def step_fused(self, copy: int = 0, stream=None) -> None:
+        """One pass as one mlq_matvec_fused launch per phase."""
+        for c in self.fused_calls(copy):
+            c(stream)
+
+    def step_chain(self, copy: int = 0, stream=None) -> None:
+        """One pass as a single mlq_decode_chain launch."""
+        self.chain_call(copy)(stream)
 
     # ---- sizes ---------------------------------------------------------------
     def weight_bytes(self) -> int:

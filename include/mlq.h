@@ -46,6 +46,12 @@
  * weight bytes into L2 (always safe: L2 is the point of coherence), but it
  * reads and writes nothing through the caches before that previous kernel
  * has completed.  Set the environment variable MLQ_PDL=0 to launch plainly.
+ * MLQ_STATIC_WEIGHTS=1 additionally lets the products issue their first
+ * weight loads before that previous kernel has finished; set it only when
+ * no work queued earlier on the stream writes the weight arrays (true for
+ * inference weights loaded once).  MLQ_FUSED_L2_PREFETCH=1 makes
+ * mlq_matvec_fused hint its whole weight range into L2 first.  Both are off
+ * by default (measured gains were small or negative on GB300).
  */
 #ifndef MLQ_H
 #define MLQ_H
@@ -60,6 +66,9 @@ extern "C" {
 #define MLQ_MAX_COLS 65536
 #define MLQ_MAX_M 16
 #define MLQ_MAX_PREFETCH_RANGES 32
+#define MLQ_FUSED_MAX_PRODUCTS 8
+#define MLQ_CHAIN_MAX_PRODUCTS 32
+#define MLQ_CHAIN_MAX_PHASES 24
 
 typedef enum {
     MLQ_OK = 0,
@@ -138,6 +147,68 @@ mlq_status mlq_gemm_q4_small_m(float *Y, int ldy, const mlq_qtensor *W, const ml
  * block-dot code as the matvec of W->type (Q4_0 or Q8_0); x->m must be 1. */
 mlq_status mlq_block_sumi(int32_t *sumi, const mlq_qtensor *W, const mlq_qact *x,
                           int r0, int r1, void *stream);
+
+/* ---- decode chains: a whole decode step in one launch ------------------ */
+
+/* One product of a chain: y[r] = sum_b (float)sumi(r, b) * W.d[r*nb+b] * dx_b
+ * for every r < W.rows (Design Spec Sec. 5 matvec), x being its phase's
+ * quantised input.  y is a device pointer.  A product with W.rows == 0 may
+ * have NULL pointers (nothing is read or written). */
+typedef struct {
+    mlq_qtensor W;
+    float *y;
+} mlq_chain_product;
+
+/* One phase: quantise x (n float32, device) to Q8_0 exactly as
+ * mlq_quantize_q8 does, then run products[first .. first+count), all of
+ * width n.  x may be the output y of a product of an EARLIER phase (the
+ * chain runs phase by phase); it must not overlap an output of its own
+ * phase.  xq_out / xd_out (both NULL, or n bytes and n/32 floats, 16-byte
+ * aligned) receive the phase's quantised input, for inspection. */
+typedef struct {
+    const float *x;
+    int n;
+    int first, count;
+    int8_t *xq_out;
+    float *xd_out;
+} mlq_chain_phase;
+
+/* One decode phase in one launch (Design Spec Sec. 6 "Forward pass": a
+ * quantised activation feeds one or more products, e.g. Wq|Wk|Wv):
+ * quantise x (n float32, device, 16-byte aligned) to Q8_0 exactly as
+ * mlq_quantize_q8 does, then for each of the nproducts products
+ * (1..MLQ_FUSED_MAX_PRODUCTS, same type, W.cols == n, n a multiple of 32
+ * and at most MLQ_MAX_COLS) write y[r] for every r < W.rows, within the
+ * tolerance of mlq_matvec_q4/_q8.  xq_out / xd_out (both NULL, or n bytes
+ * and n/32 floats, 16-byte aligned) receive the quantised x.  The outputs
+ * must not overlap x.  Built for chains of such calls under programmatic
+ * dependent launch: each call hints its own weights into L2 before waiting
+ * for the previous kernel, so consecutive phases overlap their HBM reads.
+ * No counterpart on the pages: a GPU fusion of quantize_q8 and matvec. */
+mlq_status mlq_matvec_fused(const float *x, int n, const mlq_chain_product *products,
+                            int nproducts, int8_t *xq_out, float *xd_out, void *stream);
+
+/* Bytes of workspace mlq_decode_chain needs for `nphases` phases. */
+size_t mlq_chain_workspace_bytes(int nphases);
+
+/* Run a chain of phases (Design Spec Sec. 6 "Forward pass": per layer, a
+ * norm/activation output is quantised and multiplied by one or more
+ * matrices, whose output feeds the next quantisation) in ONE cooperative
+ * launch: one CTA per SM streams the weights of every phase back to back
+ * while the phases run in order, separated by grid-wide barriers.
+ * Requirements: 1 <= nphases <= MLQ_CHAIN_MAX_PHASES, 1 <= nproducts <=
+ * MLQ_CHAIN_MAX_PRODUCTS; every product of the same type (Q4_0 or Q8_0);
+ * cols a multiple of 128 and at most MLQ_MAX_COLS; W.q, W.d, x 16-byte
+ * aligned.  Results: identical quantisation; products within the same
+ * tolerance as mlq_matvec_q4/_q8.
+ * workspace: device memory of at least mlq_chain_workspace_bytes(nphases)
+ * bytes, 4-byte aligned, owned by the caller, ZERO-FILLED before its first
+ * use; every call leaves it zero again (also after MLQ_E_TIMEOUT).  Calls
+ * that share a workspace must not overlap on the GPU.  No counterpart on
+ * the pages: a GPU scheduling of their decode step. */
+mlq_status mlq_decode_chain(const mlq_chain_phase *phases, int nphases,
+                            const mlq_chain_product *products, int nproducts,
+                            void *workspace, size_t workspace_bytes, void *stream);
 
 /* Hint n byte ranges (device pointers ptrs[i], lengths bytes[i]; the two
  * arrays live in host memory and are read during the call) into L2, e.g.

@@ -152,3 +152,51 @@ def test_arch_guard_with_faked_capability():
 
 def test_debug_wait_limit_hook(M):
     M.mlq_debug_set_wait_limit_ns(10 ** 9)
+
+
+def test_validation_chain(M):
+    from block_quantized_decode_gb300.binding import _ChainPhase, _ChainProduct
+    P = _ChainPhase
+    R = _ChainProduct
+
+    def run(phases, prods, ws=7 * A, wsb=64):
+        pa = (P * max(1, len(phases)))(*phases)
+        ra = (R * max(1, len(prods)))(*prods)
+        return call(M, "mlq_decode_chain", pa, len(phases), ra, len(prods), ws, wsb, None)
+
+    good_prod = R(qt(cols=256), 5 * A)
+    good_phase = P(6 * A, 256, 0, 1, None, None)
+    assert M.mlq_chain_workspace_bytes(3) == 16
+    assert run([], [good_prod]) == M.MLQ_E_SHAPE
+    assert run([good_phase], []) == M.MLQ_E_SHAPE
+    assert run([good_phase], [R(qt(cols=96), 5 * A)]) == M.MLQ_E_SHAPE      # not a multiple of 128
+    assert run([good_phase], [R(qt(cols=256), None)]) == M.MLQ_E_NULL
+    assert run([good_phase, P(6 * A, 256, 0, 2, None, None)], [good_prod]) == M.MLQ_E_SHAPE
+    assert run([P(6 * A, 128, 0, 1, None, None)], [good_prod]) == M.MLQ_E_SHAPE  # n != cols
+    assert run([good_phase], [good_prod, R(qt(cols=256, t=0), 5 * A)]) == M.MLQ_E_TYPE
+    assert run([P(6 * A + 4, 256, 0, 1, None, None)], [good_prod]) == M.MLQ_E_ALIGN
+    assert run([P(6 * A, 256, 0, 1, 8 * A, None)], [good_prod]) == M.MLQ_E_NULL
+    assert run([good_phase], [good_prod], ws=None) == M.MLQ_E_NULL
+    assert run([good_phase], [good_prod], ws=7 * A + 2) == M.MLQ_E_ALIGN
+    assert run([good_phase], [good_prod], wsb=4) == M.MLQ_E_SHAPE
+    assert run([good_phase] * 25, [good_prod]) == M.MLQ_E_SHAPE
+
+
+def test_validation_fused(M):
+    from block_quantized_decode_gb300.binding import _ChainProduct
+    R = _ChainProduct
+
+    def run(prods, x=6 * A, n=256, xq=None, xd=None):
+        ra = (R * max(1, len(prods)))(*prods)
+        return call(M, "mlq_matvec_fused", x, n, ra, len(prods), xq, xd, None)
+
+    good = R(qt(cols=256), 5 * A)
+    assert run([good], x=None) == M.MLQ_E_NULL
+    assert run([]) == M.MLQ_E_SHAPE
+    assert run([good] * 9) == M.MLQ_E_SHAPE
+    assert run([good], n=250) == M.MLQ_E_SHAPE
+    assert run([R(qt(cols=128), 5 * A)]) == M.MLQ_E_SHAPE
+    assert run([good, R(qt(cols=256, t=0), 5 * A)]) == M.MLQ_E_TYPE
+    assert run([good], x=6 * A + 4) == M.MLQ_E_ALIGN
+    assert run([good], xq=8 * A) == M.MLQ_E_NULL
+    assert run([R(qt(cols=256), 5 * A + 1)]) == M.MLQ_E_ALIGN

@@ -36,24 +36,27 @@ from tests import parity as PT  # noqa: E402
 from block_quantized_decode_gb300.runner import WorkloadRunner  # noqa: E402
 
 
-def run_and_check(wl, full_rows_limit=300_000_000, graph=False):
+def run_and_check(wl, full_rows_limit=300_000_000, graph=False, chain=False, fused=False):
     r = WorkloadRunner(wl, copies=1)
+    step = r.step_chain if chain else (r.step_fused if fused else r.step)
     if graph:
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
-            r.step()          # warm-up outside capture (sets kernel attributes)
+            step()            # warm-up outside capture (sets kernel attributes)
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
         for m in r.mats:
             m.y.fill_(float("nan"))
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            r.step()
+            step()
         g.replay()
     else:
-        r.step()
+        step()
     torch.cuda.synchronize()
+    if chain:
+        assert int(r.chain_ws.abs().sum()) == 0, "chain workspace not left zeroed"
     rng = np.random.default_rng(12345)
     checked = set()
     for m in r.mats:
