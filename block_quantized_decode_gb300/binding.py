@@ -27,6 +27,7 @@ EXPORTS = (
     "mlq_gemm_q4_small_m", "mlq_block_sumi", "mlq_last_device_error",
     "mlq_debug_set_wait_limit_ns", "mlq_status_str", "mlq_prefetch_l2",
     "mlq_chain_workspace_bytes", "mlq_decode_chain", "mlq_matvec_fused",
+    "mlq_decode_chain_static",
 )
 MLQ_FUSED_MAX_PRODUCTS = 8
 MLQ_CHAIN_MAX_PRODUCTS = 32
@@ -84,6 +85,8 @@ def lib() -> ctypes.CDLL:
         L.mlq_chain_workspace_bytes.restype = ctypes.c_size_t
         L.mlq_decode_chain.argtypes = [ctypes.POINTER(_ChainPhase), I, ctypes.POINTER(_ChainProduct),
                                        I, P, ctypes.c_size_t, P]
+        L.mlq_decode_chain_static.argtypes = [ctypes.POINTER(_ChainPhase), I,
+                                              ctypes.POINTER(_ChainProduct), I, P]
         L.mlq_matvec_fused.argtypes = [P, I, ctypes.POINTER(_ChainProduct), I, P, P, P]
         L.mlq_status_str.argtypes = [S]
         L.mlq_status_str.restype = ctypes.c_char_p
@@ -256,6 +259,17 @@ class FusedCall:
 def mlq_matvec_fused(x, n, products, xq_out=None, xd_out=None, stream=None) -> None:
     """Quantise x (n float32) and run every product (ChainProduct) of width n."""
     FusedCall(x, n, products, xq_out, xd_out)(stream)
+
+
+def mlq_decode_chain_static(phases, products, stream=None) -> None:
+    """mlq_decode_chain without a workspace: for callers that cannot allocate
+    device memory (see include/mlq.h).  Calls on one device must not overlap."""
+    ph = (_ChainPhase * len(phases))(*[
+        _ChainPhase(_addr(p.x), p.n, p.first, p.count, _addr(p.xq_out), _addr(p.xd_out))
+        for p in phases])
+    pr = (_ChainProduct * len(products))(*[_ChainProduct(p.W.c(), _addr(p.y)) for p in products])
+    _check(lib().mlq_decode_chain_static(ph, len(phases), pr, len(products), _stream(stream)),
+           "mlq_decode_chain_static")
 
 
 def mlq_decode_chain(phases, products, workspace, workspace_bytes=None, stream=None) -> None:

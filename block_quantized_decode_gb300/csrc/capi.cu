@@ -299,6 +299,24 @@ mlq_status mlq_decode_chain(const mlq_chain_phase *phases, int nphases,
   return from_cuda(mlq::launch_decode_chain(ctx, products[0].W.type, a));
 }
 
+mlq_status mlq_decode_chain_static(const mlq_chain_phase *phases, int nphases,
+                                   const mlq_chain_product *products, int nproducts,
+                                   void *stream) {
+  mlq::ChainArgs a;
+  mlq_status s = build_chain_args(phases, nphases, products, nproducts, &a);
+  if (s != MLQ_OK) return s;
+  if (nphases > MLQ_CHAIN_STATIC_MAX_PHASES) return MLQ_E_SHAPE;
+  mlq::LaunchCtx ctx;
+  s = make_ctx(&ctx, stream);
+  if (s != MLQ_OK) return s;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MLQ_E_CUDA;
+  }
+  return from_cuda(mlq::launch_decode_chain_static(ctx, dev, products[0].W.type, a));
+}
+
 mlq_status mlq_prefetch_l2(const void *const *ptrs, const size_t *bytes, int n, void *stream) {
   if (n < 0 || n > MLQ_MAX_PREFETCH_RANGES) return MLQ_E_SHAPE;
   if (n > 0 && (ptrs == nullptr || bytes == nullptr)) return MLQ_E_NULL;

@@ -30,6 +30,8 @@
 // workspace is zero again for the next call.  Every wait is bounded: a
 // give-up records MLQ_E_TIMEOUT, the CTA stops issuing copies, drains its
 // own copies in flight (bounded) and still takes part in the final reset.
+#include <mutex>
+
 #include "mlq_device.cuh"
 #include "mlq_launch.h"
 
@@ -363,6 +365,52 @@ cudaError_t launch_decode_chain(const LaunchCtx &ctx, int qtype, const ChainArgs
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+// ---------------------------------------------------------------------------
+// Variant without caller workspace, for callers that may not allocate device
+// memory: the barrier counters live in a fixed device array of this file
+// instead.  kStaticChainWords counters cover MLQ_CHAIN_MAX_PHASES + 1 words
+// with room to spare (256 bytes in all).  Every device that loads the
+// library holds this array until the process exits.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned g_static_chain_counters[kStaticChainWords];
+
+namespace {
+std::mutex g_static_mu;
+unsigned *g_static_addr[64] = {};
+}  // namespace
+
+cudaError_t static_chain_scratch(int device, unsigned **out) {
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (g_static_addr[device] == nullptr) {
+    // The host-side name of a __device__ array is not a device address; ask
+    // the runtime for it, with `device` current (the caller guarantees that).
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_chain_counters);
+    if (e != cudaSuccess) return e;
+    g_static_addr[device] = static_cast<unsigned *>(p);
+  }
+  *out = g_static_addr[device];
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode_chain_static(const LaunchCtx &ctx, int device, int qtype,
+                                       const ChainArgs &args) {
+  if (args.nphases + 1 > kStaticChainWords) return cudaErrorInvalidValue;
+  unsigned *counters = nullptr;
+  cudaError_t e = static_chain_scratch(device, &counters);
+  if (e != cudaSuccess) return e;
+  // The counters must start at zero.  A finished call leaves them zero, but
+  // clear them anyway (no allocation involved) so that nothing depends on
+  // how an earlier call ended.
+  e = cudaMemsetAsync(counters, 0, static_cast<size_t>(args.nphases + 1) * sizeof(unsigned),
+                      ctx.stream);
+  if (e != cudaSuccess) return e;
+  ChainArgs a = args;
+  a.counters = counters;
+  return launch_decode_chain(ctx, qtype, a);
 }
 
 }  // namespace mlq

@@ -88,6 +88,11 @@ struct ChainArgs {
   int ns, stage_bytes, xbuf_bytes;  // ring geometry (set by the launcher)
 };
 cudaError_t launch_decode_chain(const LaunchCtx &ctx, int qtype, const ChainArgs &a);
+// Same chain with its barrier counters in a fixed device array of chain.cu
+// (no workspace, no allocation); at most kStaticChainWords - 1 phases.
+constexpr int kStaticChainWords = 64;
+cudaError_t launch_decode_chain_static(const LaunchCtx &ctx, int device, int qtype,
+                                       const ChainArgs &a);
 
 // fused.cu: quantise x and run up to kFusedMaxProducts products of its width.
 constexpr int kFusedMaxProducts = 8;

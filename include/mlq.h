@@ -69,6 +69,7 @@ extern "C" {
 #define MLQ_FUSED_MAX_PRODUCTS 8
 #define MLQ_CHAIN_MAX_PRODUCTS 32
 #define MLQ_CHAIN_MAX_PHASES 24
+#define MLQ_CHAIN_STATIC_MAX_PHASES 24
 
 typedef enum {
     MLQ_OK = 0,
@@ -172,6 +173,32 @@ typedef struct {
     int8_t *xq_out;
     float *xd_out;
 } mlq_chain_phase;
+
+/* mlq_decode_chain for callers that cannot allocate device memory.
+ *
+ * Some callers may not call cudaMalloc (or any allocator) once they are
+ * running: a decode loop that, like the Design Spec's runtime, sets up all
+ * of its memory at load time and allocates nothing afterwards; code whose
+ * device allocator belongs to another framework; code that runs while a
+ * stream is being captured, where an allocation would break the capture.
+ * mlq_decode_chain needs a small caller-allocated workspace for its grid
+ * barriers; this variant takes none.  Its barrier counters live in a fixed
+ * array of 64 words (256 bytes) inside the library, which every device that
+ * loads the library keeps until the process exits.
+ *
+ * Arguments, requirements and results are those of mlq_decode_chain, with
+ * at most MLQ_CHAIN_STATIC_MAX_PHASES phases (MLQ_E_SHAPE beyond).  The
+ * caller still passes every input and output buffer.  Each call clears the
+ * counters on `stream` before its kernel (cudaMemsetAsync, which allocates
+ * nothing).  All calls on a device share the one array, so two calls whose
+ * work overlaps on the GPU (different streams, or different host threads)
+ * race and give wrong results or MLQ_E_TIMEOUT: serialise them.  The first
+ * call on each device looks up the array's device address (once, with that
+ * device current); make that first call before any stream capture.
+ * Nothing on the pages corresponds to this entry point. */
+mlq_status mlq_decode_chain_static(const mlq_chain_phase *phases, int nphases,
+                                   const mlq_chain_product *products, int nproducts,
+                                   void *stream);
 
 /* One decode phase in one launch (Design Spec Sec. 6 "Forward pass": a
  * quantised activation feeds one or more products, e.g. Wq|Wk|Wv):
