@@ -116,6 +116,12 @@ struct FusedArgs {
 };
 cudaError_t launch_matvec_fused(const LaunchCtx &ctx, int qtype, const FusedArgs &a);
 
+// gemm_mma.cu: M activation rows (2..16) against a Q4_0 matrix on the
+// tensor cores (fp16 mma.sync, exact block sums).
+cudaError_t launch_gemm_q4_mma(const LaunchCtx &ctx, const void *wq, const float *wd, int nb,
+                               const int8_t *xq, const float *xd, int M, float *Y, int ldy,
+                               int r0, int r1);
+
 // gemm_small_m.cu: M activation rows (1..16) against a Q4_0 matrix.
 cudaError_t launch_gemm_q4_small_m(const LaunchCtx &ctx, const void *wq, const float *wd, int nb,
                                    const int8_t *xq, const float *xd, int M, float *Y, int ldy,

@@ -232,3 +232,22 @@ def test_timeout_path_reports_status(lib):
     finally:
         M.mlq_debug_set_wait_limit_ns(10 ** 9)
     PT.check_matvec(oracle.Q4_0, wq, wd, rows, cols, xq, xd, 0, rows, what="after timeout")
+
+
+@pytest.mark.parametrize("Mr", [2, 8, 16])
+def test_gemm_small_m_unit_scales_exact(lib, Mr):
+    """With every scale 1 the product is a plain integer GEMM of the decoded
+    weights; all partial sums are integers below 2^24, so the result must
+    be exact: this pins the tensor-core block sums to the int32 definition."""
+    M = lib
+    rng = np.random.default_rng(50 + Mr)
+    rows, cols = 77, 512
+    wq = rng.integers(0, 256, size=(rows, cols // 2), dtype=np.uint8)
+    wd = np.ones((rows, cols // 32), dtype=np.float32)
+    Xq = rng.integers(-127, 128, size=(Mr, cols), dtype=np.int8)
+    Xd = np.ones((Mr, cols // 32), dtype=np.float32)
+    Y = torch.full((Mr, rows), float("nan"), dtype=torch.float32, device=PT.DEV)
+    M.mlq_gemm_q4_small_m(Y, rows, PT.weights_dev(oracle.Q4_0, wq, wd, rows, cols),
+                          M.QAct(PT.to_dev(Xq), PT.to_dev(Xd), cols, Mr), Mr, 0, rows)
+    want = P.decode_q4_elements(wq, cols) @ Xq.astype(np.int64).T   # [rows, Mr]
+    assert np.array_equal(Y.cpu().numpy().astype(np.int64), want.T)
