@@ -49,9 +49,10 @@ struct MmaArgs {
   int M;
   int r0, r1;
   int S;      // K-slices per tile (warps per tile)
+  int tpc;    // tiles per CTA (warps per CTA = S * tpc)
 };
 
-constexpr int kMmaWarps = 8;
+constexpr int kMmaWarps = 8;  // at most, per CTA
 
 __device__ __forceinline__ uint32_t nib_to_h2(uint32_t w) {
   // two nibbles already in bits 0..3 and 16..19 -> half2 (n0 - 8, n1 - 8)
@@ -102,7 +103,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32) gemm_q4_mma_kernel(const MmaAr
   __shared__ float red[kMmaWarps][16][16];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
-  const int tpc = kMmaWarps / a.S;  // tiles per CTA
+  const int tpc = a.tpc;
   const int tile = blockIdx.x * tpc + warp / a.S;
   const int s = warp % a.S;
   const int nb = a.nb;
@@ -143,33 +144,50 @@ __global__ void __launch_bounds__(kMmaWarps * 32) gemm_q4_mma_kernel(const MmaAr
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = 0ull;
 
-  for (int b = b0; b < b1; ++b) {
-    const uint32_t wl = v_lo ? ldg_u32(wlo + static_cast<size_t>(b) * 16) : 0x88888888u;
-    const uint32_t wh = v_hi ? ldg_u32(whi + static_cast<size_t>(b) * 16) : 0x88888888u;
-    const float sl = v_lo ? __ldg(dlo + b) : 0.0f;
-    const float sh = v_hi ? __ldg(dhi + b) : 0.0f;
-    // A fragments, step 0 (low nibbles) and step 1 (high nibbles)
-    uint32_t A0[4], A1[4];
-    A0[0] = nib_to_h2(wl);
-    A0[1] = nib_to_h2(wh);
-    A0[2] = nib_to_h2(wl >> 8);
-    A0[3] = nib_to_h2(wh >> 8);
-    A1[0] = nib_to_h2(wl >> 4);
-    A1[1] = nib_to_h2(wh >> 4);
-    A1[2] = nib_to_h2(wl >> 12);
-    A1[3] = nib_to_h2(wh >> 12);
+  // Four blocks per step: every load of the step is issued before any of
+  // its data is used, so a warp keeps ~4x more loads in flight.
+  constexpr int kB = 4;
+  for (int bb = b0; bb < b1; bb += kB) {
+    uint32_t wl[kB], wh[kB], xa[NT][kB], xb[NT][kB];
+    float sl[kB], sh[kB], dx0[NT][kB], dx1[NT][kB];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const uint32_t xa = xv[nt] ? ldg_u32(xrow[nt] + static_cast<size_t>(b) * kQK) ^ 0x80808080u : 0x80808080u;
-      const uint32_t xb = xv[nt] ? ldg_u32(xrow[nt] + static_cast<size_t>(b) * kQK + 16) ^ 0x80808080u : 0x80808080u;
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      mma16816(d, A0, s8_to_h2(xa, 0x4240u), s8_to_h2(xa, 0x4341u));
-      mma16816(d, A1, s8_to_h2(xb, 0x4240u), s8_to_h2(xb, 0x4341u));
-      const float dx0 = dv[nt][0] ? __ldg(dxrow[nt][0] + b) : 0.0f;
-      const float dx1 = dv[nt][1] ? __ldg(dxrow[nt][1] + b) : 0.0f;
-      const unsigned long long x2 = pack2(dx0, dx1);
-      scale_acc2(acc[nt][0], d[0], d[1], sl, x2);
-      scale_acc2(acc[nt][1], d[2], d[3], sh, x2);
+    for (int j = 0; j < kB; ++j) {
+      const int b = bb + j;
+      const bool in = b < b1;
+      wl[j] = (v_lo && in) ? ldg_u32(wlo + static_cast<size_t>(b) * 16) : 0x88888888u;
+      wh[j] = (v_hi && in) ? ldg_u32(whi + static_cast<size_t>(b) * 16) : 0x88888888u;
+      sl[j] = (v_lo && in) ? __ldg(dlo + b) : 0.0f;
+      sh[j] = (v_hi && in) ? __ldg(dhi + b) : 0.0f;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        xa[nt][j] = (xv[nt] && in) ? ldg_u32(xrow[nt] + static_cast<size_t>(b) * kQK) : 0u;
+        xb[nt][j] = (xv[nt] && in) ? ldg_u32(xrow[nt] + static_cast<size_t>(b) * kQK + 16) : 0u;
+        dx0[nt][j] = (dv[nt][0] && in) ? __ldg(dxrow[nt][0] + b) : 0.0f;
+        dx1[nt][j] = (dv[nt][1] && in) ? __ldg(dxrow[nt][1] + b) : 0.0f;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      // A fragments, step 0 (low nibbles) and step 1 (high nibbles)
+      uint32_t A0[4], A1[4];
+      A0[0] = nib_to_h2(wl[j]);
+      A0[1] = nib_to_h2(wh[j]);
+      A0[2] = nib_to_h2(wl[j] >> 8);
+      A0[3] = nib_to_h2(wh[j] >> 8);
+      A1[0] = nib_to_h2(wl[j] >> 4);
+      A1[1] = nib_to_h2(wh[j] >> 4);
+      A1[2] = nib_to_h2(wl[j] >> 12);
+      A1[3] = nib_to_h2(wh[j] >> 12);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint32_t ba = xa[nt][j] ^ 0x80808080u, bbits = xb[nt][j] ^ 0x80808080u;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16816(d, A0, s8_to_h2(ba, 0x4240u), s8_to_h2(ba, 0x4341u));
+        mma16816(d, A1, s8_to_h2(bbits, 0x4240u), s8_to_h2(bbits, 0x4341u));
+        const unsigned long long x2 = pack2(dx0[nt][j], dx1[nt][j]);
+        scale_acc2(acc[nt][0], d[0], d[1], sl[j], x2);
+        scale_acc2(acc[nt][1], d[2], d[3], sh[j], x2);
+      }
     }
   }
 
@@ -185,7 +203,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32) gemm_q4_mma_kernel(const MmaAr
     red[warp][g + 8][nt * 8 + 2 * t + 1] = a3;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < tpc * 16 * 16; i += kMmaWarps * 32) {
+  for (int i = threadIdx.x; i < tpc * 16 * 16; i += blockDim.x) {
     const int tl = i / 256, rr = (i / 16) % 16, m = i % 16;
     const int row = a.r0 + (blockIdx.x * tpc + tl) * 16 + rr;
     if (row < a.r1 && m < a.M && m < NT * 8) {
@@ -195,6 +213,8 @@ __global__ void __launch_bounds__(kMmaWarps * 32) gemm_q4_mma_kernel(const MmaAr
     }
   }
 }
+
+static long long ctas_limit_sms(const LaunchCtx &ctx) { return ctx.num_sms; }
 
 cudaError_t launch_gemm_q4_mma(const LaunchCtx &ctx, const void *wq, const float *wd, int nb,
                                const int8_t *xq, const float *xd, int M, float *Y, int ldy,
@@ -213,18 +233,37 @@ cudaError_t launch_gemm_q4_mma(const LaunchCtx &ctx, const void *wq, const float
   a.r0 = r0;
   a.r1 = r1;
   const long long tiles = (n + 15) / 16;
-  // enough warps to fill the GPU (about 16 per SM), slices of >= 8 blocks
-  int S = 1;
-  while (S < kMmaWarps && tiles * S < static_cast<long long>(ctx.num_sms) * 16 && nb / (2 * S) >= 8) S *= 2;
-  a.S = S;
-  const int tpc = kMmaWarps / S;
-  const long long grid = (tiles + tpc - 1) / tpc;
-  if (M <= 8) {
-    return launch_kernel(gemm_q4_mma_kernel<1>, dim3(static_cast<unsigned>(grid)), dim3(kMmaWarps * 32), 0,
-                         ctx, a);
+  // Pick the K-slice count S (warps per 16-row tile) that gives the most
+  // warps while the whole grid stays resident in one wave; a second,
+  // mostly empty wave costs more than the extra parallelism gains.
+  auto kern = M <= 8 ? gemm_q4_mma_kernel<1> : gemm_q4_mma_kernel<2>;
+  int bestS = 1, best_tpc = 4;
+  long long best_warps = -1, best_waves = 1LL << 40;
+  for (int S = 1; S <= kMmaWarps; S *= 2) {
+    if (S > 1 && nb / S < 8) break;
+    const int warps = S >= 4 ? S : 4;
+    const int tpc = warps / S;
+    const long long ctas = (tiles + tpc - 1) / tpc;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, warps * 32, 0) != cudaSuccess ||
+        per_sm < 1) {
+      cudaGetLastError();
+      per_sm = 1;
+    }
+    const long long resident = static_cast<long long>(per_sm) * ctas_limit_sms(ctx);
+    const long long waves = (ctas + resident - 1) / resident;
+    const long long total_warps = tiles * S;
+    if (waves < best_waves || (waves == best_waves && total_warps > best_warps)) {
+      best_waves = waves;
+      best_warps = total_warps;
+      bestS = S;
+      best_tpc = tpc;
+    }
   }
-  return launch_kernel(gemm_q4_mma_kernel<2>, dim3(static_cast<unsigned>(grid)), dim3(kMmaWarps * 32), 0,
-                       ctx, a);
+  a.S = bestS;
+  a.tpc = best_tpc;
+  const long long grid = (tiles + best_tpc - 1) / best_tpc;
+  return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(bestS * best_tpc * 32), 0, ctx, a);
 }
 
 }  // namespace mlq
