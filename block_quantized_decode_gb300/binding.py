@@ -30,6 +30,7 @@ EXPORTS = (
     "mlq_decode_chain_static",
 )
 MLQ_FUSED_MAX_PRODUCTS = 8
+MLQ_F_STATIC_WEIGHTS = 1
 MLQ_CHAIN_MAX_PRODUCTS = 32
 MLQ_CHAIN_MAX_PHASES = 24
 
@@ -87,7 +88,8 @@ def lib() -> ctypes.CDLL:
                                        I, P, ctypes.c_size_t, P]
         L.mlq_decode_chain_static.argtypes = [ctypes.POINTER(_ChainPhase), I,
                                               ctypes.POINTER(_ChainProduct), I, P]
-        L.mlq_matvec_fused.argtypes = [P, I, ctypes.POINTER(_ChainProduct), I, P, P, P]
+        L.mlq_matvec_fused.argtypes = [P, I, ctypes.POINTER(_ChainProduct), I, P, P,
+                                       ctypes.c_uint, P]
         L.mlq_status_str.argtypes = [S]
         L.mlq_status_str.restype = ctypes.c_char_p
         for name in EXPORTS:
@@ -245,20 +247,21 @@ class ChainCall:
 class FusedCall:
     """Marshalled arguments of one mlq_matvec_fused call."""
 
-    def __init__(self, x, n, products, xq_out=None, xd_out=None):
-        self.x, self.n = _addr(x), n
+    def __init__(self, x, n, products, xq_out=None, xd_out=None, flags: int = 0):
+        self.x, self.n, self.flags = _addr(x), n, flags
         self.pr = (_ChainProduct * len(products))(*[_ChainProduct(p.W.c(), _addr(p.y)) for p in products])
         self.npr = len(products)
         self.xq, self.xd = _addr(xq_out), _addr(xd_out)
 
     def __call__(self, stream=None) -> None:
         _check(lib().mlq_matvec_fused(self.x, self.n, self.pr, self.npr, self.xq, self.xd,
-                                      _stream(stream)), "mlq_matvec_fused")
+                                      self.flags, _stream(stream)), "mlq_matvec_fused")
 
 
-def mlq_matvec_fused(x, n, products, xq_out=None, xd_out=None, stream=None) -> None:
+def mlq_matvec_fused(x, n, products, xq_out=None, xd_out=None, flags: int = 0,
+                     stream=None) -> None:
     """Quantise x (n float32) and run every product (ChainProduct) of width n."""
-    FusedCall(x, n, products, xq_out, xd_out)(stream)
+    FusedCall(x, n, products, xq_out, xd_out, flags)(stream)
 
 
 def mlq_decode_chain_static(phases, products, stream=None) -> None:

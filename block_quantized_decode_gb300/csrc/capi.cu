@@ -196,6 +196,21 @@ mlq_status build_chain_args(const mlq_chain_phase *phases, int nphases,
 
 }  // namespace
 
+namespace mlq {
+void prefer_max_shared_impl(const void *kern) {
+  static std::mutex mu;
+  static const void *seen[256];
+  static int nseen = 0;
+  std::lock_guard<std::mutex> lk(mu);
+  for (int i = 0; i < nseen; ++i)
+    if (seen[i] == kern) return;
+  cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                       cudaSharedmemCarveoutMaxShared);
+  cudaGetLastError();
+  if (nseen < 256) seen[nseen++] = kern;
+}
+}  // namespace mlq
+
 extern "C" {
 
 mlq_status mlq_init(void) {
@@ -247,7 +262,8 @@ mlq_status mlq_gemm_q4_small_m(float *Y, int ldy, const mlq_qtensor *W, const ml
 }
 
 mlq_status mlq_matvec_fused(const float *x, int n, const mlq_chain_product *products,
-                            int nproducts, int8_t *xq_out, float *xd_out, void *stream) {
+                            int nproducts, int8_t *xq_out, float *xd_out, unsigned flags,
+                            void *stream) {
   if (x == nullptr || products == nullptr) return MLQ_E_NULL;
   if ((xq_out == nullptr) != (xd_out == nullptr)) return MLQ_E_NULL;
   if (nproducts < 1 || nproducts > MLQ_FUSED_MAX_PRODUCTS || !cols_ok(n)) return MLQ_E_SHAPE;
@@ -273,9 +289,12 @@ mlq_status mlq_matvec_fused(const float *x, int n, const mlq_chain_product *prod
   a.xd_out = xd_out;
   a.total_rows = 0;
   a.nchunks = 1;
+  if ((flags & ~static_cast<unsigned>(MLQ_F_STATIC_WEIGHTS)) != 0) return MLQ_E_SHAPE;
+  a.early = (flags & MLQ_F_STATIC_WEIGHTS) ? 1 : 0;
   mlq::LaunchCtx ctx;
   mlq_status s = make_ctx(&ctx, stream);
   if (s != MLQ_OK) return s;
+  if (!ctx.pdl) a.early = 0;  // without dependent launch there is nothing to overlap
   return from_cuda(mlq::launch_matvec_fused(ctx, type, a));
 }
 

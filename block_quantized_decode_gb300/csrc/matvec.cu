@@ -285,6 +285,7 @@ constexpr size_t kSmemBudget = 200 * 1024;
 template <int QT, int U, bool SUMI>
 static cudaError_t launch_variant(const LaunchCtx &ctx, MatvecArgs a) {
   auto kern = matvec_m1_kernel<QT, U, SUMI>;
+  prefer_max_shared(kern);
   const int n = a.r1 - a.r0;
   const size_t base = static_cast<size_t>(a.nb) * kQK + 8 * static_cast<size_t>(a.nb);
   long long grid = static_cast<long long>(ctx.num_sms) * kCtasPerSm;

@@ -307,6 +307,7 @@ template <int QT, int BL, bool SUMI>
 static cudaError_t launch_tma_variant(const LaunchCtx &ctx, const TmaArgs &a, int grid,
                                       size_t smem) {
   auto kern = matvec_tma_kernel<QT, BL, SUMI>;
+  prefer_max_shared(kern);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;

@@ -18,6 +18,19 @@ struct LaunchCtx {
                                 // their first loads may precede the dependency wait
 };
 
+// Kernels of a dependent decode chain (quantize, M = 1 products, fused
+// phases) ask for the largest shared-memory carveout.  An SM's L1/shared
+// split can only change while it is idle, so kernels of one chain with
+// different preferences could not share an SM; with one common split the
+// next kernel of a chain can become resident while the previous one is
+// still running.  (The small-M kernels keep the default: they read their
+// activations through L1.)  Done once per kernel.
+void prefer_max_shared_impl(const void *kern);
+template <typename K>
+inline void prefer_max_shared(K kern) {
+  prefer_max_shared_impl(reinterpret_cast<const void *>(kern));
+}
+
 // Launch `kern` with cudaLaunchKernelEx, optionally with programmatic
 // dependent launch, on ctx.stream.
 template <typename... KArgs, typename... Args>
@@ -111,8 +124,10 @@ struct FusedArgs {
   float *xd_out;
   int total_rows;   // set by the launcher
   int nchunks;      // set by the launcher
-  int early;        // set by the launcher: first weight loads before the dependency wait
+  int early;        // first weight loads before the dependency wait (static weights)
   int prefetch;     // set by the launcher: hint the CTA's weights into L2 first
+  int *status;      // set by the launcher
+  unsigned long long wait_ns;
 };
 cudaError_t launch_matvec_fused(const LaunchCtx &ctx, int qtype, const FusedArgs &a);
 

@@ -63,6 +63,7 @@ cudaError_t launch_quantize_q8(const LaunchCtx &ctx, const float *x, int8_t *q, 
   long long grid = (warps + 7) / 8;
   const long long cap = static_cast<long long>(ctx.num_sms) * 8;
   if (grid > cap) grid = cap;
+  prefer_max_shared(quantize_q8_kernel);
   return launch_kernel(quantize_q8_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, ctx,
                        x, q, d, nblocks);
 }

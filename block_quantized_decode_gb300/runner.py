@@ -95,8 +95,10 @@ class WorkloadRunner:
             self._chain_calls[copy] = B.ChainCall(cp, pr, self.chain_ws)
         return self._chain_calls[copy]
 
-    def fused_calls(self, copy: int = 0):
-        key = ("fused", copy)
+    def fused_calls(self, copy: int = 0, static_weights: bool = True):
+        """One mlq_matvec_fused call per phase.  The runner's weights are
+        written once at construction, so it passes MLQ_F_STATIC_WEIGHTS."""
+        key = ("fused", copy, static_weights)
         if key not in self._chain_calls:
             if self.m != 1:
                 raise ValueError("fused phases are M = 1")
@@ -106,13 +108,14 @@ class WorkloadRunner:
                                                m.spec.wtype), m.y)
                       for m in self.mats[first:first + count]]
                 calls.append(B.FusedCall(self.fp32[src], self.sources[src], pr,
-                                         self.qbuf[src].q, self.qbuf[src].d))
+                                         self.qbuf[src].q, self.qbuf[src].d,
+                                         B.MLQ_F_STATIC_WEIGHTS if static_weights else 0))
             self._chain_calls[key] = calls
         return self._chain_calls[key]
 
-    def step_fused(self, copy: int = 0, stream=None) -> None:
+    def step_fused(self, copy: int = 0, stream=None, static_weights: bool = True) -> None:
         """One pass as one mlq_matvec_fused launch per phase."""
-        for c in self.fused_calls(copy):
+        for c in self.fused_calls(copy, static_weights):
             c(stream)
 
     def step_chain(self, copy: int = 0, stream=None) -> None:

@@ -49,9 +49,10 @@
  * MLQ_STATIC_WEIGHTS=1 additionally lets the products issue their first
  * weight loads before that previous kernel has finished; set it only when
  * no work queued earlier on the stream writes the weight arrays (true for
- * inference weights loaded once).  MLQ_FUSED_L2_PREFETCH=1 makes
- * mlq_matvec_fused hint its whole weight range into L2 first.  Both are off
- * by default (measured gains were small or negative on GB300).
+ * inference weights loaded once; mlq_matvec_fused takes the same promise
+ * per call through MLQ_F_STATIC_WEIGHTS).  MLQ_FUSED_L2_PREFETCH=1 makes
+ * the register-pipelined mlq_matvec_fused kernel hint its whole weight
+ * range into L2 first.  Both are off by default.
  */
 #ifndef MLQ_H
 #define MLQ_H
@@ -209,11 +210,18 @@ mlq_status mlq_decode_chain_static(const mlq_chain_phase *phases, int nphases,
  * tolerance of mlq_matvec_q4/_q8.  xq_out / xd_out (both NULL, or n bytes
  * and n/32 floats, 16-byte aligned) receive the quantised x.  The outputs
  * must not overlap x.  Built for chains of such calls under programmatic
- * dependent launch: each call hints its own weights into L2 before waiting
- * for the previous kernel, so consecutive phases overlap their HBM reads.
+ * dependent launch.  When a CTA's share of the weights fits in shared
+ * memory, the kernel copies that share there in pieces and reduces rows as
+ * they land.  flags: 0 or MLQ_F_STATIC_WEIGHTS (anything else:
+ * MLQ_E_SHAPE).  MLQ_F_STATIC_WEIGHTS promises that no work queued earlier
+ * on the stream writes any W.q or W.d of this call (true for inference
+ * weights loaded once); the kernel may then start reading its weights
+ * while the previous kernel is still running.
  * No counterpart on the pages: a GPU fusion of quantize_q8 and matvec. */
+#define MLQ_F_STATIC_WEIGHTS 1u
 mlq_status mlq_matvec_fused(const float *x, int n, const mlq_chain_product *products,
-                            int nproducts, int8_t *xq_out, float *xd_out, void *stream);
+                            int nproducts, int8_t *xq_out, float *xd_out, unsigned flags,
+                            void *stream);
 
 /* Bytes of workspace mlq_decode_chain needs for `nphases` phases. */
 size_t mlq_chain_workspace_bytes(int nphases);

@@ -186,9 +186,9 @@ def test_validation_fused(M):
     from block_quantized_decode_gb300.binding import _ChainProduct
     R = _ChainProduct
 
-    def run(prods, x=6 * A, n=256, xq=None, xd=None):
+    def run(prods, x=6 * A, n=256, xq=None, xd=None, flags=0):
         ra = (R * max(1, len(prods)))(*prods)
-        return call(M, "mlq_matvec_fused", x, n, ra, len(prods), xq, xd, None)
+        return call(M, "mlq_matvec_fused", x, n, ra, len(prods), xq, xd, flags, None)
 
     good = R(qt(cols=256), 5 * A)
     assert run([good], x=None) == M.MLQ_E_NULL
@@ -200,3 +200,4 @@ def test_validation_fused(M):
     assert run([good], x=6 * A + 4) == M.MLQ_E_ALIGN
     assert run([good], xq=8 * A) == M.MLQ_E_NULL
     assert run([R(qt(cols=256), 5 * A + 1)]) == M.MLQ_E_ALIGN
+    assert run([good], flags=2) == M.MLQ_E_SHAPE

@@ -36,9 +36,16 @@ from tests import parity as PT  # noqa: E402
 from block_quantized_decode_gb300.runner import WorkloadRunner  # noqa: E402
 
 
-def run_and_check(wl, full_rows_limit=300_000_000, graph=False, chain=False, fused=False):
+def run_and_check(wl, full_rows_limit=300_000_000, graph=False, chain=False, fused=False,
+                  static_weights=True):
     r = WorkloadRunner(wl, copies=1)
-    step = r.step_chain if chain else (r.step_fused if fused else r.step)
+    if chain:
+        step = r.step_chain
+    elif fused:
+        def step():
+            r.step_fused(static_weights=static_weights)
+    else:
+        step = r.step
     if graph:
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())

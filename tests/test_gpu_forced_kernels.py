@@ -38,3 +38,17 @@ def test_small_m_parity_with_forced_kernel(kernel):
                         "tests/test_gpu_parity.py", "-k", "gemm"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=1200)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
+
+@pytest.mark.skipif(os.environ.get("MLQ_FUSED_KERNEL") is not None,
+                    reason="already inside a forced-kernel run")
+@pytest.mark.parametrize("kernel", ["ldg", "smem"])
+def test_fused_parity_with_forced_kernel(kernel):
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    env = dict(os.environ, MLQ_FUSED_KERNEL=kernel, PYTHONPATH=ROOT)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        "tests/test_gpu_fused.py"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=1200)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]

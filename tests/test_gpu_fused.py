@@ -32,8 +32,9 @@ def test_fused_tiny():
     run_and_check(I.tiny_q4(), fused=True)
 
 
-def test_fused_tinyllama_layer():
-    run_and_check(I.tinyllama_layer(), fused=True)
+@pytest.mark.parametrize("static", [True, False], ids=["static_weights", "plain"])
+def test_fused_tinyllama_layer(static):
+    run_and_check(I.tinyllama_layer(), fused=True, static_weights=static)
 
 
 def test_fused_tinyllama_layer_graph():
@@ -46,6 +47,15 @@ def test_fused_llama7b_ffn_q4():
 
 def test_fused_llama7b_ffn_q8_lm_head():
     run_and_check(I.llama7b_ffn_q8_lm_head(), fused=True)
+
+
+def test_fused_ragged_plain():
+    wl = I.Workload("ragged_plain", 1, [
+        I.Matvec("a", I.Q4_0, 1001, 128, "x"),
+        I.Matvec("b", I.Q4_0, 5, 128, "x"),
+        I.Matvec("c", I.Q4_0, 640, 1024, "x"),
+    ])
+    run_and_check(wl, fused=True, static_weights=False)
 
 
 def test_fused_ragged():
