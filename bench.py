@@ -434,6 +434,47 @@ def run_ours(args, wl, world, rank, local, pg):
                     "bytes_per_launch": wbytes, "us_per_launch": best * 1e6,
                     "method": f"{launches} back-to-back chain launches (one per step) in one CUDA "
                               "graph, best of 3 replays, CUDA events on the launching stream"}
+    elif graphs and path == "fused":
+        # each phase's fused launch back to back in its own graph
+        per_phase, tot_bytes, tot_s = [], 0.0, 0.0
+        launches = 2 * copies
+        for k, (src, first, count) in enumerate(r.chain_phases()):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for j in range(launches):
+                    r.fused_calls(j % copies)[k]()
+            with torch.cuda.stream(stream):
+                g.replay()
+            stream.synchronize()
+            best = None
+            for _ in range(3):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    a.record(stream)
+                    g.replay()
+                    b.record(stream)
+                stream.synchronize()
+                t = a.elapsed_time(b) / 1e3 / launches
+                best = t if best is None else min(best, t)
+            del g
+            mats = r.mats[first:first + count]
+            nbytes = sum(m.host_q.nbytes + m.host_d.nbytes for m in mats)
+            per_phase.append({"phase": "+".join(m.spec.name for m in mats),
+                              "shape": f"{sum(m.spec.rows for m in mats)}x{mats[0].spec.cols}",
+                              "us_per_launch": best * 1e6, "GBps": nbytes / best / 1e9})
+            tot_bytes += nbytes
+            tot_s += best
+        ach = tot_bytes / tot_s / 1e9
+        qt = "Q4_0" if r.mats[0].spec.wtype == I.Q4_0 else "Q8_0"
+        nph = len(per_phase)
+        roofline = {"kernel": f"matvec_fused_smem_kernel<{qt}>", "bound": "hbm", "achieved": ach,
+                    "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_source": peak_src,
+                    "traffic": ncu_traffic(f"fused_{wl.name}", ("fused.cu", "mlq_device.cuh"),
+                                           tot_bytes / nph),
+                    "bytes_per_launch": tot_bytes / nph, "us_per_launch": tot_s / nph * 1e6,
+                    "method": f"{launches} back-to-back launches of each phase in one CUDA graph, "
+                              "best of 3 replays, CUDA events on the launching stream",
+                    "per_phase": per_phase}
     elif graphs:
         shapes = {}
         for i, m in enumerate(r.mats):

@@ -21,7 +21,9 @@ from . import binding as B
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("--op", default="matvec_q4",
-                   choices=["matvec_q4", "matvec_q8", "gemm_q4", "quantize"])
+                   choices=["matvec_q4", "matvec_q8", "gemm_q4", "quantize", "fused"])
+    p.add_argument("--workload", default="tinyllama_layer",
+                   help="for --op fused: the workload whose phases run as mlq_matvec_fused calls")
     p.add_argument("--rows", type=int, default=4096)
     p.add_argument("--cols", type=int, default=11008)
     p.add_argument("--m", type=int, default=1)
@@ -34,6 +36,8 @@ def main():
     dev = torch.device("cuda:0")
     torch.cuda.set_device(0)
     B.mlq_init()
+    if a.op == "fused":
+        return fused_case(a)
     g = torch.Generator(device=dev)
     g.manual_seed(0)
     rows, cols, m = a.rows, a.cols, a.m
@@ -99,6 +103,43 @@ def main():
                       "us_per_launch": us, "us_all": times, "bytes_per_launch": moved,
                       "GBps": moved / (us * 1e-6) / 1e9,
                       "gops": 2.0 * m * rows * cols / (us * 1e-6) / 1e9 if a.op != "quantize" else 0.0}))
+
+
+def fused_case(a):
+    """One pass of a workload as mlq_matvec_fused phases, per launch group."""
+    from . import inputs as I
+    from .runner import WorkloadRunner
+    wl = I.WORKLOADS[a.workload]()
+    copies = a.copies or 3
+    r = WorkloadRunner(wl, copies=copies)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for c in range(copies):
+            r.step_fused(copy=c)
+    s.synchronize()
+    graph = None
+    if not a.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            for i in range(a.iters):
+                r.step_fused(copy=i % copies)
+    times = []
+    for _ in range(a.reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            if graph is not None:
+                graph.replay()
+            else:
+                for i in range(a.iters):
+                    r.step_fused(copy=i % copies)
+            e1.record(s)
+        s.synchronize()
+        times.append(e0.elapsed_time(e1) / a.iters * 1e3)
+    assert B.mlq_last_device_error(s) == B.MLQ_OK
+    us = min(times)
+    print(json.dumps({"op": "fused", "workload": wl.name, "copies": copies, "us_per_step": us,
+                      "bytes_per_step": r.weight_bytes(), "GBps": r.weight_bytes() / (us * 1e-6) / 1e9}))
 
 
 if __name__ == "__main__":
