@@ -53,11 +53,16 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true")
-    p.add_argument("--path", choices=["auto", "fused", "chain", "calls"], default="auto",
-                   help="fused: one mlq_matvec_fused launch per phase; chain: one "
-                        "mlq_decode_chain launch per step; calls: one C-ABI call per quantize "
-                        "and product; auto: fused for M = 1 steps under 64 MB of weights "
-                        "(latency-bound, fewer launches win), else calls")
+    p.add_argument("--path", choices=["auto", "phase", "fused", "chain", "calls"], default="auto",
+                   help="phase: one mlq_decode_phase launch per phase, each phase writing "
+                        "the next one's input already quantised; fused: one mlq_matvec_fused "
+                        "launch per phase (float inputs); chain: one mlq_decode_chain launch "
+                        "per step; calls: one C-ABI call per quantize and product; auto: fused "
+                        "for M = 1 steps under 64 MB of weights (latency-bound, fewer launches "
+                        "win), else calls")
+    p.add_argument("--phase-prefetch", choices=["none", "ahead1", "ahead2"], default="ahead2",
+                   help="phase path: each phase hints the weights of the phase one / two "
+                        "later into L2 once it has read its input")
     p.add_argument("--prefetch", choices=["none", "all", "next"], default="none",
                    help="L2 prefetch of weights through mlq_prefetch_l2: all (whole pass "
                         "first) or next (one product ahead); measured slower in-chain, so off")
@@ -317,6 +322,8 @@ def run_ours(args, wl, world, rank, local, pg):
             r.step_chain(copy=c)
         elif path == "fused":
             r.step_fused(copy=c)
+        elif path == "phase":
+            r.step_phase(copy=c, prefetch=args.phase_prefetch)
         else:
             r.step(copy=c, prefetch=pf)
     assert r.weight_bytes() == wbytes
@@ -434,15 +441,18 @@ def run_ours(args, wl, world, rank, local, pg):
                     "bytes_per_launch": wbytes, "us_per_launch": best * 1e6,
                     "method": f"{launches} back-to-back chain launches (one per step) in one CUDA "
                               "graph, best of 3 replays, CUDA events on the launching stream"}
-    elif graphs and path == "fused":
-        # each phase's fused launch back to back in its own graph
+    elif graphs and path in ("fused", "phase"):
+        # each phase's launch back to back in its own graph
+        def calls_of(c):
+            return r.fused_calls(c) if path == "fused" else r.phase_calls(
+                c, prefetch="self" if args.phase_prefetch != "none" else "none")
         per_phase, tot_bytes, tot_s = [], 0.0, 0.0
         launches = 2 * copies
         for k, (src, first, count) in enumerate(r.chain_phases()):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for j in range(launches):
-                    r.fused_calls(j % copies)[k]()
+                    calls_of(j % copies)[k]()
             with torch.cuda.stream(stream):
                 g.replay()
             stream.synchronize()
@@ -467,9 +477,11 @@ def run_ours(args, wl, world, rank, local, pg):
         ach = tot_bytes / tot_s / 1e9
         qt = "Q4_0" if r.mats[0].spec.wtype == I.Q4_0 else "Q8_0"
         nph = len(per_phase)
-        roofline = {"kernel": f"matvec_fused_smem_kernel<{qt}>", "bound": "hbm", "achieved": ach,
+        kname, ksrc = (("matvec_fused_smem_kernel", "fused.cu") if path == "fused" else
+                       ("phase_kernel", "phase.cu"))
+        roofline = {"kernel": f"{kname}<{qt}>", "bound": "hbm", "achieved": ach,
                     "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_source": peak_src,
-                    "traffic": ncu_traffic(f"fused_{wl.name}", ("fused.cu", "mlq_device.cuh"),
+                    "traffic": ncu_traffic(f"{path}_{wl.name}", (ksrc, "mlq_device.cuh"),
                                            tot_bytes / nph),
                     "bytes_per_launch": tot_bytes / nph, "us_per_launch": tot_s / nph * 1e6,
                     "method": f"{launches} back-to-back launches of each phase in one CUDA graph, "
@@ -560,10 +572,10 @@ def run_ours(args, wl, world, rank, local, pg):
                        "l2": f"inputs larger than L2: {copies} rotating weight copies "
                              f"({copies * wbytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
                        "graphs": ("one graph per cycle of %d steps" % copies) if cycle is not None else False,
-                       "path": path, "l2_prefetch": pf or "none", "parallelism": f"replicas x{world} (independent decode streams)"},
+                       "path": path, "l2_prefetch": (args.phase_prefetch if path == "phase" else pf or "none"), "parallelism": f"replicas x{world} (independent decode streams)"},
             "gops": gops, "hbm_frac": value / world / hbm,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": (1 if path == "chain" else len(r.chain_phases()) if path == "fused" else
+            "gpu_launches": (1 if path == "chain" else len(r.chain_phases()) if path in ("fused", "phase") else
                              r.kernels_per_step + {None: 0, "all": 1, "next": len(r.mats)}[pf]) * steps,
             "clocks": clk,
         }

@@ -27,7 +27,7 @@ EXPORTS = (
     "mlq_gemm_q4_small_m", "mlq_block_sumi", "mlq_last_device_error",
     "mlq_debug_set_wait_limit_ns", "mlq_status_str", "mlq_prefetch_l2",
     "mlq_chain_workspace_bytes", "mlq_decode_chain", "mlq_matvec_fused",
-    "mlq_decode_chain_static",
+    "mlq_decode_chain_static", "mlq_decode_phase",
 )
 MLQ_FUSED_MAX_PRODUCTS = 8
 MLQ_F_STATIC_WEIGHTS = 1
@@ -60,6 +60,16 @@ class _ChainPhase(ctypes.Structure):
                 ("count", ctypes.c_int), ("xq_out", ctypes.c_void_p), ("xd_out", ctypes.c_void_p)]
 
 
+class _PhaseProduct(ctypes.Structure):
+    _fields_ = [("W", _QTensor), ("y", ctypes.c_void_p), ("yq", ctypes.c_void_p),
+                ("yd", ctypes.c_void_p)]
+
+
+class _PhaseInput(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("xq", ctypes.c_void_p), ("xd", ctypes.c_void_p),
+                ("n", ctypes.c_int), ("xq_out", ctypes.c_void_p), ("xd_out", ctypes.c_void_p)]
+
+
 _lib = None
 
 
@@ -90,6 +100,8 @@ def lib() -> ctypes.CDLL:
                                               ctypes.POINTER(_ChainProduct), I, P]
         L.mlq_matvec_fused.argtypes = [P, I, ctypes.POINTER(_ChainProduct), I, P, P,
                                        ctypes.c_uint, P]
+        L.mlq_decode_phase.argtypes = [ctypes.POINTER(_PhaseInput), ctypes.POINTER(_PhaseProduct),
+                                       I, P, P, I, ctypes.c_uint, P]
         L.mlq_status_str.argtypes = [S]
         L.mlq_status_str.restype = ctypes.c_char_p
         for name in EXPORTS:
@@ -262,6 +274,43 @@ def mlq_matvec_fused(x, n, products, xq_out=None, xd_out=None, flags: int = 0,
                      stream=None) -> None:
     """Quantise x (n float32) and run every product (ChainProduct) of width n."""
     FusedCall(x, n, products, xq_out, xd_out, flags)(stream)
+
+
+@dataclass
+class PhaseProduct:
+    """One product of a phase: y = W x, and optionally y in Q8_0 (yq, yd)."""
+    W: QTensor
+    y: object
+    yq: object = None
+    yd: object = None
+
+
+class PhaseCall:
+    """Marshalled arguments of one mlq_decode_phase call.  The input is
+    float x (quantised in the launch; xq_out / xd_out receive it) or, with
+    x None, Q8_0 (xq, xd) -- e.g. the yq / yd of an earlier phase.
+    prefetch: (device pointer or tensor, bytes) ranges to hint into L2 once
+    the input has been read, e.g. the weights of the phase after next."""
+
+    def __init__(self, n, products, x=None, xq=None, xd=None, xq_out=None, xd_out=None,
+                 flags: int = 0, prefetch=()):
+        self.inp = _PhaseInput(_addr(x), _addr(xq), _addr(xd), n, _addr(xq_out), _addr(xd_out))
+        self.pr = (_PhaseProduct * len(products))(*[
+            _PhaseProduct(p.W.c(), _addr(p.y), _addr(p.yq), _addr(p.yd)) for p in products])
+        self.npr, self.flags = len(products), flags
+        self.npf = len(prefetch)
+        self.pf = (ctypes.c_void_p * max(1, self.npf))(*[_addr(p) for p, _ in prefetch])
+        self.pfb = (ctypes.c_size_t * max(1, self.npf))(*[int(b) for _, b in prefetch])
+
+    def __call__(self, stream=None) -> None:
+        _check(lib().mlq_decode_phase(ctypes.byref(self.inp), self.pr, self.npr, self.pf, self.pfb,
+                                      self.npf, self.flags, _stream(stream)), "mlq_decode_phase")
+
+
+def mlq_decode_phase(n, products, x=None, xq=None, xd=None, xq_out=None, xd_out=None,
+                     flags: int = 0, prefetch=(), stream=None) -> None:
+    """One phase: every product (PhaseProduct) of width n on one input."""
+    PhaseCall(n, products, x, xq, xd, xq_out, xd_out, flags, prefetch)(stream)
 
 
 def mlq_decode_chain_static(phases, products, stream=None) -> None:

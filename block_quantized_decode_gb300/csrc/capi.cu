@@ -268,7 +268,7 @@ mlq_status mlq_matvec_fused(const float *x, int n, const mlq_chain_product *prod
   if ((xq_out == nullptr) != (xd_out == nullptr)) return MLQ_E_NULL;
   if (nproducts < 1 || nproducts > MLQ_FUSED_MAX_PRODUCTS || !cols_ok(n)) return MLQ_E_SHAPE;
   if (!aligned(x, 16) || !aligned(xq_out, 16) || !aligned(xd_out, 16)) return MLQ_E_ALIGN;
-  mlq::FusedArgs a;
+  mlq::FusedArgs a = {};
   const uint8_t type = products[0].W.type;
   for (int j = 0; j < nproducts; ++j) {
     const mlq_chain_product &p = products[j];
@@ -291,6 +291,77 @@ mlq_status mlq_matvec_fused(const float *x, int n, const mlq_chain_product *prod
   a.nchunks = 1;
   if ((flags & ~static_cast<unsigned>(MLQ_F_STATIC_WEIGHTS)) != 0) return MLQ_E_SHAPE;
   a.early = (flags & MLQ_F_STATIC_WEIGHTS) ? 1 : 0;
+  mlq::LaunchCtx ctx;
+  mlq_status s = make_ctx(&ctx, stream);
+  if (s != MLQ_OK) return s;
+  if (!ctx.pdl) a.early = 0;  // without dependent launch there is nothing to overlap
+  return from_cuda(mlq::launch_matvec_fused(ctx, type, a));
+}
+
+static_assert(MLQ_FUSED_MAX_PRODUCTS == mlq::kFusedMaxProducts, "header and kernels agree");
+static_assert(MLQ_PHASE_MAX_PREFETCH == mlq::kPhaseMaxPrefetch, "header and kernels agree");
+
+mlq_status mlq_decode_phase(const mlq_phase_input *in, const mlq_phase_product *products,
+                            int nproducts, const void *const *prefetch,
+                            const size_t *prefetch_bytes, int nprefetch, unsigned flags,
+                            void *stream) {
+  if (in == nullptr || products == nullptr) return MLQ_E_NULL;
+  if (nprefetch < 0 || nprefetch > MLQ_PHASE_MAX_PREFETCH) return MLQ_E_SHAPE;
+  if (nprefetch > 0 && (prefetch == nullptr || prefetch_bytes == nullptr)) return MLQ_E_NULL;
+  const int n = in->n;
+  if (in->x != nullptr) {
+    if (in->xq != nullptr || in->xd != nullptr) return MLQ_E_SHAPE;  // one input, not two
+    if ((in->xq_out == nullptr) != (in->xd_out == nullptr)) return MLQ_E_NULL;
+  } else {
+    if (in->xq == nullptr || in->xd == nullptr) return MLQ_E_NULL;
+    if (in->xq_out != nullptr || in->xd_out != nullptr) return MLQ_E_SHAPE;
+  }
+  if (nproducts < 1 || nproducts > MLQ_FUSED_MAX_PRODUCTS || !cols_ok(n)) return MLQ_E_SHAPE;
+  if (!aligned(in->x, 16) || !aligned(in->xq, 16) || !aligned(in->xd, 16) ||
+      !aligned(in->xq_out, 16) || !aligned(in->xd_out, 16))
+    return MLQ_E_ALIGN;
+  if ((flags & ~static_cast<unsigned>(MLQ_F_STATIC_WEIGHTS)) != 0) return MLQ_E_SHAPE;
+  mlq::FusedArgs a = {};
+  const uint8_t type = products[0].W.type;
+  bool any_yq = false;
+  for (int j = 0; j < nproducts; ++j) {
+    const mlq_phase_product &p = products[j];
+    if (p.W.type != MLQ_Q4_0 && p.W.type != MLQ_Q8_0) return MLQ_E_TYPE;
+    if (p.W.type != type) return MLQ_E_TYPE;
+    if (p.W.cols != n || p.W.rows < 0) return MLQ_E_SHAPE;
+    if ((p.yq == nullptr) != (p.yd == nullptr)) return MLQ_E_NULL;
+    if (p.W.rows > 0 && (p.W.q == nullptr || p.W.d == nullptr || p.y == nullptr)) return MLQ_E_NULL;
+    if (!aligned(p.W.q, 16) || !aligned(p.W.d, 16) || !aligned(p.y, 4) || !aligned(p.yq, 16) ||
+        !aligned(p.yd, 16))
+      return MLQ_E_ALIGN;
+    any_yq = any_yq || p.yq != nullptr;
+    a.prod[j].wq = static_cast<const uint8_t *>(p.W.q);
+    a.prod[j].wd = p.W.d;
+    a.prod[j].y = p.y;
+    a.prod[j].rows = p.W.rows;
+    a.prod[j].yq = p.yq;
+    a.prod[j].yd = p.yd;
+  }
+  if (any_yq) {
+    for (int j = 0; j < nproducts; ++j)
+      if (products[j].W.rows % MLQ_QK != 0) return MLQ_E_SHAPE;
+  }
+  a.nproducts = nproducts;
+  a.x = in->x;
+  a.xq_in = in->xq;
+  a.xd_in = in->xd;
+  a.nb = n / MLQ_QK;
+  a.xq_out = in->xq_out;
+  a.xd_out = in->xd_out;
+  a.any_yq = any_yq ? 1 : 0;
+  a.nchunks = 1;
+  a.early = (flags & MLQ_F_STATIC_WEIGHTS) ? 1 : 0;
+  for (int i = 0; i < nprefetch; ++i) {
+    if (prefetch_bytes[i] > 0 && prefetch[i] == nullptr) return MLQ_E_NULL;
+    a.pf_ptr[a.npf] = prefetch[i];
+    a.pf_bytes[a.npf] = prefetch_bytes[i];
+    a.npf += prefetch_bytes[i] > 0 ? 1 : 0;
+  }
   mlq::LaunchCtx ctx;
   mlq_status s = make_ctx(&ctx, stream);
   if (s != MLQ_OK) return s;

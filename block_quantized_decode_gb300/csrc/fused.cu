@@ -491,14 +491,6 @@ static cudaError_t launch_fused_variant(const LaunchCtx &ctx, FusedArgs a) {
 
 template <int QT>
 static cudaError_t launch_fused_qt(const LaunchCtx &ctx, FusedArgs a) {
-  static const int mode = [] {  // MLQ_FUSED_KERNEL=ldg|smem overrides the choice (A/B timing)
-    const char *e = std::getenv("MLQ_FUSED_KERNEL");
-    return e == nullptr ? 0 : (e[0] == 'l' ? 1 : (e[0] == 's' ? 2 : 0));
-  }();
-  if (mode != 1) {
-    cudaError_t err = cudaSuccess;
-    if (try_launch_smem<QT>(ctx, a, &err)) return err;
-  }
   const int upr = QT == 1 ? a.nb : 2 * a.nb;
   if (upr <= 32) {
     a.nchunks = 1;
@@ -527,7 +519,48 @@ cudaError_t launch_matvec_fused(const LaunchCtx &ctx, int qtype, const FusedArgs
     return e != nullptr && e[0] == '1' ? 1 : 0;
   }();
   a.prefetch = pf;
-  return qtype == 1 ? launch_fused_qt<1>(ctx, a) : launch_fused_qt<0>(ctx, a);
+  // MLQ_FUSED_KERNEL=phase|smem|ldg picks the kernel for a float input
+  // without quantised outputs or L2 hints (A/B timing); the default is the
+  // shared-memory kernel above, the fastest of the three on such chains.
+  static const int mode = [] {
+    const char *e = std::getenv("MLQ_FUSED_KERNEL");
+    return e == nullptr ? 2 : (e[0] == 'l' ? 1 : (e[0] == 's' ? 2 : 0));
+  }();
+  const bool plain = a.x != nullptr && !a.any_yq && a.npf == 0;
+  if (!plain || mode == 0) {
+    const cudaError_t e = launch_phase(ctx, qtype, a);
+    if (e != cudaErrorNotSupported) return e;
+  }
+  // The phase kernel does not take this shape (or another kernel was
+  // asked for): the same results from other launches -- the products, then
+  // the quantised outputs, then the L2 hints.
+  cudaError_t e = cudaSuccess;
+  bool done = false;
+  if (plain && mode == 2 && a.total_rows > 0)
+    done = qtype == 1 ? try_launch_smem<1>(ctx, a, &e) : try_launch_smem<0>(ctx, a, &e);
+  if (!done && a.x != nullptr) {
+    e = qtype == 1 ? launch_fused_qt<1>(ctx, a) : launch_fused_qt<0>(ctx, a);
+  } else if (!done) {
+    for (int j = 0; j < a.nproducts && e == cudaSuccess; ++j) {
+      if (a.prod[j].rows > 0)
+        e = launch_matvec_m1(ctx, qtype, a.prod[j].wq, a.prod[j].wd, a.nb, a.xq_in, a.xd_in,
+                             a.prod[j].y, nullptr, 0, a.prod[j].rows);
+    }
+  }
+  for (int j = 0; j < a.nproducts && e == cudaSuccess; ++j) {
+    if (a.prod[j].yq != nullptr && a.prod[j].rows > 0)
+      e = launch_quantize_q8(ctx, a.prod[j].y, a.prod[j].yq, a.prod[j].yd, 1, a.prod[j].rows);
+  }
+  if (e == cudaSuccess && a.npf > 0) {
+    PrefetchList pl;
+    pl.n = 0;
+    for (int i = 0; i < a.npf && pl.n < kMaxPrefetchRanges; ++i) {
+      pl.ptr[pl.n] = a.pf_ptr[i];
+      pl.bytes[pl.n++] = a.pf_bytes[i];
+    }
+    e = launch_prefetch_l2(ctx, pl);
+  }
+  return e;
 }
 
 }  // namespace mlq

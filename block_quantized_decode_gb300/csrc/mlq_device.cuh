@@ -83,6 +83,21 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+// ---- per-thread asynchronous copies (cp.async, 16 bytes, L2 only) ----------
+// Unlike the bulk copies above, these progress while a kernel launched with
+// programmatic dependent launch has not yet passed griddep_wait(): measured
+// on GB300, bulk copies issued before the wait land only after the previous
+// grid has finished, 16-byte cp.async copies land at once.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the arrival counts against the count given at mbar_init).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Hint: bring [src, src + bytes) into L2.  src 16-byte aligned, bytes a
 // multiple of 16.  Never reads through L1, so it is safe before
 // griddep_wait() even if the previous kernel writes the same bytes.

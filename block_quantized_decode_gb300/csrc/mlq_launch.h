@@ -109,27 +109,46 @@ cudaError_t launch_decode_chain_static(const LaunchCtx &ctx, int device, int qty
 
 // fused.cu: quantise x and run up to kFusedMaxProducts products of its width.
 constexpr int kFusedMaxProducts = 8;
+constexpr int kPhaseMaxPrefetch = 16;
 struct FusedProduct {
   const uint8_t *wq;
   const float *wd;
   float *y;
   int rows;
+  int8_t *yq;   // optional Q8_0 copy of y, written in the same launch (rows % 32 == 0)
+  float *yd;
 };
 struct FusedArgs {
   FusedProduct prod[kFusedMaxProducts];
   int nproducts;
-  const float *x;
+  const float *x;         // float input, quantised in the prologue; or nullptr and ...
+  const int8_t *xq_in;    // ... the input already in Q8_0 (written by an earlier launch)
+  const float *xd_in;
   int nb;
   int8_t *xq_out;   // optional copy of the quantised x (written by CTA 0)
   float *xd_out;
+  int any_yq;       // some product quantises its output: rows are split in 32-row atoms there
   int total_rows;   // set by the launcher
   int nchunks;      // set by the launcher
+  int chunk_blocks; // set by the launcher (phase kernel: blocks of K per warp chunk)
+  unsigned smem_part, smem_w, smem_wd;  // set by the launcher (phase kernel: smem offsets)
   int early;        // first weight loads before the dependency wait (static weights)
+  int copy_post;    // set by the launcher (phase kernel): slice copied after the input is read
   int prefetch;     // set by the launcher: hint the CTA's weights into L2 first
   int *status;      // set by the launcher
   unsigned long long wait_ns;
+  // byte ranges to hint into L2 once the input has been read (phase kernel)
+  const void *pf_ptr[kPhaseMaxPrefetch];
+  size_t pf_bytes[kPhaseMaxPrefetch];
+  int npf;
 };
+// Every launch of a phase: the phase kernel when the CTA slices fit in
+// shared memory, else the streaming kernel of fused.cu (float input, no
+// quantised outputs) or, for the other cases, matvec + quantize launches.
 cudaError_t launch_matvec_fused(const LaunchCtx &ctx, int qtype, const FusedArgs &a);
+// phase.cu: the shared-memory phase kernel; returns cudaErrorNotSupported
+// without launching when the shape does not suit it.
+cudaError_t launch_phase(const LaunchCtx &ctx, int qtype, const FusedArgs &a);
 
 // gemm_mma.cu: M activation rows (2..16) against a Q4_0 matrix on the
 // tensor cores (fp16 mma.sync, exact block sums).

@@ -21,9 +21,10 @@ from . import binding as B
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("--op", default="matvec_q4",
-                   choices=["matvec_q4", "matvec_q8", "gemm_q4", "quantize", "fused"])
+                   choices=["matvec_q4", "matvec_q8", "gemm_q4", "quantize", "fused", "phase"])
     p.add_argument("--workload", default="tinyllama_layer",
-                   help="for --op fused: the workload whose phases run as mlq_matvec_fused calls")
+                   help="for --op fused / phase: the workload whose phases run as "
+                        "mlq_matvec_fused / mlq_decode_phase calls")
     p.add_argument("--rows", type=int, default=4096)
     p.add_argument("--cols", type=int, default=11008)
     p.add_argument("--m", type=int, default=1)
@@ -36,7 +37,7 @@ def main():
     dev = torch.device("cuda:0")
     torch.cuda.set_device(0)
     B.mlq_init()
-    if a.op == "fused":
+    if a.op in ("fused", "phase"):
         return fused_case(a)
     g = torch.Generator(device=dev)
     g.manual_seed(0)
@@ -106,23 +107,25 @@ def main():
 
 
 def fused_case(a):
-    """One pass of a workload as mlq_matvec_fused phases, per launch group."""
+    """One pass of a workload as mlq_matvec_fused (or mlq_decode_phase)
+    launches, one per phase."""
     from . import inputs as I
     from .runner import WorkloadRunner
     wl = I.WORKLOADS[a.workload]()
     copies = a.copies or 3
     r = WorkloadRunner(wl, copies=copies)
+    step = r.step_fused if a.op == "fused" else r.step_phase
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         for c in range(copies):
-            r.step_fused(copy=c)
+            step(copy=c)
     s.synchronize()
     graph = None
     if not a.no_graph:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=s):
             for i in range(a.iters):
-                r.step_fused(copy=i % copies)
+                step(copy=i % copies)
     times = []
     for _ in range(a.reps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -132,13 +135,13 @@ def fused_case(a):
                 graph.replay()
             else:
                 for i in range(a.iters):
-                    r.step_fused(copy=i % copies)
+                    step(copy=i % copies)
             e1.record(s)
         s.synchronize()
         times.append(e0.elapsed_time(e1) / a.iters * 1e3)
     assert B.mlq_last_device_error(s) == B.MLQ_OK
     us = min(times)
-    print(json.dumps({"op": "fused", "workload": wl.name, "copies": copies, "us_per_step": us,
+    print(json.dumps({"op": a.op, "workload": wl.name, "copies": copies, "us_per_step": us,
                       "bytes_per_step": r.weight_bytes(), "GBps": r.weight_bytes() / (us * 1e-6) / 1e9}))
 
 

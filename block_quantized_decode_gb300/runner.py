@@ -118,6 +118,67 @@ class WorkloadRunner:
         for c in self.fused_calls(copy, static_weights):
             c(stream)
 
+    def phase_weight_ranges(self, k: int, copy: int):
+        """(tensor, bytes) of every weight array of phase k, copy `copy`."""
+        _, first, count = self.chain_phases()[k]
+        out = []
+        for m in self.mats[first:first + count]:
+            out += [(m.q[copy], m.host_q.nbytes), (m.d[copy], m.host_d.nbytes)]
+        return out
+
+    def phase_calls(self, copy: int = 0, static_weights: bool = True, prefetch: str = "ahead2"):
+        """One mlq_decode_phase call per phase.  A product whose output is
+        the input of a later phase also writes it in Q8_0 (into that input's
+        buffer), so the later phase starts from quantised bytes; the
+        workload's float inputs are quantised by the phase that reads them.
+        prefetch: "ahead1" / "ahead2" -- each phase hints the weights of the
+        phase one / two later into L2 (past the last phase: the next pass,
+        next weight copy); "self" -- the same phase's next copy (back-to-back
+        timing of one phase); "none"."""
+        key = ("phase", copy, static_weights, prefetch)
+        if key not in self._chain_calls:
+            if self.m != 1:
+                raise ValueError("decode phases are M = 1")
+            phases = self.chain_phases()
+            pre = set()   # sources whose producer quantises them
+            for src, first, count in phases:
+                group = self.mats[first:first + count]
+                if all(m.spec.rows % I.QK == 0 for m in group):
+                    pre.update(m.spec.name for m in group if m.spec.name in self.sources)
+            flags = B.MLQ_F_STATIC_WEIGHTS if static_weights else 0
+            calls = []
+            nph = len(phases)
+            for k, (src, first, count) in enumerate(phases):
+                pf = ()
+                if prefetch in ("ahead1", "ahead2"):
+                    kk = k + (1 if prefetch == "ahead1" else 2)
+                    pf = self.phase_weight_ranges(kk % nph, (copy + kk // nph) % self.copies)
+                elif prefetch == "self":
+                    pf = self.phase_weight_ranges(k, (copy + 1) % self.copies)
+                elif prefetch != "none":
+                    raise ValueError(f"prefetch {prefetch!r}")
+                pr = []
+                for m in self.mats[first:first + count]:
+                    out = self.qbuf[m.spec.name] if m.spec.name in pre else None
+                    pr.append(B.PhaseProduct(
+                        B.QTensor(m.q[copy], m.d[copy], m.spec.rows, m.spec.cols, m.spec.wtype),
+                        m.y, out.q if out else None, out.d if out else None))
+                qa = self.qbuf[src]
+                if src in pre:
+                    calls.append(B.PhaseCall(self.sources[src], pr, xq=qa.q, xd=qa.d, flags=flags,
+                                             prefetch=pf))
+                else:
+                    calls.append(B.PhaseCall(self.sources[src], pr, x=self.fp32[src],
+                                             xq_out=qa.q, xd_out=qa.d, flags=flags, prefetch=pf))
+            self._chain_calls[key] = calls
+        return self._chain_calls[key]
+
+    def step_phase(self, copy: int = 0, stream=None, static_weights: bool = True,
+                   prefetch: str = "ahead2") -> None:
+        """One pass as one mlq_decode_phase launch per phase."""
+        for c in self.phase_calls(copy, static_weights, prefetch):
+            c(stream)
+
     def step_chain(self, copy: int = 0, stream=None) -> None:
         """One pass as a single mlq_decode_chain launch."""
         self.chain_call(copy)(stream)

@@ -223,6 +223,62 @@ mlq_status mlq_matvec_fused(const float *x, int n, const mlq_chain_product *prod
                             int nproducts, int8_t *xq_out, float *xd_out, unsigned flags,
                             void *stream);
 
+/* One product of mlq_decode_phase: y = W * (the phase input), and, when yq
+ * is not NULL, y quantised to Q8_0 in the same launch (yq: W.rows int8,
+ * yd: W.rows/32 floats, both 16-byte aligned, W.rows a multiple of 32),
+ * bytes identical to mlq_quantize_q8 applied to the stored y. */
+typedef struct {
+    mlq_qtensor W;
+    float *y;
+    int8_t *yq;
+    float *yd;
+} mlq_phase_product;
+
+/* The input of mlq_decode_phase: either float x (xq, xd NULL), quantised
+ * in the launch exactly as mlq_quantize_q8 does -- xq_out / xd_out (both
+ * NULL, or n bytes and n/32 floats) then receive that quantisation -- or,
+ * with x NULL, an input already in Q8_0 (xq: n int8, xd: n/32 floats),
+ * typically the yq / yd of a product of the previous phase; xq_out / xd_out
+ * must be NULL then.  All pointers device, 16-byte aligned. */
+typedef struct {
+    const float *x;
+    const int8_t *xq;
+    const float *xd;
+    int n;
+    int8_t *xq_out;
+    float *xd_out;
+} mlq_phase_input;
+
+/* One decode phase of the Design Spec's forward pass (Sec. 6: a quantised
+ * activation feeds one or more products -- Wq|Wk|Wv, gate|up -- and a
+ * product's output is quantised as the next product's input) in ONE launch:
+ * for each of the nproducts products (1..MLQ_FUSED_MAX_PRODUCTS, all of one
+ * type, W.cols == n, n a positive multiple of 32 and at most MLQ_MAX_COLS)
+ * y[r] for every r < W.rows, within the tolerance of mlq_matvec_q4/_q8, and
+ * each requested Q8_0 copy of y.  If any product has yq, every product's
+ * W.rows must be a multiple of 32 (MLQ_E_SHAPE otherwise).  Outputs must
+ * not overlap the input or each other.  flags: 0 or MLQ_F_STATIC_WEIGHTS
+ * (as for mlq_matvec_fused).  A chain of such calls, each taking the
+ * previous one's yq / yd, runs a decode step with no separate quantize
+ * launches: each phase quantises its outputs while they are still on chip.
+ * prefetch / prefetch_bytes (host arrays of nprefetch <= MLQ_PHASE_MAX_PREFETCH
+ * device ranges, read during the call; NULL when nprefetch == 0): a pure
+ * hint, typically the weights of the phase after next.  Once the launch has
+ * read its own input, its CTAs hint those ranges into L2, so that a chain
+ * streams the next weights from HBM while its phases run, behind no
+ * critical-path read (an SM serves its reads in order: a prefetch issued
+ * earlier would delay them).  Unaligned range ends are trimmed to 16 bytes.
+ * When a CTA's share of the weights does not fit in shared memory the call
+ * queues the same work as several launches (products, then quantize, then
+ * the prefetch).
+ * No counterpart on the pages: a GPU fusion of their quantize_q8 and
+ * matvec calls. */
+#define MLQ_PHASE_MAX_PREFETCH 16
+mlq_status mlq_decode_phase(const mlq_phase_input *in, const mlq_phase_product *products,
+                            int nproducts, const void *const *prefetch,
+                            const size_t *prefetch_bytes, int nprefetch, unsigned flags,
+                            void *stream);
+
 /* Bytes of workspace mlq_decode_chain needs for `nphases` phases. */
 size_t mlq_chain_workspace_bytes(int nphases);
 

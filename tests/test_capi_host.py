@@ -136,6 +136,10 @@ def _cuda_available():
 
 @pytest.mark.skipif(_cuda_available(), reason="checks the no-device path")
 def test_valid_call_without_device_is_arch_error(M):
+    # the fake addresses above must never reach a real device
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
     assert M.binding.raw_call("mlq_init") == M.MLQ_E_ARCH
     assert mv(M) == M.MLQ_E_ARCH
 
@@ -201,3 +205,43 @@ def test_validation_fused(M):
     assert run([good], xq=8 * A) == M.MLQ_E_NULL
     assert run([R(qt(cols=256), 5 * A + 1)]) == M.MLQ_E_ALIGN
     assert run([good], flags=2) == M.MLQ_E_SHAPE
+
+
+def test_validation_phase(M):
+    from block_quantized_decode_gb300.binding import _PhaseInput, _PhaseProduct
+    R = _PhaseProduct
+
+    def run(prods, x=6 * A, xq=None, xd=None, n=256, xq_out=None, xd_out=None, flags=0,
+            inp=True, pf=None, pfb=None, npf=0):
+        ra = (R * max(1, len(prods)))(*prods)
+        pin = ctypes.byref(_PhaseInput(x, xq, xd, n, xq_out, xd_out)) if inp else None
+        return call(M, "mlq_decode_phase", pin, ra, len(prods), pf, pfb, npf, flags, None)
+
+    good = R(qt(cols=256), 5 * A, None, None)
+    quant = R(qt(cols=256, rows=64), 5 * A, 9 * A, 10 * A)
+    assert run([good], inp=False) == M.MLQ_E_NULL
+    assert run([good], x=None) == M.MLQ_E_NULL                        # no input at all
+    assert run([good], x=None, xq=8 * A) == M.MLQ_E_NULL              # xq without xd
+    assert run([good], xq=8 * A, xd=11 * A) == M.MLQ_E_SHAPE          # two inputs
+    assert run([good], x=None, xq=8 * A, xd=11 * A, xq_out=12 * A, xd_out=13 * A) == M.MLQ_E_SHAPE
+    assert run([good], xq_out=12 * A) == M.MLQ_E_NULL
+    assert run([]) == M.MLQ_E_SHAPE
+    assert run([good] * 9) == M.MLQ_E_SHAPE
+    assert run([good], n=250) == M.MLQ_E_SHAPE
+    assert run([R(qt(cols=128), 5 * A, None, None)]) == M.MLQ_E_SHAPE
+    assert run([good, R(qt(cols=256, t=0), 5 * A, None, None)]) == M.MLQ_E_TYPE
+    assert run([good], x=6 * A + 4) == M.MLQ_E_ALIGN
+    assert run([good], x=None, xq=8 * A + 8, xd=11 * A) == M.MLQ_E_ALIGN
+    assert run([R(qt(cols=256), 5 * A, 9 * A, None)]) == M.MLQ_E_NULL  # yq without yd
+    assert run([R(qt(cols=256), 5 * A, 9 * A + 4, 10 * A)]) == M.MLQ_E_ALIGN
+    assert run([quant, R(qt(cols=256, rows=40), 5 * A, None, None)]) == M.MLQ_E_SHAPE  # 40 % 32
+    assert run([R(qt(cols=256, rows=33), 5 * A, 9 * A, 10 * A)]) == M.MLQ_E_SHAPE
+    assert run([good], flags=2) == M.MLQ_E_SHAPE
+    ptrs = (ctypes.c_void_p * 17)(*([12 * A] * 17))
+    sizes = (ctypes.c_size_t * 17)(*([4096] * 17))
+    assert run([good], pf=ptrs, pfb=sizes, npf=17) == M.MLQ_E_SHAPE   # > MLQ_PHASE_MAX_PREFETCH
+    assert run([good], pf=ptrs, pfb=sizes, npf=-1) == M.MLQ_E_SHAPE
+    assert run([good], pf=None, pfb=sizes, npf=2) == M.MLQ_E_NULL
+    assert run([good], pf=ptrs, pfb=None, npf=2) == M.MLQ_E_NULL
+    nul = (ctypes.c_void_p * 2)(12 * A, None)
+    assert run([good], pf=nul, pfb=sizes, npf=2) == M.MLQ_E_NULL      # bytes > 0 at NULL

@@ -37,10 +37,13 @@ from block_quantized_decode_gb300.runner import WorkloadRunner  # noqa: E402
 
 
 def run_and_check(wl, full_rows_limit=300_000_000, graph=False, chain=False, fused=False,
-                  static_weights=True):
+                  static_weights=True, phase=False):
     r = WorkloadRunner(wl, copies=1)
     if chain:
         step = r.step_chain
+    elif phase:
+        def step():
+            r.step_phase(static_weights=static_weights)
     elif fused:
         def step():
             r.step_fused(static_weights=static_weights)
