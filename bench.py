@@ -57,10 +57,10 @@ def parse_args():
                    help="phase: one mlq_decode_phase launch per phase, each phase writing "
                         "the next one's input already quantised; fused: one mlq_matvec_fused "
                         "launch per phase (float inputs); chain: one mlq_decode_chain launch "
-                        "per step; calls: one C-ABI call per quantize and product; auto: fused "
+                        "per step; calls: one C-ABI call per quantize and product; auto: phase "
                         "for M = 1 steps under 64 MB of weights (latency-bound, fewer launches "
                         "win), else calls")
-    p.add_argument("--phase-prefetch", choices=["none", "ahead1", "ahead2"], default="ahead2",
+    p.add_argument("--phase-prefetch", choices=["none", "ahead1", "ahead2"], default="none",
                    help="phase path: each phase hints the weights of the phase one / two "
                         "later into L2 once it has read its input")
     p.add_argument("--prefetch", choices=["none", "all", "next"], default="none",
@@ -315,7 +315,7 @@ def run_ours(args, wl, world, rank, local, pg):
     if pf == "none":
         pf = None
     path = args.path if args.path != "auto" else (
-        "fused" if r.m == 1 and wbytes < 64 * 2 ** 20 else "calls")
+        "phase" if r.m == 1 and wbytes < 64 * 2 ** 20 else "calls")
 
     def one_pass(c):
         if path == "chain":
@@ -477,8 +477,7 @@ def run_ours(args, wl, world, rank, local, pg):
         ach = tot_bytes / tot_s / 1e9
         qt = "Q4_0" if r.mats[0].spec.wtype == I.Q4_0 else "Q8_0"
         nph = len(per_phase)
-        kname, ksrc = (("matvec_fused_smem_kernel", "fused.cu") if path == "fused" else
-                       ("phase_kernel", "phase.cu"))
+        kname, ksrc = "phase_kernel", "phase.cu"
         roofline = {"kernel": f"{kname}<{qt}>", "bound": "hbm", "achieved": ach,
                     "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_source": peak_src,
                     "traffic": ncu_traffic(f"{path}_{wl.name}", (ksrc, "mlq_device.cuh"),

@@ -284,7 +284,8 @@ __global__ void __launch_bounds__(kChainThreads, 1) decode_chain_kernel(const __
       for_each_chunk(a, p, rows_per_chunk<QT>(a, nb), [&](int j, int r, int n) {
         if (stop) return;
         const int slot = use % a.ns;
-        if (!chain_wait(smem_addr(&full_bar[slot]), (use / a.ns) & 1, abort_v, a.wait_ns)) {
+        if (!warp_wait([&] { return chain_wait(smem_addr(&full_bar[slot]), (use / a.ns) & 1, abort_v,
+                                               a.wait_ns); })) {
           if (!*abort_v) set_status(a.status, kStatusTimeout);
           *abort_v = 1;
           stop = true;

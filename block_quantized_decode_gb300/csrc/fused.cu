@@ -1,22 +1,25 @@
-// fused.cu -- one decode "phase" in one launch: quantise a float32 vector
-// to Q8_0 and multiply it with one or more weight matrices of that width
-// (e.g. Wq|Wk|Wv, or gate|up).  Definitions: page "Legacy-ISA ML Inference
-// Runtime -- Design Spec", Sec. 4 (formats, block dot), Sec. 5 (quantize_q8
-// rounding, matvec), Sec. 6 "Forward pass" (a quantised activation feeds
-// several products).
+// fused.cu -- one decode "phase" in one launch, streaming variant: quantise
+// a float32 vector to Q8_0 and multiply it with one or more weight matrices
+// of that width (e.g. Wq|Wk|Wv, or gate|up).  Definitions: page "Legacy-ISA
+// ML Inference Runtime -- Design Spec", Sec. 4 (formats, block dot), Sec. 5
+// (quantize_q8 rounding, matvec), Sec. 6 "Forward pass" (a quantised
+// activation feeds several products).
 //
-// Designed for chains of dependent launches with programmatic dependent
-// launch (PDL):
+// launch_matvec_fused() (end of file) is the dispatcher of every phase
+// launch: the shared-memory phase kernel of phase.cu wherever a CTA's share
+// of the weights fits on chip, else the streaming kernel below (float input,
+// no quantised outputs), else separate matvec / quantize launches.
+//
+// The streaming kernel, for chains of dependent launches (PDL):
 //  * one CTA of 16 warps per SM, at most 64 registers per thread, so the
 //    next phase's CTA fits on the same SM while this one runs;
-//  * before waiting for the previous kernel, the CTA hints its whole weight
-//    range into L2 (cp.async.bulk.prefetch.L2: safe, L2 is the point of
-//    coherence) -- the next phase's weights thus stream from HBM while this
-//    phase computes, and its own loads mostly hit L2;
-//  * after the wait it releases its dependants at once, quantises x into
-//    shared memory (same element arithmetic as quantize.cu: identical
-//    bytes), and streams its rows with 128-bit evict-first loads, one task =
-//    (row, K-chunk of 32*U 16-byte units) per warp, software-pipelined;
+//  * with static weights the first weight loads of each warp are issued
+//    before the wait on the previous kernel; with MLQ_FUSED_L2_PREFETCH=1
+//    the CTA also hints its whole weight range into L2 first;
+//  * after the wait it quantises x into shared memory (same element
+//    arithmetic as quantize.cu: identical bytes), and streams its rows with
+//    128-bit evict-first loads, one task = (row, K-chunk of 32*U 16-byte
+//    units) per warp, software-pipelined;
 //  * block dot: dp4a; Q4_0 -8 folded via sum(qx) per block; Q8_0 halves
 //    joined with one shuffle; fixed-order reductions (deterministic).
 #include <cstdlib>
@@ -267,201 +270,6 @@ __global__ void __launch_bounds__(kFusedThreads, 2) matvec_fused_kernel(const __
   }
 }
 
-// ---------------------------------------------------------------------------
-// Shared-memory variant: when a CTA's whole weight slice fits in shared
-// memory (every TinyLlama-sized phase does), the CTA bulk-copies the slice
-// in up to kPieces pieces, each completing on its own mbarrier, and reduces
-// rows straight from shared memory as the pieces land.  With static weights
-// (the caller promises that no earlier queued work writes them) the copies
-// are issued BEFORE the wait on the previous kernel, so under programmatic
-// dependent launch this phase's weights stream in while the previous phase
-// is still running; otherwise the slice is only hinted into L2 before the
-// wait and copied after it.
-// ---------------------------------------------------------------------------
-constexpr int kPieces = 16;
-constexpr size_t kSliceBudget = 100 * 1024;  // x + slice: two CTAs must fit on one SM
-
-__device__ __forceinline__ size_t x_bytes(int nb) {
-  return (static_cast<size_t>(nb) * kQK + 8 * static_cast<size_t>(nb) + 127) / 128 * 128;
-}
-
-// Visit the CTA's pieces: f(product, first local row, rows, byte offset in the slice).
-template <int QT, typename F>
-__device__ __forceinline__ void for_each_piece(const FusedArgs &a, int ra, int rb, F &&f) {
-  const int nr = rb - ra;
-  const int rpp = nr > 0 ? (nr + kPieces / 2 - 1) / (kPieces / 2) : 1;
-  const size_t rowbytes = static_cast<size_t>(a.nb) * ((QT == 1 ? 16 : 32) + 4);
-  int off = 0, p = 0;
-  size_t boff = 0;
-  for (int j = 0; j < a.nproducts; ++j) {
-    const int lo = max(ra, off) - off, hi = min(rb, off + a.prod[j].rows) - off;
-    for (int r = lo; r < hi; r += rpp) {
-      const int n = min(rpp, hi - r);
-      f(p, j, r, n, boff);
-      boff += static_cast<size_t>(n) * rowbytes;
-      ++p;
-    }
-    off += a.prod[j].rows;
-  }
-}
-
-// Lane `lane` of the calling warp issues the copies of every piece p with
-// p % 32 == lane, so the pieces are issued in parallel.
-template <int QT>
-__device__ __forceinline__ void issue_slice(const FusedArgs &a, int ra, int rb, uint8_t *wbuf,
-                                            uint64_t *bars, int lane) {
-  const size_t rowq = static_cast<size_t>(a.nb) * (QT == 1 ? 16 : 32);
-  for_each_piece<QT>(a, ra, rb, [&](int p, int j, int r, int n, size_t boff) {
-    if ((p & 31) != lane) return;
-    const uint32_t qb = static_cast<uint32_t>(n * rowq);
-    const uint32_t db = static_cast<uint32_t>(n) * a.nb * 4;
-    const uint32_t bar = smem_addr(&bars[p]);
-    mbar_arrive_expect_tx(bar, qb + db);
-    bulk_copy_g2s(smem_addr(wbuf + boff), a.prod[j].wq + static_cast<size_t>(r) * rowq, qb, bar);
-    bulk_copy_g2s(smem_addr(wbuf + boff + qb), a.prod[j].wd + static_cast<size_t>(r) * a.nb, db, bar);
-  });
-}
-
-template <int QT>
-__device__ __forceinline__ float smem_row_dot(const uint8_t *wrow, const float *drow,
-                                              const int8_t *xq_s, const float *xd_s,
-                                              const int *sx_s, int nb, int lane) {
-  float acc = 0.0f;
-  if (QT == 1) {
-#pragma unroll 2
-    for (int u = lane; u < nb; u += 32) {
-      const uint4 w = *reinterpret_cast<const uint4 *>(wrow + u * 16);
-      const int4 xa = *reinterpret_cast<const int4 *>(xq_s + fused_half_offset(u, 0));
-      const int4 xb = *reinterpret_cast<const int4 *>(xq_s + fused_half_offset(u, 1));
-      constexpr uint32_t kLo = 0x0F0F0F0Fu;
-      int s = __dp4a(static_cast<int>(w.x & kLo), xa.x, 0);
-      s = __dp4a(static_cast<int>(w.y & kLo), xa.y, s);
-      s = __dp4a(static_cast<int>(w.z & kLo), xa.z, s);
-      s = __dp4a(static_cast<int>(w.w & kLo), xa.w, s);
-      s = __dp4a(static_cast<int>((w.x >> 4) & kLo), xb.x, s);
-      s = __dp4a(static_cast<int>((w.y >> 4) & kLo), xb.y, s);
-      s = __dp4a(static_cast<int>((w.z >> 4) & kLo), xb.z, s);
-      s = __dp4a(static_cast<int>((w.w >> 4) & kLo), xb.w, s);
-      s -= 8 * sx_s[u];
-      acc = __fmaf_rn(__fmul_rn(__int2float_rn(s), drow[u]), xd_s[u], acc);
-    }
-  } else {
-    const int upr = 2 * nb;
-    const int iters = (upr + 31) >> 5;
-#pragma unroll 2
-    for (int k = 0; k < iters; ++k) {
-      const int h = lane + 32 * k;
-      const bool valid = h < upr;
-      int s = 0;
-      if (valid) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(wrow + h * 16);
-        const int4 xa = *reinterpret_cast<const int4 *>(xq_s + h * 16);
-        s = __dp4a(static_cast<int>(w.x), xa.x, 0);
-        s = __dp4a(static_cast<int>(w.y), xa.y, s);
-        s = __dp4a(static_cast<int>(w.z), xa.z, s);
-        s = __dp4a(static_cast<int>(w.w), xa.w, s);
-      }
-      s += __shfl_xor_sync(0xffffffffu, s, 1);
-      if (valid && !(lane & 1)) acc = __fmaf_rn(__fmul_rn(__int2float_rn(s), drow[h >> 1]), xd_s[h >> 1], acc);
-    }
-  }
-  return warp_sum(acc);
-}
-
-template <int QT>
-__global__ void __launch_bounds__(kFusedThreads, 2) matvec_fused_smem_kernel(const __grid_constant__ FusedArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bars[kPieces];
-  __shared__ int abort_flag;
-  const int nb = a.nb;
-  const int K = nb * kQK;
-  int8_t *xq_s = reinterpret_cast<int8_t *>(smem);
-  float *xd_s = reinterpret_cast<float *>(smem + K);
-  int *sx_s = reinterpret_cast<int *>(smem + K + 4 * nb);
-  uint8_t *wbuf = smem + x_bytes(nb);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = a.total_rows;
-  const int ra = static_cast<int>(static_cast<long long>(n) * blockIdx.x / gridDim.x);
-  const int rb = static_cast<int>(static_cast<long long>(n) * (blockIdx.x + 1) / gridDim.x);
-  const size_t rowq = static_cast<size_t>(nb) * (QT == 1 ? 16 : 32);
-
-  if (tid == 0) {
-    for (int p = 0; p < kPieces; ++p) mbar_init(smem_addr(&bars[p]), 1);
-    abort_flag = 0;
-    fence_mbar_init();
-  }
-  __syncwarp();
-  if (warp == 0 && a.early) {
-    issue_slice<QT>(a, ra, rb, wbuf, bars, lane);  // static weights: stream before the wait
-  }
-  if (tid == 0) {
-    if (!a.early) {
-      for_each_piece<QT>(a, ra, rb, [&](int, int j, int r, int cnt, size_t) {
-        prefetch_range_l2(a.prod[j].wq + static_cast<size_t>(r) * rowq, static_cast<size_t>(cnt) * rowq,
-                          static_cast<size_t>(1) << 30);
-        prefetch_range_l2(a.prod[j].wd + static_cast<size_t>(r) * nb, static_cast<size_t>(cnt) * nb * 4,
-                          static_cast<size_t>(1) << 30);
-      });
-    }
-  }
-  // Let the next phase's kernel be scheduled now: it still waits for this
-  // grid to complete before it reads anything, and it can stream its own
-  // (static) weights meanwhile.
-  griddep_launch_dependents();
-  griddep_wait();  // x (and, without static weights, W) may come from the previous kernel
-  if (warp == 0 && !a.early) issue_slice<QT>(a, ra, rb, wbuf, bars, lane);
-  fused_quantize<QT>(a, xq_s, xd_s, sx_s, tid);
-  __syncthreads();
-
-  bool ok = true;
-  int row_base = 0;  // index in the CTA's slice of the piece's first row
-  for_each_piece<QT>(a, ra, rb, [&](int p, int j, int r, int cnt, size_t boff) {
-    const int first = (warp - row_base % kFusedWarps + kFusedWarps) % kFusedWarps;
-    row_base += cnt;
-    if (!ok || first >= cnt) return;  // none of this piece's rows is ours
-    if (!mbar_wait_bounded(smem_addr(&bars[p]), 0, a.wait_ns)) {
-      ok = false;
-      if (atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
-      return;
-    }
-    const uint8_t *sq = wbuf + boff;
-    const float *sd = reinterpret_cast<const float *>(sq + static_cast<size_t>(cnt) * rowq);
-    float *y = a.prod[j].y + r;
-    for (int i = first; i < cnt; i += kFusedWarps) {
-      const float v = smem_row_dot<QT>(sq + static_cast<size_t>(i) * rowq, sd + static_cast<size_t>(i) * nb,
-                                       xq_s, xd_s, sx_s, nb, lane);
-      if (lane == 0) y[i] = v;
-    }
-  });
-  __syncthreads();
-  if (tid == 0 && abort_flag) {  // our copies may still be landing: wait for them (bounded)
-    for_each_piece<QT>(a, ra, rb, [&](int p, int, int, int, size_t) {
-      mbar_wait_bounded(smem_addr(&bars[p]), 0, kDrainWaitNs);
-    });
-  }
-}
-
-template <int QT>
-static bool try_launch_smem(const LaunchCtx &ctx, const FusedArgs &a, cudaError_t *err) {
-  if (a.nb % 4 != 0 || a.total_rows <= 0) return false;
-  const long long grid = ctx.num_sms < a.total_rows ? ctx.num_sms : a.total_rows;
-  const long long rows_max = (a.total_rows + grid - 1) / grid;
-  const size_t rowbytes = static_cast<size_t>(a.nb) * ((QT == 1 ? 16 : 32) + 4);
-  const size_t xb = (static_cast<size_t>(a.nb) * kQK + 8 * static_cast<size_t>(a.nb) + 127) / 128 * 128;
-  const size_t smem = xb + static_cast<size_t>(rows_max) * rowbytes;
-  if (smem > kSliceBudget) return false;
-  // a piece's transaction count must stay below the mbarrier limit
-  if (((rows_max + kPieces / 2 - 1) / (kPieces / 2)) * rowbytes >= (1u << 20)) return false;
-  auto kern = matvec_fused_smem_kernel<QT>;
-  prefer_max_shared(kern);
-  if (smem > 48 * 1024) {
-    *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (*err != cudaSuccess) return true;
-  }
-  *err = launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kFusedThreads), smem, ctx, a);
-  return true;
-}
-
 template <int QT, int U>
 static cudaError_t launch_fused_variant(const LaunchCtx &ctx, FusedArgs a) {
   auto kern = matvec_fused_kernel<QT, U>;
@@ -519,28 +327,25 @@ cudaError_t launch_matvec_fused(const LaunchCtx &ctx, int qtype, const FusedArgs
     return e != nullptr && e[0] == '1' ? 1 : 0;
   }();
   a.prefetch = pf;
-  // MLQ_FUSED_KERNEL=phase|smem|ldg picks the kernel for a float input
-  // without quantised outputs or L2 hints (A/B timing); the default is the
-  // shared-memory kernel above, the fastest of the three on such chains.
+  // MLQ_FUSED_KERNEL=phase|ldg picks the kernel for a float input without
+  // quantised outputs or L2 hints (A/B timing); the default is the phase
+  // kernel (phase.cu) wherever the CTA slices fit in shared memory.
   static const int mode = [] {
     const char *e = std::getenv("MLQ_FUSED_KERNEL");
-    return e == nullptr ? 2 : (e[0] == 'l' ? 1 : (e[0] == 's' ? 2 : 0));
+    return e != nullptr && e[0] == 'l' ? 1 : 0;
   }();
   const bool plain = a.x != nullptr && !a.any_yq && a.npf == 0;
   if (!plain || mode == 0) {
     const cudaError_t e = launch_phase(ctx, qtype, a);
     if (e != cudaErrorNotSupported) return e;
   }
-  // The phase kernel does not take this shape (or another kernel was
+  // The phase kernel does not take this shape (or the streaming kernel was
   // asked for): the same results from other launches -- the products, then
   // the quantised outputs, then the L2 hints.
   cudaError_t e = cudaSuccess;
-  bool done = false;
-  if (plain && mode == 2 && a.total_rows > 0)
-    done = qtype == 1 ? try_launch_smem<1>(ctx, a, &e) : try_launch_smem<0>(ctx, a, &e);
-  if (!done && a.x != nullptr) {
+  if (a.x != nullptr) {
     e = qtype == 1 ? launch_fused_qt<1>(ctx, a) : launch_fused_qt<0>(ctx, a);
-  } else if (!done) {
+  } else {
     for (int j = 0; j < a.nproducts && e == cudaSuccess; ++j) {
       if (a.prod[j].rows > 0)
         e = launch_matvec_m1(ctx, qtype, a.prod[j].wq, a.prod[j].wd, a.nb, a.xq_in, a.xd_in,

@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(kWarps * 32) matvec_m1_kernel(const MatvecArgs
     load_task<QT, U>(cur, a, ra + rl, (t - rl * nch) * 32 * U, lane, upr);
   }
 
-  bool ok = mbar_wait_bounded(bar, 0, a.wait_ns);
+  bool ok = mbar_wait_warp(bar, 0, a.wait_ns);
   ok = __syncthreads_and(ok) != 0;
   if (!ok) {
     if (tid == 0) set_status(a.status, kStatusTimeout);

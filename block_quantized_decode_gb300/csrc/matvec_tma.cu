@@ -168,7 +168,7 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1)
     // ------------------------------ consumers ------------------------------
     const int g = warp / a.S;
     const int s = warp - g * a.S;
-    bool ok = wait_or_abort(smem_addr(&x_bar), 0, abort_v, a.wait_ns);
+    bool ok = warp_wait([&] { return wait_or_abort(smem_addr(&x_bar), 0, abort_v, a.wait_ns); });
     XRegs<BL> xr;
     int unit[BL];
 #pragma unroll
@@ -204,7 +204,8 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1)
     }
     for (int st = 0; ok && st < nstages; ++st) {
       const int slot = st % a.ns;
-      if (!wait_or_abort(smem_addr(&full_bar[slot]), (st / a.ns) & 1, abort_v, a.wait_ns)) {
+      if (!warp_wait([&] { return wait_or_abort(smem_addr(&full_bar[slot]), (st / a.ns) & 1, abort_v,
+                                                a.wait_ns); })) {
         if (!*abort_v) set_status(a.status, kStatusTimeout);
         *abort_v = 1;
         break;

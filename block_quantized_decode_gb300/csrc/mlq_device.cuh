@@ -72,6 +72,24 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// The calling warp waits as one: lane 0 runs `wait` (a bounded wait), the
+// other lanes wait at __syncwarp, which also orders the data the barrier
+// guards for them after lane 0's acquire.  All 32 lanes must call it.  One
+// poller per warp, not 32: every try_wait of every lane is an operation on
+// the same barrier word, and measured on GB300 they queue -- with 512
+// threads checking a few already-completed barriers, about 400 cycles each.
+template <typename W>
+__device__ __forceinline__ bool warp_wait(W &&wait) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait() ? 1 : 0;
+  __syncwarp();
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
+                                               unsigned long long limit_ns) {
+  return warp_wait([&] { return mbar_wait_bounded(bar, parity, limit_ns); });
+}
+
 // ---- bulk asynchronous copies (TMA, non-tensor) -----------------------------
 // Global -> shared, completion counted in bytes on `bar`.  dst, src 16-byte
 // aligned, bytes a multiple of 16.
@@ -83,21 +101,6 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
-// ---- per-thread asynchronous copies (cp.async, 16 bytes, L2 only) ----------
-// Unlike the bulk copies above, these progress while a kernel launched with
-// programmatic dependent launch has not yet passed griddep_wait(): measured
-// on GB300, bulk copies issued before the wait land only after the previous
-// grid has finished, 16-byte cp.async copies land at once.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-// Arrive on `bar` once every cp.async this thread issued so far has landed
-// (the arrival counts against the count given at mbar_init).
-__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 // Hint: bring [src, src + bytes) into L2.  src 16-byte aligned, bytes a
 // multiple of 16.  Never reads through L1, so it is safe before
 // griddep_wait() even if the previous kernel writes the same bytes.

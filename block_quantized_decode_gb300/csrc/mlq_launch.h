@@ -133,7 +133,6 @@ struct FusedArgs {
   int chunk_blocks; // set by the launcher (phase kernel: blocks of K per warp chunk)
   unsigned smem_part, smem_w, smem_wd;  // set by the launcher (phase kernel: smem offsets)
   int early;        // first weight loads before the dependency wait (static weights)
-  int copy_post;    // set by the launcher (phase kernel): slice copied after the input is read
   int prefetch;     // set by the launcher: hint the CTA's weights into L2 first
   int *status;      // set by the launcher
   unsigned long long wait_ns;

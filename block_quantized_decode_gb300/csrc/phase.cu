@@ -6,20 +6,18 @@
 // "Forward pass" (one quantised activation feeds several products, and each
 // product's output is quantised again as the next product's input).
 //
-// Design, per CTA (one per SM, 8 warps, <= 64 registers: four phases of a
-// chain fit on one SM at once):
-//  * the CTA owns a slice of rows, held whole in shared memory; every
-//    thread copies it 16 bytes at a time (cp.async), in up to 16 pieces that
-//    each complete on their own mbarrier.  With static weights the copies
-//    are issued BEFORE the wait on the previous kernel, so the weights of the
-//    next phases stream from HBM while this one computes (1-D bulk copies
-//    would not: issued before the wait, they land only after the previous
-//    grid has finished);
+// Design, per CTA (one per SM, 16 warps, <= 64 registers: the next phase's
+// CTA fits on the same SM while this one runs):
+//  * the CTA owns a slice of rows, held whole in shared memory, copied by
+//    1-D bulk copies in up to 16 pieces that each complete on their own
+//    mbarrier.  With static weights the copies are issued BEFORE the wait
+//    on the previous kernel, so the weights of the next phases stream from
+//    HBM while this one computes;
 //  * the input is either float x (quantised in the prologue by the whole
 //    CTA, same element arithmetic as quantize.cu) or already Q8_0 -- the
-//    previous phase wrote it -- and then one bulk copy per CTA brings it to
-//    shared memory (every CTA reads the same few L2 lines: one request
-//    stream per CTA, not one per warp);
+//    previous phase wrote it -- and then the CTA loads it once into shared
+//    memory (every CTA reads the same few L2 lines: one request per line
+//    and CTA, not one per warp);
 //  * warp w owns one K-chunk of at most 64 blocks (two per lane), keeps that
 //    chunk of x in registers and runs down its rows four at a time: per
 //    block one 16-byte shared load of weights, dp4a, the int32 block sum
@@ -37,8 +35,6 @@
 
 namespace mlq {
 
-constexpr int kPhWarps = 8;
-constexpr int kPhThreads = kPhWarps * 32;
 constexpr int kPhPieces = 16;
 constexpr int kPhChunk = 64;                 // blocks of K per warp chunk: two per lane
 constexpr size_t kPhBudget = 120 * 1024;     // dynamic shared memory of one CTA
@@ -78,12 +74,13 @@ __device__ __forceinline__ int phase_product(const FusedArgs &a, int g, int *loc
 // Quantise float x (nb blocks) into shared memory, eight lanes per block,
 // all loads of up to eight passes issued before any block is reduced.
 // CTA 0 also writes the copy asked for in xq_out / xd_out.
+template <int NW>
 __device__ __forceinline__ void phase_quantize(const FusedArgs &a, int8_t *xq_s, float *xd_s,
                                                int tid) {
   const int nb = a.nb;
   const int part = tid & 7;
   const bool writer = blockIdx.x == 0 && a.xq_out != nullptr;
-  constexpr int kPer = kPhThreads / 8;
+  constexpr int kPer = NW * 32 / 8;
   constexpr int kPass = 8;
   // every CTA reads all of x: start each at another block to spread the requests
   const int rot = static_cast<int>((static_cast<long long>(blockIdx.x) * 37) % nb);
@@ -139,34 +136,41 @@ struct XChunk {
 template <int QT>
 __device__ __forceinline__ void load_chunk(XChunk &c, const int8_t *xq, const float *xd, int nb,
                                            int cbeg, int cblocks, int lane) {
-  const int h = QT == 0 ? ((lane >> 2) & 1) : 0;
+  // Lanes read their two 16-byte halves in the order h, 1 - h (h = bit 2 of
+  // the lane): the eight lanes of a quarter warp then hit distinct banks.
+  const int h = (lane >> 2) & 1;
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     const int off = lane + 32 * k;
     const int u = cbeg + off;
     c.v[k] = off < cblocks && u < nb;
-    int4 h0 = make_int4(0, 0, 0, 0), h1 = h0;
+    int4 first = make_int4(0, 0, 0, 0), second = first;
     float d = 0.0f;
     if (c.v[k]) {
       const int4 *src = reinterpret_cast<const int4 *>(xq + static_cast<size_t>(u) * kQK);
-      h0 = src[0];
-      h1 = src[1];
+      first = src[h];
+      second = src[h ^ 1];
       d = xd[u];
     }
-    c.x[k][0] = h ? h1 : h0;
-    c.x[k][1] = h ? h0 : h1;
+    if (QT == 1) {  // Q4_0: x[k][0] = elements 0..15 (low nibbles), x[k][1] = 16..31
+      c.x[k][0] = h ? second : first;
+      c.x[k][1] = h ? first : second;
+    } else {        // Q8_0: kept in the lane's read order, as the weights are read
+      c.x[k][0] = first;
+      c.x[k][1] = second;
+    }
     c.d[k] = d;
     int adj = kMagicBits;
     if (QT == 1) {
       constexpr int kOnes = 0x01010101;
-      int sx = __dp4a(h0.x, kOnes, 0);
-      sx = __dp4a(h0.y, kOnes, sx);
-      sx = __dp4a(h0.z, kOnes, sx);
-      sx = __dp4a(h0.w, kOnes, sx);
-      sx = __dp4a(h1.x, kOnes, sx);
-      sx = __dp4a(h1.y, kOnes, sx);
-      sx = __dp4a(h1.z, kOnes, sx);
-      sx = __dp4a(h1.w, kOnes, sx);
+      int sx = __dp4a(first.x, kOnes, 0);
+      sx = __dp4a(first.y, kOnes, sx);
+      sx = __dp4a(first.z, kOnes, sx);
+      sx = __dp4a(first.w, kOnes, sx);
+      sx = __dp4a(second.x, kOnes, sx);
+      sx = __dp4a(second.y, kOnes, sx);
+      sx = __dp4a(second.z, kOnes, sx);
+      sx = __dp4a(second.w, kOnes, sx);
       adj -= 8 * sx;
     }
     c.adj[k] = adj;
@@ -217,6 +221,54 @@ __device__ __forceinline__ float row_part(const uint8_t *wrow, const float *drow
   return acc;
 }
 
+// Q4_0, four rows at once, one of the lane's two blocks at a time: the
+// four rows' shared-memory loads of a block are issued before any of its
+// arithmetic (independent work for the scheduler, within 64 registers).
+// Rows past the slice end (row >= nr) read the last row and contribute 0.
+__device__ __forceinline__ void rows4_q4(float acc[4], const uint8_t *wq_s, const float *wd_s,
+                                         size_t rowq, int nb, int r0, int G, int nr,
+                                         const XChunk &c, int u0) {
+  const uint8_t *wr[4];
+  const float *dr[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int row = min(r0 + G * j, nr - 1);
+    wr[j] = wq_s + static_cast<size_t>(row) * rowq;
+    dr[j] = wd_s + static_cast<size_t>(row) * nb;
+    acc[j] = 0.0f;
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    if (!c.v[k]) continue;
+    const int u = u0 + 32 * k;
+    uint4 w[4];
+    float dw[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      w[j] = *reinterpret_cast<const uint4 *>(wr[j] + u * 16);
+      dw[j] = dr[j][u];
+    }
+    constexpr uint32_t kLo = 0x0F0F0F0Fu, kHi = 0xF0F0F0F0u;
+    const int4 xa = c.x[k][0], xb = c.x[k][1];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 q = w[j];
+      int lo = __dp4a(static_cast<int>(q.x & kLo), xa.x, c.adj[k]);
+      int hi = dp4a_us(q.x & kHi, xb.x, 0);  // 16 * (high nibble) per byte: exact multiple of 16
+      lo = __dp4a(static_cast<int>(q.y & kLo), xa.y, lo);
+      hi = dp4a_us(q.y & kHi, xb.y, hi);
+      lo = __dp4a(static_cast<int>(q.z & kLo), xa.z, lo);
+      hi = dp4a_us(q.z & kHi, xb.z, hi);
+      lo = __dp4a(static_cast<int>(q.w & kLo), xa.w, lo);
+      hi = dp4a_us(q.w & kHi, xb.w, hi);
+      const float sumi = __fsub_rn(__int_as_float(lo + (hi >> 4)), kMagic);
+      acc[j] = __fmaf_rn(__fmul_rn(sumi, dw[j]), c.d[k], acc[j]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = r0 + G * j < nr ? acc[j] : 0.0f;
+}
+
 // Four per-lane partial sums -> four warp sums.  Lane l returns the sum of
 // row (l >> 3) & 3; fixed order, so the result is deterministic.
 __device__ __forceinline__ float reduce4(float a0, float a1, float a2, float a3, int lane) {
@@ -243,14 +295,19 @@ struct PieceTable {
   int lrow[kPhPieces];   // first row inside the product
 };
 
-template <int QT, int IN>
-__global__ void __launch_bounds__(kPhThreads, 4) phase_kernel(const __grid_constant__ PhaseArgs pa) {
+template <int QT, int NW>
+__global__ void __launch_bounds__(NW * 32, 32 / NW) phase_kernel(const __grid_constant__ PhaseArgs pa) {
+  // One code image for both input kinds: every phase of a chain then runs
+  // the same instructions, which stay in the SM's instruction cache.
+  const int IN = pa.a.x == nullptr ? 1 : 0;
+  constexpr int kPhWarps = NW;
+  constexpr int kPhThreads = NW * 32;
   const FusedArgs &a = pa.a;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[kPhPieces];
-  __shared__ __align__(8) uint64_t xbar;
   __shared__ PieceTable pt;
   __shared__ int abort_flag;
+  __shared__ int slice_ok;
   const int nb = a.nb;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ra = pa.bounds[blockIdx.x];
@@ -271,60 +328,88 @@ __global__ void __launch_bounds__(kPhThreads, 4) phase_kernel(const __grid_const
         pt.cnt[np] = min(rpp, hi - r);
         pt.prod[np] = j;
         pt.lrow[np] = r;
-        // bulk copies: one arrival (with the byte count); cp.async: one per thread
-        mbar_init(smem_addr(&bars[np]), a.copy_post ? 1 : kPhThreads);
+        mbar_init(smem_addr(&bars[np]), 1);  // one arrival, with the piece's byte count
         ++np;
       }
       off += a.prod[j].rows;
     }
     pt.n = np;
     abort_flag = 0;
-    mbar_init(smem_addr(&xbar), 1);
+    slice_ok = 1;
     fence_mbar_init();
   }
   __syncthreads();
   const int np = pt.n;
-  // cp.async: every thread copies 16 bytes at a time; a piece's mbarrier
-  // completes when all threads' copies up to that piece have landed.
-  auto issue_async = [&]() {
-    for (int p = 0; p < np; ++p) {
+  // Bulk copies of the slice, one piece per lane of warp 0.  With static
+  // weights they are issued before the dependency wait and land while the
+  // previous kernel runs: then the whole slice completes on ONE mbarrier,
+  // checked once per warp (each barrier check costs a few hundred cycles on
+  // an SM whose barrier unit is busy with other CTAs' incoming copies).
+  // Otherwise they are issued once the input has been read and each piece
+  // completes on its own mbarrier, so rows are reduced as pieces land.
+  const bool one_bar = a.early != 0;
+  auto issue_slice = [&]() {
+    if (warp != 0) return;
+    if (one_bar && lane == 0 && np > 0)
+      mbar_arrive_expect_tx(smem_addr(&bars[0]),
+                            static_cast<uint32_t>(nr) * static_cast<uint32_t>(rowq + 4u * nb));
+    __syncwarp();
+    if (lane < np) {
+      const int p = lane;
       const FusedProduct &pr = a.prod[pt.prod[p]];
-      const uint8_t *gq = pr.wq + static_cast<size_t>(pt.lrow[p]) * rowq;
-      const uint8_t *gd = reinterpret_cast<const uint8_t *>(pr.wd + static_cast<size_t>(pt.lrow[p]) * nb);
-      const uint32_t sq = smem_addr(wq_s + static_cast<size_t>(pt.start[p]) * rowq);
-      const uint32_t sd = smem_addr(wd_s + static_cast<size_t>(pt.start[p]) * nb);
-      const int uq = static_cast<int>(pt.cnt[p] * rowq / 16), ud = pt.cnt[p] * nb / 4;
-      for (int u = tid; u < uq + ud; u += kPhThreads) {
-        if (u < uq) cp_async16(sq + 16u * u, gq + 16 * static_cast<size_t>(u));
-        else cp_async16(sd + 16u * (u - uq), gd + 16 * static_cast<size_t>(u - uq));
-      }
-      cp_async_arrive(smem_addr(&bars[p]));
+      const uint32_t qb = static_cast<uint32_t>(pt.cnt[p] * rowq);
+      const uint32_t db = static_cast<uint32_t>(pt.cnt[p]) * nb * 4;
+      const uint32_t bar = smem_addr(&bars[one_bar ? 0 : p]);
+      if (!one_bar) mbar_arrive_expect_tx(bar, qb + db);
+      bulk_copy_g2s(smem_addr(wq_s + static_cast<size_t>(pt.start[p]) * rowq),
+                    pr.wq + static_cast<size_t>(pt.lrow[p]) * rowq, qb, bar);
+      bulk_copy_g2s(smem_addr(wd_s + static_cast<size_t>(pt.start[p]) * nb),
+                    pr.wd + static_cast<size_t>(pt.lrow[p]) * nb, db, bar);
     }
   };
-  if (a.early && !a.copy_post) issue_async();  // static weights: stream in before the wait
+  if (a.early) issue_slice();
   // Let the next phase's kernel be scheduled now: it still waits for this
   // grid to complete before it reads anything we write.
   griddep_launch_dependents();
+  if (one_bar && np > 0 && warp == kPhWarps - 1) {
+    // One warp checks the slice while the previous kernel still runs; the
+    // CTA barrier after the input publishes the result (and orders the
+    // slice's bytes) for every warp, so no warp checks it again.
+    if (!mbar_wait_warp(smem_addr(&bars[0]), 0, a.wait_ns) && lane == 0) slice_ok = 0;
+  }
   griddep_wait();  // the input (and, without static weights, W) may come from the previous kernel
-  if (!a.early && !a.copy_post) issue_async();
 
   int8_t *xq_s = reinterpret_cast<int8_t *>(smem);
   float *xd_s = reinterpret_cast<float *>(smem + static_cast<size_t>(nb) * kQK);
+  bool ok = true;
   if (IN == 0) {
-    if (nr > 0 || (blockIdx.x == 0 && a.xq_out != nullptr)) phase_quantize(a, xq_s, xd_s, tid);
+    if (nr > 0 || (blockIdx.x == 0 && a.xq_out != nullptr)) phase_quantize<NW>(a, xq_s, xd_s, tid);
     __syncthreads();
   } else if (nr > 0) {
-    // Every CTA reads the same few lines of the input: one bulk copy per CTA
-    // (not one load per warp) keeps the requests to those L2 lines few.
-    if (tid == 0) {
-      const uint32_t qb = static_cast<uint32_t>(nb) * kQK, db = static_cast<uint32_t>(nb) * 4;
-      mbar_arrive_expect_tx(smem_addr(&xbar), qb + db);
-      bulk_copy_g2s(smem_addr(xq_s), a.xq_in, qb, smem_addr(&xbar));
-      bulk_copy_g2s(smem_addr(xd_s), a.xd_in, db, smem_addr(&xbar));
+    // The Q8_0 input (n bytes + n/32 scales): one 16-byte load per thread
+    // and unit, into shared memory; each CTA reads each line once.
+    const int uq = nb * 2, nu = nb * 2 + nb / 4;
+    for (int base = 0; base < nu; base += 4 * kPhThreads) {  // all loads before any store
+      int4 v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int u = base + j * kPhThreads + tid;
+        if (u < nu)
+          v[j] = u < uq ? __ldcg(reinterpret_cast<const int4 *>(a.xq_in) + u)
+                        : __ldcg(reinterpret_cast<const int4 *>(a.xd_in) + (u - uq));
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int u = base + j * kPhThreads + tid;
+        if (u < uq) reinterpret_cast<int4 *>(xq_s)[u] = v[j];
+        else if (u < nu) reinterpret_cast<int4 *>(xd_s)[u - uq] = v[j];
+      }
     }
-    if (!mbar_wait_bounded(smem_addr(&xbar), 0, a.wait_ns)) {
-      if (atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
-    }
+    __syncthreads();
+  }
+  if (one_bar && nr > 0 && !slice_ok) {
+    ok = false;
+    if (tid == 0 && atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
   }
   const int C = a.nchunks;                 // 1, 2, 4 or 8
   const int c = warp & (C - 1);            // this warp's chunk
@@ -333,27 +418,12 @@ __global__ void __launch_bounds__(kPhThreads, 4) phase_kernel(const __grid_const
   const int u0 = c * a.chunk_blocks + lane;
   const bool direct = C == 1 && !a.any_yq;
   float *part_s = reinterpret_cast<float *>(smem + a.smem_part);
-  bool ok = abort_flag == 0;
   XChunk xc;
   if (nr > 0) load_chunk<QT>(xc, xq_s, xd_s, nb, c * a.chunk_blocks, a.chunk_blocks, lane);
-  // The input has landed: only now queue the slice's bulk copies and the L2
-  // hints (an SM serves its reads in order, so anything queued first would
-  // delay the input).  The copies mostly hit L2 when an earlier phase hinted
-  // them.
-  if (a.copy_post) {
-    if (warp == 0 && lane < np) {
-      const int p = lane;
-      const FusedProduct &pr = a.prod[pt.prod[p]];
-      const uint32_t qb = static_cast<uint32_t>(pt.cnt[p] * rowq);
-      const uint32_t db = static_cast<uint32_t>(pt.cnt[p]) * nb * 4;
-      const uint32_t bar = smem_addr(&bars[p]);
-      mbar_arrive_expect_tx(bar, qb + db);
-      bulk_copy_g2s(smem_addr(wq_s + static_cast<size_t>(pt.start[p]) * rowq),
-                    pr.wq + static_cast<size_t>(pt.lrow[p]) * rowq, qb, bar);
-      bulk_copy_g2s(smem_addr(wd_s + static_cast<size_t>(pt.start[p]) * nb),
-                    pr.wd + static_cast<size_t>(pt.lrow[p]) * nb, db, bar);
-    }
-  }
+  // The input has landed: only now queue (non-static) weight copies and the
+  // L2 hints (an SM serves its reads in order, so anything queued first
+  // would delay the input).
+  if (!a.early) issue_slice();
   if (a.npf > 0 && warp == kPhWarps - 1) {
     // this CTA's share of the ranges to hint into L2, 16 KB per lane step
     size_t total = 0;
@@ -377,22 +447,26 @@ __global__ void __launch_bounds__(kPhThreads, 4) phase_kernel(const __grid_const
     int pw = 0;  // pieces [0, pw) have landed
     for (int r0 = i0; r0 < nr; r0 += 4 * G) {
       const int rlast = min(nr - 1, r0 + 3 * G);
-      while (pw < np && pt.start[pw] <= rlast) {
-        if (!mbar_wait_bounded(smem_addr(&bars[pw]), 0, a.wait_ns)) {
+      while (!one_bar && pw < np && pt.start[pw] <= rlast) {
+        if (!mbar_wait_warp(smem_addr(&bars[pw]), 0, a.wait_ns)) {
           ok = false;
-          if (atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
+          if (lane == 0 && atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
           break;
         }
         ++pw;
       }
       if (!ok) break;
       float acc[4];
+      if (QT == 1) {
+        rows4_q4(acc, wq_s, wd_s, rowq, nb, r0, G, nr, xc, u0);
+      } else {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int row = r0 + G * j;
-        acc[j] = row < nr ? row_part<QT>(wq_s + static_cast<size_t>(row) * rowq,
-                                         wd_s + static_cast<size_t>(row) * nb, xc, u0, lane)
-                          : 0.0f;
+        for (int j = 0; j < 4; ++j) {
+          const int row = r0 + G * j;
+          acc[j] = row < nr ? row_part<QT>(wq_s + static_cast<size_t>(row) * rowq,
+                                           wd_s + static_cast<size_t>(row) * nb, xc, u0, lane)
+                            : 0.0f;
+        }
       }
       const float v = reduce4(acc[0], acc[1], acc[2], acc[3], lane);
       const int row = r0 + G * (lane >> 3);
@@ -409,16 +483,21 @@ __global__ void __launch_bounds__(kPhThreads, 4) phase_kernel(const __grid_const
   }
   if (!direct) {
     __syncthreads();
+    // Each row's float value: the sum of its K-chunks in a fixed order.
+    // Rows of a product with a quantised output are stored by the warp that
+    // quantises their 32-row block (below); with one K-chunk the other rows
+    // are stored in the same pass, so one CTA barrier suffices.
     for (int row = tid; row < nr; row += kPhThreads) {
-      float v = part_s[row * C];
-      for (int cc = 1; cc < C; ++cc) v += part_s[row * C + cc];
       int lr;
       const int j = phase_product(a, ra + row, &lr);
+      if (C == 1 && a.prod[j].yq != nullptr) continue;
+      float v = part_s[row * C];
+      for (int cc = 1; cc < C; ++cc) v += part_s[row * C + cc];
       a.prod[j].y[lr] = v;
       part_s[row * C] = v;
     }
     if (a.any_yq) {
-      __syncthreads();
+      if (C > 1) __syncthreads();
       // quantise each whole 32-row block of a product that asks for it,
       // from exactly the float values stored in y; one warp per block
       int t = 0;
@@ -429,6 +508,7 @@ __global__ void __launch_bounds__(kPhThreads, 4) phase_kernel(const __grid_const
         for (int g = lo; g < hi; g += kQK, ++t) {
           if ((t & (kPhWarps - 1)) != warp) continue;
           const float v = part_s[(g - ra + lane) * C];
+          if (C == 1) a.prod[j].y[g - off + lane] = v;
           uint32_t m = __float_as_uint(fabsf(v));
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -441,13 +521,12 @@ __global__ void __launch_bounds__(kPhThreads, 4) phase_kernel(const __grid_const
       }
     }
   }
-  // after a give-up our copies may still be landing: wait for them
-  cp_async_wait_all();
-  __syncthreads();
-  if (tid == 0 && abort_flag) {
-    if (IN == 1 && nr > 0) mbar_wait_bounded(smem_addr(&xbar), 0, kDrainWaitNs);
-    if (a.copy_post)
-      for (int p = 0; p < np; ++p) mbar_wait_bounded(smem_addr(&bars[p]), 0, kDrainWaitNs);
+  // Gave up a wait: our copies may still be landing, wait for them (bounded).
+  // With one barrier every warp knows the outcome since the input barrier;
+  // with pieces a warp may have given up alone, so the CTA syncs first.
+  if (!one_bar) __syncthreads();
+  if (tid == 0 && (one_bar ? !ok : abort_flag != 0)) {
+    for (int p = 0; p < (one_bar ? 1 : np); ++p) mbar_wait_bounded(smem_addr(&bars[p]), 0, kDrainWaitNs);
   }
 }
 
@@ -510,8 +589,10 @@ static int plan_rows(const FusedArgs &a, int total, int grid, int *bounds) {
   return mx;
 }
 
-template <int QT, int IN>
+template <int QT, int NW>
 static cudaError_t launch_phase_t(const LaunchCtx &ctx, const FusedArgs &args) {
+  const int IN = args.x == nullptr ? 1 : 0;
+  constexpr int kPhWarps = NW;
   PhaseArgs pa;
   pa.a = args;
   FusedArgs &a = pa.a;
@@ -535,28 +616,27 @@ static cudaError_t launch_phase_t(const LaunchCtx &ctx, const FusedArgs &args) {
   a.smem_wd = static_cast<unsigned>(xs + ps + rows_max * rowq);
   const size_t smem = a.smem_wd + static_cast<size_t>(rows_max) * nb * 4;
   if (smem > kPhBudget) return cudaErrorNotSupported;
-  // MLQ_PHASE_COPY=pre|post: copy the slice with cp.async before the wait
-  // (static weights), or with bulk copies once the input has been read.
-  static const int post = [] {
-    const char *e = std::getenv("MLQ_PHASE_COPY");
-    return e != nullptr && e[0] == 'p' && e[1] == 'r' ? 0 : 1;
-  }();
-  a.copy_post = post;
-  auto kern = phase_kernel<QT, IN>;
+  auto kern = phase_kernel<QT, NW>;
   prefer_max_shared(kern);
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kPhThreads), smem, ctx, pa);
+  return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(NW * 32), smem, ctx, pa);
 }
 
 cudaError_t launch_phase(const LaunchCtx &ctx, int qtype, const FusedArgs &a) {
   static_assert(sizeof(PhaseArgs) <= 4096, "kernel parameters");
-  const bool in_q = a.x == nullptr;
-  if (qtype == 1) return in_q ? launch_phase_t<1, 1>(ctx, a) : launch_phase_t<1, 0>(ctx, a);
-  return in_q ? launch_phase_t<0, 1>(ctx, a) : launch_phase_t<0, 0>(ctx, a);
+  // MLQ_PHASE_WARPS=16|8: CTA width (A/B timing).  16 warps (two CTAs per
+  // SM) reduce a slice faster; 8 would let four phases share an SM, which
+  // measured slower on the TinyLlama layer chain.
+  static const int wide = [] {
+    const char *e = std::getenv("MLQ_PHASE_WARPS");
+    return !(e != nullptr && e[0] == '8');
+  }();
+  if (wide) return qtype == 1 ? launch_phase_t<1, 16>(ctx, a) : launch_phase_t<0, 16>(ctx, a);
+  return qtype == 1 ? launch_phase_t<1, 8>(ctx, a) : launch_phase_t<0, 8>(ctx, a);
 }
 
 }  // namespace mlq

@@ -126,7 +126,7 @@ class WorkloadRunner:
             out += [(m.q[copy], m.host_q.nbytes), (m.d[copy], m.host_d.nbytes)]
         return out
 
-    def phase_calls(self, copy: int = 0, static_weights: bool = True, prefetch: str = "ahead2"):
+    def phase_calls(self, copy: int = 0, static_weights: bool = True, prefetch: str = "none"):
         """One mlq_decode_phase call per phase.  A product whose output is
         the input of a later phase also writes it in Q8_0 (into that input's
         buffer), so the later phase starts from quantised bytes; the
@@ -174,7 +174,7 @@ class WorkloadRunner:
         return self._chain_calls[key]
 
     def step_phase(self, copy: int = 0, stream=None, static_weights: bool = True,
-                   prefetch: str = "ahead2") -> None:
+                   prefetch: str = "none") -> None:
         """One pass as one mlq_decode_phase launch per phase."""
         for c in self.phase_calls(copy, static_weights, prefetch):
             c(stream)

@@ -42,7 +42,7 @@ def test_small_m_parity_with_forced_kernel(kernel):
 
 @pytest.mark.skipif(os.environ.get("MLQ_FUSED_KERNEL") is not None,
                     reason="already inside a forced-kernel run")
-@pytest.mark.parametrize("kernel", ["ldg", "smem", "phase"])
+@pytest.mark.parametrize("kernel", ["ldg", "phase"])
 def test_fused_parity_with_forced_kernel(kernel):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
@@ -54,16 +54,14 @@ def test_fused_parity_with_forced_kernel(kernel):
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
 
 
-@pytest.mark.skipif(os.environ.get("MLQ_PHASE_COPY") is not None,
-                    reason="already inside a forced-copy run")
-@pytest.mark.parametrize("copy", ["pre", "post"])
-def test_phase_parity_with_forced_copy(copy):
-    """The phase kernel's two slice-copy schedules (cp.async before the
-    dependency wait, bulk copies once the input has landed)."""
+@pytest.mark.skipif(os.environ.get("MLQ_PHASE_WARPS") is not None,
+                    reason="already inside a forced-width run")
+def test_phase_parity_with_narrow_ctas():
+    """The phase kernel with 8-warp CTAs (four per SM) instead of 16."""
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    env = dict(os.environ, MLQ_PHASE_COPY=copy, PYTHONPATH=ROOT)
+    env = dict(os.environ, MLQ_PHASE_WARPS="8", PYTHONPATH=ROOT)
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
                         "tests/test_gpu_phase.py"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=1200)
