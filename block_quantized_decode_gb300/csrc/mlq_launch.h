@@ -132,6 +132,8 @@ struct FusedArgs {
   int nchunks;      // set by the launcher
   int chunk_blocks; // set by the launcher (phase kernel: blocks of K per warp chunk)
   unsigned smem_part, smem_w, smem_wd;  // set by the launcher (phase kernel: smem offsets)
+  int ring_rows, ring_slots;            // set by the launcher (ring phase kernel: stage geometry)
+  unsigned ring_stage, ring_dq;         //   stage bytes; offset of a stage's scales
   int early;        // first weight loads before the dependency wait (static weights)
   int prefetch;     // set by the launcher: hint the CTA's weights into L2 first
   int *status;      // set by the launcher
@@ -145,9 +147,11 @@ struct FusedArgs {
 // shared memory, else the streaming kernel of fused.cu (float input, no
 // quantised outputs) or, for the other cases, matvec + quantize launches.
 cudaError_t launch_matvec_fused(const LaunchCtx &ctx, int qtype, const FusedArgs &a);
-// phase.cu: the shared-memory phase kernel; returns cudaErrorNotSupported
-// without launching when the shape does not suit it.
+// phase.cu: the shared-memory phase kernel, else the ring phase kernel;
+// returns cudaErrorNotSupported without launching when neither suits.
 cudaError_t launch_phase(const LaunchCtx &ctx, int qtype, const FusedArgs &a);
+// phase_ring.cu: the ring phase kernel alone (same contract).
+cudaError_t launch_phase_ring(const LaunchCtx &ctx, int qtype, const FusedArgs &a);
 
 // gemm_mma.cu: M activation rows (2..16) against a Q4_0 matrix on the
 // tensor cores (fp16 mma.sync, exact block sums).

@@ -1,0 +1,297 @@
+// phase_ring.cu -- one decode phase per launch for weight slices too large
+// to hold in shared memory (the Llama-7B-sized products, the lm_head): the
+// same phase as phase.cu -- products sharing one input, float or Q8_0
+// input, optional Q8_0 outputs in whole 32-row blocks -- with the CTA's
+// rows streamed through a ring of shared-memory stages.  Definitions: page
+// "Legacy-ISA ML Inference Runtime -- Design Spec", Sec. 4 (Q4_0 / Q8_0
+// blocks, block dot), Sec. 5 (quantize_q8 rounding, matvec), Sec. 6
+// "Forward pass".
+//
+// Per CTA (one per SM; two fit on an SM, so the next phase's CTA is already
+// resident while this one runs):
+//  * a producer warp copies the CTA's rows, stage by stage, with 1-D bulk
+//    copies (rows of one product per stage, quants then scales), completion
+//    on a full mbarrier per ring slot; with static weights it starts before
+//    the dependency wait, so the ring is full when the phase begins and the
+//    HBM stream continues across the launch boundary;
+//  * 8 consumer warps read the input (as phase.cu: the Q8_0 input loaded
+//    once per CTA, or float x quantised in the CTA), keep their K-chunk of it
+//    in registers, reduce each stage -- warp (chunk c, group g) takes one
+//    four-row group per stage -- and free the slot on an empty mbarrier;
+//  * per-chunk partial sums are added in a fixed order, y is stored, and the
+//    32-row blocks of products with a quantised output are quantised from
+//    exactly the stored floats.
+// Consumer-only synchronisation uses a named barrier (the producer never
+// joins it).  Every wait is bounded; on a give-up the CTA records
+// MLQ_E_TIMEOUT and its copies in flight are drained before it exits.
+#include "phase_common.cuh"
+
+#include <cstdlib>
+
+namespace mlq {
+
+constexpr int kRingWarps = 8;                        // consumer warps
+constexpr int kRingThreads = (kRingWarps + 1) * 32;  // + the producer warp
+constexpr int kRingMaxSlots = 8;
+constexpr size_t kRingBudget = 110 * 1024;      // two CTAs per SM
+constexpr size_t kRingBudgetWide = 200 * 1024;  // one CTA per SM (very long rows)
+
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"r"(kRingWarps * 32) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive1(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Bounded wait that also gives up once another warp of the CTA has aborted.
+__device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity, const volatile int *abort_flag,
+                                          unsigned long long limit_ns) {
+  if (limit_ns == 0) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = sm_cycles(), lim = limit_cycles(limit_ns);
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (sm_cycles() - t0 > lim) return false;
+  }
+}
+
+// The CTA's stages: runs of at most R rows of [ra, rb), never spanning two
+// products.  Producer and consumers walk them in the same order.
+struct StageIter {
+  int j, off, r;  // current product, its first row, next row (concatenated numbering)
+};
+__device__ __forceinline__ int stage_next(StageIter &it, const FusedArgs &a, int rb, int R,
+                                          int *j, int *lrow) {
+  while (it.r < rb && it.r >= it.off + a.prod[it.j].rows) {
+    it.off += a.prod[it.j].rows;
+    ++it.j;
+  }
+  if (it.r >= rb) return 0;
+  const int end = min(rb, it.off + a.prod[it.j].rows);
+  const int n = min(R, end - it.r);
+  *j = it.j;
+  *lrow = it.r - it.off;
+  it.r += n;
+  return n;
+}
+
+template <int QT>
+__global__ void __launch_bounds__(kRingThreads, 2) phase_ring_kernel(const __grid_constant__ PhaseArgs pa) {
+  const FusedArgs &a = pa.a;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[kRingMaxSlots];
+  __shared__ __align__(8) uint64_t empty_bar[kRingMaxSlots];
+  __shared__ int abort_flag;
+  volatile int *abort_v = &abort_flag;
+  const int IN = a.x == nullptr ? 1 : 0;
+  const int nb = a.nb;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ra = pa.bounds[blockIdx.x];
+  const int rb = pa.bounds[blockIdx.x + 1];
+  const int nr = rb - ra;
+  const size_t rowq = static_cast<size_t>(nb) * (QT == 1 ? 16 : 32);
+  const int C = a.nchunks, cblk = a.chunk_blocks;
+  const int G = kRingWarps / C;  // warps per chunk; a stage has R = 4 * G rows
+  const int R = a.ring_rows, ns = a.ring_slots;
+  const size_t stage_bytes = a.ring_stage, dq = a.ring_dq;
+  int8_t *xq_s = reinterpret_cast<int8_t *>(smem);
+  float *xd_s = reinterpret_cast<float *>(smem + static_cast<size_t>(nb) * kQK);
+  float *part_s = reinterpret_cast<float *>(smem + a.smem_part);
+  uint8_t *ring = smem + a.smem_w;
+
+  if (tid == 0) {
+    for (int s = 0; s < ns; ++s) {
+      mbar_init(smem_addr(&full_bar[s]), 1);
+      mbar_init(smem_addr(&empty_bar[s]), kRingWarps);  // one arrival per consumer warp
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // The next phase's kernel may be scheduled now (it waits for this grid to
+  // complete before it reads anything we write).
+  griddep_launch_dependents();
+
+  if (warp == kRingWarps) {
+    // ------------------------------ producer ------------------------------
+    if (lane != 0 || nr == 0) return;
+    if (!a.early) griddep_wait();  // weights written by earlier work: wait for it first
+    StageIter it{0, 0, ra};
+    int s = 0, j, lrow, n;
+    while ((n = stage_next(it, a, rb, R, &j, &lrow)) > 0) {
+      const int slot = s % ns;
+      if (s >= ns && !ring_wait(smem_addr(&empty_bar[slot]), ((s / ns) - 1) & 1, abort_v, a.wait_ns)) {
+        if (atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
+        break;
+      }
+      if (*abort_v) break;
+      const uint32_t qb = static_cast<uint32_t>(n * rowq), db = static_cast<uint32_t>(n) * nb * 4;
+      uint8_t *dst = ring + static_cast<size_t>(slot) * stage_bytes;
+      const uint32_t fb = smem_addr(&full_bar[slot]);
+      mbar_arrive_expect_tx(fb, qb + db);
+      bulk_copy_g2s(smem_addr(dst), a.prod[j].wq + static_cast<size_t>(lrow) * rowq, qb, fb);
+      bulk_copy_g2s(smem_addr(dst + dq), a.prod[j].wd + static_cast<size_t>(lrow) * nb, db, fb);
+      ++s;
+    }
+    if (*abort_v) {  // copies may still be landing: the last ns issued stages (bounded)
+      for (int t = s > ns ? s - ns : 0; t < s; ++t)
+        mbar_wait_bounded(smem_addr(&full_bar[t % ns]), (t / ns) & 1, kDrainWaitNs);
+    }
+    return;
+  }
+
+  // ------------------------------ consumers ------------------------------
+  griddep_wait();  // the input may come from the previous kernel
+  if (IN == 0) {
+    if (nr > 0 || (blockIdx.x == 0 && a.xq_out != nullptr)) phase_quantize<kRingWarps>(a, xq_s, xd_s, tid);
+  } else if (nr > 0) {
+    const int uq = nb * 2, nu = nb * 2 + nb / 4;
+    for (int base = 0; base < nu; base += 4 * kRingWarps * 32) {  // all loads before any store
+      int4 v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int u = base + q * kRingWarps * 32 + tid;
+        if (u < nu)
+          v[q] = u < uq ? __ldcg(reinterpret_cast<const int4 *>(a.xq_in) + u)
+                        : __ldcg(reinterpret_cast<const int4 *>(a.xd_in) + (u - uq));
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int u = base + q * kRingWarps * 32 + tid;
+        if (u < uq) reinterpret_cast<int4 *>(xq_s)[u] = v[q];
+        else if (u < nu) reinterpret_cast<int4 *>(xd_s)[u - uq] = v[q];
+      }
+    }
+  }
+  consumers_sync();
+  if (nr == 0) return;
+
+  const int c = warp & (C - 1), g = warp / C;
+  const int u0 = c * cblk + lane;
+  XChunk xc;
+  load_chunk<QT>(xc, xq_s, xd_s, nb, c * cblk, cblk, lane);
+  bool ok = true;
+  StageIter it{0, 0, ra};
+  int s = 0, j, lrow, n;
+  while ((n = stage_next(it, a, rb, R, &j, &lrow)) > 0) {
+    const int slot = s % ns;
+    const int srow = it.r - n - ra;  // the stage's first row in the CTA's slice
+    ok = warp_wait([&] { return ring_wait(smem_addr(&full_bar[slot]), (s / ns) & 1, abort_v, a.wait_ns); });
+    if (!ok) {
+      if (lane == 0 && atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
+      break;
+    }
+    const uint8_t *wq_s = ring + static_cast<size_t>(slot) * stage_bytes;
+    const float *wd_s = reinterpret_cast<const float *>(wq_s + dq);
+    float acc[4];
+    if (QT == 1) {
+      rows4_q4(acc, wq_s, wd_s, rowq, nb, g, G, n, xc, u0);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int row = g + G * q;
+        acc[q] = row < n ? row_part<QT>(wq_s + static_cast<size_t>(row) * rowq,
+                                        wd_s + static_cast<size_t>(row) * nb, xc, u0, lane)
+                         : 0.0f;
+      }
+    }
+    const float v = reduce4(acc[0], acc[1], acc[2], acc[3], lane);
+    const int row = g + G * (lane >> 3);
+    if ((lane & 7) == 0 && row < n) part_s[(srow + row) * C + c] = v;
+    __syncwarp();
+    if (lane == 0) mbar_arrive1(smem_addr(&empty_bar[slot]));
+    ++s;
+  }
+  consumers_sync();
+  if (*abort_v) return;
+
+  // y: the K-chunks of each row added in a fixed order, product by product
+  for (int jj = 0, off = 0; jj < a.nproducts; off += a.prod[jj].rows, ++jj) {
+    const int lo = max(ra, off), hi = min(rb, off + a.prod[jj].rows);
+    for (int gr = lo + tid; gr < hi; gr += kRingWarps * 32) {
+      const int r = gr - ra;
+      float v = part_s[r * C];
+      for (int cc = 1; cc < C; ++cc) v += part_s[r * C + cc];
+      a.prod[jj].y[gr - off] = v;
+      part_s[r * C] = v;
+    }
+  }
+  if (a.any_yq) {
+    consumers_sync();
+    // each whole 32-row block of a product with a quantised output, from
+    // exactly the stored floats; one warp per block
+    int t = 0;
+    for (int jj = 0, off = 0; jj < a.nproducts; off += a.prod[jj].rows, ++jj) {
+      const int lo = max(ra, off), hi = min(rb, off + a.prod[jj].rows);
+      if (a.prod[jj].yq == nullptr || hi <= lo) continue;
+      for (int gr = lo; gr < hi; gr += kQK, ++t) {
+        if ((t & (kRingWarps - 1)) != warp) continue;
+        const float v = part_s[(gr - ra + lane) * C];
+        uint32_t m = __float_as_uint(fabsf(v));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float amax = __uint_as_float(m);
+        const float dd = amax / 127.0f;
+        const float id = amax != 0.0f ? 127.0f / amax : 0.0f;
+        a.prod[jj].yq[gr - off + lane] = static_cast<int8_t>(quant_one(v, id));
+        if (lane == 0) a.prod[jj].yd[(gr - off) / kQK] = dd;
+      }
+    }
+  }
+}
+
+template <int QT>
+static cudaError_t launch_ring_t(const LaunchCtx &ctx, const FusedArgs &args) {
+  PhaseArgs pa;
+  pa.a = args;
+  FusedArgs &a = pa.a;
+  const int nb = a.nb;
+  if (a.total_rows <= 0 || nb % 4 != 0) return cudaErrorNotSupported;
+  int grid = ctx.num_sms < a.total_rows ? ctx.num_sms : a.total_rows;
+  grid = grid < kPhMaxGrid ? grid : kPhMaxGrid;
+  const int rows_max = plan_rows(a, a.total_rows, grid, pa.bounds);
+  const size_t rowq = static_cast<size_t>(nb) * (QT == 1 ? 16 : 32);
+  auto up128 = [](size_t v) { return (v + 127) / 128 * 128; };
+  const size_t xs = up128(static_cast<size_t>(nb) * (kQK + 4));
+  // Geometry: the fewest K-chunks (a power of two, at most 64 blocks each,
+  // at most one per consumer warp) whose ring of >= 2 stages of R = 4 * G
+  // rows fits the budget; two CTAs per SM if possible, else one.
+  for (size_t budget : {kRingBudget, kRingBudgetWide}) {
+    for (int C = 1; C <= kRingWarps; C *= 2) {
+      if (C * kPhChunk < nb) continue;
+      const int R = 4 * (kRingWarps / C);
+      const size_t dq = up128(static_cast<size_t>(R) * rowq);
+      const size_t stage = up128(dq + static_cast<size_t>(R) * nb * 4);
+      const size_t ps = up128(static_cast<size_t>(rows_max) * C * 4);
+      const size_t fixed = xs + ps;
+      if (fixed + 2 * stage > budget) continue;
+      int ns = static_cast<int>((budget - fixed) / stage);
+      ns = ns < kRingMaxSlots ? ns : kRingMaxSlots;
+      a.nchunks = C;
+      a.chunk_blocks = (nb + C - 1) / C;
+      a.ring_rows = R;
+      a.ring_slots = ns;
+      a.ring_stage = static_cast<unsigned>(stage);
+      a.ring_dq = static_cast<unsigned>(dq);
+      a.smem_part = static_cast<unsigned>(xs);
+      a.smem_w = static_cast<unsigned>(fixed);
+      const size_t smem = fixed + static_cast<size_t>(ns) * stage;
+      auto kern = phase_ring_kernel<QT>;
+      prefer_max_shared(kern);
+      if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+      }
+      return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kRingThreads), smem, ctx, pa);
+    }
+  }
+  return cudaErrorNotSupported;
+}
+
+cudaError_t launch_phase_ring(const LaunchCtx &ctx, int qtype, const FusedArgs &a) {
+  return qtype == 1 ? launch_ring_t<1>(ctx, a) : launch_ring_t<0>(ctx, a);
+}
+
+}  // namespace mlq

@@ -66,3 +66,18 @@ def test_phase_parity_with_narrow_ctas():
                         "tests/test_gpu_phase.py"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=1200)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
+
+@pytest.mark.skipif(os.environ.get("MLQ_PHASE_KERNEL") is not None,
+                    reason="already inside a forced-kernel run")
+def test_phase_parity_with_ring_kernel():
+    """Every phase through the ring kernel (weights streamed through shared
+    memory stages), including the shapes the shared-memory kernel takes."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    env = dict(os.environ, MLQ_PHASE_KERNEL="ring", PYTHONPATH=ROOT)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        "tests/test_gpu_phase.py", "tests/test_gpu_fused.py"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=1200)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
