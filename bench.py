@@ -58,8 +58,8 @@ def parse_args():
                         "the next one's input already quantised; fused: one mlq_matvec_fused "
                         "launch per phase (float inputs); chain: one mlq_decode_chain launch "
                         "per step; calls: one C-ABI call per quantize and product; auto: phase "
-                        "for M = 1 steps under 64 MB of weights (latency-bound, fewer launches "
-                        "win), else calls")
+                        "for M = 1 (one launch per phase, measured fastest at every size), "
+                        "calls for M > 1")
     p.add_argument("--phase-prefetch", choices=["none", "ahead1", "ahead2"], default="none",
                    help="phase path: each phase hints the weights of the phase one / two "
                         "later into L2 once it has read its input")
@@ -166,6 +166,27 @@ class ClockSampler:
                 "sm_max_mhz": max(x[2] for x in use),
                 "samples": len(use), "window": "timed region" if inside else "whole run",
                 "reasons": sorted(set().union(*[x[3] for x in use]))}
+
+
+def phase_kernel_of(r, num_sms: int):
+    """The kernel that streams most of a pass's weight bytes on the phase
+    path: phase_kernel when a CTA's share of a phase's rows fits in shared
+    memory (about 120 KB with the input), else phase_ring_kernel.  An
+    estimate of the library's choice, used to label the roofline only."""
+    fit = ring = 0
+    for _, first, count in r.chain_phases():
+        mats = r.mats[first:first + count]
+        rows = sum(m.spec.rows for m in mats)
+        nb = mats[0].spec.cols // 32
+        rowb = nb * ((16 if mats[0].spec.wtype == 1 else 32) + 4)
+        share = -(-rows // max(1, min(num_sms, rows))) + 16  # + uneven 32-row splits
+        smem = -(-(nb * 36) // 128) * 128 + share * rowb
+        nbytes = sum(m.host_q.nbytes + m.host_d.nbytes for m in mats)
+        if smem <= 120 * 1024:
+            fit += nbytes
+        else:
+            ring += nbytes
+    return ("phase_kernel", "phase.cu") if fit >= ring else ("phase_ring_kernel", "phase_ring.cu")
 
 
 def ncu_traffic(profile: str, sources, bytes_per_launch: float):
@@ -315,7 +336,7 @@ def run_ours(args, wl, world, rank, local, pg):
     if pf == "none":
         pf = None
     path = args.path if args.path != "auto" else (
-        "phase" if r.m == 1 and wbytes < 64 * 2 ** 20 else "calls")
+        "phase" if r.m == 1 else "calls")
 
     def one_pass(c):
         if path == "chain":
@@ -477,10 +498,11 @@ def run_ours(args, wl, world, rank, local, pg):
         ach = tot_bytes / tot_s / 1e9
         qt = "Q4_0" if r.mats[0].spec.wtype == I.Q4_0 else "Q8_0"
         nph = len(per_phase)
-        kname, ksrc = "phase_kernel", "phase.cu"
+        kname, ksrc = phase_kernel_of(r, props.multi_processor_count)
         roofline = {"kernel": f"{kname}<{qt}>", "bound": "hbm", "achieved": ach,
                     "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_source": peak_src,
-                    "traffic": ncu_traffic(f"{path}_{wl.name}", (ksrc, "mlq_device.cuh"),
+                    "traffic": ncu_traffic(f"{ksrc[:-3]}_{wl.name}",
+                                           (ksrc, "phase_common.cuh", "mlq_device.cuh"),
                                            tot_bytes / nph),
                     "bytes_per_launch": tot_bytes / nph, "us_per_launch": tot_s / nph * 1e6,
                     "method": f"{launches} back-to-back launches of each phase in one CUDA graph, "

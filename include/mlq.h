@@ -268,9 +268,10 @@ typedef struct {
  * streams the next weights from HBM while its phases run, behind no
  * critical-path read (an SM serves its reads in order: a prefetch issued
  * earlier would delay them).  Unaligned range ends are trimmed to 16 bytes.
- * When a CTA's share of the weights does not fit in shared memory the call
- * queues the same work as several launches (products, then quantize, then
- * the prefetch).
+ * A CTA's share of the weights is held whole in shared memory when it fits,
+ * else streamed through a ring of shared-memory stages (K <= 16384); other
+ * shapes (K not a multiple of 128, longer rows) get the same work as several
+ * launches (products, then quantize, then the prefetch).
  * No counterpart on the pages: a GPU fusion of their quantize_q8 and
  * matvec calls. */
 #define MLQ_PHASE_MAX_PREFETCH 16
