@@ -258,7 +258,7 @@ mlq_status mlq_gemm_q4_small_m(float *Y, int ldy, const mlq_qtensor *W, const ml
   s = make_ctx(&ctx, stream);
   if (s != MLQ_OK) return s;
   return from_cuda(mlq::launch_gemm_q4_small_m(ctx, W->q, W->d, W->cols / MLQ_QK, X->q, X->d, M,
-                                               Y, ldy, r0, r1));
+                                               Y, ldy, r0, r1, W->rows));
 }
 
 mlq_status mlq_matvec_fused(const float *x, int n, const mlq_chain_product *products,

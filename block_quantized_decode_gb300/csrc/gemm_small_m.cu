@@ -15,6 +15,7 @@
 // recovers sumi with no per-block correction term.  Activation blocks are
 // read through L1 (they are shared by every warp of the SM).
 #include <cstdlib>
+#include <cstring>
 
 #include "mlq_device.cuh"
 #include "mlq_launch.h"
@@ -188,15 +189,18 @@ static cudaError_t launch_gemm_mm(const LaunchCtx &ctx, GemmArgs a) {
 }
 
 // Kernel choice, measured on GB300 (11008 x 4096 and 4096 x 11008 Q4_0):
-// the tensor-core kernel (gemm_mma.cu) wins from M = 8 on (M = 16: 36-40 us
-// vs 76-83 us), this dp4a kernel below (M = 2: 11 us vs 19-24 us).
-// MLQ_GEMM_KERNEL=dp4a|mma overrides (A/B timing).
+// the tensor-core kernels win from M = 8 on, this dp4a kernel below at
+// small M (M = 2: 11 us vs 19-24 us).  Of the tensor-core kernels the
+// cluster kernel (gemm_mma_cluster.cu) is the default; the register-load
+// kernel (gemm_mma.cu) serves the shapes it does not take (K above 16384).
+// MLQ_GEMM_KERNEL=dp4a|mma|mma_ldg overrides (A/B timing, tests).
 static int gemm_override() {
   static const int v = [] {
     const char *e = std::getenv("MLQ_GEMM_KERNEL");
     if (e == nullptr) return 0;
-    if (e[0] == 'd') return 1;
-    if (e[0] == 'm') return 2;
+    if (std::strcmp(e, "dp4a") == 0) return 1;
+    if (std::strcmp(e, "mma") == 0) return 2;
+    if (std::strcmp(e, "mma_ldg") == 0) return 3;
     return 0;
   }();
   return v;
@@ -204,10 +208,16 @@ static int gemm_override() {
 
 cudaError_t launch_gemm_q4_small_m(const LaunchCtx &ctx, const void *wq, const float *wd, int nb,
                                    const int8_t *xq, const float *xd, int M, float *Y, int ldy,
-                                   int r0, int r1) {
+                                   int r0, int r1,
+                                   int rows) {
   if (r1 <= r0 || M <= 0) return cudaSuccess;
   const int o = gemm_override();
-  if (o == 2 || (o == 0 && M >= 8)) return launch_gemm_q4_mma(ctx, wq, wd, nb, xq, xd, M, Y, ldy, r0, r1);
+  if (o == 3) return launch_gemm_q4_mma(ctx, wq, wd, nb, xq, xd, M, Y, ldy, r0, r1);
+  if (o == 2 || (o == 0 && M >= 8)) {
+    const cudaError_t e = launch_gemm_q4_mma_cluster(ctx, wq, wd, nb, xq, xd, M, Y, ldy, r0, r1, rows);
+    if (e != cudaErrorNotSupported) return e;
+    return launch_gemm_q4_mma(ctx, wq, wd, nb, xq, xd, M, Y, ldy, r0, r1);
+  }
   GemmArgs a;
   a.wq = static_cast<const uint8_t *>(wq);
   a.wd = wd;

@@ -159,9 +159,19 @@ cudaError_t launch_gemm_q4_mma(const LaunchCtx &ctx, const void *wq, const float
                                const int8_t *xq, const float *xd, int M, float *Y, int ldy,
                                int r0, int r1);
 
+// gemm_mma_cluster.cu: the same product streaming the weights through
+// per-warp TMA rings, K split over a thread-block cluster.  `rows` is the
+// row count of W (the tensor copies describe the whole matrix).
+// cudaErrorNotSupported when K is above 16384, nb is not a multiple of 4,
+// or the device cannot hold one cluster.
+cudaError_t launch_gemm_q4_mma_cluster(const LaunchCtx &ctx, const void *wq, const float *wd,
+                                       int nb, const int8_t *xq, const float *xd, int M, float *Y,
+                                       int ldy, int r0, int r1, int rows);
+
 // gemm_small_m.cu: M activation rows (1..16) against a Q4_0 matrix.
 cudaError_t launch_gemm_q4_small_m(const LaunchCtx &ctx, const void *wq, const float *wd, int nb,
                                    const int8_t *xq, const float *xd, int M, float *Y, int ldy,
-                                   int r0, int r1);
+                                   int r0, int r1,
+                                   int rows);
 
 }  // namespace mlq
