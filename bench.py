@@ -353,7 +353,14 @@ def run_ours(args, wl, world, rank, local, pg):
     # ---- graphs: one per weight copy (plain), one per copy instrumented
     dominant = "matvec_m1_kernel<Q4_0>" if r.m == 1 and any(
         m.spec.wtype == I.Q4_0 for m in r.mats) else (
-        "matvec_m1_kernel<Q8_0>" if r.m == 1 else "gemm_q4_small_m")
+        "matvec_m1_kernel<Q8_0>" if r.m == 1 else
+        "gemm_q4_mma_cluster_kernel" if r.m >= 8 else "gemm_q4_small_m_dp4a_kernel")
+    # the dominant kernel's sources and committed ncu summary (for the traffic figure)
+    kernel_src = (("matvec.cu", "mlq_device.cuh") if r.m == 1 else
+                  ("gemm_mma_cluster.cu", "mma_frag.cuh", "mlq_device.cuh") if r.m >= 8 else
+                  ("gemm_small_m.cu", "mlq_device.cuh"))
+    kernel_profile = ("matvec_q4" if r.m == 1 else
+                      "gemm_mma_cluster" if r.m >= 8 else "gemm_small_m")
     with torch.cuda.stream(stream):
         for c in range(copies):  # eager warm-up of every copy (kernel attributes, caches)
             one_pass(c)
@@ -544,13 +551,21 @@ def run_ours(args, wl, world, rank, local, pg):
         ach = tot_bytes / tot_s / 1e9
         roofline = {"kernel": dominant, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
                     "frac": ach / hbm, "peak_source": peak_src,
-                    "traffic": ncu_traffic(f"matvec_q4_{wl.name}", ("matvec.cu", "mlq_device.cuh"),
+                    "traffic": ncu_traffic(f"{kernel_profile}_{wl.name}", kernel_src,
                                            tot_bytes / sum(p["per_step"] for p in per_shape)),
                     "bytes_per_launch": tot_bytes / sum(p["per_step"] for p in per_shape),
                     "us_per_launch": tot_s / sum(p["per_step"] for p in per_shape) * 1e6,
                     "method": f"{launches} back-to-back launches per shape in one CUDA graph, "
                               "best of 3 replays, CUDA events on the launching stream",
                     "per_shape": per_shape}
+        if r.m >= 8:
+            # the tensor-core side of the same launches: 2 M N K per product
+            flops = sum(2.0 * r.m * r.mats[idx[0]].spec.rows * r.mats[idx[0]].spec.cols * len(idx)
+                        for idx in shapes.values())
+            tf = flops / tot_s / 1e12
+            bf16 = peaks.get("bf16_tflops")
+            roofline["tensor"] = {"achieved": tf, "unit": "TFLOP/s", "operands": "fp16 mma.sync",
+                                  "peak_bf16_dense": bf16, "frac": tf / bf16 if bf16 else None}
 
     # ---- end to end: pinned host input -> step -> outputs to pinned host
     host_out = r.outputs_to_host()

@@ -63,6 +63,7 @@
 #include <cuda_fp16.h>
 
 #include <atomic>
+#include <cstdlib>
 
 #include "mlq_device.cuh"
 #include "mlq_launch.h"
@@ -72,7 +73,8 @@ namespace mlq {
 
 constexpr int kMcConsumers = 16;                 // warps
 constexpr int kMcThreads = kMcConsumers * 32;
-constexpr int kMcSlots = 4;                      // stages in the ring
+constexpr int kMcMaxSlots = 8;                   // stages in the ring, at most (at least 4)
+constexpr int kMcFirst = 3;                      // stages copied before the activations are staged
 constexpr int kMcChunk = 8;                      // blocks per stage (128 bytes of a Q4_0 row)
 constexpr int kMcMaxRows = 160;                  // rows per round (tensor box height)
 constexpr int kMcMaxTpw = kMcMaxRows / 32;       // tiles of one parity in a round
@@ -83,8 +85,8 @@ constexpr int kMcXcBlock = 128;                  // -(C_g, C_g, C_g+8, C_g+8) fo
 constexpr int kMcXRaw = 16 * (kQK + 4);          // raw activation bytes and scale per block
 constexpr int kMcTileBytes = 1024;               // one warp's partial (or sum) of one tile
 constexpr int kMcMaxCluster = 8;
+constexpr int kMcSmemLimit = 227 * 1024 - 256;   // dynamic shared memory, leaving room for the barriers
 constexpr int kMcXTasks = kMcMaxPart * 32 / (kMcConsumers * 32);
-constexpr int kMcXPerBlock = kMcXfBlock + kMcXdBlock + kMcXcBlock + kMcXRaw;
 static_assert(kMcConsumers == 2 * kMcChunk, "two warps per block of a stage");
 
 struct McArgs {
@@ -102,7 +104,10 @@ struct McArgs {
   int xblocks;   // activation blocks held per CTA (largest part, whole chunks)
   int slot_q;    // bytes of a stage's weight box, 1024-aligned
   int slot_d;    // bytes of a stage's scale box, 128-aligned
-  int ring;      // bytes of the ring area (stages; partials and tile sums reuse it)
+  int slots;     // stages in the ring
+  int ring;      // bytes of the ring area
+  int xraw;      // offset of the raw activations: in ring slots kMcFirst.. or after the fragments
+  int parts;     // offset of the partials and tile sums: 0 (they reuse the ring) or their own area
   int early;     // weights are not written by earlier queued work: copy before the wait
 };
 
@@ -131,6 +136,12 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile(
       "barrier.cluster.arrive.release.aligned;\n\t"
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The same without ordering: only that every thread of the cluster got here.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile(
+      "barrier.cluster.arrive.relaxed.aligned;\n\t"
+      "barrier.cluster.wait.aligned;" ::: "memory");
 }
 __device__ __forceinline__ float4 ld_cluster_f4(uint32_t local, int rank) {
   uint32_t remote;
@@ -247,8 +258,8 @@ __global__ void __launch_bounds__(kMcThreads, 1)
     gemm_q4_mma_cluster_kernel(const __grid_constant__ McParams prm) {
   const McArgs &a = prm.a;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kMcSlots];
-  __shared__ __align__(8) uint64_t empty_bar[kMcSlots];
+  __shared__ __align__(8) uint64_t full_bar[kMcMaxSlots];
+  __shared__ __align__(8) uint64_t empty_bar[kMcMaxSlots];
   __shared__ __align__(8) uint64_t x_bar;
   __shared__ int abort_flag;
   volatile int *abort_v = &abort_flag;
@@ -267,22 +278,24 @@ __global__ void __launch_bounds__(kMcThreads, 1)
       min(a.r1, a.r0 + 8 * static_cast<int>(static_cast<long long>(a.units) * (c + 1) / a.G));
   const int rounds = (row_hi - row_lo + a.H - 1) / a.H;
 
-  // shared memory: [ring | fragments | scale pairs | start values | raw activations | raw scales]
+  // shared memory: [ring (weight boxes, then scale boxes) | fragments | scale pairs | start
+  // values | (raw activations and scales, unless in ring slots kMcFirst..) | (partials)]
+  const int S = a.slots;
   const uint32_t raw_s = smem_addr(smem_raw);
   const uint32_t base_s = (raw_s + 1023u) & ~1023u;
   uint8_t *base = smem_raw + (base_s - raw_s);
-  const uint32_t ringq_s = base_s, ringd_s = base_s + kMcSlots * a.slot_q;
-  const float *ringd = reinterpret_cast<const float *>(base + kMcSlots * a.slot_q);
+  const uint32_t ringq_s = base_s, ringd_s = base_s + S * a.slot_q;
+  const float *ringd = reinterpret_cast<const float *>(base + S * a.slot_q);
   uint8_t *xf = base + a.ring;
   uint8_t *xdx = xf + static_cast<size_t>(a.xblocks) * kMcXfBlock;
   uint8_t *xcc = xdx + static_cast<size_t>(a.xblocks) * kMcXdBlock;
-  uint8_t *xraw = xcc + static_cast<size_t>(a.xblocks) * kMcXcBlock;  // 16 rows x xblocks x 32 B
+  uint8_t *xraw = base + a.xraw;  // 16 rows x xblocks x 32 B
   const float *xdraw = reinterpret_cast<const float *>(xraw + 16 * a.xblocks * kQK);  // 16 x xblocks
 
   if (rounds <= 0) return;  // the whole cluster has no rows
 
   if (tid == 0) {
-    for (int s = 0; s < kMcSlots; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(smem_addr(&full_bar[s]), 1);
       mbar_init(smem_addr(&empty_bar[s]), kMcConsumers);
     }
@@ -292,14 +305,17 @@ __global__ void __launch_bounds__(kMcThreads, 1)
   }
   __syncthreads();
 
-  // Thread 0 copies stage k of a round (rows y..y+H, blocks kb0 + 8k).  A
-  // slot is refilled once all warps released the stage it held.
-  uint32_t issued = 0;  // stages copied, over all rounds (thread 0)
+  // Thread 0 copies the stages in order: stage n is stage k = n % cp of round
+  // n / cp (rows y..y+H, blocks kb0 + 8k).  A slot is refilled once all
+  // warps released the stage it held.  With a separate partials area the
+  // copies run ahead into the next round while this one is reduced.
+  const int total = rounds * cp;
+  uint32_t issued = 0;  // stages copied (thread 0)
   auto issue = [&](int k, int y) -> bool {
-    const int slot = issued % kMcSlots;
-    if (issued >= kMcSlots) {
-      const uint32_t n = issued - kMcSlots;  // the stage that held this slot
-      if (!mc_wait(smem_addr(&empty_bar[slot]), (n / kMcSlots) & 1u, abort_v, a.wait_ns)) {
+    const int slot = issued % S;
+    if (static_cast<int>(issued) >= S) {
+      const uint32_t n = issued - S;  // the stage that held this slot
+      if (!mc_wait(smem_addr(&empty_bar[slot]), (n / S) & 1u, abort_v, a.wait_ns)) {
         if (atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
         return false;
       }
@@ -312,10 +328,14 @@ __global__ void __launch_bounds__(kMcThreads, 1)
     ++issued;
     return true;
   };
-  constexpr int kAhead = kMcSlots - 1;  // stages in flight while one is consumed
-  int next = 0;                         // next stage of the round to copy (thread 0)
-  if (tid == 0 && a.early)              // static weights: before the dependency wait
-    while (next < cp && next < kAhead && issue(next, row_lo)) ++next;
+  auto issue_next = [&]() -> bool {
+    return issue(static_cast<int>(issued) % cp, row_lo + static_cast<int>(issued) / cp * a.H);
+  };
+  // Stages 0..kMcFirst-1 go first (slots kMcFirst.. may hold the raw
+  // activations until they are converted), the rest of the ring after.
+  if (tid == 0 && a.early)  // static weights: before the dependency wait
+    while (static_cast<int>(issued) < min(total, kMcFirst) && issue_next()) {
+    }
 
   griddep_wait();  // the activations (and, unless static, the weights) come from earlier work
   griddep_launch_dependents();
@@ -326,7 +346,8 @@ __global__ void __launch_bounds__(kMcThreads, 1)
     mbar_arrive_expect_tx(xb, static_cast<uint32_t>(16 * a.xblocks * (kQK + 4)));
     tma_load_2d(smem_addr(xraw), &prm.xq, kb0 * (kQK / 8), 0, xb);
     tma_load_2d(smem_addr(xdraw), &prm.xd, kb0, 0, xb);
-    while (next < cp && next < kAhead && issue(next, row_lo)) ++next;
+    while (static_cast<int>(issued) < min(total, kMcFirst) && issue_next()) {
+    }
   }
   if (!warp_wait([&] { return mc_wait(smem_addr(&x_bar), 0, abort_v, a.wait_ns); })) {
     if (lane == 0 && atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
@@ -397,10 +418,12 @@ __global__ void __launch_bounds__(kMcThreads, 1)
     const int rlo = row_lo + r * a.H;
     const int rhi = min(row_hi, rlo + a.H);  // rows of this round
     const int tiles = (rhi - rlo + 15) / 16;
-    if (r > 0 && tid == 0) {
-      next = 0;
-      fence_proxy_async();  // the ring held partials and tile sums last round
-      while (next < cp && next < kAhead && !*abort_v && issue(next, rlo)) ++next;
+    // copies may run up to this stage (exclusive), S - 1 ahead of the one consumed
+    const int limit = a.parts != 0 ? total : (r + 1) * cp;
+    if (tid == 0 && (r == 0 || a.parts == 0)) {
+      if (r > 0) fence_proxy_async();  // the ring held partials and tile sums last round
+      while (static_cast<int>(issued) < min(limit, r * cp + S - 1) && !*abort_v && issue_next()) {
+      }
     }
 
     // acc[i][h][e]: tile 2i + (warp / 8), rows 2t, 2t+1 of half h, m = g + 8e
@@ -409,14 +432,18 @@ __global__ void __launch_bounds__(kMcThreads, 1)
     for (int i = 0; i < kMcMaxTpw; ++i) acc[i][0][0] = acc[i][0][1] = acc[i][1][0] = acc[i][1][1] = 0ull;
     const int nt = (tiles - par + 1) / 2;  // this warp's tiles
     for (int k = 0; k < cp; ++k, ++used) {
-      const int slot = used % kMcSlots;
+      const int slot = used % S;
       if (*abort_v) continue;
       const uint32_t fb = smem_addr(&full_bar[slot]);
-      const uint32_t ph = (used / kMcSlots) & 1u;
+      const uint32_t ph = (used / S) & 1u;
       if (!warp_wait([&] { return mc_wait(fb, ph, abort_v, a.wait_ns); })) {
         if (lane == 0 && atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
         continue;
       }
+      // refill the slot of the previous stage (all warps have most likely
+      // released it) before this one is computed: S - 1 stages stay in flight
+      if (tid == 0 && static_cast<int>(issued) < min(limit, static_cast<int>(used) + S) && !*abort_v)
+        issue_next();
       const int jb = k * kMcChunk + jw;  // part-local block
       const uint4 xa = *reinterpret_cast<const uint4 *>(xf + static_cast<size_t>(jb) * kMcXfBlock + lane * 16);
       const uint4 xb =
@@ -436,22 +463,20 @@ __global__ void __launch_bounds__(kMcThreads, 1)
       }
       __syncwarp();  // every lane is done with the stage
       if (lane == 0) mbar_arrive(smem_addr(&empty_bar[slot]));
-      // refill the slot of the previous stage, which the other warps have
-      // most likely released by now
-      if (tid == 0 && next < cp && !*abort_v && issue(next, rlo)) ++next;
     }
     if (tid == 0 && *abort_v) {
       // copies still landing after an abort (bounded)
-      for (uint32_t n = issued > kMcSlots ? issued - kMcSlots : 0; n < issued; ++n)
-        mbar_wait_bounded(smem_addr(&full_bar[n % kMcSlots]), (n / kMcSlots) & 1u, kDrainWaitNs);
+      for (uint32_t n = static_cast<int>(issued) > S ? issued - S : 0; n < issued; ++n)
+        mbar_wait_bounded(smem_addr(&full_bar[n % S]), (n / S) & 1u, kDrainWaitNs);
       mbar_wait_bounded(smem_addr(&x_bar), 0, kDrainWaitNs);
     }
     __syncthreads();
     if (*abort_v) used = issued = 0;  // results are void; keep the counters simple
 
-    // Partials: warp w, tile slot i -> 1 KB at (w * tpw + i), in the ring.
+    // Partials: warp w, tile slot i -> 1 KB at (w * tpw + i), in the ring
+    // or their own area.
     const int tpw = (tiles + 1) / 2;
-    uint8_t *parts = base;
+    uint8_t *parts = base + a.parts;
 #pragma unroll
     for (int i = 0; i < kMcMaxTpw; ++i) {
       if (i < nt) {
@@ -490,7 +515,7 @@ __global__ void __launch_bounds__(kMcThreads, 1)
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const int idx = tid + q * kMcThreads;
-      if ((idx >> 6) < tiles) *reinterpret_cast<float4 *>(base + idx * 16) = sum[q];
+      if ((idx >> 6) < tiles) *reinterpret_cast<float4 *>(parts + idx * 16) = sum[q];
     }
     cluster_sync();
 
@@ -501,7 +526,7 @@ __global__ void __launch_bounds__(kMcThreads, 1)
       const int f = tid & 63, idx = tau * 64 + f;
       float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       for (int q = 0; q < a.P; ++q) {
-        const float4 u = ld_cluster_f4(base_s + idx * 16, q);
+        const float4 u = ld_cluster_f4(base_s + a.parts + idx * 16, q);
         v.x += u.x;
         v.y += u.y;
         v.z += u.z;
@@ -516,7 +541,7 @@ __global__ void __launch_bounds__(kMcThreads, 1)
         if (m < a.M && rw < rhi) a.Y[static_cast<size_t>(m) * a.ldy + rw] = vals[e];
       }
     }
-    cluster_sync();  // no CTA refills its ring while others read its tile sums
+    cluster_sync_relaxed();  // no CTA reuses the area of its tile sums while others read them
   }
 }
 
@@ -553,16 +578,35 @@ static bool encode_2d(CUtensorMap *map, CUtensorMapDataType type, const void *pt
 // Clusters of P CTAs that fit on the device at once, by (P, activation chunks).
 static std::atomic<int> g_mc_clusters[kMcMaxCluster + 1][kMcMaxPart / kMcChunk + 1];
 
-static size_t mc_smem(int xblocks, int ring) {
-  return 1024 + static_cast<size_t>(ring) + static_cast<size_t>(xblocks) * kMcXPerBlock;
-}
-static int mc_ring(int H) {
+// Shared-memory layout of a launch (byte offsets from the 1024-aligned base).
+struct McLayout {
+  int slots, ring, xraw, parts;
+  size_t bytes;  // dynamic shared memory, alignment slack included
+};
+static bool mc_layout(int H, int xblocks, bool multi_round, McLayout *L) {
   const int slot_q = (H * kMcChunk * 16 + 1023) / 1024 * 1024;
   const int slot_d = (H * kMcChunk * 4 + 127) / 128 * 128;
   const int tiles = (H + 15) / 16;
-  const int parts = kMcConsumers * ((tiles + 1) / 2) * kMcTileBytes;  // partials reuse the ring
-  const int stages = kMcSlots * (slot_q + slot_d);
-  return stages > parts ? stages : parts;
+  const int parts = kMcConsumers * ((tiles + 1) / 2) * kMcTileBytes;
+  const int xfixed = xblocks * (kMcXfBlock + kMcXdBlock + kMcXcBlock);
+  const int raw = xblocks * kMcXRaw;
+  // most slots first; partials in their own area (several rounds) when it fits
+  for (int own = multi_round ? 1 : 0; own >= 0; --own) {
+    for (int S = kMcMaxSlots; S >= 4; --S) {
+      const bool alias = (S - kMcFirst) * slot_q >= raw;
+      const int stages = S * (slot_q + slot_d);
+      const int ring = own ? stages : (stages > parts ? stages : parts);
+      const size_t bytes = 1024 + static_cast<size_t>(ring) + xfixed + (alias ? 0 : raw) + (own ? parts : 0);
+      if (bytes > static_cast<size_t>(kMcSmemLimit)) continue;
+      L->slots = S;
+      L->ring = ring;
+      L->xraw = alias ? kMcFirst * slot_q : ring + xfixed;
+      L->parts = own ? ring + xfixed + (alias ? 0 : raw) : 0;
+      L->bytes = bytes;
+      return true;
+    }
+  }
+  return false;
 }
 
 cudaError_t launch_gemm_q4_mma_cluster(const LaunchCtx &ctx, const void *wq, const float *wd,
@@ -571,7 +615,13 @@ cudaError_t launch_gemm_q4_mma_cluster(const LaunchCtx &ctx, const void *wq, con
   const int n = r1 - r0;
   if (n <= 0 || M <= 0) return cudaSuccess;
   const int nchunks = (nb + kMcChunk - 1) / kMcChunk;
-  const int P = (nchunks * kMcChunk + kMcMaxPart - 1) / kMcMaxPart;
+  // the fewest K-parts whose activations fit (MLQ_MMA_CLUSTER=P asks for more: A/B timing)
+  static const int p_env = [] {
+    const char *e = std::getenv("MLQ_MMA_CLUSTER");
+    return e != nullptr ? std::atoi(e) : 0;
+  }();
+  const int p_min = (nchunks * kMcChunk + kMcMaxPart - 1) / kMcMaxPart;
+  const int P = p_env > p_min && p_env <= kMcMaxCluster && p_env <= nchunks ? p_env : p_min;
   // the scale map needs 16-byte row strides
   if (M > 16 || P > kMcMaxCluster || nb % 4 != 0) return cudaErrorNotSupported;
   McParams prm;
@@ -590,9 +640,8 @@ cudaError_t launch_gemm_q4_mma_cluster(const LaunchCtx &ctx, const void *wq, con
   a.xblocks = part_chunks * kMcChunk;
   a.units = (n + 7) / 8;
   auto kern = gemm_q4_mma_cluster_kernel;
-  static const cudaError_t attr = cudaFuncSetAttribute(
-      kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      static_cast<int>(mc_smem(kMcMaxPart, mc_ring(kMcMaxRows))));
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMcSmemLimit);
   if (attr != cudaSuccess) return attr;
 
   cudaLaunchConfig_t cfg = {};
@@ -610,9 +659,9 @@ cudaError_t launch_gemm_q4_mma_cluster(const LaunchCtx &ctx, const void *wq, con
 
   int clusters = g_mc_clusters[P][part_chunks].load(std::memory_order_relaxed);
   if (clusters == 0) {
-    // with the largest rounds: smaller ones only use less shared memory
+    // with the most shared memory a launch may take
     cfg.gridDim = dim3(static_cast<unsigned>(P * ctx.num_sms));
-    cfg.dynamicSmemBytes = mc_smem(a.xblocks, mc_ring(kMcMaxRows));
+    cfg.dynamicSmemBytes = kMcSmemLimit;
     if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
       cudaGetLastError();
       return cudaErrorNotSupported;
@@ -626,7 +675,14 @@ cudaError_t launch_gemm_q4_mma_cluster(const LaunchCtx &ctx, const void *wq, con
   a.H = 8 * ((per_cluster / 8 + nrounds - 1) / nrounds);
   a.slot_q = (a.H * kMcChunk * 16 + 1023) / 1024 * 1024;
   a.slot_d = (a.H * kMcChunk * 4 + 127) / 128 * 128;
-  a.ring = mc_ring(a.H);
+  // with several rounds, partials in their own area when it fits: the next
+  // round's copies then overlap this round's reduction
+  McLayout L;
+  if (!mc_layout(a.H, a.xblocks, nrounds > 1, &L)) return cudaErrorNotSupported;
+  a.slots = L.slots;
+  a.ring = L.ring;
+  a.xraw = L.xraw;
+  a.parts = L.parts;
   const size_t rowq = static_cast<size_t>(nb) * 16;
   if (!encode_2d(&prm.wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, rowq, static_cast<uint64_t>(rows), rowq,
                  kMcChunk * 16, static_cast<uint32_t>(a.H), CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -642,7 +698,7 @@ cudaError_t launch_gemm_q4_mma_cluster(const LaunchCtx &ctx, const void *wq, con
                  static_cast<uint32_t>(a.xblocks), 16, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorNotSupported;
   cfg.gridDim = dim3(static_cast<unsigned>(a.G * P));
-  cfg.dynamicSmemBytes = mc_smem(a.xblocks, a.ring);
+  cfg.dynamicSmemBytes = L.bytes;
   cfg.numAttrs = ctx.pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, prm);
 }

@@ -208,6 +208,30 @@ def test_gemm_small_m_parity(lib, Mr, rows, cols):
     assert nb > 0
 
 
+@pytest.mark.parametrize("rows,cols", [(24576, 4096), (8192, 16384)])
+def test_gemm_small_m_many_rows(lib, rows, cols):
+    """Enough rows that a cluster of the tensor-core kernel takes several
+    rounds (more than 160 rows each), at two K-part counts; checked on
+    sampled row windows, with an offset row range and a padded ldy."""
+    M = lib
+    Mr = 16
+    rng = np.random.default_rng(rows + cols)
+    wq, wd = rand_q4(rng, rows, cols)
+    X = rand_x(rng, Mr, cols)
+    Xq, Xd = oracle.quantize_q8(X)
+    r0, r1, ldy = 5, rows - 3, rows + 7
+    Y = torch.full((Mr, ldy), float("nan"), dtype=torch.float32, device=PT.DEV)
+    W = PT.weights_dev(oracle.Q4_0, wq, wd, rows, cols)
+    M.mlq_gemm_q4_small_m(Y, ldy, W, M.QAct(PT.to_dev(Xq), PT.to_dev(Xd), cols, Mr), Mr, r0, r1)
+    Yg = Y.cpu().numpy()
+    assert np.all(np.isnan(Yg[:, :r0])) and np.all(np.isnan(Yg[:, r1:]))
+    assert np.all(np.isfinite(Yg[:, r0:r1]))
+    wins = [(r0, r0 + 32), (r1 - 32, r1)] + [(a, a + 32) for a in rng.integers(r0, r1 - 32, 6)]
+    for m in range(Mr):
+        PT.check_matvec(oracle.Q4_0, wq, wd, rows, cols, Xq[m], Xd[m], r0, r1, windows=wins,
+                        y_gpu=Yg[m], what=f"M=16 {rows}x{cols} row m={m}")
+
+
 # ---------------------------------------------------------------------------
 # bounded device waits
 # ---------------------------------------------------------------------------
