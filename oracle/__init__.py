@@ -65,7 +65,17 @@ class Oracle:
         L.mlqo_block_sumi.argtypes = [P, I, P, I, I, P, I, I]
         L.mlqo_matvec.argtypes = [P, I, P, P, I, I, P, P, I, I]
         L.mlqo_gemm_small_m.argtypes = [P, I, I, P, P, I, I, P, P, I, I, I]
-        for f in (L.mlqo_quantize_q8, L.mlqo_block_sumi, L.mlqo_matvec, L.mlqo_gemm_small_m):
+        F = ctypes.c_float
+        L.mlqo_rmsnorm.argtypes = [P, P, P, I, F]
+        L.mlqo_softmax.argtypes = [P, I]
+        L.mlqo_silu_mul.argtypes = [P, P, I]
+        L.mlqo_add.argtypes = [P, P, I]
+        L.mlqo_rope_tables.argtypes = [P, P, I, I, F]
+        L.mlqo_rope.argtypes = [P, P, P, P, I, I, I]
+        L.mlqo_attention.argtypes = [P, P, P, P, I, I, I, I]
+        for f in (L.mlqo_quantize_q8, L.mlqo_block_sumi, L.mlqo_matvec, L.mlqo_gemm_small_m,
+                  L.mlqo_rmsnorm, L.mlqo_softmax, L.mlqo_silu_mul, L.mlqo_add, L.mlqo_rope_tables,
+                  L.mlqo_rope, L.mlqo_attention):
             f.restype = ctypes.c_int
         self.lib = L
         self.path = path
@@ -127,6 +137,63 @@ class Oracle:
         return Y
 
 
+def _f32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _ok(rc: int, what: str):
+    if rc != 0:
+        raise ValueError(f"oracle {what}: bad arguments")
+
+
+class _LayerOps:
+    """The floating-point steps of a decode layer (Design Spec Sec. 5 and 6);
+    each returns new float32 arrays and leaves its inputs unchanged."""
+
+    def rmsnorm(self, x, w, eps: float) -> np.ndarray:
+        x, w = _f32(x), _f32(w)
+        o = np.empty_like(x)
+        _ok(self.lib.mlqo_rmsnorm(_ptr(o), _ptr(x), _ptr(w), x.size, eps), "rmsnorm")
+        return o
+
+    def softmax(self, x) -> np.ndarray:
+        y = _f32(x).copy()
+        _ok(self.lib.mlqo_softmax(_ptr(y), y.size), "softmax")
+        return y
+
+    def silu_mul(self, g, u) -> np.ndarray:
+        y, u = _f32(g).copy(), _f32(u)
+        _ok(self.lib.mlqo_silu_mul(_ptr(y), _ptr(u), y.size), "silu_mul")
+        return y
+
+    def add(self, y, x) -> np.ndarray:
+        out, x = _f32(y).copy(), _f32(x)
+        _ok(self.lib.mlqo_add(_ptr(out), _ptr(x), out.size), "add")
+        return out
+
+    def rope_tables(self, max_seq: int, head_dim: int, theta: float):
+        c = np.empty((max_seq, head_dim // 2), dtype=np.float32)
+        s = np.empty_like(c)
+        _ok(self.lib.mlqo_rope_tables(_ptr(c), _ptr(s), max_seq, head_dim, theta), "rope_tables")
+        return c, s
+
+    def rope(self, q, k, cos_row, sin_row, head_dim: int, n_heads: int, n_kv_heads: int):
+        q2, k2 = _f32(q).copy(), _f32(k).copy()
+        _ok(self.lib.mlqo_rope(_ptr(q2), _ptr(k2), _ptr(_f32(cos_row)), _ptr(_f32(sin_row)),
+                               head_dim, n_heads, n_kv_heads), "rope")
+        return q2, k2
+
+    def attention(self, q, kc, vc, n_pos: int, head_dim: int, n_heads: int, n_kv_heads: int):
+        o = np.empty(n_heads * head_dim, dtype=np.float32)
+        _ok(self.lib.mlqo_attention(_ptr(o), _ptr(_f32(q)), _ptr(_f32(kc)), _ptr(_f32(vc)), n_pos,
+                                    head_dim, n_heads, n_kv_heads), "attention")
+        return o
+
+
+for _name in ("rmsnorm", "softmax", "silu_mul", "add", "rope_tables", "rope", "attention"):
+    setattr(Oracle, _name, getattr(_LayerOps, _name))
+
+
 def default() -> Oracle:
     global _default
     if _default is None:
@@ -148,3 +215,31 @@ def matvec(*a, **k):
 
 def gemm_small_m(*a, **k):
     return default().gemm_small_m(*a, **k)
+
+
+def rmsnorm(*a, **k):
+    return default().rmsnorm(*a, **k)
+
+
+def softmax(*a, **k):
+    return default().softmax(*a, **k)
+
+
+def silu_mul(*a, **k):
+    return default().silu_mul(*a, **k)
+
+
+def add(*a, **k):
+    return default().add(*a, **k)
+
+
+def rope_tables(*a, **k):
+    return default().rope_tables(*a, **k)
+
+
+def rope(*a, **k):
+    return default().rope(*a, **k)
+
+
+def attention(*a, **k):
+    return default().attention(*a, **k)

@@ -44,6 +44,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define ORACLE_QK 32
@@ -167,5 +168,143 @@ int mlqo_gemm_small_m(float *Y, int ldy, int type, const uint8_t *wq, const floa
                              Xq + (size_t)m * cols, Xd + (size_t)m * nb, r0, r1);
         if (rc != 0) return rc;
     }
+    return 0;
+}
+
+
+/* ========================================================================
+ * The floating-point steps of a decode layer around the products.
+ *
+ * Source: the page "Legacy-ISA ML Inference Runtime -- Design Spec",
+ * Sec. 5 (Kernel Interface: ml_k_rmsnorm, ml_k_softmax, ml_k_rope,
+ * ml_k_silu_mul, ml_k_add, ml_k_dot_f32, ml_k_axpy_f32, and the notes on
+ * RoPE: interleaved pairs (2i, 2i+1), freq_i = theta^(-2i/head_dim),
+ * cos/sin tables of [max_seq][head_dim/2] precomputed at load) and Sec. 6
+ * (Forward pass per token: attention per head as dot_f32 / sqrt(hd),
+ * softmax, sum of axpy over positions; GQA: the KV head of query head h is
+ * h / (n_heads / n_kv_heads)).  The page fixes float32 interfaces but not
+ * the internal precision of these steps, so they are computed here in
+ * double and rounded to float once per output (readings listed in
+ * the design doc):
+ *   - rmsnorm: o_j = w_j * x_j / sqrt(sum_i x_i^2 / n + eps)
+ *   - softmax: x_j = exp(x_j - max) / sum_i exp(x_i - max)
+ *   - silu_mul: g_j = g_j / (1 + exp(-g_j)) * u_j
+ *   - rope: (a, b) -> (a cos - b sin, a sin + b cos) on every pair of every
+ *     q head and k head, with the float tables given
+ *   - attention over positions t = 0..n_pos-1 of a float32 KV cache whose
+ *     row t holds the n_kv_heads heads of K (or V) one after another.
+ * ====================================================================== */
+
+int mlqo_rmsnorm(float *o, const float *x, const float *w, int n, float eps)
+{
+    if (n <= 0) return -1;
+    double ss = 0.0;
+    for (int i = 0; i < n; ++i) ss += (double)x[i] * (double)x[i];
+    const double inv = 1.0 / sqrt(ss / (double)n + (double)eps);
+    for (int j = 0; j < n; ++j) o[j] = (float)((double)w[j] * ((double)x[j] * inv));
+    return 0;
+}
+
+int mlqo_softmax(float *x, int n)
+{
+    if (n <= 0) return -1;
+    double mx = x[0];
+    for (int i = 1; i < n; ++i) if (x[i] > mx) mx = x[i];
+    double sum = 0.0;
+    for (int i = 0; i < n; ++i) sum += exp((double)x[i] - mx);
+    for (int j = 0; j < n; ++j) x[j] = (float)(exp((double)x[j] - mx) / sum);
+    return 0;
+}
+
+int mlqo_silu_mul(float *g, const float *u, int n)
+{
+    if (n < 0) return -1;
+    for (int j = 0; j < n; ++j) {
+        const double a = g[j];
+        g[j] = (float)(a / (1.0 + exp(-a)) * (double)u[j]);
+    }
+    return 0;
+}
+
+int mlqo_add(float *y, const float *x, int n)
+{
+    if (n < 0) return -1;
+    for (int j = 0; j < n; ++j) y[j] = (float)((double)y[j] + (double)x[j]);
+    return 0;
+}
+
+/* Row `pos` of the cos/sin tables: angle_i = pos * theta^(-2i/head_dim). */
+int mlqo_rope_tables(float *cos_t, float *sin_t, int max_seq, int head_dim, float theta)
+{
+    if (head_dim <= 0 || head_dim % 2 != 0 || max_seq <= 0) return -1;
+    const int half = head_dim / 2;
+    for (int pos = 0; pos < max_seq; ++pos)
+        for (int i = 0; i < half; ++i) {
+            const double freq = pow((double)theta, -2.0 * i / (double)head_dim);
+            const double ang = (double)pos * freq;
+            cos_t[(size_t)pos * half + i] = (float)cos(ang);
+            sin_t[(size_t)pos * half + i] = (float)sin(ang);
+        }
+    return 0;
+}
+
+static void rope_head(float *v, const float *c, const float *s, int head_dim)
+{
+    for (int i = 0; i < head_dim / 2; ++i) {
+        const double a = v[2 * i], b = v[2 * i + 1];
+        v[2 * i] = (float)(a * c[i] - b * s[i]);
+        v[2 * i + 1] = (float)(a * s[i] + b * c[i]);
+    }
+}
+
+/* q: n_heads x head_dim, k: n_kv_heads x head_dim, both rotated in place;
+ * cos_t, sin_t: the table rows of the position (head_dim/2 each). */
+int mlqo_rope(float *q, float *k, const float *cos_t, const float *sin_t, int head_dim,
+              int n_heads, int n_kv_heads)
+{
+    if (head_dim <= 0 || head_dim % 2 != 0 || n_heads < 0 || n_kv_heads < 0) return -1;
+    for (int h = 0; h < n_heads; ++h) rope_head(q + (size_t)h * head_dim, cos_t, sin_t, head_dim);
+    for (int h = 0; h < n_kv_heads; ++h) rope_head(k + (size_t)h * head_dim, cos_t, sin_t, head_dim);
+    return 0;
+}
+
+/* o: n_heads x head_dim.  For query head h with KV head g = h / (n_heads /
+ * n_kv_heads): s_t = dot(q_h, K[t][g]) / sqrt(head_dim) for t < n_pos,
+ * softmax over t, o_h = sum_t p_t V[t][g] accumulated in t order. */
+int mlqo_attention(float *o, const float *q, const float *kc, const float *vc, int n_pos,
+                   int head_dim, int n_heads, int n_kv_heads)
+{
+    if (n_pos <= 0 || head_dim <= 0 || n_heads <= 0 || n_kv_heads <= 0 ||
+        n_heads % n_kv_heads != 0)
+        return -1;
+    const int kv_dim = n_kv_heads * head_dim, group = n_heads / n_kv_heads;
+    double *p = (double *)malloc((size_t)n_pos * sizeof(double));
+    if (p == NULL) return -2;
+    for (int h = 0; h < n_heads; ++h) {
+        const int g = h / group;
+        const float *qh = q + (size_t)h * head_dim;
+        /* scores: dot_f32(q_h, K_t) / sqrt(hd) */
+        for (int t = 0; t < n_pos; ++t) {
+            const float *kt = kc + (size_t)t * kv_dim + (size_t)g * head_dim;
+            double dot = 0.0;
+            for (int i = 0; i < head_dim; ++i) dot += (double)qh[i] * (double)kt[i];
+            p[t] = dot / sqrt((double)head_dim);
+        }
+        /* softmax over the positions */
+        double mx = p[0], sum = 0.0;
+        for (int t = 1; t < n_pos; ++t) if (p[t] > mx) mx = p[t];
+        for (int t = 0; t < n_pos; ++t) { p[t] = exp(p[t] - mx); sum += p[t]; }
+        for (int t = 0; t < n_pos; ++t) p[t] /= sum;
+        /* o_h = sum over t of axpy(p_t, V_t) */
+        double *acc = (double *)calloc((size_t)head_dim, sizeof(double));
+        if (acc == NULL) { free(p); return -2; }
+        for (int t = 0; t < n_pos; ++t) {
+            const float *vt = vc + (size_t)t * kv_dim + (size_t)g * head_dim;
+            for (int i = 0; i < head_dim; ++i) acc[i] += p[t] * (double)vt[i];
+        }
+        for (int i = 0; i < head_dim; ++i) o[(size_t)h * head_dim + i] = (float)acc[i];
+        free(acc);
+    }
+    free(p);
     return 0;
 }

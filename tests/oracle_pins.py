@@ -278,7 +278,123 @@ def pin_small_m_rows_independent(O, seed=5):
         assert abs(float(Y[m, 5]) - ex) <= tol + 1e-300
 
 
+# ----------------------------------------------------------------------------
+# the floating-point steps of a decode layer (Design Spec Sec. 5 and Sec. 6)
+# ----------------------------------------------------------------------------
+def pin_rmsnorm_closed_form(O):
+    """x = (3, 4, 0, 0): the mean square is 25/4; with eps = 11/4 the root is
+    exactly 3, so o = w * x / 3 exactly.  Leaving out the mean, putting eps
+    outside the root or dropping w all break it."""
+    x = np.array([3, 4, 0, 0], np.float32)
+    w = np.array([3, 3, 1, 1], np.float32)
+    o = O.rmsnorm(x, w, 2.75)
+    assert np.array_equal(o, np.array([3, 4, 0, 0], np.float32)), o
+    # degree-0 homogeneity without eps: rmsnorm(c x) = rmsnorm(x)
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal(96).astype(np.float32)
+    w = rng.uniform(0.5, 2, 96).astype(np.float32)
+    a, b = O.rmsnorm(x, w, 0.0), O.rmsnorm(np.float32(8) * x, w, 0.0)
+    assert np.allclose(a, b, rtol=4 * U, atol=0)
+    # the root mean square of the normalised vector with unit weights is 1
+    o = O.rmsnorm(x, np.ones(96, np.float32), 0.0).astype(np.float64)
+    assert abs(np.sqrt(np.mean(o * o)) - 1.0) < 1e-6
+
+
+def pin_softmax_values(O):
+    """exp of (0, ln 2, ln 3) is (1, 2, 3): the result is (1/6, 1/3, 1/2);
+    adding 1000 to every input changes nothing (no overflow either)."""
+    v = np.array([0.0, np.log(2.0), np.log(3.0)], np.float32)
+    y = O.softmax(v).astype(np.float64)
+    assert np.allclose(y, [1 / 6, 1 / 3, 1 / 2], rtol=1e-6, atol=0), y
+    y2 = O.softmax(v + np.float32(1000)).astype(np.float64)
+    assert np.all(np.isfinite(y2)) and np.allclose(y2, [1 / 6, 1 / 3, 1 / 2], rtol=1e-4, atol=0)
+    rng = np.random.default_rng(22)
+    z = O.softmax(rng.standard_normal(257).astype(np.float32) * 5).astype(np.float64)
+    assert abs(z.sum() - 1.0) < 1e-5 and np.all(z > 0)
+
+
+def pin_silu_mul_values(O):
+    """silu(x) = x sigma(x): silu(0) = 0, silu(ln 3) = (3/4) ln 3, and
+    silu(x) - silu(-x) = x for every x (sigma(x) + sigma(-x) = 1)."""
+    g = np.array([0.0, np.log(3.0)], np.float32)
+    y = O.silu_mul(g, np.array([5.0, 2.0], np.float32)).astype(np.float64)
+    assert y[0] == 0.0 and abs(y[1] - 2 * 0.75 * float(np.float32(np.log(3.0)))) < 1e-6
+    rng = np.random.default_rng(23)
+    x = rng.uniform(-6, 6, 200).astype(np.float32)
+    one = np.ones(200, np.float32)
+    d = O.silu_mul(x, one).astype(np.float64) - O.silu_mul(-x, one).astype(np.float64)
+    assert np.allclose(d, x.astype(np.float64), rtol=0, atol=2e-6)
+
+
+def pin_add_exact(O):
+    """y += x is one rounded float32 addition per element."""
+    rng = np.random.default_rng(24)
+    y = rng.standard_normal(100).astype(np.float32)
+    x = rng.standard_normal(100).astype(np.float32)
+    assert np.array_equal(O.add(y, x), (y + x).astype(np.float32))
+
+
+def pin_rope_tables_and_pairs(O):
+    """Tables: position 0 is the identity; with head_dim 4 and theta 100 the
+    second pair turns at 100^(-1/2) = 0.1 per position.  Rotation: the pairs
+    are (2i, 2i+1), each turned by +angle; a q head (1, 0, 0, 1) at position
+    1 becomes (cos 1, sin 1, -sin 0.1, cos 0.1)."""
+    import math
+    c, s = O.rope_tables(4, 4, 100.0)
+    assert np.array_equal(c[0], [1, 1]) and np.array_equal(s[0], [0, 0])
+    assert abs(float(c[3, 1]) - math.cos(0.3)) < 1e-7 and abs(float(s[3, 1]) - math.sin(0.3)) < 1e-7
+    assert abs(float(c[2, 0]) - math.cos(2.0)) < 1e-7
+    q = np.array([1, 0, 0, 1, 0.5, -2, 3, 1], np.float32)  # two q heads
+    k = np.array([0, 1, 1, 0], np.float32)                   # one k head
+    q2, k2 = O.rope(q, k, c[1], s[1], 4, 2, 1)
+    want = [math.cos(1), math.sin(1), -math.sin(0.1), math.cos(0.1)]
+    assert np.allclose(q2[:4], want, atol=1e-7), q2
+    assert np.allclose(k2, [-math.sin(1), math.cos(1), math.cos(0.1), math.sin(0.1)], atol=1e-7), k2
+    # each pair keeps its length
+    n0 = np.hypot(q[4::2], q[5::2])
+    n1 = np.hypot(q2[4::2], q2[5::2])
+    assert np.allclose(n0, n1, rtol=1e-6)
+
+
+def pin_attention_cases(O):
+    """One position: o = V_0.  Zero query: uniform weights, o = mean of V.
+    Scale: with q . K_0 = 2 and head_dim 4 the score is 2 / 2 = 1, so two
+    positions with V = (1, 0) give e / (1 + e).  GQA: with 4 query heads and
+    2 KV heads, heads 0, 1 read KV head 0 and heads 2, 3 read KV head 1."""
+    import math
+    hd, nh, nkv = 4, 4, 2
+    rng = np.random.default_rng(25)
+    q = rng.standard_normal(nh * hd).astype(np.float32)
+    kc = rng.standard_normal((3, nkv * hd)).astype(np.float32)
+    vc = rng.standard_normal((3, nkv * hd)).astype(np.float32)
+    o = O.attention(q, kc, vc, 1, hd, nh, nkv)
+    for h in range(nh):
+        g = h // (nh // nkv)
+        assert np.array_equal(o[h * hd:(h + 1) * hd], vc[0, g * hd:(g + 1) * hd])
+    o = O.attention(np.zeros(nh * hd, np.float32), kc, vc, 3, hd, nh, nkv)
+    for h in range(nh):
+        g = h // (nh // nkv)
+        assert np.allclose(o[h * hd:(h + 1) * hd], vc[:, g * hd:(g + 1) * hd].astype(np.float64).mean(0),
+                           rtol=1e-6, atol=1e-7)
+    q1 = np.zeros(hd, np.float32); q1[0] = 1
+    k2 = np.zeros((2, hd), np.float32); k2[0, 0] = 2
+    v2 = np.zeros((2, hd), np.float32); v2[0, :] = 1
+    o = O.attention(q1, k2, v2, 2, hd, 1, 1)
+    assert np.allclose(o, math.e / (1 + math.e), rtol=1e-6), o
+    # distinct constant V per KV head: the mapping shows in every output
+    vconst = np.repeat(np.array([[10.0, 20.0]], np.float32), 4, axis=1).reshape(1, -1)
+    vconst = np.repeat(vconst, 3, axis=0)
+    o = O.attention(q, kc, vconst, 3, hd, nh, nkv)
+    assert np.allclose(o.reshape(nh, hd)[:, 0], [10, 10, 20, 20], rtol=1e-6), o
+
+
 ALL_PINS = [
+    pin_rmsnorm_closed_form,
+    pin_softmax_values,
+    pin_silu_mul_values,
+    pin_add_exact,
+    pin_rope_tables_and_pairs,
+    pin_attention_cases,
     pin_golden_quantize,
     pin_golden_block_dot,
     pin_quantize_invariants,

@@ -32,6 +32,18 @@ MUTANTS = [
     ("dot_drops_last", "for (int j = 0; j < ORACLE_QK; ++j) s +=", "for (int j = 0; j < ORACLE_QK - 1; ++j) s +="),
     ("row_range_from_zero", "for (int r = r0; r < r1; ++r) {\n        float sum", "for (int r = 0; r < r1; ++r) {\n        float sum"),
     ("small_m_row_stride", "Y + (size_t)m * ldy", "Y + (size_t)m * rows"),
+    ("rmsnorm_no_mean", "sqrt(ss / (double)n + (double)eps)", "sqrt(ss + (double)eps)"),
+    ("rmsnorm_eps_outside", "sqrt(ss / (double)n + (double)eps)", "(sqrt(ss / (double)n) + (double)eps)"),
+    ("softmax_no_max_in_sum", "sum += exp((double)x[i] - mx);", "sum += exp((double)x[i]);"),
+    ("silu_sign", "a / (1.0 + exp(-a))", "a / (1.0 + exp(a))"),
+    ("add_subtracts", "(double)y[j] + (double)x[j]", "(double)y[j] - (double)x[j]"),
+    ("rope_freq_halved", "-2.0 * i / (double)head_dim", "-1.0 * i / (double)head_dim"),
+    ("rope_sign", "a * c[i] - b * s[i]", "a * c[i] + b * s[i]"),
+    ("rope_k_not_rotated", "for (int h = 0; h < n_kv_heads; ++h) rope_head", "for (int h = 0; h < 0; ++h) rope_head"),
+    ("attention_no_scale", "p[t] = dot / sqrt((double)head_dim);", "p[t] = dot;"),
+    ("attention_gqa_modulo", "const int g = h / group;", "const int g = h % n_kv_heads;"),
+    ("attention_drops_last", "for (int t = 0; t < n_pos; ++t) {\n            const float *vt",
+     "for (int t = 0; t < n_pos - 1; ++t) {\n            const float *vt"),
 ]
 
 
