@@ -262,6 +262,56 @@ class OraclePass:
             fp[mv.name] = Y
 
 
+class OracleLayerPass:
+    """One token through one decode layer with the oracle (Design Spec Sec. 6
+    forward pass): the same seeded inputs as the GPU layer, the products'
+    rows split over `threads` host threads."""
+
+    def __init__(self, shape, threads: int):
+        import numpy as np
+        from concurrent.futures import ThreadPoolExecutor
+
+        import oracle
+        from block_quantized_decode_gb300 import inputs as I
+        self.np, self.O, self.s, self.threads = np, oracle, shape, threads
+        self.pool = ThreadPoolExecutor(max_workers=threads)
+        self.W = {name: I.weights(shape.wtype, rows, cols, shape.seed + i) + (rows, cols)
+                  for i, (name, rows, cols) in enumerate(shape.mats())}
+        self.att_norm = I.norm_weights(shape.dim, shape.seed + 10)
+        self.ffn_norm = I.norm_weights(shape.dim, shape.seed + 11)
+        self.kc = np.zeros((shape.pos + 1, shape.kv_dim), np.float32)
+        self.vc = np.zeros_like(self.kc)
+        self.kc[:shape.pos] = I.kv_history(shape.pos, shape.kv_dim, shape.seed + 12)
+        self.vc[:shape.pos] = I.kv_history(shape.pos, shape.kv_dim, shape.seed + 13)
+        self.x0 = I.activations(1, shape.dim, shape.seed + 14)[0]
+        self.cos, self.sin = oracle.rope_tables(shape.pos + 1, shape.head_dim, shape.rope_theta)
+        self.weight_bytes = sum(q.nbytes + d.nbytes for q, d, _, _ in self.W.values())
+        self.ops = sum(2 * rows * cols for _, _, rows, cols in self.W.values())
+
+    def _mv(self, name, xq, xd):
+        q, d, rows, cols = self.W[name]
+        y = self.np.zeros(rows, dtype=self.np.float32)
+        cuts = [rows * t // self.threads for t in range(self.threads + 1)]
+        futs = [self.pool.submit(self.O.matvec, self.s.wtype, q, d, rows, cols, xq, xd, a, b, y)
+                for a, b in zip(cuts, cuts[1:]) if b > a]
+        for f in futs:
+            f.result()
+        return y
+
+    def run(self):
+        O, s = self.O, self.s
+        x = self.x0.copy()
+        h = O.quantize_q8(O.rmsnorm(x, self.att_norm, s.norm_eps))
+        q, k, v = (self._mv(n, *h) for n in ("wq", "wk", "wv"))
+        q, k = O.rope(q, k, self.cos[s.pos], self.sin[s.pos], s.head_dim, s.n_heads, s.n_kv_heads)
+        self.kc[s.pos], self.vc[s.pos] = k, v
+        o = O.attention(q, self.kc, self.vc, s.pos + 1, s.head_dim, s.n_heads, s.n_kv_heads)
+        x = O.add(x, self._mv("wo", *O.quantize_q8(o)))
+        h = O.quantize_q8(O.rmsnorm(x, self.ffn_norm, s.norm_eps))
+        g = O.silu_mul(self._mv("w1", *h), self._mv("w3", *h))
+        return O.add(x, self._mv("w2", *O.quantize_q8(g)))
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -270,7 +320,8 @@ def host_cores() -> int:
 
 
 def time_oracle(wl, seconds: float, threads: int, max_steps: int | None = None):
-    op = OraclePass(wl, threads)
+    from block_quantized_decode_gb300 import inputs as I
+    op = OracleLayerPass(wl, threads) if isinstance(wl, I.LayerShape) else OraclePass(wl, threads)
     op.run()  # warm (page-in, thread start)
     n, t0 = 0, time.perf_counter()
     while True:
@@ -288,8 +339,10 @@ def time_oracle(wl, seconds: float, threads: int, max_steps: int | None = None):
 def run_reference(args, wl, world, rank):
     if rank != 0:
         return 0
+    from block_quantized_decode_gb300 import inputs as I
     threads = host_cores()
-    op = OraclePass(wl, threads)
+    layer = isinstance(wl, I.LayerShape)
+    op = OracleLayerPass(wl, threads) if layer else OraclePass(wl, threads)
     for _ in range(min(max(0, args.warmup), 3)):
         op.run()
     t0 = time.perf_counter()
@@ -303,7 +356,7 @@ def run_reference(args, wl, world, rank):
         "steps": steps, "warmup": args.warmup, "ms_per_step": el / steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8 dot -> int32, f32 accumulate (CPU oracle)", "data": "synthetic",
-        "config": {"workload": wl.name, "M": wl.m, "weight_bytes_per_step": op.weight_bytes},
+        "config": {"workload": wl.name, "M": 1 if layer else wl.m, "weight_bytes_per_step": op.weight_bytes},
         "gops": op.ops * args.steps / el / 1e9,
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"{steps} full passes of {wl.name} after {args.warmup} warm-up"},
@@ -619,16 +672,200 @@ def run_ours(args, wl, world, rank, local, pg):
     return 0
 
 
+def run_layer(args, shape, world, rank, local, pg):
+    """A whole decode layer (Design Spec Sec. 6) per step: the ten launches
+    of DecodeLayer.step for one token at position shape.pos, captured in a
+    CUDA graph per weight copy.  value = weight bytes per step / step time
+    (the metric's weight GB/s); the KV-cache bytes the attention reads are
+    reported beside it."""
+    import torch
+
+    import block_quantized_decode_gb300 as M
+    from block_quantized_decode_gb300.layer import DecodeLayer
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    M.mlq_init()
+    props = torch.cuda.get_device_properties(local)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
+    probe = DecodeLayer(shape, copies=1, device=f"cuda:{local}")
+    wbytes = probe.weight_bytes()
+    copies = args.copies or max(2, math.ceil(3 * l2 / wbytes))
+    del probe
+    L = DecodeLayer(shape, copies=copies, device=f"cuda:{local}")
+    L.x.copy_(torch.from_numpy(L.x_in))
+    kvb = L.kv_bytes()
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for c in range(copies):
+            L.step(copy=c, stream=stream)
+    stream.synchronize()
+    graphs = []
+    cycle = None
+    if not args.no_graph:
+        for c in range(copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                L.step(copy=c, stream=stream)
+            graphs.append(g)
+        cycle = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cycle, stream=stream):
+            for c in range(copies):
+                L.step(copy=c, stream=stream)
+
+    def do_step(i):
+        if graphs:
+            graphs[i % copies].replay()
+        else:
+            L.step(copy=i % copies, stream=stream)
+
+    def do_steps(n):
+        i = 0
+        if cycle is not None:
+            while n - i >= copies:
+                cycle.replay()
+                i += copies
+        while i < n:
+            do_step(i)
+            i += 1
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    warm = max(args.warmup, copies if cycle is not None else 0)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a0.record(stream)
+        do_steps(warm)
+        a1.record(stream)
+    stream.synchronize()
+    steps = args.steps
+    if steps <= 0:
+        per = a0.elapsed_time(a1) / 1e3 / max(1, warm)
+        steps = max(10, int(args.seconds / max(per, 1e-7)))
+        steps = int(max_over_ranks(pg, float(steps), dev))
+    barrier(pg, local)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        do_steps(steps)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    barrier(pg, local)
+    clk = clocks.stop(t_host0, t_host1)
+    ms = e0.elapsed_time(e1)
+    ms_max = max_over_ranks(pg, ms, dev)
+    value = world * wbytes * steps / (ms_max / 1e3) / 1e9
+    peaks, peak_src = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+
+    # ---- per launch: each of the ten launches replayed back to back in its
+    # own graph (the products on rotating weight copies), CUDA events
+    names = ["rmsnorm_att", "qkv", "rope", "attention", "wo", "add_rmsnorm_ffn", "ffn",
+             "silu_mul", "down", "add"]
+    per_launch = {}
+    for nm in names:
+        reps = 2 * copies
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(reps):
+                L.launch(nm, copy=j % copies, stream=stream)
+        with torch.cuda.stream(stream):
+            g.replay()
+        stream.synchronize()
+        best = None
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+            stream.synchronize()
+            t = a.elapsed_time(b) / 1e3 / reps
+            best = t if best is None else min(best, t)
+        per_launch[nm] = best * 1e6
+        del g
+    phase_b = {n: sum(L.host[m][0].nbytes + L.host[m][1].nbytes for m in ms)
+               for n, ms in (("qkv", ("wq", "wk", "wv")), ("wo", ("wo",)), ("ffn", ("w1", "w3")),
+                             ("down", ("w2",)))}
+    ph_us = sum(per_launch[n] for n in phase_b)
+    ach = sum(phase_b.values()) / (ph_us * 1e-6) / 1e9
+    roofline = {"kernel": "phase_kernel", "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                "frac": ach / hbm, "peak_source": peak_src,
+                "traffic": ncu_traffic("phase_tinyllama1.1b_layer_q4_0",
+                                       ("phase.cu", "phase_common.cuh", "mlq_device.cuh"),
+                                       sum(phase_b.values()) / 4),
+                "bytes_per_launch": sum(phase_b.values()) / 4, "us_per_launch": ph_us / 4,
+                "method": "each of the ten launches replayed back to back in its own graph "
+                          "(products on rotating weight copies), best of 3, CUDA events",
+                "us_per_launch_kind": per_launch}
+
+    # ---- end to end: x from pinned host memory, the step, x back to pinned host
+    host_x = torch.empty(shape.dim, dtype=torch.float32).pin_memory()
+    e2e_steps = min(steps, 500)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        with torch.cuda.stream(stream):
+            L.x.copy_(L.x_host, non_blocking=True)
+            do_step(i)
+            host_x.copy_(L.x, non_blocking=True)
+        stream.synchronize()
+    e2e_s = max_over_ranks(pg, time.perf_counter() - t0, dev)
+    e2e = {"value": world * wbytes * e2e_steps / e2e_s / 1e9, "unit": UNIT,
+           "h2d_bytes_per_step": 4 * shape.dim, "d2h_bytes_per_step": 4 * shape.dim,
+           "steps": e2e_steps, "how": "wall clock; per step: pinned H2D of x, graph replay of the "
+                                      "ten C-ABI calls, D2H of x, stream sync"}
+    assert M.mlq_last_device_error(stream) == M.MLQ_OK
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        threads = host_cores()
+        op, n, el = time_oracle(shape, args.cpu_seconds, threads)
+        cpu = {"value": op.weight_bytes * n / el / 1e9, "unit": UNIT, "cores": threads,
+               "kind": "oracle",
+               "sample": f"{n} tokens through the layer in {el:.1f} s, product rows split over "
+                         f"{threads} threads"}
+    if rank == 0:
+        ops = sum(2 * rows * cols for _, rows, cols in shape.mats())
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+            "warmup": warm, "ms_per_step": ms_max / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "q4_0 products: int8 dot -> int32, f32 accumulate; f32 norm, rope, attention",
+            "data": "synthetic",
+            "config": {"workload": shape.name, "M": 1, "pos": shape.pos,
+                       "matrices": [f"{n}:{r}x{c}:q4_0" for n, r, c in shape.mats()],
+                       "weight_bytes_per_step": wbytes, "kv_bytes_per_step": kvb,
+                       "hbm_frac_with_kv": (wbytes + kvb) * world * steps / (ms_max / 1e3) / 1e9 / hbm,
+                       "l2": f"inputs larger than L2: {copies} rotating weight copies "
+                             f"({copies * wbytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
+                       "graphs": ("one graph per cycle of %d steps" % copies) if cycle is not None else False,
+                       "path": "layer", "parallelism": f"replicas x{world} (independent decode streams)"},
+            "gops": world * ops * steps / (ms_max / 1e3) / 1e9, "hbm_frac": value / world / hbm,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": L.launches_per_step * steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     from block_quantized_decode_gb300 import inputs as I
-    if args.workload not in I.WORKLOADS:
-        raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(I.WORKLOADS)}")
-    wl = I.WORKLOADS[args.workload]()
+    if args.workload not in I.WORKLOADS and args.workload not in I.LAYERS:
+        raise SystemExit(f"unknown workload {args.workload}; choose from "
+                         f"{sorted(I.WORKLOADS) + sorted(I.LAYERS)}")
+    wl = (I.LAYERS[args.workload] if args.workload in I.LAYERS else I.WORKLOADS[args.workload])()
     world, rank, local, pg = dist_setup(args)
     try:
         if args.impl == "reference":
             return run_reference(args, wl, world, rank)
+        if isinstance(wl, I.LayerShape):
+            return run_layer(args, wl, world, rank, local, pg)
         return run_ours(args, wl, world, rank, local, pg)
     finally:
         if pg is not None:

@@ -1,5 +1,6 @@
 """GB300 (sm_103a) block-quantized decode: Q8_0 activation quantiser,
 M = 1 Q4_0 / Q8_0 matrix-vector products and the small-M batched product,
+the decode steps around them (rmsnorm, RoPE, GQA attention, silu_mul, add),
 behind the C ABI of libmlq.so (include/mlq.h).
 
 The Python names below are the C entry points of the same names; they only
@@ -12,4 +13,6 @@ from .binding import (  # noqa: F401
     MLQ_F_STATIC_WEIGHTS, MlqError, QAct, QTensor, lib, mlq_block_sumi, mlq_debug_set_wait_limit_ns,
     mlq_gemm_q4_small_m, mlq_init, mlq_last_device_error, mlq_matvec_q4, mlq_matvec_q8,
     mlq_prefetch_l2, mlq_quantize_q8, mlq_status_str,
+    MLQ_MAX_SEQ, MLQ_MAX_HEAD_DIM, mlq_rmsnorm, mlq_add_rmsnorm, mlq_add, mlq_softmax, mlq_silu_mul,
+    mlq_rope_tables, mlq_rope, mlq_attention,
 )

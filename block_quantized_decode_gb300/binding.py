@@ -28,7 +28,11 @@ EXPORTS = (
     "mlq_debug_set_wait_limit_ns", "mlq_status_str", "mlq_prefetch_l2",
     "mlq_chain_workspace_bytes", "mlq_decode_chain", "mlq_matvec_fused",
     "mlq_decode_chain_static", "mlq_decode_phase",
+    "mlq_rmsnorm", "mlq_add_rmsnorm", "mlq_add", "mlq_softmax", "mlq_silu_mul",
+    "mlq_rope_tables", "mlq_rope", "mlq_attention",
 )
+MLQ_MAX_SEQ = 32768
+MLQ_MAX_HEAD_DIM = 256
 MLQ_FUSED_MAX_PRODUCTS = 8
 MLQ_F_STATIC_WEIGHTS = 1
 MLQ_CHAIN_MAX_PRODUCTS = 32
@@ -102,6 +106,15 @@ def lib() -> ctypes.CDLL:
                                        ctypes.c_uint, P]
         L.mlq_decode_phase.argtypes = [ctypes.POINTER(_PhaseInput), ctypes.POINTER(_PhaseProduct),
                                        I, P, P, I, ctypes.c_uint, P]
+        F = ctypes.c_float
+        L.mlq_rmsnorm.argtypes = [P, P, P, I, F, QA, P]
+        L.mlq_add_rmsnorm.argtypes = [P, P, P, I, F, P, QA, P]
+        L.mlq_add.argtypes = [P, P, I, P]
+        L.mlq_softmax.argtypes = [P, I, P]
+        L.mlq_silu_mul.argtypes = [P, P, I, QA, P]
+        L.mlq_rope_tables.argtypes = [P, P, I, I, F, P]
+        L.mlq_rope.argtypes = [P, P, P, P, I, I, I, P, P, P, P]
+        L.mlq_attention.argtypes = [P, QA, P, P, P, I, I, I, I, P]
         L.mlq_status_str.argtypes = [S]
         L.mlq_status_str.restype = ctypes.c_char_p
         for name in EXPORTS:
@@ -205,6 +218,53 @@ def mlq_block_sumi(sumi, W: QTensor, x: QAct, r0: int, r1: int, stream=None) -> 
     cw, cx = W.c(), x.c()
     _check(lib().mlq_block_sumi(_addr(sumi), ctypes.byref(cw), ctypes.byref(cx), r0, r1,
                                 _stream(stream)), "mlq_block_sumi")
+
+
+# ---- the floating-point steps of a decode layer --------------------------
+def _qa_ref(q: "QAct | None"):
+    return None if q is None else ctypes.byref(q.c())
+
+
+def mlq_rmsnorm(o, x, w, n: int, eps: float, oq: "QAct | None" = None, stream=None) -> None:
+    _check(lib().mlq_rmsnorm(_addr(o), _addr(x), _addr(w), n, eps, _qa_ref(oq), _stream(stream)),
+           "mlq_rmsnorm")
+
+
+def mlq_add_rmsnorm(x, y, w, n: int, eps: float, o=None, oq: "QAct | None" = None,
+                    stream=None) -> None:
+    _check(lib().mlq_add_rmsnorm(_addr(x), _addr(y), _addr(w), n, eps, _addr(o), _qa_ref(oq),
+                                 _stream(stream)), "mlq_add_rmsnorm")
+
+
+def mlq_add(y, x, n: int, stream=None) -> None:
+    _check(lib().mlq_add(_addr(y), _addr(x), n, _stream(stream)), "mlq_add")
+
+
+def mlq_softmax(x, n: int, stream=None) -> None:
+    _check(lib().mlq_softmax(_addr(x), n, _stream(stream)), "mlq_softmax")
+
+
+def mlq_silu_mul(g, u, n: int, gq: "QAct | None" = None, stream=None) -> None:
+    _check(lib().mlq_silu_mul(_addr(g), _addr(u), n, _qa_ref(gq), _stream(stream)), "mlq_silu_mul")
+
+
+def mlq_rope_tables(cos_t, sin_t, max_seq: int, head_dim: int, theta: float, stream=None) -> None:
+    _check(lib().mlq_rope_tables(_addr(cos_t), _addr(sin_t), max_seq, head_dim, theta,
+                                 _stream(stream)), "mlq_rope_tables")
+
+
+def mlq_rope(q, k, cos_row, sin_row, head_dim: int, n_heads: int, n_kv_heads: int, k_out=None,
+             v=None, v_out=None, stream=None) -> None:
+    _check(lib().mlq_rope(_addr(q), _addr(k), _addr(cos_row), _addr(sin_row), head_dim, n_heads,
+                          n_kv_heads, _addr(k_out), _addr(v), _addr(v_out), _stream(stream)),
+           "mlq_rope")
+
+
+def mlq_attention(o, q, k_cache, v_cache, n_pos: int, head_dim: int, n_heads: int,
+                  n_kv_heads: int, oq: "QAct | None" = None, stream=None) -> None:
+    _check(lib().mlq_attention(_addr(o), _qa_ref(oq), _addr(q), _addr(k_cache), _addr(v_cache),
+                               n_pos, head_dim, n_heads, n_kv_heads, _stream(stream)),
+           "mlq_attention")
 
 
 def mlq_prefetch_l2(ranges, stream=None) -> None:

@@ -423,6 +423,129 @@ mlq_status mlq_prefetch_l2(const void *const *ptrs, const size_t *bytes, int n, 
   return from_cuda(mlq::launch_prefetch_l2(ctx, list));
 }
 
+// ---- the floating-point steps of a decode layer -------------------------------
+namespace {
+// An optional Q8_0 output of n elements (one row): both arrays or none.
+mlq_status check_q8_out(const mlq_qact *o, int n) {
+  if (o == nullptr) return MLQ_OK;
+  if (o->q == nullptr || o->d == nullptr) return MLQ_E_NULL;
+  if (!cols_ok(n) || o->n != n || o->m != 1) return MLQ_E_SHAPE;
+  if (!aligned(o->q, 16) || !aligned(o->d, 16)) return MLQ_E_ALIGN;
+  return MLQ_OK;
+}
+bool floats_ok(const void *p) { return aligned(p, 4); }
+}  // namespace
+
+mlq_status mlq_rmsnorm(float *o, const float *x, const float *w, int n, float eps, mlq_qact *oq,
+                       void *stream) {
+  if (x == nullptr || w == nullptr || (o == nullptr && oq == nullptr)) return MLQ_E_NULL;
+  if (n < 1 || n > MLQ_MAX_COLS || !(eps >= 0.0f)) return MLQ_E_SHAPE;
+  if (!floats_ok(x) || !floats_ok(w) || !floats_ok(o)) return MLQ_E_ALIGN;
+  mlq_status s = check_q8_out(oq, n);
+  if (s != MLQ_OK) return s;
+  mlq::LaunchCtx ctx;
+  if ((s = make_ctx(&ctx, stream)) != MLQ_OK) return s;
+  return from_cuda(mlq::launch_rmsnorm_q8(ctx, const_cast<float *>(x), nullptr, w, o,
+                                          oq ? oq->q : nullptr, oq ? oq->d : nullptr, n, eps));
+}
+
+mlq_status mlq_add_rmsnorm(float *x, const float *y, const float *w, int n, float eps, float *o,
+                           mlq_qact *oq, void *stream) {
+  if (x == nullptr || y == nullptr || w == nullptr || (o == nullptr && oq == nullptr)) return MLQ_E_NULL;
+  if (n < 1 || n > MLQ_MAX_COLS || !(eps >= 0.0f)) return MLQ_E_SHAPE;
+  if (!floats_ok(x) || !floats_ok(y) || !floats_ok(w) || !floats_ok(o)) return MLQ_E_ALIGN;
+  mlq_status s = check_q8_out(oq, n);
+  if (s != MLQ_OK) return s;
+  mlq::LaunchCtx ctx;
+  if ((s = make_ctx(&ctx, stream)) != MLQ_OK) return s;
+  return from_cuda(mlq::launch_rmsnorm_q8(ctx, x, y, w, o, oq ? oq->q : nullptr,
+                                          oq ? oq->d : nullptr, n, eps));
+}
+
+mlq_status mlq_add(float *y, const float *x, int n, void *stream) {
+  if (y == nullptr || x == nullptr) return MLQ_E_NULL;
+  if (n < 1 || n > MLQ_MAX_COLS) return MLQ_E_SHAPE;
+  if (!floats_ok(y) || !floats_ok(x)) return MLQ_E_ALIGN;
+  mlq::LaunchCtx ctx;
+  mlq_status s = make_ctx(&ctx, stream);
+  if (s != MLQ_OK) return s;
+  return from_cuda(mlq::launch_add(ctx, y, x, n));
+}
+
+mlq_status mlq_softmax(float *x, int n, void *stream) {
+  if (x == nullptr) return MLQ_E_NULL;
+  if (n < 1 || n > MLQ_MAX_COLS) return MLQ_E_SHAPE;
+  if (!floats_ok(x)) return MLQ_E_ALIGN;
+  mlq::LaunchCtx ctx;
+  mlq_status s = make_ctx(&ctx, stream);
+  if (s != MLQ_OK) return s;
+  return from_cuda(mlq::launch_softmax(ctx, x, n));
+}
+
+mlq_status mlq_silu_mul(float *g, const float *u, int n, mlq_qact *gq, void *stream) {
+  if (g == nullptr || u == nullptr) return MLQ_E_NULL;
+  if (n < 1 || n > MLQ_MAX_COLS) return MLQ_E_SHAPE;
+  if (!floats_ok(g) || !floats_ok(u)) return MLQ_E_ALIGN;
+  mlq_status s = check_q8_out(gq, n);
+  if (s != MLQ_OK) return s;
+  mlq::LaunchCtx ctx;
+  if ((s = make_ctx(&ctx, stream)) != MLQ_OK) return s;
+  return from_cuda(mlq::launch_silu_mul_q8(ctx, g, u, n, gq ? gq->q : nullptr, gq ? gq->d : nullptr));
+}
+
+mlq_status mlq_rope_tables(float *cos_t, float *sin_t, int max_seq, int head_dim, float theta,
+                           void *stream) {
+  if (cos_t == nullptr || sin_t == nullptr) return MLQ_E_NULL;
+  if (max_seq < 1 || max_seq > MLQ_MAX_SEQ || head_dim < 2 || head_dim > MLQ_MAX_HEAD_DIM ||
+      head_dim % 2 != 0 || !(theta > 0.0f))
+    return MLQ_E_SHAPE;
+  if (!floats_ok(cos_t) || !floats_ok(sin_t)) return MLQ_E_ALIGN;
+  mlq::LaunchCtx ctx;
+  mlq_status s = make_ctx(&ctx, stream);
+  if (s != MLQ_OK) return s;
+  return from_cuda(mlq::launch_rope_tables(ctx, cos_t, sin_t, max_seq, head_dim, theta));
+}
+
+namespace {
+bool heads_ok(int head_dim, int n_heads, int n_kv_heads) {
+  return head_dim >= 2 && head_dim <= MLQ_MAX_HEAD_DIM && head_dim % 2 == 0 && n_heads >= 1 &&
+         n_kv_heads >= 1 && n_heads % n_kv_heads == 0 &&
+         static_cast<long long>(n_heads) * head_dim <= MLQ_MAX_COLS;
+}
+}  // namespace
+
+mlq_status mlq_rope(float *q, float *k, const float *cos_row, const float *sin_row, int head_dim,
+                    int n_heads, int n_kv_heads, float *k_out, const float *v, float *v_out,
+                    void *stream) {
+  if (q == nullptr || k == nullptr || cos_row == nullptr || sin_row == nullptr) return MLQ_E_NULL;
+  if ((v == nullptr) != (v_out == nullptr)) return MLQ_E_NULL;
+  if (!heads_ok(head_dim, n_heads, n_kv_heads)) return MLQ_E_SHAPE;
+  if (!floats_ok(q) || !floats_ok(k) || !floats_ok(cos_row) || !floats_ok(sin_row) ||
+      !floats_ok(k_out) || !floats_ok(v) || !floats_ok(v_out))
+    return MLQ_E_ALIGN;
+  mlq::LaunchCtx ctx;
+  mlq_status s = make_ctx(&ctx, stream);
+  if (s != MLQ_OK) return s;
+  return from_cuda(mlq::launch_rope_call(ctx, q, k, k_out, v, v_out, cos_row, sin_row, head_dim,
+                                         n_heads, n_kv_heads));
+}
+
+mlq_status mlq_attention(float *o, mlq_qact *oq, const float *q, const float *k_cache,
+                         const float *v_cache, int n_pos, int head_dim, int n_heads, int n_kv_heads,
+                         void *stream) {
+  if (o == nullptr || q == nullptr || k_cache == nullptr || v_cache == nullptr) return MLQ_E_NULL;
+  if (!heads_ok(head_dim, n_heads, n_kv_heads) || n_pos < 1 || n_pos > MLQ_MAX_SEQ) return MLQ_E_SHAPE;
+  if (oq != nullptr && head_dim % MLQ_QK != 0) return MLQ_E_SHAPE;
+  if (!floats_ok(o) || !floats_ok(q) || !floats_ok(k_cache) || !floats_ok(v_cache)) return MLQ_E_ALIGN;
+  mlq_status s = check_q8_out(oq, n_heads * head_dim);
+  if (s != MLQ_OK) return s;
+  mlq::LaunchCtx ctx;
+  if ((s = make_ctx(&ctx, stream)) != MLQ_OK) return s;
+  return from_cuda(mlq::launch_attention_call(ctx, o, oq ? oq->q : nullptr, oq ? oq->d : nullptr, q,
+                                              k_cache, v_cache, n_pos, head_dim, n_heads,
+                                              n_kv_heads));
+}
+
 mlq_status mlq_last_device_error(void *stream) {
   DevInfo *d = nullptr;
   mlq_status s = device_info(&d);

@@ -168,6 +168,24 @@ cudaError_t launch_gemm_q4_mma_cluster(const LaunchCtx &ctx, const void *wq, con
                                        int nb, const int8_t *xq, const float *xd, int M, float *Y,
                                        int ldy, int r0, int r1, int rows);
 
+// layer.cu: the floating-point steps of a decode layer (each one launch).
+cudaError_t launch_rmsnorm_q8(const LaunchCtx &ctx, float *x, const float *y, const float *w,
+                              float *h, int8_t *hq, float *hd, int n, float eps);
+cudaError_t launch_add(const LaunchCtx &ctx, float *y, const float *x, int n);
+cudaError_t launch_softmax(const LaunchCtx &ctx, float *x, int n);
+cudaError_t launch_silu_mul_q8(const LaunchCtx &ctx, float *g, const float *u, int n, int8_t *gq,
+                               float *gd);
+cudaError_t launch_rope_tables(const LaunchCtx &ctx, float *cos_t, float *sin_t, int max_seq,
+                               int head_dim, float theta);
+struct RopeArgs;
+struct AttnArgs;
+cudaError_t launch_rope_call(const LaunchCtx &ctx, float *q, float *k, float *k_out, const float *v,
+                             float *v_out, const float *cos_t, const float *sin_t, int head_dim,
+                             int n_heads, int n_kv_heads);
+cudaError_t launch_attention_call(const LaunchCtx &ctx, float *o, int8_t *oq, float *od,
+                                  const float *q, const float *kc, const float *vc, int n_pos,
+                                  int head_dim, int n_heads, int n_kv_heads);
+
 // gemm_small_m.cu: M activation rows (1..16) against a Q4_0 matrix.
 cudaError_t launch_gemm_q4_small_m(const LaunchCtx &ctx, const void *wq, const float *wd, int nb,
                                    const int8_t *xq, const float *xd, int M, float *Y, int ldy,

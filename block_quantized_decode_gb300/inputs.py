@@ -138,3 +138,60 @@ WORKLOADS = {
     "small_m4": lambda: small_m(4),
     "small_m16": lambda: small_m(16),
 }
+
+
+# --------------------------------------------------------------------------
+# A whole decode layer (Design Spec Sec. 6 forward pass) with random weights:
+# the seven Q4_0 products of a TinyLlama-1.1B layer, its two rmsnorm weight
+# vectors (uniform in [0.5, 1.5]), the RoPE tables (theta 10000) and a KV
+# cache whose first `pos` positions hold N(0, 1) values; the token's input x
+# is N(0, 1).  Seeds: base + tensor index, as above.
+# --------------------------------------------------------------------------
+@dataclass
+class LayerShape:
+    name: str = "tinyllama1.1b_decode_layer_q4_0"
+    dim: int = 2048
+    n_heads: int = 32
+    n_kv_heads: int = 4
+    hidden: int = 5632
+    max_seq: int = 2048
+    pos: int = 255            # the token's position: attention covers pos + 1 positions
+    rope_theta: float = 10000.0
+    norm_eps: float = 1e-5
+    wtype: int = Q4_0
+    seed: int = 0
+
+    @property
+    def head_dim(self) -> int:
+        return self.dim // self.n_heads
+
+    @property
+    def kv_dim(self) -> int:
+        return self.n_kv_heads * self.head_dim
+
+    def mats(self):
+        """(name, rows, cols) of the seven products, in forward-pass order."""
+        d, kv, hd = self.dim, self.kv_dim, self.hidden
+        return [("wq", d, d), ("wk", kv, d), ("wv", kv, d), ("wo", d, d),
+                ("w1", hd, d), ("w3", hd, d), ("w2", d, hd)]
+
+
+def norm_weights(n: int, seed: int) -> np.ndarray:
+    """float32 [n] uniform in [0.5, 1.5]."""
+    rng = np.random.default_rng(seed)
+    return rng.uniform(0.5, 1.5, size=n).astype(np.float32)
+
+
+def kv_history(n_pos: int, kv_dim: int, seed: int) -> np.ndarray:
+    """float32 [n_pos, kv_dim] ~ N(0, 1): the cached K or V rows of earlier tokens."""
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal(size=(n_pos, kv_dim)).astype(np.float32)
+
+
+def tinyllama_decode_layer(pos: int = 255) -> LayerShape:
+    return LayerShape(pos=pos)
+
+
+LAYERS = {
+    "tinyllama_decode_layer": tinyllama_decode_layer,
+}

@@ -66,6 +66,8 @@ extern "C" {
 #define MLQ_QK 32
 #define MLQ_MAX_COLS 65536
 #define MLQ_MAX_M 16
+#define MLQ_MAX_SEQ 32768
+#define MLQ_MAX_HEAD_DIM 256
 #define MLQ_MAX_PREFETCH_RANGES 32
 #define MLQ_FUSED_MAX_PRODUCTS 8
 #define MLQ_CHAIN_MAX_PRODUCTS 32
@@ -149,6 +151,65 @@ mlq_status mlq_gemm_q4_small_m(float *Y, int ldy, const mlq_qtensor *W, const ml
  * block-dot code as the matvec of W->type (Q4_0 or Q8_0); x->m must be 1. */
 mlq_status mlq_block_sumi(int32_t *sumi, const mlq_qtensor *W, const mlq_qact *x,
                           int r0, int r1, void *stream);
+
+/* ---- the floating-point steps of a decode layer ------------------------ */
+/* Page "Legacy-ISA ML Inference Runtime -- Design Spec", Sec. 5 (ml_k_rmsnorm,
+ * ml_k_softmax, ml_k_rope, ml_k_silu_mul, ml_k_add, ml_k_dot_f32,
+ * ml_k_axpy_f32) and Sec. 6 (forward pass per token, GQA).  All arrays are
+ * float32 on the device, 4-byte aligned; an optional Q8_0 output (one row,
+ * ->n equal to the vector length, a multiple of 32, q and d 16-byte
+ * aligned) receives exactly the bytes mlq_quantize_q8 would give for the
+ * float32 result.  Float results match the definitions within relative
+ * error 1e-5 (Sec. 7); sums are taken in a fixed order (deterministic).
+ * Errors: MLQ_E_NULL for a missing pointer, MLQ_E_SHAPE for sizes out of
+ * range, MLQ_E_ALIGN, MLQ_E_ARCH, MLQ_E_CUDA.  Calls are asynchronous on
+ * `stream`; the caller owns every buffer. */
+
+/* o = w * x / sqrt(mean(x^2) + eps), n elements; o (float) and/or oq (Q8_0)
+ * may be NULL but not both.  o may alias x. */
+mlq_status mlq_rmsnorm(float *o, const float *x, const float *w, int n, float eps, mlq_qact *oq,
+                       void *stream);
+
+/* The residual step of the forward pass followed by the next rmsnorm: x += y
+ * (x is written back), then o = rmsnorm(x) as mlq_rmsnorm. */
+mlq_status mlq_add_rmsnorm(float *x, const float *y, const float *w, int n, float eps, float *o,
+                           mlq_qact *oq, void *stream);
+
+/* y += x, n elements. */
+mlq_status mlq_add(float *y, const float *x, int n, void *stream);
+
+/* x = exp(x - max) / sum(exp(x - max)) in place, n elements. */
+mlq_status mlq_softmax(float *x, int n, void *stream);
+
+/* g = g / (1 + exp(-g)) * u in place, n elements; gq (Q8_0 of the result) or
+ * NULL. */
+mlq_status mlq_silu_mul(float *g, const float *u, int n, mlq_qact *gq, void *stream);
+
+/* RoPE tables [max_seq][head_dim/2]: cos and sin of pos * theta^(-2i/head_dim)
+ * (computed in double, rounded to float). */
+mlq_status mlq_rope_tables(float *cos_t, float *sin_t, int max_seq, int head_dim, float theta,
+                           void *stream);
+
+/* Rotate the interleaved pairs (2i, 2i+1) of every head of q (n_heads x
+ * head_dim) and k (n_kv_heads x head_dim) by the angles of one position:
+ * cos_row / sin_row are that row of the tables.  q is rotated in place; the
+ * rotated k goes to k_out (a KV cache row) or, if k_out is NULL, back to k.
+ * v, v_out: NULL, or v (n_kv_heads x head_dim) is copied to v_out (the V
+ * cache row).  n_heads % n_kv_heads == 0, head_dim even and <= 256. */
+mlq_status mlq_rope(float *q, float *k, const float *cos_row, const float *sin_row, int head_dim,
+                    int n_heads, int n_kv_heads, float *k_out, const float *v, float *v_out,
+                    void *stream);
+
+/* Attention of one token over n_pos cached positions: for query head h and
+ * its KV head g = h / (n_heads / n_kv_heads), s_t = dot(q_h, K[t][g]) /
+ * sqrt(head_dim) for t < n_pos, p = softmax(s), o_h = sum_t p_t V[t][g].
+ * K and V caches: row t holds the n_kv_heads heads of position t, one after
+ * another (row length n_kv_heads * head_dim).  oq: NULL, or the Q8_0 of o
+ * (n_heads * head_dim elements; head_dim a multiple of 32).
+ * 1 <= n_pos <= MLQ_MAX_SEQ. */
+mlq_status mlq_attention(float *o, mlq_qact *oq, const float *q, const float *k_cache,
+                         const float *v_cache, int n_pos, int head_dim, int n_heads, int n_kv_heads,
+                         void *stream);
 
 /* ---- decode chains: a whole decode step in one launch ------------------ */
 

@@ -245,3 +245,52 @@ def test_validation_phase(M):
     assert run([good], pf=ptrs, pfb=None, npf=2) == M.MLQ_E_NULL
     nul = (ctypes.c_void_p * 2)(12 * A, None)
     assert run([good], pf=nul, pfb=sizes, npf=2) == M.MLQ_E_NULL      # bytes > 0 at NULL
+
+
+def test_validation_layer_steps(M):
+    """The decode-layer steps reject bad arguments before touching the device."""
+    B = ctypes.byref
+    x, w, o = 5 * A, 6 * A, 7 * A
+    # rmsnorm / add_rmsnorm
+    assert call(M, "mlq_rmsnorm", None, x, w, 256, 1e-5, None, None) == M.MLQ_E_NULL   # no output
+    assert call(M, "mlq_rmsnorm", o, None, w, 256, 1e-5, None, None) == M.MLQ_E_NULL
+    assert call(M, "mlq_rmsnorm", o, x, w, 0, 1e-5, None, None) == M.MLQ_E_SHAPE
+    assert call(M, "mlq_rmsnorm", o, x, w, 256, -1.0, None, None) == M.MLQ_E_SHAPE
+    assert call(M, "mlq_rmsnorm", o, x, w, 256, float("nan"), None, None) == M.MLQ_E_SHAPE
+    assert call(M, "mlq_rmsnorm", o + 2, x, w, 256, 1e-5, None, None) == M.MLQ_E_ALIGN
+    assert call(M, "mlq_rmsnorm", o, x, w, 250, 1e-5, B(qa(n=250)), None) == M.MLQ_E_SHAPE  # Q8 needs n % 32
+    assert call(M, "mlq_rmsnorm", o, x, w, 256, 1e-5, B(qa(n=128)), None) == M.MLQ_E_SHAPE  # qa->n != n
+    assert call(M, "mlq_rmsnorm", o, x, w, 256, 1e-5, B(qa(n=256, m=2)), None) == M.MLQ_E_SHAPE
+    assert call(M, "mlq_rmsnorm", o, x, w, 256, 1e-5, B(qa(q=3 * A + 8, n=256)), None) == M.MLQ_E_ALIGN
+    assert call(M, "mlq_rmsnorm", o, x, w, 256, 1e-5, B(qa(q=None, n=256)), None) == M.MLQ_E_NULL
+    assert call(M, "mlq_add_rmsnorm", x, None, w, 256, 1e-5, o, None, None) == M.MLQ_E_NULL
+    assert call(M, "mlq_add_rmsnorm", x, o, w, 256, 1e-5, None, None, None) == M.MLQ_E_NULL
+    # add, softmax, silu_mul
+    assert call(M, "mlq_add", None, x, 16, None) == M.MLQ_E_NULL
+    assert call(M, "mlq_add", o, x, 0, None) == M.MLQ_E_SHAPE
+    assert call(M, "mlq_softmax", None, 16, None) == M.MLQ_E_NULL
+    assert call(M, "mlq_softmax", o, 70000, None) == M.MLQ_E_SHAPE
+    assert call(M, "mlq_silu_mul", o, None, 64, None, None) == M.MLQ_E_NULL
+    assert call(M, "mlq_silu_mul", o, x, 64, B(qa(n=32)), None) == M.MLQ_E_SHAPE
+    # rope tables and rope
+    assert call(M, "mlq_rope_tables", o, None, 16, 64, 1e4, None) == M.MLQ_E_NULL
+    assert call(M, "mlq_rope_tables", o, x, 16, 63, 1e4, None) == M.MLQ_E_SHAPE      # odd head_dim
+    assert call(M, "mlq_rope_tables", o, x, 0, 64, 1e4, None) == M.MLQ_E_SHAPE
+    assert call(M, "mlq_rope_tables", o, x, 16, 64, 0.0, None) == M.MLQ_E_SHAPE
+    rope = lambda **k: call(M, "mlq_rope", k.get("q", o), k.get("k", x), k.get("c", w), 8 * A,
+                            k.get("hd", 64), k.get("nh", 32), k.get("nkv", 4), k.get("ko", None),
+                            k.get("v", None), k.get("vo", None), None)
+    assert rope(q=None) == M.MLQ_E_NULL
+    assert rope(v=9 * A) == M.MLQ_E_NULL                     # v without v_out
+    assert rope(nkv=5) == M.MLQ_E_SHAPE                      # 32 % 5
+    assert rope(hd=512) == M.MLQ_E_SHAPE
+    assert rope(ko=9 * A + 1) == M.MLQ_E_ALIGN
+    # attention
+    att = lambda **k: call(M, "mlq_attention", k.get("o", o), k.get("oq", None), x, w, 8 * A,
+                           k.get("npos", 17), k.get("hd", 64), k.get("nh", 32), k.get("nkv", 4), None)
+    assert att(o=None) == M.MLQ_E_NULL
+    assert att(npos=0) == M.MLQ_E_SHAPE
+    assert att(npos=40000) == M.MLQ_E_SHAPE
+    assert att(nkv=3) == M.MLQ_E_SHAPE
+    assert att(hd=48, oq=B(qa(n=48 * 32))) == M.MLQ_E_SHAPE  # Q8 output needs head_dim % 32
+    assert att(oq=B(qa(n=1024))) == M.MLQ_E_SHAPE            # n_heads * head_dim = 2048
