@@ -516,9 +516,10 @@ def run_ours(args, wl, world, rank, local, pg):
         del g
         ach = wbytes / best / 1e9
         qt = "Q4_0" if r.mats[0].spec.wtype == I.Q4_0 else "Q8_0"
-        roofline = {"kernel": f"decode_chain_kernel<{qt}>", "bound": "hbm", "achieved": ach,
+        roofline = {"kernel": f"decode_stream_kernel<{qt}>", "bound": "hbm", "achieved": ach,
                     "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_source": peak_src,
-                    "traffic": ncu_traffic(f"chain_{wl.name}", ("chain.cu", "mlq_device.cuh"), wbytes),
+                    "traffic": ncu_traffic(f"chain_{wl.name}", ("stream.cu", "phase_common.cuh",
+                                                                "mlq_device.cuh"), wbytes),
                     "bytes_per_launch": wbytes, "us_per_launch": best * 1e6,
                     "method": f"{launches} back-to-back chain launches (one per step) in one CUDA "
                               "graph, best of 3 replays, CUDA events on the launching stream"}

@@ -30,6 +30,8 @@
 // workspace is zero again for the next call.  Every wait is bounded: a
 // give-up records MLQ_E_TIMEOUT, the CTA stops issuing copies, drains its
 // own copies in flight (bounded) and still takes part in the final reset.
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "mlq_device.cuh"
@@ -331,6 +333,13 @@ __global__ void __launch_bounds__(kChainThreads, 1) decode_chain_kernel(const __
 }
 
 cudaError_t launch_decode_chain(const LaunchCtx &ctx, int qtype, const ChainArgs &args_in) {
+  // The streaming kernel of stream.cu is the default; this one takes the
+  // shapes it does not (K above 16384) and MLQ_CHAIN_KERNEL=legacy.
+  const char *kind = std::getenv("MLQ_CHAIN_KERNEL");
+  if (kind == nullptr || std::strcmp(kind, "legacy") != 0) {
+    const cudaError_t e = launch_decode_stream(ctx, qtype, args_in);
+    if (e != cudaErrorNotSupported) return e;
+  }
   ChainArgs a = args_in;
   const size_t nbmax = static_cast<size_t>(a.kmax) / kQK;
   a.xbuf_bytes = static_cast<int>((static_cast<size_t>(a.kmax) + 8 * nbmax + 127) / 128 * 128);

@@ -101,6 +101,10 @@ struct ChainArgs {
   int ns, stage_bytes, xbuf_bytes;  // ring geometry (set by the launcher)
 };
 cudaError_t launch_decode_chain(const LaunchCtx &ctx, int qtype, const ChainArgs &a);
+// stream.cu: the same chain with the weight stream running ahead across
+// phases and in-chain Q8_0 hand-offs; cudaErrorNotSupported (nothing
+// launched) when a phase is wider than its consumer warps can hold.
+cudaError_t launch_decode_stream(const LaunchCtx &ctx, int qtype, const ChainArgs &a);
 // Same chain with its barrier counters in a fixed device array of chain.cu
 // (no workspace, no allocation); at most kStaticChainWords - 1 phases.
 constexpr int kStaticChainWords = 64;

@@ -51,13 +51,12 @@ __device__ __forceinline__ int phase_product(const FusedArgs &a, int g, int *loc
 
 // Quantise float x (nb blocks) into shared memory, eight lanes per block,
 // all loads of up to eight passes issued before any block is reduced.
-// CTA 0 also writes the copy asked for in xq_out / xd_out.
+// With `writer`, the CTA also writes the quantisation to xq_out / xd_out.
 template <int NW>
-__device__ __forceinline__ void phase_quantize(const FusedArgs &a, int8_t *xq_s, float *xd_s,
-                                               int tid) {
-  const int nb = a.nb;
+__device__ __forceinline__ void quantize_input(const float *x, int nb, int8_t *xq_out,
+                                               float *xd_out, bool writer, int8_t *xq_s,
+                                               float *xd_s, int tid) {
   const int part = tid & 7;
-  const bool writer = blockIdx.x == 0 && a.xq_out != nullptr;
   constexpr int kPer = NW * 32 / 8;
   constexpr int kPass = 8;
   // every CTA reads all of x: start each at another block to spread the requests
@@ -69,7 +68,7 @@ __device__ __forceinline__ void phase_quantize(const FusedArgs &a, int8_t *xq_s,
       const int i = base0 + p * kPer + (tid >> 3);
       const int b = i + rot < nb ? i + rot : i + rot - nb;
       v[p] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (i < nb) v[p] = __ldcg(reinterpret_cast<const float4 *>(a.x + static_cast<size_t>(b) * kQK + part * 4));
+      if (i < nb) v[p] = __ldcg(reinterpret_cast<const float4 *>(x + static_cast<size_t>(b) * kQK + part * 4));
     }
 #pragma unroll
     for (int p = 0; p < kPass; ++p) {
@@ -92,12 +91,18 @@ __device__ __forceinline__ void phase_quantize(const FusedArgs &a, int8_t *xq_s,
         *reinterpret_cast<uint32_t *>(xq_s + b * kQK + part * 4) = packed;
         if (part == 0) xd_s[b] = dd;
         if (writer) {
-          *reinterpret_cast<uint32_t *>(a.xq_out + static_cast<size_t>(b) * kQK + part * 4) = packed;
-          if (part == 0) a.xd_out[b] = dd;
+          *reinterpret_cast<uint32_t *>(xq_out + static_cast<size_t>(b) * kQK + part * 4) = packed;
+          if (part == 0) xd_out[b] = dd;
         }
       }
     }
   }
+}
+template <int NW>
+__device__ __forceinline__ void phase_quantize(const FusedArgs &a, int8_t *xq_s, float *xd_s,
+                                               int tid) {
+  quantize_input<NW>(a.x, a.nb, a.xq_out, a.xd_out, blockIdx.x == 0 && a.xq_out != nullptr, xq_s,
+                     xd_s, tid);
 }
 
 // A warp's chunk of the quantised input: lane l holds blocks u0 and u0 + 32

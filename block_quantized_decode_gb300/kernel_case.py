@@ -21,10 +21,11 @@ from . import binding as B
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("--op", default="matvec_q4",
-                   choices=["matvec_q4", "matvec_q8", "gemm_q4", "quantize", "fused", "phase"])
+                   choices=["matvec_q4", "matvec_q8", "gemm_q4", "quantize", "fused", "phase", "chain"])
     p.add_argument("--workload", default="tinyllama_layer",
-                   help="for --op fused / phase: the workload whose phases run as "
-                        "mlq_matvec_fused / mlq_decode_phase calls")
+                   help="for --op fused / phase / chain: the workload whose phases run as "
+                        "mlq_matvec_fused / mlq_decode_phase calls, or as one "
+                        "mlq_decode_chain call")
     p.add_argument("--rows", type=int, default=4096)
     p.add_argument("--cols", type=int, default=11008)
     p.add_argument("--m", type=int, default=1)
@@ -37,7 +38,7 @@ def main():
     dev = torch.device("cuda:0")
     torch.cuda.set_device(0)
     B.mlq_init()
-    if a.op in ("fused", "phase"):
+    if a.op in ("fused", "phase", "chain"):
         return fused_case(a)
     g = torch.Generator(device=dev)
     g.manual_seed(0)
@@ -108,13 +109,13 @@ def main():
 
 def fused_case(a):
     """One pass of a workload as mlq_matvec_fused (or mlq_decode_phase)
-    launches, one per phase."""
+    launches, one per phase, or as one mlq_decode_chain launch."""
     from . import inputs as I
     from .runner import WorkloadRunner
     wl = I.WORKLOADS[a.workload]()
     copies = a.copies or 3
     r = WorkloadRunner(wl, copies=copies)
-    step = r.step_fused if a.op == "fused" else r.step_phase
+    step = {"fused": r.step_fused, "phase": r.step_phase, "chain": r.step_chain}[a.op]
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         for c in range(copies):

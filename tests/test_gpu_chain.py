@@ -27,6 +27,18 @@ def lib():
     assert M.mlq_last_device_error() == M.MLQ_OK
 
 
+@pytest.fixture(params=["stream", "stream_float_inputs", "legacy"], autouse=True)
+def chain_kernel(request, monkeypatch):
+    """Each chain test runs on the streaming kernel (the default), on the
+    streaming kernel with every phase quantising its float input itself
+    (no in-chain Q8_0 hand-off), and on the legacy kernel."""
+    if request.param == "stream_float_inputs":
+        monkeypatch.setenv("MLQ_CHAIN_QIN", "0")
+    elif request.param == "legacy":
+        monkeypatch.setenv("MLQ_CHAIN_KERNEL", "legacy")
+    yield request.param
+
+
 from tests.test_gpu_configs import run_and_check  # noqa: E402
 from block_quantized_decode_gb300.runner import WorkloadRunner  # noqa: E402
 
@@ -71,6 +83,39 @@ def test_chain_ragged_q8():
         I.Matvec("b", I.Q8_0, 640, 256, "x"),
         I.Matvec("c", I.Q8_0, 155, 640, "b"),
     ])
+    run_and_check(wl, chain=True)
+
+
+def test_chain_handoffs_and_wide_rows():
+    """In-chain Q8_0 hand-offs over several phases in a row (outputs of
+    whole 32-row blocks feeding the next phase), a phase with a product whose
+    rows are not whole blocks (the phase after it quantises its float input
+    itself), the widest rows the streaming kernel holds (K = 16384) and a
+    narrow one (K = 128)."""
+    wl = I.Workload("handoffs", 1, [
+        I.Matvec("a", I.Q4_0, 512, 16384, "x"),
+        I.Matvec("b", I.Q4_0, 16384, 512, "a"),
+        I.Matvec("c", I.Q4_0, 128, 16384, "b"),
+        I.Matvec("d", I.Q4_0, 4096, 128, "c"),
+        I.Matvec("e", I.Q4_0, 77, 128, "c"),
+        I.Matvec("f", I.Q4_0, 64, 4096, "d"),
+    ])
+    run_and_check(wl, chain=True)
+
+
+def test_chain_widest_stream_rows():
+    """K = 20480: sixteen K-chunks of 40 blocks, one row per stage."""
+    wl = I.Workload("wide", 1, [
+        I.Matvec("a", I.Q8_0, 300, 20480, "x"),
+        I.Matvec("b", I.Q8_0, 640, 20480, "x"),
+    ])
+    run_and_check(wl, chain=True)
+
+
+def test_chain_wider_than_stream_falls_back():
+    """K = 40960 is wider than the streaming kernel's warps hold in
+    registers: the call still runs (on the legacy kernel) and is correct."""
+    wl = I.Workload("wider", 1, [I.Matvec("a", I.Q8_0, 300, 40960, "x")])
     run_and_check(wl, chain=True)
 
 
