@@ -25,6 +25,7 @@ _LIB = os.path.join(_HERE, "libmlq_oracle.so")
 Q8_0 = 0
 Q4_0 = 1
 QK = 32
+QKK = 256   # Q4_K-style super-block
 
 _default = None
 
@@ -73,9 +74,13 @@ class Oracle:
         L.mlqo_rope_tables.argtypes = [P, P, I, I, F]
         L.mlqo_rope.argtypes = [P, P, P, P, I, I, I]
         L.mlqo_attention.argtypes = [P, P, P, P, I, I, I, I]
+        L.mlqo_quantize_q8k.argtypes = [P, P, P, P, I, I]
+        L.mlqo_block_sums_q4k.argtypes = [P, P, P, P, I, I, P, P, I, I]
+        L.mlqo_matvec_q4k.argtypes = [P, P, P, P, P, I, I, P, P, P, I, I]
         for f in (L.mlqo_quantize_q8, L.mlqo_block_sumi, L.mlqo_matvec, L.mlqo_gemm_small_m,
                   L.mlqo_rmsnorm, L.mlqo_softmax, L.mlqo_silu_mul, L.mlqo_add, L.mlqo_rope_tables,
-                  L.mlqo_rope, L.mlqo_attention):
+                  L.mlqo_rope, L.mlqo_attention, L.mlqo_quantize_q8k, L.mlqo_block_sums_q4k,
+                  L.mlqo_matvec_q4k):
             f.restype = ctypes.c_int
         self.lib = L
         self.path = path
@@ -137,6 +142,59 @@ class Oracle:
         return Y
 
 
+class _Q4KOps:
+    """Q4_K-style super-blocks (page "SKaiNET-native-kernels", "Proving an
+    optimization is safe before writing it"); the layout is the one stated
+    in mlq_oracle.c."""
+
+    def quantize_q8k(self, x: np.ndarray):
+        """x float32 [k] or [m, k] -> (q int8, d float32 per 256, bsums int32 per 32)."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        squeeze = x.ndim == 1
+        x2 = x.reshape(1, -1) if squeeze else x
+        m, k = x2.shape
+        q = np.empty((m, k), dtype=np.int8)
+        d = np.empty((m, k // QKK), dtype=np.float32)
+        bs = np.empty((m, k // QK), dtype=np.int32)
+        _ok(self.lib.mlqo_quantize_q8k(_ptr(q), _ptr(d), _ptr(bs), _ptr(x2), m, k), "quantize_q8k")
+        return (q[0], d[0], bs[0]) if squeeze else (q, d, bs)
+
+    def block_sums_q4k(self, wq, ws, rows: int, cols: int, xq, xbs, r0: int = 0,
+                       r1: int | None = None):
+        """(ISUM, MSUM) int32 [r1 - r0, cols/256] for rows [r0, r1)."""
+        r1 = rows if r1 is None else r1
+        nsb = cols // QKK
+        isum = np.zeros((max(r1 - r0, 0), nsb), dtype=np.int32)
+        msum = np.zeros_like(isum)
+        _ok(self.lib.mlqo_block_sums_q4k(_ptr(isum), _ptr(msum), _ptr(_u8(wq)), _ptr(_u8(ws)), rows,
+                                         cols, _ptr(_i8(xq)), _ptr(_i32(xbs)), r0, r1),
+            "block_sums_q4k")
+        return isum, msum
+
+    def matvec_q4k(self, wq, ws, wd, wdmin, rows: int, cols: int, xq, xd, xbs, r0: int = 0,
+                   r1: int | None = None, y: np.ndarray | None = None) -> np.ndarray:
+        """y[r] for r in [r0, r1); other entries of y are left as they are."""
+        r1 = rows if r1 is None else r1
+        if y is None:
+            y = np.zeros(rows, dtype=np.float32)
+        _ok(self.lib.mlqo_matvec_q4k(_ptr(y), _ptr(_u8(wq)), _ptr(_u8(ws)), _ptr(_f32(wd)),
+                                     _ptr(_f32(wdmin)), rows, cols, _ptr(_i8(xq)), _ptr(_f32(xd)),
+                                     _ptr(_i32(xbs)), r0, r1), "matvec_q4k")
+        return y
+
+
+def _u8(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.uint8)
+
+
+def _i8(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int8)
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
 def _f32(a) -> np.ndarray:
     return np.ascontiguousarray(a, dtype=np.float32)
 
@@ -192,6 +250,8 @@ class _LayerOps:
 
 for _name in ("rmsnorm", "softmax", "silu_mul", "add", "rope_tables", "rope", "attention"):
     setattr(Oracle, _name, getattr(_LayerOps, _name))
+for _name in ("quantize_q8k", "block_sums_q4k", "matvec_q4k"):
+    setattr(Oracle, _name, getattr(_Q4KOps, _name))
 
 
 def default() -> Oracle:
@@ -243,3 +303,15 @@ def rope(*a, **k):
 
 def attention(*a, **k):
     return default().attention(*a, **k)
+
+
+def quantize_q8k(x):
+    return default().quantize_q8k(x)
+
+
+def block_sums_q4k(*a, **k):
+    return default().block_sums_q4k(*a, **k)
+
+
+def matvec_q4k(*a, **k):
+    return default().matvec_q4k(*a, **k)

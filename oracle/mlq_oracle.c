@@ -51,17 +51,17 @@
 
 enum { ORACLE_Q8_0 = 0, ORACLE_Q4_0 = 1 };
 
-/* ---- Sec. 4 / Sec. 5: Q8_0 quantisation of one block of 32 floats ---- */
-static void quantize_block(int8_t *q, float *d, const float *x)
+/* ---- Sec. 4 / Sec. 5: Q8_0 quantisation of `len` floats with one scale ---- */
+static void quantize_span(int8_t *q, float *d, const float *x, int len)
 {
     float amax = 0.0f;
-    for (int j = 0; j < ORACLE_QK; ++j) {
+    for (int j = 0; j < len; ++j) {
         float a = fabsf(x[j]);
         if (a > amax) amax = a;
     }
     float dd = amax / 127.0f;                        /* d = max|x| / 127      */
     float id = (amax != 0.0f) ? 127.0f / amax : 0.0f; /* id = 127 / amax      */
-    for (int j = 0; j < ORACLE_QK; ++j) {
+    for (int j = 0; j < len; ++j) {
         float v = x[j] * id;                         /* one rounded multiply  */
         v = v + copysignf(0.5f, x[j]);               /* one rounded add       */
         v = truncf(v);
@@ -73,6 +73,12 @@ static void quantize_block(int8_t *q, float *d, const float *x)
         q[j] = qq;
     }
     *d = dd;
+}
+
+/* One block of 32 floats (Sec. 4: QK = 32). */
+static void quantize_block(int8_t *q, float *d, const float *x)
+{
+    quantize_span(q, d, x, ORACLE_QK);
 }
 
 /* Quantise m rows of k floats (row-major) into q[m*k] and d[m*(k/32)].
@@ -306,5 +312,108 @@ int mlqo_attention(float *o, const float *q, const float *kc, const float *vc, i
         free(acc);
     }
     free(p);
+    return 0;
+}
+
+/* ========================================================================
+ * Q4_K-style super-blocks with the sub-block scale folded in the integer
+ * domain.
+ *
+ * Source: the page "SKaiNET-native-kernels", section "Proving an
+ * optimization is safe before writing it": 4-bit weight nibbles w in
+ * [0, 15], 32 elements per sub-block, a 6-bit sub-block scale s <= 63,
+ * 8 sub-blocks per block, activations quantised to int8 (|a| <= 127); the
+ * sum over the 8 sub-blocks of s_b * sum_i a_i w_i fits int32 with ~70x
+ * headroom (8*63*32*127*15 = 3.07e7), so it is formed in integers and
+ * converted to float once per block; the format keeps per-32 asymmetric
+ * minima.  Readings where the page is silent (listed in the design doc):
+ *   - a block ("super-block") is 256 elements = 8 sub-blocks of 32; per
+ *     super-block a float32 scale d and a float32 scale of the minima dmin;
+ *     per sub-block a 6-bit scale s_b and a 6-bit minimum m_b, one per byte;
+ *     element value = d*s_b*n - dmin*m_b;
+ *   - layout, rows row-major: q = the nibbles, 16 bytes per sub-block in
+ *     the Q4_0 order (byte j: element j in the low nibble, element j+16 in
+ *     the high nibble); s = 16 bytes per super-block, the 8 sub-block
+ *     scales then the 8 sub-block minima; d and dmin = one float32 each per
+ *     super-block;
+ *   - activations quantised per 256 elements with the Q8_0 rounding rule
+ *     (one float32 scale per 256), plus the int32 sum of each 32-element
+ *     sub-block of the quants;
+ *   - per super-block ISUM = sum_b s_b * sum_i a_i n_i and MSUM = sum_b m_b *
+ *     sum_i a_i, both int32, and y += ((float)ISUM * d - (float)MSUM * dmin)
+ *     * dx in float32, super-blocks in increasing order, nothing fused.
+ * ====================================================================== */
+#define ORACLE_QKK 256
+#define ORACLE_SUBS (ORACLE_QKK / ORACLE_QK)
+
+int mlqo_quantize_q8k(int8_t *q, float *d, int32_t *bsums, const float *x, int m, int k)
+{
+    if (k <= 0 || k % ORACLE_QKK != 0 || m < 0) return -1;
+    const int nsb = k / ORACLE_QKK;
+    for (int r = 0; r < m; ++r)
+        for (int B = 0; B < nsb; ++B) {
+            const size_t e0 = (size_t)r * k + (size_t)B * ORACLE_QKK;
+            quantize_span(q + e0, d + (size_t)r * nsb + B, x + e0, ORACLE_QKK);
+            for (int b = 0; b < ORACLE_SUBS; ++b) {
+                int32_t t = 0;
+                for (int i = 0; i < ORACLE_QK; ++i) t += q[e0 + (size_t)b * ORACLE_QK + i];
+                bsums[((size_t)r * nsb + B) * ORACLE_SUBS + b] = t;
+            }
+        }
+    return 0;
+}
+
+/* ISUM and MSUM of row r, super-block B (the integer-domain fold). */
+static void q4k_block_sums(int32_t *isum, int32_t *msum, const uint8_t *wq, const uint8_t *ws,
+                           int nsb, int r, int B, const int8_t *xq, const int32_t *xbs)
+{
+    const uint8_t *sm = ws + ((size_t)r * nsb + B) * 16;   /* scales, then minima */
+    int32_t is = 0, ms = 0;
+    for (int b = 0; b < ORACLE_SUBS; ++b) {
+        const size_t sb = (size_t)B * ORACLE_SUBS + b;             /* sub-block of the row */
+        const uint8_t *bytes = wq + ((size_t)r * nsb * ORACLE_SUBS + sb) * 16;
+        const int8_t *a = xq + sb * ORACLE_QK;
+        int32_t dot = 0;
+        for (int j = 0; j < 16; ++j) {
+            dot += (int32_t)(bytes[j] & 0x0F) * a[j];
+            dot += (int32_t)(bytes[j] >> 4) * a[j + 16];
+        }
+        is += (int32_t)sm[b] * dot;
+        ms += (int32_t)sm[8 + b] * xbs[sb];
+    }
+    *isum = is;
+    *msum = ms;
+}
+
+int mlqo_block_sums_q4k(int32_t *isum, int32_t *msum, const uint8_t *wq, const uint8_t *ws,
+                        int rows, int cols, const int8_t *xq, const int32_t *xbs, int r0, int r1)
+{
+    if (cols <= 0 || cols % ORACLE_QKK != 0 || r0 < 0 || r1 > rows || r0 > r1) return -1;
+    const int nsb = cols / ORACLE_QKK;
+    for (int r = r0; r < r1; ++r)
+        for (int B = 0; B < nsb; ++B)
+            q4k_block_sums(isum + (size_t)(r - r0) * nsb + B, msum + (size_t)(r - r0) * nsb + B,
+                           wq, ws, nsb, r, B, xq, xbs);
+    return 0;
+}
+
+int mlqo_matvec_q4k(float *y, const uint8_t *wq, const uint8_t *ws, const float *wd,
+                    const float *wdmin, int rows, int cols, const int8_t *xq, const float *xd,
+                    const int32_t *xbs, int r0, int r1)
+{
+    if (cols <= 0 || cols % ORACLE_QKK != 0 || r0 < 0 || r1 > rows || r0 > r1) return -1;
+    const int nsb = cols / ORACLE_QKK;
+    for (int r = r0; r < r1; ++r) {
+        float yr = 0.0f;
+        for (int B = 0; B < nsb; ++B) {
+            int32_t is, ms;
+            q4k_block_sums(&is, &ms, wq, ws, nsb, r, B, xq, xbs);
+            const float t = (float)is * wd[(size_t)r * nsb + B];
+            const float u = (float)ms * wdmin[(size_t)r * nsb + B];
+            const float v = (t - u) * xd[B];
+            yr = yr + v;
+        }
+        y[r] = yr;
+    }
     return 0;
 }

@@ -388,6 +388,164 @@ def pin_attention_cases(O):
     assert np.allclose(o.reshape(nh, hd)[:, 0], [10, 10, 20, 20], rtol=1e-6), o
 
 
+# ----------------------------------------------------------------------------
+# Q4_K-style super-blocks (page "SKaiNET-native-kernels", section "Proving an
+# optimization is safe before writing it"; the layout reading is the one
+# stated in the oracle: q nibbles in the Q4_0 order per 32-element sub-block,
+# s = per super-block 8 scales then 8 minima, d and dmin float32 per
+# super-block; value = d * s_b * n - dmin * m_b; activations per 256 with
+# the Q8_0 rounding rule and int32 sums per 32)
+# ----------------------------------------------------------------------------
+QKK = 256
+
+
+def decode_q4k_nibbles(wq: np.ndarray, cols: int) -> np.ndarray:
+    """Unsigned nibbles n in [0, 15] of every element, [rows, cols] int64."""
+    rows = wq.shape[0]
+    qb = wq.reshape(rows, cols // QK, 16).astype(np.int64)
+    out = np.empty((rows, cols), dtype=np.int64)
+    for e in range(QK):
+        out[:, e::QK] = (qb[:, :, e] & 0xF) if e < 16 else (qb[:, :, e - 16] >> 4)
+    return out
+
+
+def q4k_sub_params(ws: np.ndarray, cols: int):
+    """Per-sub-block scale s_b and minimum m_b, each [rows, cols/32] int64."""
+    rows = ws.shape[0]
+    sm = ws.reshape(rows, cols // QKK, 16).astype(np.int64)
+    return sm[:, :, :8].reshape(rows, -1), sm[:, :, 8:].reshape(rows, -1)
+
+
+def random_q4k(rng, rows, cols, smax=63):
+    nsb = cols // QKK
+    wq = rng.integers(0, 256, size=(rows, cols // 2), dtype=np.uint8)
+    ws = rng.integers(0, smax + 1, size=(rows, nsb * 16), dtype=np.uint8)
+    wd = rng.uniform(1e-4, 1e-3, size=(rows, nsb)).astype(np.float32)
+    wdmin = rng.uniform(1e-4, 1e-3, size=(rows, nsb)).astype(np.float32)
+    return wq, ws, wd, wdmin
+
+
+def pin_q4k_overflow_bound(O):
+    """The page's bound is attained and fits int32: all nibbles 15, all
+    sub-block scales 63, every activation +127 (or -127) gives |ISUM| =
+    8*63*32*127*15 = 30,723,840, about 70x below 2^31 - 1; MSUM with all
+    minima 63 is 8*63*(32*127)."""
+    cols = QKK
+    wq = np.full((1, cols // 2), 0xFF, dtype=np.uint8)
+    ws = np.full((1, 16), 63, dtype=np.uint8)
+    for sign in (1, -1):
+        xq = np.full(cols, 127 * sign, dtype=np.int8)
+        xbs = np.full(cols // QK, 32 * 127 * sign, dtype=np.int32)
+        isum, msum = O.block_sums_q4k(wq, ws, 1, cols, xq, xbs)
+        assert int(isum[0, 0]) == sign * 8 * 63 * 32 * 127 * 15 == sign * 30723840, isum
+        assert int(msum[0, 0]) == sign * 8 * 63 * 32 * 127, msum
+    assert 30723840 * 69 < 2 ** 31 - 1 < 30723840 * 70
+
+
+def pin_q4k_bruteforce_fp64(O, seed=21):
+    """Integer sums exactly, and y within the float32 rounding bound, against
+    fp64 brute force over the dequantised elements (d*s_b*n - dmin*m_b) *
+    (dx*q) on tiny matrices."""
+    rng = np.random.default_rng(seed)
+    for trial in range(12):
+        rows = int(rng.integers(1, 6))
+        cols = QKK * int(rng.integers(1, 4))
+        nsb = cols // QKK
+        wq, ws, wd, wdmin = random_q4k(rng, rows, cols)
+        x = rng.standard_normal(cols).astype(np.float32)
+        xq, xd, xbs = O.quantize_q8k(x)
+        y = O.matvec_q4k(wq, ws, wd, wdmin, rows, cols, xq, xd, xbs)
+        isum, msum = O.block_sums_q4k(wq, ws, rows, cols, xq, xbs)
+        n = decode_q4k_nibbles(wq, cols)
+        s_b, m_b = q4k_sub_params(ws, cols)
+        qx = xq.astype(np.int64)
+        for r in range(rows):
+            exact, absterms = 0.0, 0.0
+            for B in range(nsb):
+                I = M = 0
+                acc = 0.0
+                for sb in range(B * 8, B * 8 + 8):
+                    e = slice(sb * QK, sb * QK + QK)
+                    I += int(s_b[r, sb]) * int(np.dot(n[r, e], qx[e]))
+                    M += int(m_b[r, sb]) * int(qx[e].sum())
+                    for k in range(sb * QK, sb * QK + QK):
+                        w = float(wd[r, B]) * float(s_b[r, sb]) * float(n[r, k]) - \
+                            float(wdmin[r, B]) * float(m_b[r, sb])
+                        acc += w * (float(xd[B]) * float(qx[k]))
+                assert int(isum[r, B]) == I and int(msum[r, B]) == M, (trial, r, B)
+                exact += acc
+                absterms += (abs(I * float(wd[r, B])) + abs(M * float(wdmin[r, B]))) * float(xd[B])
+            tol = (nsb + 5) * U * (1 + 1e-6) * absterms + 1e-300
+            assert abs(float(y[r]) - exact) <= tol, (trial, r, float(y[r]), exact, tol)
+
+
+def pin_q4k_special_cases(O, seed=22):
+    """d = dx = 1, dmin = 0 and unit scales reduce the product to a plain
+    integer matvec of the unsigned nibbles; d = 0, dmin = 1 leaves minus
+    the minima-weighted sums of the activation quants."""
+    rng = np.random.default_rng(seed)
+    rows, cols = 5, 2 * QKK
+    nsb = cols // QKK
+    wq = rng.integers(0, 256, size=(rows, cols // 2), dtype=np.uint8)
+    ws = np.zeros((rows, nsb * 16), dtype=np.uint8)
+    ws.reshape(rows, nsb, 16)[:, :, :8] = 1
+    ws.reshape(rows, nsb, 16)[:, :, 8:] = rng.integers(0, 64, size=(rows, nsb, 8))
+    xq = rng.integers(-127, 128, size=cols, dtype=np.int8)
+    xbs = xq.astype(np.int64).reshape(-1, QK).sum(axis=1).astype(np.int32)
+    ones = np.ones((rows, nsb), np.float32)
+    zeros = np.zeros((rows, nsb), np.float32)
+    y = O.matvec_q4k(wq, ws, ones, zeros, rows, cols, xq, np.ones(nsb, np.float32), xbs)
+    ref = decode_q4k_nibbles(wq, cols) @ xq.astype(np.int64)
+    assert np.array_equal(y.astype(np.int64), ref) and np.all(np.abs(ref) < 2 ** 24), (y, ref)
+    y = O.matvec_q4k(wq, ws, zeros, ones, rows, cols, xq, np.ones(nsb, np.float32), xbs)
+    _, m_b = q4k_sub_params(ws, cols)
+    ref = -(m_b * xbs.astype(np.int64)[None, :]).sum(axis=1)
+    assert np.array_equal(y.astype(np.int64), ref), (y, ref)
+
+
+def pin_q8k_quantizer(O, seed=23):
+    """Per-256 quantisation with the Q8_0 rule: where every 32-element
+    sub-block holds the 256-block's largest magnitude, the quants and scale
+    equal those of the (separately pinned) Q8_0 quantiser; the sub-block
+    sums are the integer sums of the quants; an all-zero block gives d = 0."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((3, 2 * QKK)).astype(np.float32)
+    for r in range(3):
+        for B in range(2):
+            blk = x[r, B * QKK:(B + 1) * QKK]
+            amax = np.float32(np.abs(blk).max() * 1.5)
+            for sb in range(8):
+                blk[sb * QK + int(rng.integers(0, QK))] = amax if rng.random() < 0.5 else -amax
+    x[2, QKK:] = 0.0
+    q, d, bs = O.quantize_q8k(x)
+    q0, d0 = O.quantize_q8(x)
+    assert np.array_equal(q, q0)
+    assert np.array_equal(np.repeat(d, 8, axis=1).view(np.uint32), d0.view(np.uint32))
+    assert np.array_equal(bs, q.astype(np.int64).reshape(3, -1, QK).sum(axis=2))
+    assert d[2, 1] == 0 and not np.any(q[2, QKK:])
+    # generic blocks: one scale per 256, d = max|x| / 127, and every element
+    # within d/2 of q*d (the dequantisation bound, plus float32 rounding)
+    x = (rng.standard_normal((4, 4 * QKK)) * 10.0 ** rng.uniform(-3, 3, (4, 1))).astype(np.float32)
+    q, d, _ = O.quantize_q8k(x)
+    blocks = x.reshape(4, -1, QKK)
+    amax = np.abs(blocks).max(axis=2)
+    assert np.array_equal(d.view(np.uint32), (amax / np.float32(127)).astype(np.float32).view(np.uint32))
+    err = np.abs(blocks.astype(np.float64) - q.reshape(4, -1, QKK) * d.astype(np.float64)[:, :, None])
+    assert np.all(err <= d.astype(np.float64)[:, :, None] * (0.5 + 127 * 3 * U + 2.0 ** -18))
+
+
+def pin_q4k_row_range(O, seed=24):
+    """Only rows [r0, r1) are written."""
+    rng = np.random.default_rng(seed)
+    rows, cols = 6, QKK
+    wq, ws, wd, wdmin = random_q4k(rng, rows, cols)
+    xq, xd, xbs = O.quantize_q8k(rng.standard_normal(cols).astype(np.float32))
+    full = O.matvec_q4k(wq, ws, wd, wdmin, rows, cols, xq, xd, xbs)
+    y = np.full(rows, 7.0, np.float32)
+    O.matvec_q4k(wq, ws, wd, wdmin, rows, cols, xq, xd, xbs, r0=2, r1=5, y=y)
+    assert np.array_equal(y[2:5], full[2:5]) and np.all(y[[0, 1, 5]] == 7.0)
+
+
 ALL_PINS = [
     pin_rmsnorm_closed_form,
     pin_softmax_values,
@@ -402,4 +560,9 @@ ALL_PINS = [
     pin_unit_scales_integer_matvec,
     pin_row_range,
     pin_small_m_rows_independent,
+    pin_q4k_overflow_bound,
+    pin_q4k_bruteforce_fp64,
+    pin_q4k_special_cases,
+    pin_q8k_quantizer,
+    pin_q4k_row_range,
 ]

@@ -42,6 +42,16 @@ MUTANTS = [
     ("rope_k_not_rotated", "for (int h = 0; h < n_kv_heads; ++h) rope_head", "for (int h = 0; h < 0; ++h) rope_head"),
     ("attention_no_scale", "p[t] = dot / sqrt((double)head_dim);", "p[t] = dot;"),
     ("attention_gqa_modulo", "const int g = h / group;", "const int g = h % n_kv_heads;"),
+    ("q4k_min_added", "const float v = (t - u) * xd[B];", "const float v = (t + u) * xd[B];"),
+    ("q4k_first_scale_only", "is += (int32_t)sm[b] * dot;", "is += (int32_t)sm[0] * dot;"),
+    ("q4k_min_from_scales", "ms += (int32_t)sm[8 + b] * xbs[sb];", "ms += (int32_t)sm[b] * xbs[sb];"),
+    ("q4k_high_nibble_low_x", "dot += (int32_t)(bytes[j] >> 4) * a[j + 16];",
+     "dot += (int32_t)(bytes[j] >> 4) * a[j];"),
+    ("q4k_dmin_row0", "(float)ms * wdmin[(size_t)r * nsb + B]", "(float)ms * wdmin[B]"),
+    ("q4k_no_accumulate", "yr = yr + v;", "yr = v;"),
+    ("q8k_bsum_drops_first", "for (int i = 0; i < ORACLE_QK; ++i) t += q[", "for (int i = 1; i < ORACLE_QK; ++i) t += q["),
+    ("q8k_one_scale", "quantize_span(q + e0, d + (size_t)r * nsb + B, x + e0, ORACLE_QKK);",
+     "quantize_span(q + e0, d + (size_t)r * nsb + B, x + e0, ORACLE_QK); quantize_span(q + e0 + ORACLE_QK, d + (size_t)r * nsb + B, x + e0 + ORACLE_QK, ORACLE_QKK - ORACLE_QK);"),
     ("attention_drops_last", "for (int t = 0; t < n_pos; ++t) {\n            const float *vt",
      "for (int t = 0; t < n_pos - 1; ++t) {\n            const float *vt"),
 ]
