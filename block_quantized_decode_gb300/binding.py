@@ -30,7 +30,9 @@ EXPORTS = (
     "mlq_decode_chain_static", "mlq_decode_phase",
     "mlq_rmsnorm", "mlq_add_rmsnorm", "mlq_add", "mlq_softmax", "mlq_silu_mul",
     "mlq_rope_tables", "mlq_rope", "mlq_attention",
+    "mlq_quantize_q8k", "mlq_matvec_q4k", "mlq_block_sums_q4k",
 )
+MLQ_QKK = 256
 MLQ_MAX_SEQ = 32768
 MLQ_MAX_HEAD_DIM = 256
 MLQ_FUSED_MAX_PRODUCTS = 8
@@ -53,6 +55,16 @@ class _QTensor(ctypes.Structure):
 class _QAct(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("d", ctypes.c_void_p), ("n", ctypes.c_int),
                 ("m", ctypes.c_int)]
+
+
+class _Q4KTensor(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("s", ctypes.c_void_p), ("d", ctypes.c_void_p),
+                ("dmin", ctypes.c_void_p), ("rows", ctypes.c_int), ("cols", ctypes.c_int)]
+
+
+class _Q8KAct(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("d", ctypes.c_void_p), ("bsums", ctypes.c_void_p),
+                ("n", ctypes.c_int)]
 
 
 class _ChainProduct(ctypes.Structure):
@@ -115,6 +127,10 @@ def lib() -> ctypes.CDLL:
         L.mlq_rope_tables.argtypes = [P, P, I, I, F, P]
         L.mlq_rope.argtypes = [P, P, P, P, I, I, I, P, P, P, P]
         L.mlq_attention.argtypes = [P, QA, P, P, P, I, I, I, I, P]
+        KT, KA = ctypes.POINTER(_Q4KTensor), ctypes.POINTER(_Q8KAct)
+        L.mlq_quantize_q8k.argtypes = [KA, P, I, P]
+        L.mlq_matvec_q4k.argtypes = [P, KT, KA, I, I, P]
+        L.mlq_block_sums_q4k.argtypes = [P, P, KT, KA, I, I, P]
         L.mlq_status_str.argtypes = [S]
         L.mlq_status_str.restype = ctypes.c_char_p
         for name in EXPORTS:
@@ -218,6 +234,52 @@ def mlq_block_sumi(sumi, W: QTensor, x: QAct, r0: int, r1: int, stream=None) -> 
     cw, cx = W.c(), x.c()
     _check(lib().mlq_block_sumi(_addr(sumi), ctypes.byref(cw), ctypes.byref(cx), r0, r1,
                                 _stream(stream)), "mlq_block_sumi")
+
+
+# ---- Q4_K-style super-blocks ------------------------------------------------
+@dataclass
+class Q4KTensor:
+    """Q4_K-style weights on the device: q nibbles, s (per super-block 8
+    sub-block scales then 8 minima), d and dmin (float32 per super-block)."""
+    q: object
+    s: object
+    d: object
+    dmin: object
+    rows: int
+    cols: int
+
+    def c(self) -> _Q4KTensor:
+        return _Q4KTensor(_addr(self.q), _addr(self.s), _addr(self.d), _addr(self.dmin), self.rows,
+                          self.cols)
+
+
+@dataclass
+class Q8KAct:
+    """Activations for Q4_K products: q int8 [n], d float32 [n/256], bsums int32 [n/32]."""
+    q: object
+    d: object
+    bsums: object
+    n: int
+
+    def c(self) -> _Q8KAct:
+        return _Q8KAct(_addr(self.q), _addr(self.d), _addr(self.bsums), self.n)
+
+
+def mlq_quantize_q8k(out: Q8KAct, x, k: int, stream=None) -> None:
+    co = out.c()
+    _check(lib().mlq_quantize_q8k(ctypes.byref(co), _addr(x), k, _stream(stream)), "mlq_quantize_q8k")
+
+
+def mlq_matvec_q4k(y, W: Q4KTensor, x: Q8KAct, r0: int, r1: int, stream=None) -> None:
+    cw, cx = W.c(), x.c()
+    _check(lib().mlq_matvec_q4k(_addr(y), ctypes.byref(cw), ctypes.byref(cx), r0, r1,
+                                _stream(stream)), "mlq_matvec_q4k")
+
+
+def mlq_block_sums_q4k(isum, msum, W: Q4KTensor, x: Q8KAct, r0: int, r1: int, stream=None) -> None:
+    cw, cx = W.c(), x.c()
+    _check(lib().mlq_block_sums_q4k(_addr(isum), _addr(msum), ctypes.byref(cw), ctypes.byref(cx), r0,
+                                    r1, _stream(stream)), "mlq_block_sums_q4k")
 
 
 # ---- the floating-point steps of a decode layer --------------------------

@@ -423,6 +423,59 @@ mlq_status mlq_prefetch_l2(const void *const *ptrs, const size_t *bytes, int n, 
   return from_cuda(mlq::launch_prefetch_l2(ctx, list));
 }
 
+// ---- Q4_K-style super-blocks ---------------------------------------------------
+namespace {
+bool q4k_cols_ok(int cols) { return cols > 0 && cols % 256 == 0 && cols <= MLQ_MAX_COLS; }
+
+mlq_status check_q4k(const mlq_q4k_tensor *W, const mlq_q8k_act *x, int r0, int r1) {
+  if (W == nullptr || x == nullptr) return MLQ_E_NULL;
+  if (W->q == nullptr || W->s == nullptr || W->d == nullptr || W->dmin == nullptr) return MLQ_E_NULL;
+  if (x->q == nullptr || x->d == nullptr || x->bsums == nullptr) return MLQ_E_NULL;
+  if (!q4k_cols_ok(W->cols) || W->rows < 0 || x->n != W->cols) return MLQ_E_SHAPE;
+  if (r0 < 0 || r1 < r0 || r1 > W->rows) return MLQ_E_SHAPE;
+  if (!aligned(W->q, 16) || !aligned(W->s, 16) || !aligned(W->d, 4) || !aligned(W->dmin, 4))
+    return MLQ_E_ALIGN;
+  if (!aligned(x->q, 16) || !aligned(x->d, 16) || !aligned(x->bsums, 16)) return MLQ_E_ALIGN;
+  return MLQ_OK;
+}
+
+mlq_status q4k_common(float *y, int32_t *isum, int32_t *msum, const mlq_q4k_tensor *W,
+                      const mlq_q8k_act *x, int r0, int r1, void *stream) {
+  mlq_status s = check_q4k(W, x, r0, r1);
+  if (s != MLQ_OK) return s;
+  if (y != nullptr && !aligned(y, 4)) return MLQ_E_ALIGN;
+  if (isum != nullptr && (!aligned(isum, 4) || !aligned(msum, 4))) return MLQ_E_ALIGN;
+  mlq::LaunchCtx ctx;
+  if ((s = make_ctx(&ctx, stream)) != MLQ_OK) return s;
+  return from_cuda(mlq::launch_matvec_q4k(ctx, W->q, W->s, W->d, W->dmin, W->cols / 256, x->q, x->d,
+                                          x->bsums, y, isum, msum, r0, r1));
+}
+}  // namespace
+
+mlq_status mlq_quantize_q8k(mlq_q8k_act *out, const float *x, int k, void *stream) {
+  if (out == nullptr || x == nullptr || out->q == nullptr || out->d == nullptr || out->bsums == nullptr)
+    return MLQ_E_NULL;
+  if (!q4k_cols_ok(k) || out->n != k) return MLQ_E_SHAPE;
+  if (!aligned(x, 16) || !aligned(out->q, 16) || !aligned(out->d, 16) || !aligned(out->bsums, 16))
+    return MLQ_E_ALIGN;
+  mlq::LaunchCtx ctx;
+  mlq_status s = make_ctx(&ctx, stream);
+  if (s != MLQ_OK) return s;
+  return from_cuda(mlq::launch_quantize_q8k(ctx, x, out->q, out->d, out->bsums, k));
+}
+
+mlq_status mlq_matvec_q4k(float *y, const mlq_q4k_tensor *W, const mlq_q8k_act *x, int r0, int r1,
+                          void *stream) {
+  if (y == nullptr) return MLQ_E_NULL;
+  return q4k_common(y, nullptr, nullptr, W, x, r0, r1, stream);
+}
+
+mlq_status mlq_block_sums_q4k(int32_t *isum, int32_t *msum, const mlq_q4k_tensor *W,
+                              const mlq_q8k_act *x, int r0, int r1, void *stream) {
+  if (isum == nullptr || msum == nullptr) return MLQ_E_NULL;
+  return q4k_common(nullptr, isum, msum, W, x, r0, r1, stream);
+}
+
 // ---- the floating-point steps of a decode layer -------------------------------
 namespace {
 // An optional Q8_0 output of n elements (one row): both arrays or none.

@@ -172,6 +172,16 @@ cudaError_t launch_gemm_q4_mma_cluster(const LaunchCtx &ctx, const void *wq, con
                                        int nb, const int8_t *xq, const float *xd, int M, float *Y,
                                        int ldy, int r0, int r1, int rows);
 
+// q4k.cu: Q4_K-style super-blocks (per-256 activation quantiser; M = 1
+// product with the sub-block scales folded in int32; isum/msum non-null
+// selects the integer-sums test hook instead of y).
+cudaError_t launch_quantize_q8k(const LaunchCtx &ctx, const float *x, int8_t *q, float *d,
+                                int32_t *bsums, int k);
+cudaError_t launch_matvec_q4k(const LaunchCtx &ctx, const void *wq, const void *ws, const float *wd,
+                              const float *wdmin, int nsb, const int8_t *xq, const float *xd,
+                              const int32_t *xbs, float *y, int32_t *isum, int32_t *msum, int r0,
+                              int r1);
+
 // layer.cu: the floating-point steps of a decode layer (each one launch).
 cudaError_t launch_rmsnorm_q8(const LaunchCtx &ctx, float *x, const float *y, const float *w,
                               float *h, int8_t *hq, float *hd, int n, float eps);

@@ -1,0 +1,347 @@
+// q4k.cu -- Q4_K-style super-block weights: the per-256 activation
+// quantiser and the M = 1 product with the sub-block scales folded in the
+// integer domain.
+//
+// Definitions: page "SKaiNET-native-kernels", section "Proving an
+// optimization is safe before writing it": 4-bit weight nibbles n in
+// [0, 15], 32 elements per sub-block, 6-bit sub-block scales s_b, 8
+// sub-blocks per block, int8 activations, and per-32 asymmetric minima m_b.
+// Because |sum_b s_b sum_i a_i n_i| <= 8*63*32*127*15 = 3.07e7 < 2^31, the
+// scaled sub-block sums are added in int32 and converted to float once per
+// 256-element super-block.  Layout (rows row-major): q = 16 nibble bytes
+// per sub-block in the Q4_0 order (byte j: element j low, j + 16 high);
+// s = 16 bytes per super-block, the 8 scales then the 8 minima; d, dmin =
+// float32 per super-block.  Element value d*s_b*n - dmin*m_b.  Activations:
+// Q8_0 rounding with one scale per 256 and int32 sums per 32.  For each
+// super-block B of row r (the same float operations, in the same order, as
+// the plain definition):
+//   ISUM = sum_b s_b * sum_i a_i n_i,   MSUM = sum_b m_b * bsum_b,
+//   y[r] += ((float)ISUM * d - (float)MSUM * dmin) * dx_B.
+// (Even 8-bit scales and minima stay inside int32: 8*255*32*127*15 < 2^31.)
+//
+// The product streams weights like the other M = 1 kernels: one CTA per SM
+// (at most), a producer warp filling a ring of shared-memory stages of R
+// rows -- the nibbles and the scale/minimum bytes by bulk copies (their row
+// strides are multiples of 16 bytes), d and dmin by 4-byte asynchronous
+// copies (their row stride need not be), all completing on the stage's
+// full barrier -- and 8 consumer warps.  A warp takes one row at a time:
+// lane l works on sub-block l (+32, +64, ...), 8 lanes per super-block; the
+// lane's scaled integer dot and minimum term are added across its 8 lanes
+// with integer shuffles, and the group's first lane does the float
+// arithmetic of the super-block.
+#include "mlq_device.cuh"
+#include "mlq_launch.h"
+
+namespace mlq {
+
+constexpr int kQKK = 256;
+constexpr int kKSubs = kQKK / kQK;                 // sub-blocks per super-block
+constexpr int kKWarps = 8;                         // consumer warps
+constexpr int kKThreads = (kKWarps + 1) * 32;      // + the producer warp
+constexpr int kKSlots = 8;
+constexpr size_t kKBudget = 220 * 1024;
+constexpr size_t kKStageTarget = 32 * 1024;
+
+// ---- quantiser ------------------------------------------------------------
+// One warp per 256-element block; lane l holds elements 8l .. 8l + 7, and
+// the four lanes of each 32-element sub-block add their quants for bsums.
+__global__ void __launch_bounds__(256) quantize_q8k_kernel(const float *__restrict__ x, int8_t *q,
+                                                           float *d, int32_t *bsums, int nblocks) {
+  const int blk = static_cast<int>((blockIdx.x * static_cast<unsigned>(blockDim.x) + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  griddep_wait();
+  if (blk >= nblocks) return;
+  const float4 *src = reinterpret_cast<const float4 *>(x + static_cast<size_t>(blk) * kQKK + lane * 8);
+  const float4 a = src[0], b = src[1];
+  const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = max(m, __float_as_uint(fabsf(v[i])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float amax = __uint_as_float(m);
+  const float dd = amax / 127.0f;
+  const float id = amax != 0.0f ? 127.0f / amax : 0.0f;
+  int qs[8];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    qs[i] = quant_one(v[i], id);
+    sum += qs[i];
+  }
+  uint2 packed;
+  packed.x = (qs[0] & 0xff) | ((qs[1] & 0xff) << 8) | ((qs[2] & 0xff) << 16) |
+             (static_cast<uint32_t>(qs[3] & 0xff) << 24);
+  packed.y = (qs[4] & 0xff) | ((qs[5] & 0xff) << 8) | ((qs[6] & 0xff) << 16) |
+             (static_cast<uint32_t>(qs[7] & 0xff) << 24);
+  *reinterpret_cast<uint2 *>(q + static_cast<size_t>(blk) * kQKK + lane * 8) = packed;
+  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+  if ((lane & 3) == 0) bsums[static_cast<size_t>(blk) * kKSubs + (lane >> 2)] = sum;
+  if (lane == 0) d[blk] = dd;
+}
+
+cudaError_t launch_quantize_q8k(const LaunchCtx &ctx, const float *x, int8_t *q, float *d,
+                                int32_t *bsums, int k) {
+  const int nblocks = k / kQKK;
+  if (nblocks <= 0) return cudaSuccess;
+  const int per = 256 / 32;
+  return launch_kernel(quantize_q8k_kernel, dim3(static_cast<unsigned>((nblocks + per - 1) / per)),
+                       dim3(256), 0, ctx, x, q, d, bsums, nblocks);
+}
+
+// ---- product ----------------------------------------------------------------
+struct Q4KArgs {
+  const uint8_t *wq, *ws;
+  const float *wd, *wdmin;
+  const int8_t *xq;
+  const float *xd;
+  const int32_t *xbs;
+  float *y;
+  int32_t *isum, *msum;  // test hook: per-super-block integer sums instead of y
+  int nsb, r0, r1;
+  int R, ns;                                    // rows per stage, ring slots
+  unsigned stage_bytes, stage_s, stage_d;       // stage size; offsets of s and of d, dmin
+  unsigned smem_ring;
+  int *status;
+  unsigned long long wait_ns;
+};
+
+__device__ __forceinline__ void k_consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kKWarps * 32) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst_smem, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst_smem)), "l"(src) : "memory");
+}
+// The stage's full barrier counts one arrival per producer lane once that
+// lane's earlier 4-byte copies have landed.
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool k_wait(uint32_t bar, uint32_t parity, const volatile int *abort_flag,
+                                       unsigned long long limit_ns) {
+  if (limit_ns == 0) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = sm_cycles(), lim = limit_cycles(limit_ns);
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (sm_cycles() - t0 > lim) return false;
+  }
+}
+
+template <bool SUMS>
+__global__ void __launch_bounds__(kKThreads, 1) matvec_q4k_kernel(const __grid_constant__ Q4KArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[kKSlots];
+  __shared__ __align__(8) uint64_t empty_bar[kKSlots];
+  __shared__ int abort_flag;
+  volatile int *abort_v = &abort_flag;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nsb = a.nsb, nsub = nsb * kKSubs, K = nsb * kQKK;
+  const size_t rowq = static_cast<size_t>(nsb) * (kQKK / 2), rows_s = static_cast<size_t>(nsb) * 16;
+  const int n_all = a.r1 - a.r0;
+  const int ra = a.r0 + static_cast<int>(static_cast<long long>(n_all) * blockIdx.x / gridDim.x);
+  const int rb = a.r0 + static_cast<int>(static_cast<long long>(n_all) * (blockIdx.x + 1) / gridDim.x);
+  const int R = a.R, ns = a.ns;
+  int8_t *xq_s = reinterpret_cast<int8_t *>(smem);
+  int32_t *xbs_s = reinterpret_cast<int32_t *>(smem + K);
+  float *xd_s = reinterpret_cast<float *>(smem + K + 4 * nsub);
+  uint8_t *ring = smem + a.smem_ring;
+
+  if (tid == 0) {
+    for (int k = 0; k < ns; ++k) {
+      mbar_init(smem_addr(&full_bar[k]), 1 + 32);  // the bulk-copy arrival + 32 producer lanes
+      mbar_init(smem_addr(&empty_bar[k]), kKWarps);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  griddep_launch_dependents();
+  griddep_wait();  // x (and, conservatively, the weights) may come from earlier work
+
+  if (warp == kKWarps) {
+    // ------------------------------ producer ------------------------------
+    int s = 0;
+    for (int r = ra; r < rb; r += R, ++s) {
+      const int n = min(R, rb - r);
+      const int slot = s % ns;
+      if (s >= ns && !warp_wait([&] {
+            return k_wait(smem_addr(&empty_bar[slot]), ((s / ns) - 1) & 1, abort_v, a.wait_ns);
+          })) {
+        if (lane == 0 && atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
+        break;
+      }
+      if (*abort_v) break;
+      uint8_t *dst = ring + static_cast<size_t>(slot) * a.stage_bytes;
+      const uint32_t fb = smem_addr(&full_bar[slot]);
+      if (lane == 0) {
+        const uint32_t qb = static_cast<uint32_t>(n * rowq), sb = static_cast<uint32_t>(n * rows_s);
+        mbar_arrive_expect_tx(fb, qb + sb);
+        bulk_copy_g2s(smem_addr(dst), a.wq + static_cast<size_t>(r) * rowq, qb, fb);
+        bulk_copy_g2s(smem_addr(dst + a.stage_s), a.ws + static_cast<size_t>(r) * rows_s, sb, fb);
+      }
+      float *dd = reinterpret_cast<float *>(dst + a.stage_d);
+      float *dm = dd + static_cast<size_t>(R) * nsb;
+      for (int e = lane; e < n * nsb; e += 32) {
+        cp_async4(dd + e, a.wd + static_cast<size_t>(r) * nsb + e);
+        cp_async4(dm + e, a.wdmin + static_cast<size_t>(r) * nsb + e);
+      }
+      cp_async_arrive(fb);
+    }
+    if (*abort_v && lane == 0) {  // copies may still be landing: the last issued stages (bounded)
+      for (int t = s > ns ? s - ns : 0; t < s; ++t)
+        mbar_wait_bounded(smem_addr(&full_bar[t % ns]), (t / ns) & 1, kDrainWaitNs);
+    }
+    return;
+  }
+
+  // ------------------------------ consumers ------------------------------
+  if (rb <= ra) return;
+  {  // the activation vector into shared memory, all loads before any store
+    const int uq = K / 16, ub = nsub / 4;
+    for (int base = 0; base < uq + ub; base += 2 * kKWarps * 32) {
+      int4 v[2];
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        const int u = base + p * kKWarps * 32 + tid;
+        if (u < uq) v[p] = __ldg(reinterpret_cast<const int4 *>(a.xq) + u);
+        else if (u < uq + ub) v[p] = __ldg(reinterpret_cast<const int4 *>(a.xbs) + (u - uq));
+      }
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        const int u = base + p * kKWarps * 32 + tid;
+        if (u < uq) reinterpret_cast<int4 *>(xq_s)[u] = v[p];
+        else if (u < uq + ub) reinterpret_cast<int4 *>(xbs_s)[u - uq] = v[p];
+      }
+    }
+    for (int u = tid; u < nsb; u += kKWarps * 32) xd_s[u] = __ldg(a.xd + u);
+  }
+  k_consumers_sync();
+
+  int s = 0;
+  for (int r = ra; r < rb; r += R, ++s) {
+    const int n = min(R, rb - r);
+    const int slot = s % ns;
+    if (!warp_wait([&] { return k_wait(smem_addr(&full_bar[slot]), (s / ns) & 1, abort_v, a.wait_ns); })) {
+      if (lane == 0 && atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
+      return;
+    }
+    const uint8_t *stq = ring + static_cast<size_t>(slot) * a.stage_bytes;
+    const uint8_t *sts = stq + a.stage_s;
+    const float *std_ = reinterpret_cast<const float *>(stq + a.stage_d);
+    const float *stm = std_ + static_cast<size_t>(R) * nsb;
+    for (int i = warp; i < n; i += kKWarps) {
+      const uint8_t *wrow = stq + static_cast<size_t>(i) * rowq;
+      const uint8_t *srow = sts + static_cast<size_t>(i) * rows_s;
+      float acc = 0.0f;
+      for (int u0 = 0; u0 < nsub; u0 += 32) {
+        const int u = u0 + lane;
+        const bool valid = u < nsub;  // whole groups of 8 lanes (nsub is a multiple of 8)
+        int is = 0, ms = 0;
+        if (valid) {
+          const uint4 w = *reinterpret_cast<const uint4 *>(wrow + static_cast<size_t>(u) * 16);
+          const int4 xa = *reinterpret_cast<const int4 *>(xq_s + static_cast<size_t>(u) * kQK);
+          const int4 xb = *reinterpret_cast<const int4 *>(xq_s + static_cast<size_t>(u) * kQK + 16);
+          const int B = u >> 3, j = u & 7;
+          constexpr uint32_t kLo = 0x0F0F0F0Fu;
+          int dot = 0;
+          asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"(w.x & kLo), "r"(xa.x));
+          asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"(w.y & kLo), "r"(xa.y));
+          asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"(w.z & kLo), "r"(xa.z));
+          asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"(w.w & kLo), "r"(xa.w));
+          asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"((w.x >> 4) & kLo), "r"(xb.x));
+          asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"((w.y >> 4) & kLo), "r"(xb.y));
+          asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"((w.z >> 4) & kLo), "r"(xb.z));
+          asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"((w.w >> 4) & kLo), "r"(xb.w));
+          is = static_cast<int>(srow[B * 16 + j]) * dot;
+          ms = static_cast<int>(srow[B * 16 + 8 + j]) * xbs_s[u];
+        }
+        // the super-block's 8 sub-blocks: integer sums, exact
+        is += __shfl_xor_sync(0xffffffffu, is, 1);
+        ms += __shfl_xor_sync(0xffffffffu, ms, 1);
+        is += __shfl_xor_sync(0xffffffffu, is, 2);
+        ms += __shfl_xor_sync(0xffffffffu, ms, 2);
+        is += __shfl_xor_sync(0xffffffffu, is, 4);
+        ms += __shfl_xor_sync(0xffffffffu, ms, 4);
+        if (valid && (lane & 7) == 0) {
+          const int B = u >> 3;
+          if (SUMS) {
+            a.isum[static_cast<size_t>(r + i - a.r0) * nsb + B] = is;
+            a.msum[static_cast<size_t>(r + i - a.r0) * nsb + B] = ms;
+          } else {
+            const float t = __fmul_rn(__int2float_rn(is), std_[static_cast<size_t>(i) * nsb + B]);
+            const float um = __fmul_rn(__int2float_rn(ms), stm[static_cast<size_t>(i) * nsb + B]);
+            acc = __fadd_rn(acc, __fmul_rn(__fsub_rn(t, um), xd_s[B]));
+          }
+        }
+      }
+      if (!SUMS) {
+        acc += __shfl_xor_sync(0xffffffffu, acc, 8);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 16);
+        if (lane == 0) a.y[r + i] = acc;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&empty_bar[slot])) : "memory");
+  }
+}
+
+cudaError_t launch_matvec_q4k(const LaunchCtx &ctx, const void *wq, const void *ws, const float *wd,
+                              const float *wdmin, int nsb, const int8_t *xq, const float *xd,
+                              const int32_t *xbs, float *y, int32_t *isum, int32_t *msum, int r0,
+                              int r1) {
+  const int n = r1 - r0;
+  if (n <= 0) return cudaSuccess;
+  auto up = [](size_t v, size_t a) { return (v + a - 1) / a * a; };
+  const size_t K = static_cast<size_t>(nsb) * kQKK;
+  const size_t rowq = static_cast<size_t>(nsb) * (kQKK / 2), rows_s = static_cast<size_t>(nsb) * 16;
+  const size_t rowbytes = rowq + rows_s + 8 * static_cast<size_t>(nsb);
+  const size_t xs = up(K + 4 * (K / kQK) + 4 * static_cast<size_t>(nsb), 128);
+  int R = static_cast<int>(kKStageTarget / rowbytes);
+  if (R < 1) R = 1;
+  int grid = ctx.num_sms;
+  if (grid > (n + R - 1) / R) grid = (n + R - 1) / R;
+  const int rows_cta = (n + grid - 1) / grid;
+  if (R > rows_cta) R = rows_cta;
+  const size_t stage_s = R * rowq;                       // multiple of 128
+  const size_t stage_d = stage_s + R * rows_s;           // multiple of 16
+  const size_t stage = up(stage_d + 8 * static_cast<size_t>(R) * nsb, 128);
+  if (xs + 2 * stage > kKBudget) return cudaErrorNotSupported;
+  int ns = static_cast<int>((kKBudget - xs) / stage);
+  if (ns > kKSlots) ns = kKSlots;
+  const int stages_cta = (rows_cta + R - 1) / R;
+  if (ns > stages_cta) ns = stages_cta < 2 ? 2 : stages_cta;
+  Q4KArgs a;
+  a.wq = static_cast<const uint8_t *>(wq);
+  a.ws = static_cast<const uint8_t *>(ws);
+  a.wd = wd;
+  a.wdmin = wdmin;
+  a.xq = xq;
+  a.xd = xd;
+  a.xbs = xbs;
+  a.y = y;
+  a.isum = isum;
+  a.msum = msum;
+  a.nsb = nsb;
+  a.r0 = r0;
+  a.r1 = r1;
+  a.R = R;
+  a.ns = ns;
+  a.stage_bytes = static_cast<unsigned>(stage);
+  a.stage_s = static_cast<unsigned>(stage_s);
+  a.stage_d = static_cast<unsigned>(stage_d);
+  a.smem_ring = static_cast<unsigned>(xs);
+  a.status = ctx.status;
+  a.wait_ns = ctx.wait_ns;
+  const size_t smem = xs + static_cast<size_t>(ns) * stage;
+  auto kern = isum != nullptr ? matvec_q4k_kernel<true> : matvec_q4k_kernel<false>;
+  prefer_max_shared(kern);
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kKThreads), smem, ctx, a);
+}
+
+}  // namespace mlq

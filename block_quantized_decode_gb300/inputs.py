@@ -47,6 +47,25 @@ def weights(wtype: int, rows: int, cols: int, seed: int):
     return q4_weights(rows, cols, seed) if wtype == Q4_0 else q8_weights(rows, cols, seed)
 
 
+QKK = 256
+
+
+def q4k_weights(rows: int, cols: int, seed: int, lo: float = 1e-4, hi: float = 1e-3):
+    """Q4_K-style weights: uniform nibble bytes; per super-block 8 sub-block
+    scales and 8 minima uniform in the 6-bit range [0, 63]; d and dmin
+    uniform [lo, hi) float32 (so d * s_b spans about the Q4_0 scales'
+    range).  Returns (q [rows, cols/2] u8, s [rows, cols/256*16] u8,
+    d [rows, cols/256] f32, dmin [rows, cols/256] f32)."""
+    assert cols % QKK == 0
+    rng = np.random.default_rng(seed)
+    nsb = cols // QKK
+    q = rng.integers(0, 256, size=(rows, cols // 2), dtype=np.uint8)
+    s = rng.integers(0, 64, size=(rows, nsb * 16), dtype=np.uint8)
+    d = rng.uniform(lo, hi, size=(rows, nsb)).astype(np.float32)
+    dmin = rng.uniform(lo, hi, size=(rows, nsb)).astype(np.float32)
+    return q, s, d, dmin
+
+
 def activations(m: int, k: int, seed: int) -> np.ndarray:
     """float32 [m, k] ~ N(0, 1)."""
     rng = np.random.default_rng(seed)

@@ -21,7 +21,8 @@ from . import binding as B
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("--op", default="matvec_q4",
-                   choices=["matvec_q4", "matvec_q8", "gemm_q4", "quantize", "fused", "phase", "chain"])
+                   choices=["matvec_q4", "matvec_q8", "gemm_q4", "quantize", "fused", "phase", "chain",
+                            "matvec_q4k"])
     p.add_argument("--workload", default="tinyllama_layer",
                    help="for --op fused / phase / chain: the workload whose phases run as "
                         "mlq_matvec_fused / mlq_decode_phase calls, or as one "
@@ -40,6 +41,8 @@ def main():
     B.mlq_init()
     if a.op in ("fused", "phase", "chain"):
         return fused_case(a)
+    if a.op == "matvec_q4k":
+        return q4k_case(a)
     g = torch.Generator(device=dev)
     g.manual_seed(0)
     rows, cols, m = a.rows, a.cols, a.m
@@ -105,6 +108,56 @@ def main():
                       "us_per_launch": us, "us_all": times, "bytes_per_launch": moved,
                       "GBps": moved / (us * 1e-6) / 1e9,
                       "gops": 2.0 * m * rows * cols / (us * 1e-6) / 1e9 if a.op != "quantize" else 0.0}))
+
+
+def q4k_case(a):
+    """Back-to-back mlq_matvec_q4k launches over rotating weight copies."""
+    from . import inputs as I
+    rows, cols = a.rows, a.cols
+    q, s, d, dmin = I.q4k_weights(rows, cols, seed=0)
+    wbytes = q.nbytes + s.nbytes + d.nbytes + dmin.nbytes
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    copies = a.copies or max(1, math.ceil(3 * l2 / wbytes))
+    copies = min(copies, a.iters)
+    dev = torch.device("cuda:0")
+    Ws = []
+    for c in range(copies):
+        Ws.append(B.Q4KTensor(*(torch.from_numpy(t).to(dev) for t in (q, s, d, dmin)), rows, cols))
+    x = torch.from_numpy(I.activations(1, cols, seed=1)[0]).to(dev)
+    act = B.Q8KAct(torch.empty(cols, dtype=torch.int8, device=dev),
+                   torch.empty(cols // 256, dtype=torch.float32, device=dev),
+                   torch.empty(cols // 32, dtype=torch.int32, device=dev), cols)
+    B.mlq_quantize_q8k(act, x, cols)
+    y = torch.empty(rows, dtype=torch.float32, device=dev)
+    s_ = torch.cuda.Stream()
+    with torch.cuda.stream(s_):
+        for i in range(copies):
+            B.mlq_matvec_q4k(y, Ws[i], act, 0, rows)
+    s_.synchronize()
+    graph = None
+    if not a.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s_):
+            for i in range(a.iters):
+                B.mlq_matvec_q4k(y, Ws[i % copies], act, 0, rows)
+    times = []
+    for _ in range(a.reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s_):
+            e0.record(s_)
+            if graph is not None:
+                graph.replay()
+            else:
+                for i in range(a.iters):
+                    B.mlq_matvec_q4k(y, Ws[i % copies], act, 0, rows)
+            e1.record(s_)
+        s_.synchronize()
+        times.append(e0.elapsed_time(e1) / a.iters * 1e3)
+    assert B.mlq_last_device_error(s_) == B.MLQ_OK
+    us = min(times)
+    print(json.dumps({"op": a.op, "rows": rows, "cols": cols, "copies": copies, "us_per_launch": us,
+                      "us_all": times, "bytes_per_launch": wbytes, "GBps": wbytes / (us * 1e-6) / 1e9,
+                      "gops": 2.0 * rows * cols / (us * 1e-6) / 1e9}))
 
 
 def fused_case(a):

@@ -152,6 +152,64 @@ mlq_status mlq_gemm_q4_small_m(float *Y, int ldy, const mlq_qtensor *W, const ml
 mlq_status mlq_block_sumi(int32_t *sumi, const mlq_qtensor *W, const mlq_qact *x,
                           int r0, int r1, void *stream);
 
+/* ---- Q4_K-style super-blocks ------------------------------------------- */
+/* Page "SKaiNET-native-kernels", section "Proving an optimization is safe
+ * before writing it": 4-bit nibbles n in [0, 15], 32-element sub-blocks
+ * with a 6-bit scale s_b and a 6-bit minimum m_b, 8 sub-blocks per
+ * 256-element super-block with a float32 scale d and a float32 scale of the
+ * minima dmin; element value d*s_b*n - dmin*m_b.  The sub-block scales are
+ * folded in the integer domain: per super-block the int32 sums
+ *   ISUM = sum_b s_b * sum_i a_i n_i,   MSUM = sum_b m_b * sum_i a_i
+ * (|ISUM| <= 8*63*32*127*15 = 3.07e7; with any byte values, 8*255*32*127*15
+ * still fits int32) are converted to float once.
+ * Layout (the page gives none; rows row-major, all device pointers):
+ *   q:    rows x cols/2 bytes, 16 per 32-element sub-block in the Q4_0
+ *         order (byte j: element j in the low nibble, j + 16 in the high);
+ *   s:    rows x cols/256 x 16 bytes: per super-block the 8 sub-block
+ *         scales, then the 8 sub-block minima;
+ *   d, dmin: rows x cols/256 float32.
+ * cols a positive multiple of 256, at most MLQ_MAX_COLS; q and s 16-byte
+ * aligned, d and dmin 4-byte aligned. */
+typedef struct {
+    const void *q;
+    const void *s;
+    const float *d;
+    const float *dmin;
+    int rows, cols;
+} mlq_q4k_tensor;
+
+/* Activations for Q4_K products: n int8 quants q, n/256 float32 scales d
+ * (one per 256 elements) and n/32 int32 sums of the quants per 32 elements
+ * (bsums).  q, d and bsums 16-byte aligned device pointers. */
+typedef struct {
+    int8_t *q;
+    float *d;
+    int32_t *bsums;
+    int n;
+} mlq_q8k_act;
+
+/* Quantise k float32 (x, device, 16-byte aligned) per 256 elements with the
+ * rule of mlq_quantize_q8 (amax over the 256, d = amax/127, id = 127/amax,
+ * q = trunc(x*id + copysign(0.5, x)) without fused multiply-add, clamp to
+ * [-127, 127], NaN -> 0), and write the per-32 sums of the quants.
+ * Bit-identical to that definition.  Requires out->n == k, k a positive
+ * multiple of 256, at most MLQ_MAX_COLS. */
+mlq_status mlq_quantize_q8k(mlq_q8k_act *out, const float *x, int k, void *stream);
+
+/* For r in [r0, r1):
+ *   y[r] = sum_B ((float)ISUM(r, B) * W->d[r*nsb + B]
+ *                 - (float)MSUM(r, B) * W->dmin[r*nsb + B]) * x->d[B],
+ * nsb = cols/256, each term in float32 in that order; the sum over B is
+ * taken in an order other than B = 0, 1, ... and agrees with the in-order
+ * sum within 1e-5 * sum_B |term_B| per row.  x->n == W->cols. */
+mlq_status mlq_matvec_q4k(float *y, const mlq_q4k_tensor *W, const mlq_q8k_act *x, int r0, int r1,
+                          void *stream);
+
+/* Test hook: isum[(r - r0)*nsb + B] = ISUM(r, B), msum[...] = MSUM(r, B)
+ * for r in [r0, r1), computed by the same code as mlq_matvec_q4k. */
+mlq_status mlq_block_sums_q4k(int32_t *isum, int32_t *msum, const mlq_q4k_tensor *W,
+                              const mlq_q8k_act *x, int r0, int r1, void *stream);
+
 /* ---- the floating-point steps of a decode layer ------------------------ */
 /* Page "Legacy-ISA ML Inference Runtime -- Design Spec", Sec. 5 (ml_k_rmsnorm,
  * ml_k_softmax, ml_k_rope, ml_k_silu_mul, ml_k_add, ml_k_dot_f32,

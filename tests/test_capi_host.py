@@ -294,3 +294,44 @@ def test_validation_layer_steps(M):
     assert att(nkv=3) == M.MLQ_E_SHAPE
     assert att(hd=48, oq=B(qa(n=48 * 32))) == M.MLQ_E_SHAPE  # Q8 output needs head_dim % 32
     assert att(oq=B(qa(n=1024))) == M.MLQ_E_SHAPE            # n_heads * head_dim = 2048
+
+
+def test_validation_q4k(M):
+    from block_quantized_decode_gb300.binding import _Q4KTensor, _Q8KAct
+
+    def kt(q=A, s_=2 * A, d=7 * A, dmin=8 * A, rows=64, cols=512):
+        return _Q4KTensor(q, s_, d, dmin, rows, cols)
+
+    def ka(q=3 * A, d=4 * A, bs=9 * A, n=512):
+        return _Q8KAct(q, d, bs, n)
+
+    def mvk(y=5 * A, W=None, x=None, r0=0, r1=64):
+        W = kt() if W is None else W
+        x = ka() if x is None else x
+        return call(M, "mlq_matvec_q4k", y, ctypes.byref(W), ctypes.byref(x), r0, r1, None)
+
+    assert mvk(y=None) == M.MLQ_E_NULL
+    assert mvk(W=kt(s_=0)) == M.MLQ_E_NULL
+    assert mvk(W=kt(dmin=0)) == M.MLQ_E_NULL
+    assert mvk(x=ka(bs=0)) == M.MLQ_E_NULL
+    assert mvk(W=kt(cols=384), x=ka(n=384)) == M.MLQ_E_SHAPE       # not whole super-blocks
+    assert mvk(W=kt(cols=65792), x=ka(n=65792)) == M.MLQ_E_SHAPE   # > MLQ_MAX_COLS
+    assert mvk(x=ka(n=256)) == M.MLQ_E_SHAPE
+    assert mvk(r0=3, r1=2) == M.MLQ_E_SHAPE
+    assert mvk(r1=65) == M.MLQ_E_SHAPE
+    assert mvk(W=kt(q=A + 8)) == M.MLQ_E_ALIGN
+    assert mvk(W=kt(s_=2 * A + 4)) == M.MLQ_E_ALIGN
+    assert mvk(W=kt(d=7 * A + 2)) == M.MLQ_E_ALIGN
+    assert mvk(x=ka(bs=9 * A + 4)) == M.MLQ_E_ALIGN
+    assert mvk(y=5 * A + 1) == M.MLQ_E_ALIGN
+    sums = lambda i=10 * A, m=11 * A: call(M, "mlq_block_sums_q4k", i, m, ctypes.byref(kt()),
+                                           ctypes.byref(ka()), 0, 64, None)
+    assert sums(m=None) == M.MLQ_E_NULL
+    assert sums(i=10 * A + 2) == M.MLQ_E_ALIGN
+    qk = lambda out, x=6 * A, k=512: call(M, "mlq_quantize_q8k", ctypes.byref(out), x, k, None)
+    assert qk(ka(), x=None) == M.MLQ_E_NULL
+    assert qk(ka(bs=0)) == M.MLQ_E_NULL
+    assert qk(ka(n=480), k=480) == M.MLQ_E_SHAPE
+    assert qk(ka(n=512), k=256) == M.MLQ_E_SHAPE
+    assert qk(ka(), x=6 * A + 4) == M.MLQ_E_ALIGN
+    assert qk(ka(d=4 * A + 4)) == M.MLQ_E_ALIGN
