@@ -312,6 +312,44 @@ class OracleLayerPass:
         return O.add(x, self._mv("w2", *O.quantize_q8(g)))
 
 
+class OracleQ4KPass:
+    """One pass of a Q4KWorkload with the oracle: quantise each input per
+    256, then every product with rows split statically over `threads` host
+    threads (the oracle's own [r0, r1) interface)."""
+
+    def __init__(self, wl, threads: int):
+        import numpy as np
+        from concurrent.futures import ThreadPoolExecutor
+
+        import oracle
+        from block_quantized_decode_gb300 import inputs as I
+        self.np, self.O, self.wl, self.threads = np, oracle, wl, threads
+        self.pool = ThreadPoolExecutor(max_workers=threads)
+        self.W = {name: I.q4k_weights(rows, cols, seed=wl.seed + i) + (rows, cols)
+                  for i, (name, rows, cols, _) in enumerate(wl.mats)}
+        self.x0 = I.activations(1, wl.mats[0][2], seed=wl.seed + 1000)[0]
+        self.weight_bytes = sum(q.nbytes + s.nbytes + d.nbytes + dm.nbytes
+                                for q, s, d, dm, _, _ in self.W.values())
+        self.ops = sum(2 * rows * cols for _, rows, cols, _ in wl.mats)
+
+    def run(self):
+        O, np = self.O, self.np
+        vecs = {"x": self.x0}
+        acts = {}
+        for name, rows, cols, inp in self.wl.mats:
+            if inp not in acts:
+                acts[inp] = O.quantize_q8k(vecs[inp])
+            q, s, d, dm, _, _ = self.W[name]
+            y = np.zeros(rows, dtype=np.float32)
+            cuts = [rows * t // self.threads for t in range(self.threads + 1)]
+            futs = [self.pool.submit(O.matvec_q4k, q, s, d, dm, rows, cols, *acts[inp], a, b, y)
+                    for a, b in zip(cuts, cuts[1:]) if b > a]
+            for f in futs:
+                f.result()
+            vecs[name] = y
+        return vecs
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -319,9 +357,17 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def time_oracle(wl, seconds: float, threads: int, max_steps: int | None = None):
+def oracle_pass(wl, threads: int):
     from block_quantized_decode_gb300 import inputs as I
-    op = OracleLayerPass(wl, threads) if isinstance(wl, I.LayerShape) else OraclePass(wl, threads)
+    if isinstance(wl, I.LayerShape):
+        return OracleLayerPass(wl, threads)
+    if isinstance(wl, I.Q4KWorkload):
+        return OracleQ4KPass(wl, threads)
+    return OraclePass(wl, threads)
+
+
+def time_oracle(wl, seconds: float, threads: int, max_steps: int | None = None):
+    op = oracle_pass(wl, threads)
     op.run()  # warm (page-in, thread start)
     n, t0 = 0, time.perf_counter()
     while True:
@@ -341,8 +387,8 @@ def run_reference(args, wl, world, rank):
         return 0
     from block_quantized_decode_gb300 import inputs as I
     threads = host_cores()
-    layer = isinstance(wl, I.LayerShape)
-    op = OracleLayerPass(wl, threads) if layer else OraclePass(wl, threads)
+    layer = isinstance(wl, (I.LayerShape, I.Q4KWorkload))
+    op = oracle_pass(wl, threads)
     for _ in range(min(max(0, args.warmup), 3)):
         op.run()
     t0 = time.perf_counter()
@@ -854,19 +900,195 @@ def run_layer(args, shape, world, rank, local, pg):
     return 0
 
 
+def run_q4k(args, wl, world, rank, local, pg):
+    """A pass of Q4_K-style products per step (per input one
+    mlq_quantize_q8k, then its mlq_matvec_q4k calls), captured in a CUDA
+    graph per weight copy.  value = weight bytes (nibbles, scale/minimum
+    bytes, d, dmin) per step / step time."""
+    import torch
+
+    import block_quantized_decode_gb300 as M
+    from block_quantized_decode_gb300.runner import Q4KRunner
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    M.mlq_init()
+    props = torch.cuda.get_device_properties(local)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
+    probe = Q4KRunner(wl, copies=1, device=f"cuda:{local}")
+    wbytes = probe.weight_bytes()
+    del probe
+    copies = args.copies or max(2, math.ceil(3 * l2 / wbytes))
+    r = Q4KRunner(wl, copies=copies, device=f"cuda:{local}")
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for c in range(copies):
+            r.step(copy=c, stream=stream)
+    stream.synchronize()
+    graphs, cycle = [], None
+    if not args.no_graph:
+        for c in range(copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                r.step(copy=c, stream=stream)
+            graphs.append(g)
+        cycle = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cycle, stream=stream):
+            for c in range(copies):
+                r.step(copy=c, stream=stream)
+
+    def do_step(i):
+        if graphs:
+            graphs[i % copies].replay()
+        else:
+            r.step(copy=i % copies, stream=stream)
+
+    def do_steps(n):
+        i = 0
+        if cycle is not None:
+            while n - i >= copies:
+                cycle.replay()
+                i += copies
+        while i < n:
+            do_step(i)
+            i += 1
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    warm = max(args.warmup, copies if cycle is not None else 0)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a0.record(stream)
+        do_steps(warm)
+        a1.record(stream)
+    stream.synchronize()
+    steps = args.steps
+    if steps <= 0:
+        per = a0.elapsed_time(a1) / 1e3 / max(1, warm)
+        steps = max(10, int(args.seconds / max(per, 1e-7)))
+        steps = int(max_over_ranks(pg, float(steps), dev))
+    barrier(pg, local)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        do_steps(steps)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    barrier(pg, local)
+    clk = clocks.stop(t_host0, t_host1)
+    ms_max = max_over_ranks(pg, e0.elapsed_time(e1), dev)
+    value = world * wbytes * steps / (ms_max / 1e3) / 1e9
+    peaks, peak_src = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+
+    # ---- the dominant kernel: each product's launches back to back in its
+    # own graph over rotating weight copies, CUDA events on the stream
+    per_prod, tot_b, tot_s = {}, 0.0, 0.0
+    for name, rows, cols, _ in wl.mats:
+        reps = 2 * copies
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(reps):
+                r.product(name, copy=j % copies, stream=stream)
+        with torch.cuda.stream(stream):
+            g.replay()
+        stream.synchronize()
+        best = None
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+            stream.synchronize()
+            t = a.elapsed_time(b) / 1e3 / reps
+            best = t if best is None else min(best, t)
+        del g
+        q, s_, d, dm, _, _ = r.host[name]
+        nb = q.nbytes + s_.nbytes + d.nbytes + dm.nbytes
+        per_prod[f"{name}:{rows}x{cols}"] = {"us": best * 1e6, "GBps": nb / best / 1e9}
+        tot_b += nb
+        tot_s += best
+    ach = tot_b / tot_s / 1e9
+    nprod = len(wl.mats)
+    roofline = {"kernel": "matvec_q4k_kernel", "bound": "hbm", "achieved": ach, "peak": hbm,
+                "unit": "GB/s", "frac": ach / hbm, "peak_source": peak_src,
+                "traffic": ncu_traffic(f"matvec_q4k_{wl.name}", ("q4k.cu", "mlq_device.cuh"),
+                                       tot_b / nprod),
+                "bytes_per_launch": tot_b / nprod, "us_per_launch": tot_s / nprod * 1e6,
+                "method": "each product's launches back to back in its own graph over rotating "
+                          "weight copies, best of 3, CUDA events on the launching stream",
+                "per_product": per_prod}
+
+    # ---- end to end: x from pinned host memory, the step, the last output back
+    last = wl.mats[-1][0]
+    host_y = torch.empty(r.y[last].numel(), dtype=torch.float32).pin_memory()
+    e2e_steps = min(steps, 500)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        with torch.cuda.stream(stream):
+            r.x.copy_(r.x_pinned, non_blocking=True)
+            do_step(i)
+            host_y.copy_(r.y[last], non_blocking=True)
+        stream.synchronize()
+    e2e_s = max_over_ranks(pg, time.perf_counter() - t0, dev)
+    e2e = {"value": world * wbytes * e2e_steps / e2e_s / 1e9, "unit": UNIT,
+           "h2d_bytes_per_step": r.x.numel() * 4, "d2h_bytes_per_step": host_y.numel() * 4,
+           "steps": e2e_steps, "how": "wall clock; per step: pinned H2D of x, graph replay of the "
+                                      "C-ABI calls, D2H of the last product's output, stream sync"}
+    assert M.mlq_last_device_error(stream) == M.MLQ_OK
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        threads = host_cores()
+        op, n, el = time_oracle(wl, args.cpu_seconds, threads)
+        cpu = {"value": op.weight_bytes * n / el / 1e9, "unit": UNIT, "cores": threads,
+               "kind": "oracle",
+               "sample": f"{n} passes of {wl.name} in {el:.1f} s, product rows split over "
+                         f"{threads} threads"}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+            "warmup": warm, "ms_per_step": ms_max / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "q4_k products: u4 x s8 dot -> int32, sub-block scales folded in int32, "
+                     "f32 per super-block",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "M": 1,
+                       "matrices": [f"{n}:{rw}x{c}:q4_k" for n, rw, c, _ in wl.mats],
+                       "weight_bytes_per_step": wbytes,
+                       "l2": f"inputs larger than L2: {copies} rotating weight copies "
+                             f"({copies * wbytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
+                       "graphs": ("one graph per cycle of %d steps" % copies) if cycle is not None else False,
+                       "path": "calls", "parallelism": f"replicas x{world} (independent decode streams)"},
+            "gops": world * r.ops() * steps / (ms_max / 1e3) / 1e9, "hbm_frac": value / world / hbm,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": r.launches_per_step * steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     from block_quantized_decode_gb300 import inputs as I
-    if args.workload not in I.WORKLOADS and args.workload not in I.LAYERS:
-        raise SystemExit(f"unknown workload {args.workload}; choose from "
-                         f"{sorted(I.WORKLOADS) + sorted(I.LAYERS)}")
-    wl = (I.LAYERS[args.workload] if args.workload in I.LAYERS else I.WORKLOADS[args.workload])()
+    known = {**I.WORKLOADS, **I.LAYERS, **I.Q4K_WORKLOADS}
+    if args.workload not in known:
+        raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(known)}")
+    wl = known[args.workload]()
     world, rank, local, pg = dist_setup(args)
     try:
         if args.impl == "reference":
             return run_reference(args, wl, world, rank)
         if isinstance(wl, I.LayerShape):
             return run_layer(args, wl, world, rank, local, pg)
+        if isinstance(wl, I.Q4KWorkload):
+            return run_q4k(args, wl, world, rank, local, pg)
         return run_ours(args, wl, world, rank, local, pg)
     finally:
         if pg is not None:

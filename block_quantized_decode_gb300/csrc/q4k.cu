@@ -19,15 +19,22 @@
 //   y[r] += ((float)ISUM * d - (float)MSUM * dmin) * dx_B.
 // (Even 8-bit scales and minima stay inside int32: 8*255*32*127*15 < 2^31.)
 //
-// The product streams weights like the other M = 1 kernels: one CTA per SM
-// (at most), a producer warp filling a ring of shared-memory stages of R
+// The product streams weights like the other M = 1 kernels: a CTA per SM
+// (two fit on an SM, so that under programmatic dependent launch the next
+// product's CTA streams its weights while this one finishes; with static
+// weights its producer starts before the dependency wait), a producer warp
+// filling a ring of shared-memory stages of R
 // rows -- the nibbles and the scale/minimum bytes by bulk copies (their row
 // strides are multiples of 16 bytes), d and dmin by 4-byte asynchronous
 // copies (their row stride need not be), all completing on the stage's
-// full barrier -- and 8 consumer warps.  A warp takes one row at a time:
-// lane l works on sub-block l (+32, +64, ...), 8 lanes per super-block; the
+// full barrier -- and 16 consumer warps.  A stage's rows go to the warps
+// whole, or, when a stage holds fewer rows than warps, each row is split in
+// P parts over its columns of 64 sub-blocks (part p takes columns p, p + P,
+// ...; the parts' float sums are added in part order at the end).  Within
+// a part, lane l works on sub-block l (+32, ...), 8 lanes per super-block; the
 // lane's scaled integer dot and minimum term are added across its 8 lanes
-// with integer shuffles, and the group's first lane does the float
+// with integer shuffles (two sub-block columns at a time, so that two
+// shuffle chains overlap), and the group's first lane does the float
 // arithmetic of the super-block.
 #include "mlq_device.cuh"
 #include "mlq_launch.h"
@@ -36,10 +43,12 @@ namespace mlq {
 
 constexpr int kQKK = 256;
 constexpr int kKSubs = kQKK / kQK;                 // sub-blocks per super-block
-constexpr int kKWarps = 8;                         // consumer warps
+constexpr int kKWarps = 16;                        // consumer warps (17 warps: at most 96 registers)
 constexpr int kKThreads = (kKWarps + 1) * 32;      // + the producer warp
 constexpr int kKSlots = 8;
-constexpr size_t kKBudget = 220 * 1024;
+constexpr size_t kKBudget = 110 * 1024;        // two CTAs per SM: the next launch's CTA can stream
+                                                // its weights while this one finishes
+constexpr size_t kKBudgetWide = 220 * 1024;    // one CTA per SM (very long rows)
 constexpr size_t kKStageTarget = 32 * 1024;
 
 // ---- quantiser ------------------------------------------------------------
@@ -101,6 +110,9 @@ struct Q4KArgs {
   int32_t *isum, *msum;  // test hook: per-super-block integer sums instead of y
   int nsb, r0, r1;
   int R, ns;                                    // rows per stage, ring slots
+  int P;                                        // parts per row (P > 1: partial sums in smem_part)
+  int early;                                    // weights not written by earlier work
+  unsigned smem_part;
   unsigned stage_bytes, stage_s, stage_d;       // stage size; offsets of s and of d, dmin
   unsigned smem_ring;
   int *status;
@@ -131,7 +143,7 @@ __device__ __forceinline__ bool k_wait(uint32_t bar, uint32_t parity, const vola
 }
 
 template <bool SUMS>
-__global__ void __launch_bounds__(kKThreads, 1) matvec_q4k_kernel(const __grid_constant__ Q4KArgs a) {
+__global__ void __launch_bounds__(kKThreads, 2) matvec_q4k_kernel(const __grid_constant__ Q4KArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kKSlots];
   __shared__ __align__(8) uint64_t empty_bar[kKSlots];
@@ -148,6 +160,8 @@ __global__ void __launch_bounds__(kKThreads, 1) matvec_q4k_kernel(const __grid_c
   int32_t *xbs_s = reinterpret_cast<int32_t *>(smem + K);
   float *xd_s = reinterpret_cast<float *>(smem + K + 4 * nsub);
   uint8_t *ring = smem + a.smem_ring;
+  float *part_s = reinterpret_cast<float *>(smem + a.smem_part);
+  const int P = a.P;
 
   if (tid == 0) {
     for (int k = 0; k < ns; ++k) {
@@ -159,10 +173,10 @@ __global__ void __launch_bounds__(kKThreads, 1) matvec_q4k_kernel(const __grid_c
   }
   __syncthreads();
   griddep_launch_dependents();
-  griddep_wait();  // x (and, conservatively, the weights) may come from earlier work
 
   if (warp == kKWarps) {
     // ------------------------------ producer ------------------------------
+    if (!a.early) griddep_wait();  // weights written by earlier work: wait for it first
     int s = 0;
     for (int r = ra; r < rb; r += R, ++s) {
       const int n = min(R, rb - r);
@@ -198,6 +212,7 @@ __global__ void __launch_bounds__(kKThreads, 1) matvec_q4k_kernel(const __grid_c
   }
 
   // ------------------------------ consumers ------------------------------
+  griddep_wait();  // x may come from the previous kernel
   if (rb <= ra) return;
   {  // the activation vector into shared memory, all loads before any store
     const int uq = K / 16, ub = nsub / 4;
@@ -226,65 +241,88 @@ __global__ void __launch_bounds__(kKThreads, 1) matvec_q4k_kernel(const __grid_c
     const int slot = s % ns;
     if (!warp_wait([&] { return k_wait(smem_addr(&full_bar[slot]), (s / ns) & 1, abort_v, a.wait_ns); })) {
       if (lane == 0 && atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
-      return;
+      break;  // every consumer warp still reaches the final sync
     }
     const uint8_t *stq = ring + static_cast<size_t>(slot) * a.stage_bytes;
     const uint8_t *sts = stq + a.stage_s;
     const float *std_ = reinterpret_cast<const float *>(stq + a.stage_d);
     const float *stm = std_ + static_cast<size_t>(R) * nsb;
-    for (int i = warp; i < n; i += kKWarps) {
+    for (int task = warp; task < n * P; task += kKWarps) {
+      const int i = task % n, part = task / n;
       const uint8_t *wrow = stq + static_cast<size_t>(i) * rowq;
       const uint8_t *srow = sts + static_cast<size_t>(i) * rows_s;
       float acc = 0.0f;
-      for (int u0 = 0; u0 < nsub; u0 += 32) {
-        const int u = u0 + lane;
-        const bool valid = u < nsub;  // whole groups of 8 lanes (nsub is a multiple of 8)
-        int is = 0, ms = 0;
-        if (valid) {
-          const uint4 w = *reinterpret_cast<const uint4 *>(wrow + static_cast<size_t>(u) * 16);
-          const int4 xa = *reinterpret_cast<const int4 *>(xq_s + static_cast<size_t>(u) * kQK);
-          const int4 xb = *reinterpret_cast<const int4 *>(xq_s + static_cast<size_t>(u) * kQK + 16);
-          const int B = u >> 3, j = u & 7;
-          constexpr uint32_t kLo = 0x0F0F0F0Fu;
-          int dot = 0;
-          asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"(w.x & kLo), "r"(xa.x));
-          asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"(w.y & kLo), "r"(xa.y));
-          asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"(w.z & kLo), "r"(xa.z));
-          asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"(w.w & kLo), "r"(xa.w));
-          asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"((w.x >> 4) & kLo), "r"(xb.x));
-          asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"((w.y >> 4) & kLo), "r"(xb.y));
-          asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"((w.z >> 4) & kLo), "r"(xb.z));
-          asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"((w.w >> 4) & kLo), "r"(xb.w));
-          is = static_cast<int>(srow[B * 16 + j]) * dot;
-          ms = static_cast<int>(srow[B * 16 + 8 + j]) * xbs_s[u];
+      for (int u0 = 64 * part; u0 < nsub; u0 += 64 * P) {
+        int is[2], ms[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int u = u0 + 32 * h + lane;
+          is[h] = 0;
+          ms[h] = 0;
+          if (u < nsub) {  // whole groups of 8 lanes (nsub is a multiple of 8)
+            const uint4 w = *reinterpret_cast<const uint4 *>(wrow + static_cast<size_t>(u) * 16);
+            const int4 xa = *reinterpret_cast<const int4 *>(xq_s + static_cast<size_t>(u) * kQK);
+            const int4 xb = *reinterpret_cast<const int4 *>(xq_s + static_cast<size_t>(u) * kQK + 16);
+            const int B = u >> 3, j = u & 7;
+            constexpr uint32_t kLo = 0x0F0F0F0Fu;
+            int dot = 0;
+            asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"(w.x & kLo), "r"(xa.x));
+            asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"(w.y & kLo), "r"(xa.y));
+            asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"(w.z & kLo), "r"(xa.z));
+            asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"(w.w & kLo), "r"(xa.w));
+            asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"((w.x >> 4) & kLo), "r"(xb.x));
+            asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"((w.y >> 4) & kLo), "r"(xb.y));
+            asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"((w.z >> 4) & kLo), "r"(xb.z));
+            asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(dot) : "r"((w.w >> 4) & kLo), "r"(xb.w));
+            is[h] = static_cast<int>(srow[B * 16 + j]) * dot;
+            ms[h] = static_cast<int>(srow[B * 16 + 8 + j]) * xbs_s[u];
+          }
         }
-        // the super-block's 8 sub-blocks: integer sums, exact
-        is += __shfl_xor_sync(0xffffffffu, is, 1);
-        ms += __shfl_xor_sync(0xffffffffu, ms, 1);
-        is += __shfl_xor_sync(0xffffffffu, is, 2);
-        ms += __shfl_xor_sync(0xffffffffu, ms, 2);
-        is += __shfl_xor_sync(0xffffffffu, is, 4);
-        ms += __shfl_xor_sync(0xffffffffu, ms, 4);
-        if (valid && (lane & 7) == 0) {
-          const int B = u >> 3;
-          if (SUMS) {
-            a.isum[static_cast<size_t>(r + i - a.r0) * nsb + B] = is;
-            a.msum[static_cast<size_t>(r + i - a.r0) * nsb + B] = ms;
-          } else {
-            const float t = __fmul_rn(__int2float_rn(is), std_[static_cast<size_t>(i) * nsb + B]);
-            const float um = __fmul_rn(__int2float_rn(ms), stm[static_cast<size_t>(i) * nsb + B]);
-            acc = __fadd_rn(acc, __fmul_rn(__fsub_rn(t, um), xd_s[B]));
+        // each super-block's 8 sub-blocks: integer sums, exact
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            is[h] += __shfl_xor_sync(0xffffffffu, is[h], o);
+            ms[h] += __shfl_xor_sync(0xffffffffu, ms[h], o);
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int u = u0 + 32 * h + lane;
+          if (u < nsub && (lane & 7) == 0) {
+            const int B = u >> 3;
+            if (SUMS) {
+              a.isum[static_cast<size_t>(r + i - a.r0) * nsb + B] = is[h];
+              a.msum[static_cast<size_t>(r + i - a.r0) * nsb + B] = ms[h];
+            } else {
+              const float t = __fmul_rn(__int2float_rn(is[h]), std_[static_cast<size_t>(i) * nsb + B]);
+              const float um = __fmul_rn(__int2float_rn(ms[h]), stm[static_cast<size_t>(i) * nsb + B]);
+              acc = __fadd_rn(acc, __fmul_rn(__fsub_rn(t, um), xd_s[B]));
+            }
           }
         }
       }
       if (!SUMS) {
         acc += __shfl_xor_sync(0xffffffffu, acc, 8);
         acc += __shfl_xor_sync(0xffffffffu, acc, 16);
-        if (lane == 0) a.y[r + i] = acc;
+        if (lane == 0) {
+          if (P == 1) a.y[r + i] = acc;
+          else part_s[static_cast<size_t>(r + i - ra) * P + part] = acc;
+        }
       }
     }
     __syncwarp();
     if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&empty_bar[slot])) : "memory");
+  }
+  if (!SUMS && P > 1) {  // the parts of each row, added in part order
+    k_consumers_sync();
+    if (*abort_v) return;
+    for (int i = tid; i < rb - ra; i += kKWarps * 32) {
+      float v = part_s[static_cast<size_t>(i) * P];
+      for (int p = 1; p < P; ++p) v = __fadd_rn(v, part_s[static_cast<size_t>(i) * P + p]);
+      a.y[ra + i] = v;
+    }
   }
 }
 
@@ -305,11 +343,22 @@ cudaError_t launch_matvec_q4k(const LaunchCtx &ctx, const void *wq, const void *
   if (grid > (n + R - 1) / R) grid = (n + R - 1) / R;
   const int rows_cta = (n + grid - 1) / grid;
   if (R > rows_cta) R = rows_cta;
+  // parts per row: enough that every warp has work when a stage holds few rows
+  const int cols64 = (nsb * kKSubs + 63) / 64;
+  int P = R >= kKWarps ? 1 : kKWarps / R;
+  if (P > cols64) P = cols64;
+  if (P < 1) P = 1;
+  size_t part = isum != nullptr || P == 1 ? 0 : up(static_cast<size_t>(rows_cta) * P * 4, 128);
+  if (part > 32 * 1024) {  // very many rows per CTA: whole rows per warp
+    P = 1;
+    part = 0;
+  }
   const size_t stage_s = R * rowq;                       // multiple of 128
   const size_t stage_d = stage_s + R * rows_s;           // multiple of 16
   const size_t stage = up(stage_d + 8 * static_cast<size_t>(R) * nsb, 128);
-  if (xs + 2 * stage > kKBudget) return cudaErrorNotSupported;
-  int ns = static_cast<int>((kKBudget - xs) / stage);
+  const size_t budget = xs + part + 2 * stage <= kKBudget ? kKBudget : kKBudgetWide;
+  if (xs + part + 2 * stage > budget) return cudaErrorNotSupported;
+  int ns = static_cast<int>((budget - xs - part) / stage);
   if (ns > kKSlots) ns = kKSlots;
   const int stages_cta = (rows_cta + R - 1) / R;
   if (ns > stages_cta) ns = stages_cta < 2 ? 2 : stages_cta;
@@ -332,10 +381,13 @@ cudaError_t launch_matvec_q4k(const LaunchCtx &ctx, const void *wq, const void *
   a.stage_bytes = static_cast<unsigned>(stage);
   a.stage_s = static_cast<unsigned>(stage_s);
   a.stage_d = static_cast<unsigned>(stage_d);
-  a.smem_ring = static_cast<unsigned>(xs);
+  a.P = P;
+  a.early = ctx.early_weights ? 1 : 0;
+  a.smem_part = static_cast<unsigned>(xs);
+  a.smem_ring = static_cast<unsigned>(xs + part);
   a.status = ctx.status;
   a.wait_ns = ctx.wait_ns;
-  const size_t smem = xs + static_cast<size_t>(ns) * stage;
+  const size_t smem = xs + part + static_cast<size_t>(ns) * stage;
   auto kern = isum != nullptr ? matvec_q4k_kernel<true> : matvec_q4k_kernel<false>;
   prefer_max_shared(kern);
   const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

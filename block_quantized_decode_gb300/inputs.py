@@ -214,3 +214,29 @@ def tinyllama_decode_layer(pos: int = 255) -> LayerShape:
 LAYERS = {
     "tinyllama_decode_layer": tinyllama_decode_layer,
 }
+
+
+# ---- Q4_K-style super-block workloads ---------------------------------------
+@dataclass
+class Q4KWorkload:
+    """M = 1 products on Q4_K-style weights.  mats: (name, rows, cols,
+    input) with input "x" (the workload's float input) or the name of an
+    earlier product whose output is the input; every input is quantised per
+    256 before the first product that reads it."""
+    name: str
+    mats: list
+    seed: int = 0
+
+
+def tinyllama_layer_q4k() -> Q4KWorkload:
+    """The projections of one TinyLlama-1.1B layer in Q4_K (the model the
+    page runs as Q4_K_M): Wq 2048x2048, Wk / Wv 256x2048, Wo 2048x2048,
+    gate / up 5632x2048, down 2048x5632."""
+    d, kv, ff = 2048, 256, 5632
+    return Q4KWorkload("tinyllama1.1b_layer_q4k", [
+        ("wq", d, d, "x"), ("wk", kv, d, "x"), ("wv", kv, d, "x"),
+        ("wo", d, d, "wq"), ("w_gate", ff, d, "wo"), ("w_up", ff, d, "wo"),
+        ("w_down", d, ff, "w_gate")])
+
+
+Q4K_WORKLOADS = {"tinyllama_layer_q4k": tinyllama_layer_q4k}

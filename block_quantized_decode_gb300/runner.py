@@ -267,3 +267,56 @@ class _null:
 
     def __exit__(self, *a):
         return False
+
+
+class Q4KRunner:
+    """Device buffers and one pass of a Q4KWorkload through the C ABI: per
+    input, mlq_quantize_q8k, then every mlq_matvec_q4k that reads it."""
+
+    def __init__(self, wl: I.Q4KWorkload, copies: int = 1, device: str = "cuda:0"):
+        self.wl = wl
+        self.copies = copies
+        self.dev = torch.device(device)
+        self.host = {}
+        self.W = [dict() for _ in range(copies)]
+        self.y = {}
+        self.src = {}
+        for i, (name, rows, cols, inp) in enumerate(wl.mats):
+            q, s, d, dmin = I.q4k_weights(rows, cols, seed=wl.seed + i)
+            self.host[name] = (q, s, d, dmin, rows, cols)
+            for c in range(copies):
+                self.W[c][name] = B.Q4KTensor(*(torch.from_numpy(t).to(self.dev) for t in (q, s, d, dmin)),
+                                              rows, cols)
+            self.y[name] = torch.zeros(rows, dtype=torch.float32, device=self.dev)
+            self.src.setdefault(inp, cols)
+        x_cols = self.src["x"]
+        self.x_host = I.activations(1, x_cols, seed=wl.seed + 1000)[0]
+        self.x = torch.from_numpy(self.x_host).to(self.dev)
+        self.x_pinned = torch.from_numpy(self.x_host).pin_memory()
+        self.act = {}
+        for name, k in self.src.items():
+            self.act[name] = B.Q8KAct(torch.empty(k, dtype=torch.int8, device=self.dev),
+                                      torch.empty(k // I.QKK, dtype=torch.float32, device=self.dev),
+                                      torch.empty(k // I.QK, dtype=torch.int32, device=self.dev), k)
+        self.launches_per_step = len(self.src) + len(wl.mats)
+
+    def vec(self, name):
+        return self.x if name == "x" else self.y[name]
+
+    def step(self, copy: int = 0, stream=None) -> None:
+        done = set()
+        for name, rows, cols, inp in self.wl.mats:
+            if inp not in done:
+                B.mlq_quantize_q8k(self.act[inp], self.vec(inp), cols, stream)
+                done.add(inp)
+            B.mlq_matvec_q4k(self.y[name], self.W[copy][name], self.act[inp], 0, rows, stream)
+
+    def product(self, name: str, copy: int = 0, stream=None) -> None:
+        rows, inp = self.host[name][4], [m[3] for m in self.wl.mats if m[0] == name][0]
+        B.mlq_matvec_q4k(self.y[name], self.W[copy][name], self.act[inp], 0, rows, stream)
+
+    def weight_bytes(self) -> int:
+        return sum(q.nbytes + s.nbytes + d.nbytes + dm.nbytes for q, s, d, dm, _, _ in self.host.values())
+
+    def ops(self) -> int:
+        return sum(2 * rows * cols for _, rows, cols, _ in self.wl.mats)

@@ -181,3 +181,29 @@ def test_q4k_tinyllama_layer_shapes_sampled(M):
                  om[r0:r0 + 8].astype(np.float32) * dmin[r0:r0 + 8]) * xd[None, :]
             bound = REL * np.abs(t.astype(np.float64)).sum(axis=1)
             assert np.all(np.abs(yg[r0:r0 + 8] - yo[r0:r0 + 8]) <= bound)
+
+
+def test_q4k_layer_pass_through_runner(M):
+    """The bench's Q4_K pass (per input mlq_quantize_q8k, then its products,
+    outputs feeding later inputs): every quantised input bit-exact against
+    the oracle's quantisation of the GPU's float vector, every product's
+    y within the bound on the GPU's own quantised input."""
+    from block_quantized_decode_gb300.runner import Q4KRunner
+    wl = I.tinyllama_layer_q4k()
+    r = Q4KRunner(wl, copies=1)
+    r.step()
+    torch.cuda.synchronize()
+    for name, rows, cols, inp in wl.mats:
+        xv = r.vec(inp).cpu().numpy()
+        oq, od, obs = oracle.quantize_q8k(xv)
+        act = r.act[inp]
+        assert np.array_equal(act.q.cpu().numpy(), oq), f"{name}: quantised input differs"
+        assert np.array_equal(act.d.cpu().numpy().view(np.uint32), od.view(np.uint32))
+        assert np.array_equal(act.bsums.cpu().numpy(), obs)
+        q, s, d, dmin, _, _ = r.host[name]
+        yo = oracle.matvec_q4k(q, s, d, dmin, rows, cols, oq, od, obs)
+        oi, om = oracle.block_sums_q4k(q, s, rows, cols, oq, obs)
+        t = (oi.astype(np.float32) * d - om.astype(np.float32) * dmin) * od[None, :]
+        bound = REL * np.abs(t.astype(np.float64)).sum(axis=1)
+        yg = r.y[name].cpu().numpy()
+        assert np.all(np.abs(yg.astype(np.float64) - yo) <= bound), name
