@@ -77,10 +77,16 @@ class Oracle:
         L.mlqo_quantize_q8k.argtypes = [P, P, P, P, I, I]
         L.mlqo_block_sums_q4k.argtypes = [P, P, P, P, I, I, P, P, I, I]
         L.mlqo_matvec_q4k.argtypes = [P, P, P, P, P, I, I, P, P, P, I, I]
+        L.mlqo_half_to_float.argtypes = [ctypes.c_uint16]
+        L.mlqo_half_to_float.restype = ctypes.c_float
+        L.mlqo_quantize_blk.argtypes = [P, P, P, P, I, I]
+        L.mlqo_block_sumi_nbits.argtypes = [P, P, P, I, I, I, I, P, I, I]
+        L.mlqo_matvec_nbits.argtypes = [P, P, P, I, P, I, I, I, I, P, P, I, I]
         for f in (L.mlqo_quantize_q8, L.mlqo_block_sumi, L.mlqo_matvec, L.mlqo_gemm_small_m,
                   L.mlqo_rmsnorm, L.mlqo_softmax, L.mlqo_silu_mul, L.mlqo_add, L.mlqo_rope_tables,
                   L.mlqo_rope, L.mlqo_attention, L.mlqo_quantize_q8k, L.mlqo_block_sums_q4k,
-                  L.mlqo_matvec_q4k):
+                  L.mlqo_matvec_q4k, L.mlqo_quantize_blk, L.mlqo_block_sumi_nbits,
+                  L.mlqo_matvec_nbits):
             f.restype = ctypes.c_int
         self.lib = L
         self.path = path
@@ -183,6 +189,49 @@ class _Q4KOps:
         return y
 
 
+class _NBitsOps:
+    """Block length 32 / 128, float32 / binary16 scales, 8-bit weights in
+    the packed signed form with per-block zero points (page "ONNX Runtime",
+    "How we got there", items 3-5); the layout is the one stated in
+    mlq_oracle.c."""
+
+    def half_to_float(self, bits: int) -> float:
+        return float(self.lib.mlqo_half_to_float(int(bits) & 0xFFFF))
+
+    def quantize_blk(self, x: np.ndarray, blk: int):
+        """x float32 [k] -> (q int8 [k], d float32 [k/blk], bsums int32 [k/blk])."""
+        x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+        k = x.size
+        q = np.empty(k, dtype=np.int8)
+        d = np.empty(k // blk, dtype=np.float32)
+        bs = np.empty(k // blk, dtype=np.int32)
+        _ok(self.lib.mlqo_quantize_blk(_ptr(q), _ptr(d), _ptr(bs), _ptr(x), k, blk), "quantize_blk")
+        return q, d, bs
+
+    def block_sumi_nbits(self, wq, zp, rows: int, cols: int, bits: int, blk: int, xq, r0: int = 0,
+                         r1: int | None = None) -> np.ndarray:
+        r1 = rows if r1 is None else r1
+        out = np.zeros((max(r1 - r0, 0), cols // blk), dtype=np.int32)
+        zptr = None if zp is None else _ptr(_u8(zp))
+        _ok(self.lib.mlqo_block_sumi_nbits(_ptr(out), _ptr(_u8(wq.view(np.uint8))), zptr, rows, cols,
+                                           bits, blk, _ptr(_i8(xq)), r0, r1), "block_sumi_nbits")
+        return out
+
+    def matvec_nbits(self, wq, scales, zp, rows: int, cols: int, bits: int, blk: int, xq, xd,
+                     r0: int = 0, r1: int | None = None, y: np.ndarray | None = None) -> np.ndarray:
+        """scales: float32, or float16 (passed as their binary16 bit patterns)."""
+        r1 = rows if r1 is None else r1
+        if y is None:
+            y = np.zeros(rows, dtype=np.float32)
+        f16 = scales.dtype == np.float16
+        sc = np.ascontiguousarray(scales.view(np.uint16) if f16 else _f32(scales))
+        zptr = None if zp is None else _ptr(_u8(zp))
+        _ok(self.lib.mlqo_matvec_nbits(_ptr(y), _ptr(_u8(wq.view(np.uint8))), _ptr(sc), 1 if f16 else 0,
+                                       zptr, rows, cols, bits, blk, _ptr(_i8(xq)), _ptr(_f32(xd)),
+                                       r0, r1), "matvec_nbits")
+        return y
+
+
 def _u8(a) -> np.ndarray:
     return np.ascontiguousarray(a, dtype=np.uint8)
 
@@ -252,6 +301,8 @@ for _name in ("rmsnorm", "softmax", "silu_mul", "add", "rope_tables", "rope", "a
     setattr(Oracle, _name, getattr(_LayerOps, _name))
 for _name in ("quantize_q8k", "block_sums_q4k", "matvec_q4k"):
     setattr(Oracle, _name, getattr(_Q4KOps, _name))
+for _name in ("half_to_float", "quantize_blk", "block_sumi_nbits", "matvec_nbits"):
+    setattr(Oracle, _name, getattr(_NBitsOps, _name))
 
 
 def default() -> Oracle:
@@ -315,3 +366,15 @@ def block_sums_q4k(*a, **k):
 
 def matvec_q4k(*a, **k):
     return default().matvec_q4k(*a, **k)
+
+
+def quantize_blk(*a, **k):
+    return default().quantize_blk(*a, **k)
+
+
+def block_sumi_nbits(*a, **k):
+    return default().block_sumi_nbits(*a, **k)
+
+
+def matvec_nbits(*a, **k):
+    return default().matvec_nbits(*a, **k)

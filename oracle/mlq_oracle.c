@@ -417,3 +417,117 @@ int mlqo_matvec_q4k(float *y, const uint8_t *wq, const uint8_t *ws, const float 
     }
     return 0;
 }
+
+/* ========================================================================
+ * Block length 128 or 32, float32 or binary16 scales, 8-bit weights with a
+ * zero point in the packed signed form.
+ *
+ * Source: the page "ONNX Runtime" (SpaceMiT X60), "How we got there":
+ * item 3 (AMD's Qwen2.5-0.5B export uses block_size = 128; a BlkLen = 128
+ * CompInt8 path with int8 activations), item 4 (8-bit weights packed as
+ * signed B' = B - 128 with flat scales, and a per-block correction
+ * -scale * (zp - 128) that vanishes when the zero point is 128 or absent),
+ * item 5 (panels with float16 scales).  What the method computes is the
+ * plain product of the dequantised blocks: per block b of row r,
+ *   sumi = sum_i w_i * a_i,  w_i = n_i - 8 (4-bit, symmetric)  or
+ *                            w_i = B_i - zp_b = B'_i + 128 - zp_b (8-bit),
+ *   y[r] += ((float)sumi * scale_b) * dx_b   in float32, blocks in order.
+ * The signed-offset correction reaches the same int32 sumi exactly:
+ * sum (B' + 128 - zp) a = sum B' a + (128 - zp) sum a; the oracle forms
+ * sumi from w_i directly.  Readings where the page is silent (listed in
+ * the design doc):
+ *   - 4-bit blocks of `blk` elements pack element j in the low nibble and
+ *     element j + blk/2 in the high nibble of byte j (the Q4_0 order, which
+ *     it equals for blk = 32); 4-bit weights have no zero points;
+ *   - 8-bit weights are stored as B' (int8) with one uint8 zero point per
+ *     block (NULL: 128 for every block);
+ *   - scales are one per block, float32 or IEEE 754 binary16 (converted to
+ *     float32 exactly, below, from the binary16 definition);
+ *   - activations are quantised per `blk` elements with the Q8_0 rule (one
+ *     float32 scale per block), plus the int32 sum of each block's quants.
+ * ====================================================================== */
+
+/* IEEE 754 binary16 -> float (every binary16 value is a float32 value):
+ * sign bit 15, exponent bits 14..10 (bias 15), fraction bits 9..0;
+ * exponent 0: subnormal (fraction * 2^-24); exponent 31: inf or NaN. */
+float mlqo_half_to_float(uint16_t h)
+{
+    const int sign = (h >> 15) & 1;
+    const int e = (h >> 10) & 0x1F;
+    const int f = h & 0x3FF;
+    float v;
+    if (e == 0)       v = ldexpf((float)f, -24);
+    else if (e == 31) v = f ? NAN : INFINITY;
+    else              v = ldexpf((float)(f + 1024), e - 25);
+    return sign ? -v : v;
+}
+
+int mlqo_quantize_blk(int8_t *q, float *d, int32_t *bsums, const float *x, int k, int blk)
+{
+    if (blk <= 0 || k <= 0 || k % blk != 0) return -1;
+    for (int b = 0; b < k / blk; ++b) {
+        quantize_span(q + (size_t)b * blk, d + b, x + (size_t)b * blk, blk);
+        int32_t t = 0;
+        for (int i = 0; i < blk; ++i) t += q[(size_t)b * blk + i];
+        bsums[b] = t;
+    }
+    return 0;
+}
+
+/* Weight element i of block b of row r (n - 8, or B' + 128 - zp). */
+static int32_t nbits_weight(const uint8_t *wq, const uint8_t *zp, int bits, int blk, int cols,
+                            int r, int b, int i)
+{
+    const size_t nb = (size_t)(cols / blk);
+    if (bits == 4) {
+        const uint8_t *blkb = wq + ((size_t)r * nb + b) * (blk / 2);
+        const int n = i < blk / 2 ? (blkb[i] & 0x0F) : (blkb[i - blk / 2] >> 4);
+        return n - 8;
+    }
+    const int8_t bp = (int8_t)wq[((size_t)r * nb + b) * blk + i];
+    const int z = zp ? zp[(size_t)r * nb + b] : 128;
+    return (int32_t)bp + 128 - z;
+}
+
+int mlqo_block_sumi_nbits(int32_t *sumi, const uint8_t *wq, const uint8_t *zp, int rows, int cols,
+                          int bits, int blk, const int8_t *xq, int r0, int r1)
+{
+    if ((bits != 4 && bits != 8) || (blk != 32 && blk != 128) || cols <= 0 || cols % blk != 0) return -1;
+    if (bits == 4 && zp != NULL) return -1;
+    if (r0 < 0 || r1 > rows || r0 > r1) return -1;
+    const int nb = cols / blk;
+    for (int r = r0; r < r1; ++r)
+        for (int b = 0; b < nb; ++b) {
+            int32_t s = 0;
+            for (int i = 0; i < blk; ++i)
+                s += nbits_weight(wq, zp, bits, blk, cols, r, b, i) * (int32_t)xq[(size_t)b * blk + i];
+            sumi[(size_t)(r - r0) * nb + b] = s;
+        }
+    return 0;
+}
+
+/* scales: float32 (scale_f16 = 0) or binary16 bit patterns (scale_f16 = 1). */
+int mlqo_matvec_nbits(float *y, const uint8_t *wq, const void *scales, int scale_f16,
+                      const uint8_t *zp, int rows, int cols, int bits, int blk, const int8_t *xq,
+                      const float *xd, int r0, int r1)
+{
+    if ((bits != 4 && bits != 8) || (blk != 32 && blk != 128) || cols <= 0 || cols % blk != 0) return -1;
+    if (bits == 4 && zp != NULL) return -1;
+    if (r0 < 0 || r1 > rows || r0 > r1) return -1;
+    const int nb = cols / blk;
+    for (int r = r0; r < r1; ++r) {
+        float acc = 0.0f;
+        for (int b = 0; b < nb; ++b) {
+            int32_t s = 0;
+            for (int i = 0; i < blk; ++i)
+                s += nbits_weight(wq, zp, bits, blk, cols, r, b, i) * (int32_t)xq[(size_t)b * blk + i];
+            const size_t si = (size_t)r * nb + b;
+            const float sc = scale_f16 ? mlqo_half_to_float(((const uint16_t *)scales)[si])
+                                       : ((const float *)scales)[si];
+            const float t = (float)s * sc;
+            acc = acc + t * xd[b];
+        }
+        y[r] = acc;
+    }
+    return 0;
+}

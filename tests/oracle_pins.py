@@ -546,6 +546,130 @@ def pin_q4k_row_range(O, seed=24):
     assert np.array_equal(y[2:5], full[2:5]) and np.all(y[[0, 1, 5]] == 7.0)
 
 
+# ----------------------------------------------------------------------------
+# block length 32 / 128, float32 / binary16 scales, 8-bit weights in the
+# packed signed form B' = B - 128 with per-block zero points (page "ONNX
+# Runtime", "How we got there", items 3-5)
+# ----------------------------------------------------------------------------
+def nbits_elements(wq, zp, rows, cols, bits, blk) -> np.ndarray:
+    """Weight values w = n - 8 (4-bit: element j of a block in the low
+    nibble of byte j, element j + blk/2 in its high nibble) or B' + 128 - zp
+    (8-bit), [rows, cols] int64, written from the stated format."""
+    nb = cols // blk
+    if bits == 4:
+        qb = wq.reshape(rows, nb, blk // 2).astype(np.int64)
+        w = np.concatenate([qb & 0xF, qb >> 4], axis=2) - 8
+        return w.reshape(rows, cols)
+    bp = wq.view(np.int8).reshape(rows, nb, blk).astype(np.int64)
+    z = np.full((rows, nb), 128, np.int64) if zp is None else zp.reshape(rows, nb).astype(np.int64)
+    return (bp + 128 - z[:, :, None]).reshape(rows, cols)
+
+
+def random_nbits(rng, rows, cols, bits, blk, f16, with_zp):
+    nb = cols // blk
+    if bits == 4:
+        wq = rng.integers(0, 256, size=(rows, cols // 2), dtype=np.uint8)
+    else:
+        wq = rng.integers(-128, 128, size=(rows, cols), dtype=np.int8)
+    sc = rng.uniform(1e-4, 1e-2, size=(rows, nb)).astype(np.float16 if f16 else np.float32)
+    zp = rng.integers(0, 256, size=(rows, nb), dtype=np.uint8) if (bits == 8 and with_zp) else None
+    return wq, sc, zp
+
+
+def pin_half_to_float_all_patterns(O):
+    """The binary16 decoder against numpy's float16 on every bit pattern."""
+    pats = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = pats.view(np.float16).astype(np.float32)
+    got = np.array([O.half_to_float(int(p)) for p in range(0, 1 << 16, 1)], dtype=np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def pin_nbits_reduces_to_q4_0_and_q8_0(O, seed=31):
+    """Block length 32 with float32 scales: the 4-bit product is the Q4_0
+    product (same nibble order), the 8-bit product with every zero point
+    128 (or none) is the Q8_0 product of B' (both pinned above)."""
+    rng = np.random.default_rng(seed)
+    rows, cols = 6, 128
+    xq = rng.integers(-127, 128, size=cols, dtype=np.int8)
+    xd = rng.uniform(1e-3, 1e-1, size=cols // QK).astype(np.float32)
+    wq4 = rng.integers(0, 256, size=(rows, cols // 2), dtype=np.uint8)
+    sc = rng.uniform(1e-3, 1e-2, size=(rows, cols // QK)).astype(np.float32)
+    assert np.array_equal(O.matvec_nbits(wq4, sc, None, rows, cols, 4, 32, xq, xd).view(np.uint32),
+                          O.matvec(Q4_0, wq4, sc, rows, cols, xq, xd).view(np.uint32))
+    wq8 = rng.integers(-128, 128, size=(rows, cols), dtype=np.int8)
+    wq8[wq8 == -128] = -127    # the Q8_0 range
+    ref = O.matvec(Q8_0, wq8, sc, rows, cols, xq, xd)
+    for zp in (None, np.full((rows, cols // 32), 128, np.uint8)):
+        y = O.matvec_nbits(wq8, sc, zp, rows, cols, 8, 32, xq, xd)
+        assert np.array_equal(y.view(np.uint32), ref.view(np.uint32))
+
+
+def pin_nbits_bruteforce_fp64(O, seed=32):
+    """Every combination of bits, block length, scale type and zero points:
+    block sums exact against int64 sums of the decoded elements, y within the
+    float32 summation bound of fp64 brute force over dequantised elements."""
+    rng = np.random.default_rng(seed)
+    for bits in (4, 8):
+        for blk in (32, 128):
+            for f16 in (False, True):
+                for with_zp in ((False, True) if bits == 8 else (False,)):
+                    rows, cols = int(rng.integers(1, 5)), blk * int(rng.integers(1, 4))
+                    nb = cols // blk
+                    wq, sc, zp = random_nbits(rng, rows, cols, bits, blk, f16, with_zp)
+                    x = rng.standard_normal(cols).astype(np.float32)
+                    xq, xd, xbs = O.quantize_blk(x, blk)
+                    y = O.matvec_nbits(wq, sc, zp, rows, cols, bits, blk, xq, xd)
+                    sumi = O.block_sumi_nbits(wq, zp, rows, cols, bits, blk, xq)
+                    w = nbits_elements(wq, zp, rows, cols, bits, blk)
+                    s32 = sc.astype(np.float64)
+                    for r in range(rows):
+                        exact, absterms = 0.0, 0.0
+                        for b in range(nb):
+                            e = slice(b * blk, (b + 1) * blk)
+                            s = int(np.dot(w[r, e], xq[e].astype(np.int64)))
+                            assert int(sumi[r, b]) == s, (bits, blk, f16, with_zp, r, b)
+                            exact += float(np.sum((w[r, e] * s32[r, b]) * (xq[e].astype(np.float64) * float(xd[b]))))
+                            absterms += abs(s * s32[r, b] * float(xd[b]))
+                        tol = (nb + 2) * U * (1 + 1e-6) * absterms + 1e-300
+                        assert abs(float(y[r]) - exact) <= tol, (bits, blk, f16, r, float(y[r]), exact)
+
+
+def pin_nbits_signed_offset_and_bound(O, seed=33):
+    """8-bit: the signed packing B' = B - 128 with zero point zp gives the
+    weight B - zp (checked on B = 0, 128, 255 against zp = 0, 128, 255);
+    the largest |sumi| a 128-block can reach, 255*127*128 = 4,145,280, is
+    attained exactly and fits int32; the block-128 quantiser matches the
+    Q8_0 one where each 32-element part holds the block's largest value."""
+    cols, blk = 128, 128
+    for B in (0, 128, 255):
+        for z in (0, 128, 255):
+            wq = np.full((1, cols), B - 128, np.int8)
+            xq = np.ones(cols, np.int8)
+            s = O.block_sumi_nbits(wq, np.array([[z]], np.uint8), 1, cols, 8, blk, xq)
+            assert int(s[0, 0]) == (B - z) * cols, (B, z, s)
+    wq = np.full((1, cols), 127, np.int8)          # B = 255
+    s = O.block_sumi_nbits(wq, np.array([[0]], np.uint8), 1, cols, 8, blk, np.full(cols, 127, np.int8))
+    assert int(s[0, 0]) == 255 * 127 * 128 == 4145280 < 2 ** 31
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal(4 * blk).astype(np.float32)
+    for b in range(4):
+        amax = np.float32(np.abs(x[b * blk:(b + 1) * blk]).max() * 1.25)
+        for part in range(4):
+            x[b * blk + part * 32 + int(rng.integers(0, 32))] = amax
+    q, d, bs = O.quantize_blk(x, blk)
+    q0, d0 = O.quantize_q8(x)
+    assert np.array_equal(q, q0) and np.array_equal(np.repeat(d, 4).view(np.uint32), d0.view(np.uint32))
+    assert np.array_equal(bs, q.astype(np.int64).reshape(4, blk).sum(axis=1))
+    xg = (rng.standard_normal(8 * blk) * 10.0 ** rng.uniform(-3, 3)).astype(np.float32)
+    q, d, _ = O.quantize_blk(xg, blk)
+    amax = np.abs(xg.reshape(-1, blk)).max(axis=1)
+    assert np.array_equal(d.view(np.uint32), (amax / np.float32(127)).astype(np.float32).view(np.uint32))
+    err = np.abs(xg.reshape(-1, blk).astype(np.float64) - q.reshape(-1, blk) * d.astype(np.float64)[:, None])
+    assert np.all(err <= d.astype(np.float64)[:, None] * (0.5 + 127 * 3 * U + 2.0 ** -18))
+
+
 ALL_PINS = [
     pin_rmsnorm_closed_form,
     pin_softmax_values,
@@ -565,4 +689,8 @@ ALL_PINS = [
     pin_q4k_special_cases,
     pin_q8k_quantizer,
     pin_q4k_row_range,
+    pin_half_to_float_all_patterns,
+    pin_nbits_reduces_to_q4_0_and_q8_0,
+    pin_nbits_bruteforce_fp64,
+    pin_nbits_signed_offset_and_bound,
 ]

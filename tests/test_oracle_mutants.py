@@ -52,6 +52,14 @@ MUTANTS = [
     ("q8k_bsum_drops_first", "for (int i = 0; i < ORACLE_QK; ++i) t += q[", "for (int i = 1; i < ORACLE_QK; ++i) t += q["),
     ("q8k_one_scale", "quantize_span(q + e0, d + (size_t)r * nsb + B, x + e0, ORACLE_QKK);",
      "quantize_span(q + e0, d + (size_t)r * nsb + B, x + e0, ORACLE_QK); quantize_span(q + e0 + ORACLE_QK, d + (size_t)r * nsb + B, x + e0 + ORACLE_QK, ORACLE_QKK - ORACLE_QK);"),
+    ("half_bias_14", "v = ldexpf((float)(f + 1024), e - 25);", "v = ldexpf((float)(f + 1024), e - 24);"),
+    ("half_subnormal_implicit", "if (e == 0)       v = ldexpf((float)f, -24);", "if (e == 0)       v = ldexpf((float)(f + 1024), -24);"),
+    ("nbits_high_at_16", "(blkb[i] & 0x0F) : (blkb[i - blk / 2] >> 4)", "(blkb[i] & 0x0F) : (blkb[(i - blk / 2) % 16] >> 4)"),
+    ("nbits_zp_sign", "return (int32_t)bp + 128 - z;", "return (int32_t)bp - 128 + z;"),
+    ("nbits_zp_ignored", "const int z = zp ? zp[(size_t)r * nb + b] : 128;", "const int z = 128;"),
+    ("nbits_x_block0", "* (int32_t)xq[(size_t)b * blk + i];\n            const size_t si", "* (int32_t)xq[i];\n            const size_t si"),
+    ("nbits_scale_row0", "((const float *)scales)[si];", "((const float *)scales)[b];"),
+    ("blk_bsum_drops_last", "for (int i = 0; i < blk; ++i) t += q[", "for (int i = 0; i < blk - 1; ++i) t += q["),
     ("attention_drops_last", "for (int t = 0; t < n_pos; ++t) {\n            const float *vt",
      "for (int t = 0; t < n_pos - 1; ++t) {\n            const float *vt"),
 ]
