@@ -350,6 +350,44 @@ class OracleQ4KPass:
         return vecs
 
 
+class OracleNBitsPass:
+    """One pass of an NBitsWorkload with the oracle (per input the per-block
+    quantiser, then every product with rows split over `threads` threads)."""
+
+    def __init__(self, wl, threads: int):
+        import numpy as np
+        from concurrent.futures import ThreadPoolExecutor
+
+        import oracle
+        from block_quantized_decode_gb300 import inputs as I
+        self.np, self.O, self.wl, self.threads = np, oracle, wl, threads
+        self.pool = ThreadPoolExecutor(max_workers=threads)
+        self.W = {name: I.nbits_weights(rows, cols, wl.bits, wl.blk, wl.f16, wl.with_zp, seed=wl.seed + i)
+                  for i, (name, rows, cols, _) in enumerate(wl.mats)}
+        self.x0 = I.activations(1, wl.mats[0][2], seed=wl.seed + 1000)[0]
+        self.weight_bytes = sum(q.nbytes + sc.nbytes + (0 if zp is None else zp.nbytes)
+                                for q, sc, zp in self.W.values())
+        self.ops = sum(2 * rows * cols for _, rows, cols, _ in wl.mats)
+
+    def run(self):
+        O, np, wl = self.O, self.np, self.wl
+        vecs = {"x": self.x0}
+        acts = {}
+        for name, rows, cols, inp in wl.mats:
+            if inp not in acts:
+                acts[inp] = O.quantize_blk(vecs[inp], wl.blk)
+            q, sc, zp = self.W[name]
+            xq, xd, _ = acts[inp]
+            y = np.zeros(rows, dtype=np.float32)
+            cuts = [rows * t // self.threads for t in range(self.threads + 1)]
+            futs = [self.pool.submit(O.matvec_nbits, q, sc, zp, rows, cols, wl.bits, wl.blk, xq, xd, a, b, y)
+                    for a, b in zip(cuts, cuts[1:]) if b > a]
+            for f in futs:
+                f.result()
+            vecs[name] = y
+        return vecs
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -363,6 +401,8 @@ def oracle_pass(wl, threads: int):
         return OracleLayerPass(wl, threads)
     if isinstance(wl, I.Q4KWorkload):
         return OracleQ4KPass(wl, threads)
+    if isinstance(wl, I.NBitsWorkload):
+        return OracleNBitsPass(wl, threads)
     return OraclePass(wl, threads)
 
 
@@ -387,7 +427,7 @@ def run_reference(args, wl, world, rank):
         return 0
     from block_quantized_decode_gb300 import inputs as I
     threads = host_cores()
-    layer = isinstance(wl, (I.LayerShape, I.Q4KWorkload))
+    layer = isinstance(wl, (I.LayerShape, I.Q4KWorkload, I.NBitsWorkload))
     op = oracle_pass(wl, threads)
     for _ in range(min(max(0, args.warmup), 3)):
         op.run()
@@ -901,14 +941,21 @@ def run_layer(args, shape, world, rank, local, pg):
 
 
 def run_q4k(args, wl, world, rank, local, pg):
-    """A pass of Q4_K-style products per step (per input one
-    mlq_quantize_q8k, then its mlq_matvec_q4k calls), captured in a CUDA
-    graph per weight copy.  value = weight bytes (nibbles, scale/minimum
-    bytes, d, dmin) per step / step time."""
+    """A pass of products on the other weight formats per step: Q4_K-style
+    super-blocks (per input one mlq_quantize_q8k, then its mlq_matvec_q4k
+    calls) or blocks of 32 / 128 with float16 scales and signed-offset 8-bit
+    weights (mlq_quantize_blk, mlq_matvec_nbits), captured in a CUDA graph
+    per weight copy.  value = weight bytes (quants and all scale, minimum and
+    zero-point bytes) per step / step time."""
     import torch
 
+    import numpy as np
+
     import block_quantized_decode_gb300 as M
-    from block_quantized_decode_gb300.runner import Q4KRunner
+    from block_quantized_decode_gb300 import inputs as I
+    from block_quantized_decode_gb300.runner import NBitsRunner, Q4KRunner
+    nbits = isinstance(wl, I.NBitsWorkload)
+    Q4KRunner = NBitsRunner if nbits else Q4KRunner
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -1007,16 +1054,16 @@ def run_q4k(args, wl, world, rank, local, pg):
             t = a.elapsed_time(b) / 1e3 / reps
             best = t if best is None else min(best, t)
         del g
-        q, s_, d, dm, _, _ = r.host[name]
-        nb = q.nbytes + s_.nbytes + d.nbytes + dm.nbytes
+        nb = sum(a.nbytes for a in r.host[name] if isinstance(a, np.ndarray))
         per_prod[f"{name}:{rows}x{cols}"] = {"us": best * 1e6, "GBps": nb / best / 1e9}
         tot_b += nb
         tot_s += best
     ach = tot_b / tot_s / 1e9
     nprod = len(wl.mats)
-    roofline = {"kernel": "matvec_q4k_kernel", "bound": "hbm", "achieved": ach, "peak": hbm,
+    kname, ksrc = (("matvec_nbits_kernel", "nbits.cu") if nbits else ("matvec_q4k_kernel", "q4k.cu"))
+    roofline = {"kernel": kname, "bound": "hbm", "achieved": ach, "peak": hbm,
                 "unit": "GB/s", "frac": ach / hbm, "peak_source": peak_src,
-                "traffic": ncu_traffic(f"matvec_q4k_{wl.name}", ("q4k.cu", "mlq_device.cuh"),
+                "traffic": ncu_traffic(f"{kname.replace('_kernel', '')}_{wl.name}", (ksrc, "mlq_device.cuh"),
                                        tot_b / nprod),
                 "bytes_per_launch": tot_b / nprod, "us_per_launch": tot_s / nprod * 1e6,
                 "method": "each product's launches back to back in its own graph over rotating "
@@ -1055,11 +1102,14 @@ def run_q4k(args, wl, world, rank, local, pg):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
             "warmup": warm, "ms_per_step": ms_max / steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": "q4_k products: u4 x s8 dot -> int32, sub-block scales folded in int32, "
-                     "f32 per super-block",
+            "dtype": (f"{'u4' if wl.bits == 4 else 's8 (B-128)'} x s8 dot -> int32 per block of "
+                      f"{wl.blk}, {'f16' if wl.f16 else 'f32'} scales, f32 accumulate" if nbits else
+                      "q4_k products: u4 x s8 dot -> int32, sub-block scales folded in int32, "
+                      "f32 per super-block"),
             "data": "synthetic",
             "config": {"workload": wl.name, "M": 1,
-                       "matrices": [f"{n}:{rw}x{c}:q4_k" for n, rw, c, _ in wl.mats],
+                       "matrices": [f"{n}:{rw}x{c}:" + (f"{'int4' if wl.bits == 4 else 'int8'}_blk{wl.blk}"
+                                                        if nbits else "q4_k") for n, rw, c, _ in wl.mats],
                        "weight_bytes_per_step": wbytes,
                        "l2": f"inputs larger than L2: {copies} rotating weight copies "
                              f"({copies * wbytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
@@ -1077,7 +1127,7 @@ def run_q4k(args, wl, world, rank, local, pg):
 def main():
     args = parse_args()
     from block_quantized_decode_gb300 import inputs as I
-    known = {**I.WORKLOADS, **I.LAYERS, **I.Q4K_WORKLOADS}
+    known = {**I.WORKLOADS, **I.LAYERS, **I.Q4K_WORKLOADS, **I.NBITS_WORKLOADS}
     if args.workload not in known:
         raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(known)}")
     wl = known[args.workload]()
@@ -1087,7 +1137,7 @@ def main():
             return run_reference(args, wl, world, rank)
         if isinstance(wl, I.LayerShape):
             return run_layer(args, wl, world, rank, local, pg)
-        if isinstance(wl, I.Q4KWorkload):
+        if isinstance(wl, (I.Q4KWorkload, I.NBitsWorkload)):
             return run_q4k(args, wl, world, rank, local, pg)
         return run_ours(args, wl, world, rank, local, pg)
     finally:

@@ -1,6 +1,7 @@
 """GB300 (sm_103a) block-quantized decode: Q8_0 activation quantiser,
 M = 1 Q4_0 / Q8_0 matrix-vector products and the small-M batched product,
 Q4_K-style super-block products (per-256 quantiser, integer-domain scales),
+block-128 / float16-scale / signed-offset 8-bit products,
 the decode steps around them (rmsnorm, RoPE, GQA attention, silu_mul, add),
 behind the C ABI of libmlq.so (include/mlq.h).
 
@@ -17,4 +18,5 @@ from .binding import (  # noqa: F401
     MLQ_MAX_SEQ, MLQ_MAX_HEAD_DIM, mlq_rmsnorm, mlq_add_rmsnorm, mlq_add, mlq_softmax, mlq_silu_mul,
     mlq_rope_tables, mlq_rope, mlq_attention,
     MLQ_QKK, Q4KTensor, Q8KAct, mlq_quantize_q8k, mlq_matvec_q4k, mlq_block_sums_q4k,
+    NBitsTensor, BlkAct, mlq_quantize_blk, mlq_matvec_nbits, mlq_block_sumi_nbits,
 )

@@ -31,6 +31,7 @@ EXPORTS = (
     "mlq_rmsnorm", "mlq_add_rmsnorm", "mlq_add", "mlq_softmax", "mlq_silu_mul",
     "mlq_rope_tables", "mlq_rope", "mlq_attention",
     "mlq_quantize_q8k", "mlq_matvec_q4k", "mlq_block_sums_q4k",
+    "mlq_quantize_blk", "mlq_matvec_nbits", "mlq_block_sumi_nbits",
 )
 MLQ_QKK = 256
 MLQ_MAX_SEQ = 32768
@@ -65,6 +66,18 @@ class _Q4KTensor(ctypes.Structure):
 class _Q8KAct(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("d", ctypes.c_void_p), ("bsums", ctypes.c_void_p),
                 ("n", ctypes.c_int)]
+
+
+class _NBitsTensor(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("zp", ctypes.c_void_p),
+                ("rows", ctypes.c_int), ("cols", ctypes.c_int), ("bits", ctypes.c_int),
+                ("blk", ctypes.c_int), ("scale_f16", ctypes.c_int), ("scale_ld", ctypes.c_int),
+                ("zp_ld", ctypes.c_int)]
+
+
+class _BlkAct(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("d", ctypes.c_void_p), ("bsums", ctypes.c_void_p),
+                ("n", ctypes.c_int), ("blk", ctypes.c_int)]
 
 
 class _ChainProduct(ctypes.Structure):
@@ -131,6 +144,10 @@ def lib() -> ctypes.CDLL:
         L.mlq_quantize_q8k.argtypes = [KA, P, I, P]
         L.mlq_matvec_q4k.argtypes = [P, KT, KA, I, I, P]
         L.mlq_block_sums_q4k.argtypes = [P, P, KT, KA, I, I, P]
+        NT, BA = ctypes.POINTER(_NBitsTensor), ctypes.POINTER(_BlkAct)
+        L.mlq_quantize_blk.argtypes = [BA, P, I, P]
+        L.mlq_matvec_nbits.argtypes = [P, NT, BA, I, I, P]
+        L.mlq_block_sumi_nbits.argtypes = [P, NT, BA, I, I, P]
         L.mlq_status_str.argtypes = [S]
         L.mlq_status_str.restype = ctypes.c_char_p
         for name in EXPORTS:
@@ -280,6 +297,58 @@ def mlq_block_sums_q4k(isum, msum, W: Q4KTensor, x: Q8KAct, r0: int, r1: int, st
     cw, cx = W.c(), x.c()
     _check(lib().mlq_block_sums_q4k(_addr(isum), _addr(msum), ctypes.byref(cw), ctypes.byref(cx), r0,
                                     r1, _stream(stream)), "mlq_block_sums_q4k")
+
+
+# ---- block length 32 / 128, float16 scales, signed-offset 8-bit ------------
+@dataclass
+class NBitsTensor:
+    """Block-quantised weights: q (4-bit nibbles or 8-bit B' = B - 128),
+    scales [rows, scale_ld] float32 or float16, optional zero points
+    [rows, zp_ld] uint8 (8-bit only)."""
+    q: object
+    scales: object
+    zp: object
+    rows: int
+    cols: int
+    bits: int
+    blk: int
+    scale_f16: int
+    scale_ld: int
+    zp_ld: int = 0
+
+    def c(self) -> _NBitsTensor:
+        return _NBitsTensor(_addr(self.q), _addr(self.scales), _addr(self.zp), self.rows, self.cols,
+                            self.bits, self.blk, self.scale_f16, self.scale_ld, self.zp_ld)
+
+
+@dataclass
+class BlkAct:
+    """Activations quantised per blk: q int8 [n], d float32 [n/blk], bsums int32 [n/blk]."""
+    q: object
+    d: object
+    bsums: object
+    n: int
+    blk: int
+
+    def c(self) -> _BlkAct:
+        return _BlkAct(_addr(self.q), _addr(self.d), _addr(self.bsums), self.n, self.blk)
+
+
+def mlq_quantize_blk(out: BlkAct, x, k: int, stream=None) -> None:
+    co = out.c()
+    _check(lib().mlq_quantize_blk(ctypes.byref(co), _addr(x), k, _stream(stream)), "mlq_quantize_blk")
+
+
+def mlq_matvec_nbits(y, W: NBitsTensor, x: BlkAct, r0: int, r1: int, stream=None) -> None:
+    cw, cx = W.c(), x.c()
+    _check(lib().mlq_matvec_nbits(_addr(y), ctypes.byref(cw), ctypes.byref(cx), r0, r1,
+                                  _stream(stream)), "mlq_matvec_nbits")
+
+
+def mlq_block_sumi_nbits(sumi, W: NBitsTensor, x: BlkAct, r0: int, r1: int, stream=None) -> None:
+    cw, cx = W.c(), x.c()
+    _check(lib().mlq_block_sumi_nbits(_addr(sumi), ctypes.byref(cw), ctypes.byref(cx), r0, r1,
+                                      _stream(stream)), "mlq_block_sumi_nbits")
 
 
 # ---- the floating-point steps of a decode layer --------------------------

@@ -476,6 +476,66 @@ mlq_status mlq_block_sums_q4k(int32_t *isum, int32_t *msum, const mlq_q4k_tensor
   return q4k_common(nullptr, isum, msum, W, x, r0, r1, stream);
 }
 
+// ---- block length 32 / 128, float16 scales, signed-offset 8-bit ---------------
+namespace {
+mlq_status check_nbits(const mlq_nbits_tensor *W, const mlq_blk_act *x, int r0, int r1) {
+  if (W == nullptr || x == nullptr) return MLQ_E_NULL;
+  if (W->q == nullptr || W->scales == nullptr || x->q == nullptr || x->d == nullptr || x->bsums == nullptr)
+    return MLQ_E_NULL;
+  if (W->bits != 4 && W->bits != 8) return MLQ_E_TYPE;
+  if (W->scale_f16 != 0 && W->scale_f16 != 1) return MLQ_E_TYPE;
+  if (W->bits == 4 && W->zp != nullptr) return MLQ_E_TYPE;
+  if (W->blk != 32 && W->blk != 128) return MLQ_E_SHAPE;
+  if (W->cols <= 0 || W->cols % W->blk != 0 || W->cols > MLQ_MAX_COLS || W->rows < 0) return MLQ_E_SHAPE;
+  if (x->n != W->cols || x->blk != W->blk) return MLQ_E_SHAPE;
+  if (r0 < 0 || r1 < r0 || r1 > W->rows) return MLQ_E_SHAPE;
+  const int nb = W->cols / W->blk;
+  if (W->scale_ld < nb || (W->scale_ld * (W->scale_f16 ? 2 : 4)) % 16 != 0) return MLQ_E_SHAPE;
+  if (W->zp != nullptr && (W->zp_ld < nb || W->zp_ld % 16 != 0)) return MLQ_E_SHAPE;
+  if (!aligned(W->q, 16) || !aligned(W->scales, 16) || !aligned(W->zp, 16)) return MLQ_E_ALIGN;
+  if (!aligned(x->q, 16) || !aligned(x->d, 4) || !aligned(x->bsums, 4)) return MLQ_E_ALIGN;
+  return MLQ_OK;
+}
+
+mlq_status nbits_common(float *y, int32_t *sumi, const mlq_nbits_tensor *W, const mlq_blk_act *x,
+                        int r0, int r1, void *stream) {
+  mlq_status s = check_nbits(W, x, r0, r1);
+  if (s != MLQ_OK) return s;
+  if (!aligned(y != nullptr ? static_cast<const void *>(y) : static_cast<const void *>(sumi), 4))
+    return MLQ_E_ALIGN;
+  mlq::LaunchCtx ctx;
+  if ((s = make_ctx(&ctx, stream)) != MLQ_OK) return s;
+  return from_cuda(mlq::launch_matvec_nbits(ctx, W->bits, W->blk, W->q, W->scales, W->scale_f16,
+                                            W->scale_ld, W->zp, W->zp_ld, W->cols, x->q, x->d,
+                                            x->bsums, y, sumi, r0, r1));
+}
+}  // namespace
+
+mlq_status mlq_quantize_blk(mlq_blk_act *out, const float *x, int k, void *stream) {
+  if (out == nullptr || x == nullptr || out->q == nullptr || out->d == nullptr || out->bsums == nullptr)
+    return MLQ_E_NULL;
+  if (out->blk != 32 && out->blk != 128) return MLQ_E_SHAPE;
+  if (k <= 0 || k % out->blk != 0 || k > MLQ_MAX_COLS || out->n != k) return MLQ_E_SHAPE;
+  if (!aligned(x, 16) || !aligned(out->q, 16) || !aligned(out->d, 4) || !aligned(out->bsums, 4))
+    return MLQ_E_ALIGN;
+  mlq::LaunchCtx ctx;
+  mlq_status s = make_ctx(&ctx, stream);
+  if (s != MLQ_OK) return s;
+  return from_cuda(mlq::launch_quantize_blk(ctx, x, out->q, out->d, out->bsums, k, out->blk));
+}
+
+mlq_status mlq_matvec_nbits(float *y, const mlq_nbits_tensor *W, const mlq_blk_act *x, int r0, int r1,
+                            void *stream) {
+  if (y == nullptr) return MLQ_E_NULL;
+  return nbits_common(y, nullptr, W, x, r0, r1, stream);
+}
+
+mlq_status mlq_block_sumi_nbits(int32_t *sumi, const mlq_nbits_tensor *W, const mlq_blk_act *x, int r0,
+                                int r1, void *stream) {
+  if (sumi == nullptr) return MLQ_E_NULL;
+  return nbits_common(nullptr, sumi, W, x, r0, r1, stream);
+}
+
 // ---- the floating-point steps of a decode layer -------------------------------
 namespace {
 // An optional Q8_0 output of n elements (one row): both arrays or none.

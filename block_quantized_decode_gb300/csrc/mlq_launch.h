@@ -182,6 +182,15 @@ cudaError_t launch_matvec_q4k(const LaunchCtx &ctx, const void *wq, const void *
                               const int32_t *xbs, float *y, int32_t *isum, int32_t *msum, int r0,
                               int r1);
 
+// nbits.cu: blocks of 32 or 128, float32 / binary16 scales, 4-bit or
+// signed-offset 8-bit weights (sumi non-null: the integer test hook).
+cudaError_t launch_quantize_blk(const LaunchCtx &ctx, const float *x, int8_t *q, float *d,
+                                int32_t *bsums, int k, int blk);
+cudaError_t launch_matvec_nbits(const LaunchCtx &ctx, int bits, int blk, const void *wq, const void *sc,
+                                int sc_f16, int sc_ld, const uint8_t *zp, int zp_ld, int cols,
+                                const int8_t *xq, const float *xd, const int32_t *xbs, float *y,
+                                int32_t *sumi, int r0, int r1);
+
 // layer.cu: the floating-point steps of a decode layer (each one launch).
 cudaError_t launch_rmsnorm_q8(const LaunchCtx &ctx, float *x, const float *y, const float *w,
                               float *h, int8_t *hq, float *hd, int n, float eps);

@@ -339,6 +339,8 @@ cudaError_t launch_matvec_q4k(const LaunchCtx &ctx, const void *wq, const void *
   const size_t xs = up(K + 4 * (K / kQK) + 4 * static_cast<size_t>(nsb), 128);
   int R = static_cast<int>(kKStageTarget / rowbytes);
   if (R < 1) R = 1;
+  const int per_sm = (n + ctx.num_sms - 1) / ctx.num_sms;  // spread the rows over every SM
+  if (R > per_sm) R = per_sm;
   int grid = ctx.num_sms;
   if (grid > (n + R - 1) / R) grid = (n + R - 1) / R;
   const int rows_cta = (n + grid - 1) / grid;

@@ -240,3 +240,70 @@ def tinyllama_layer_q4k() -> Q4KWorkload:
 
 
 Q4K_WORKLOADS = {"tinyllama_layer_q4k": tinyllama_layer_q4k}
+
+
+
+# ---- block length 32 / 128, float16 scales, signed-offset 8-bit weights ----
+def nbits_weights(rows: int, cols: int, bits: int, blk: int, f16: bool, with_zp: bool, seed: int):
+    """4-bit: nibble bytes uniform; 8-bit: B' = B - 128 uniform int8; scales
+    U[1e-3, 1e-2] (4-bit) or U[1e-4, 1e-3] (8-bit), float32 or float16;
+    8-bit zero points uniform in [120, 136] around the usual 128 (None when
+    not requested).  Returns (q, scales [rows, cols/blk], zp or None)."""
+    rng = np.random.default_rng(seed)
+    nb = cols // blk
+    if bits == 4:
+        q = rng.integers(0, 256, size=(rows, cols // 2), dtype=np.uint8)
+        lo, hi = 1e-3, 1e-2
+    else:
+        q = rng.integers(-128, 128, size=(rows, cols), dtype=np.int8)
+        lo, hi = 1e-4, 1e-3
+    sc = rng.uniform(lo, hi, size=(rows, nb)).astype(np.float16 if f16 else np.float32)
+    zp = rng.integers(120, 137, size=(rows, nb), dtype=np.uint8) if (bits == 8 and with_zp) else None
+    return q, sc, zp
+
+
+def pad_rows(a: np.ndarray, align_bytes: int = 16) -> np.ndarray:
+    """Copy of a [rows, n] array with each row padded (zeros) to a multiple of
+    align_bytes; the padded row length in elements is the array's width."""
+    per = align_bytes // a.itemsize
+    ld = (a.shape[1] + per - 1) // per * per
+    out = np.zeros((a.shape[0], ld), dtype=a.dtype)
+    out[:, :a.shape[1]] = a
+    return out
+
+
+@dataclass
+class NBitsWorkload:
+    """M = 1 products on blocks of `blk` with `bits`-bit weights; mats as in
+    Q4KWorkload; every input is quantised per `blk` before the first
+    product that reads it."""
+    name: str
+    mats: list
+    bits: int
+    blk: int
+    f16: bool
+    with_zp: bool
+    seed: int = 0
+
+
+def _qwen_mats():
+    d, kv, ff = 896, 128, 4864   # Qwen2.5-0.5B: hidden 896, 2 KV heads of 64, intermediate 4864
+    return [("wq", d, d, "x"), ("wk", kv, d, "x"), ("wv", kv, d, "x"), ("wo", d, d, "wq"),
+            ("w_gate", ff, d, "wo"), ("w_up", ff, d, "wo"), ("w_down", d, ff, "w_gate")]
+
+
+def qwen_layer_int4_blk128() -> NBitsWorkload:
+    """One Qwen2.5-0.5B layer's projections as AMD's int4 export stores
+    them: 4-bit weights in blocks of 128, float32 scales."""
+    return NBitsWorkload("qwen2.5-0.5b_layer_int4_blk128", _qwen_mats(), 4, 128, False, False)
+
+
+def qwen_layer_int8_sq8() -> NBitsWorkload:
+    """The same projections as the int8 export in the signed-offset form:
+    8-bit weights B' = B - 128 in blocks of 32, float16 scales, per-block
+    zero points around 128."""
+    return NBitsWorkload("qwen2.5-0.5b_layer_int8_sq8", _qwen_mats(), 8, 32, True, True)
+
+
+NBITS_WORKLOADS = {"qwen_layer_int4_blk128": qwen_layer_int4_blk128,
+                   "qwen_layer_int8_sq8": qwen_layer_int8_sq8}

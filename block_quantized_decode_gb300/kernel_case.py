@@ -22,7 +22,7 @@ def main():
     p = argparse.ArgumentParser()
     p.add_argument("--op", default="matvec_q4",
                    choices=["matvec_q4", "matvec_q8", "gemm_q4", "quantize", "fused", "phase", "chain",
-                            "matvec_q4k"])
+                            "matvec_q4k", "matvec_nbits"])
     p.add_argument("--workload", default="tinyllama_layer",
                    help="for --op fused / phase / chain: the workload whose phases run as "
                         "mlq_matvec_fused / mlq_decode_phase calls, or as one "
@@ -34,6 +34,10 @@ def main():
     p.add_argument("--reps", type=int, default=5)
     p.add_argument("--copies", type=int, default=0)
     p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--bits", type=int, default=8, help="for --op matvec_nbits: 4 or 8")
+    p.add_argument("--blk", type=int, default=32, help="for --op matvec_nbits: 32 or 128")
+    p.add_argument("--f16", action="store_true", help="for --op matvec_nbits: float16 scales")
+    p.add_argument("--zp", action="store_true", help="for --op matvec_nbits: 8-bit zero points")
     a = p.parse_args()
 
     dev = torch.device("cuda:0")
@@ -41,7 +45,7 @@ def main():
     B.mlq_init()
     if a.op in ("fused", "phase", "chain"):
         return fused_case(a)
-    if a.op == "matvec_q4k":
+    if a.op in ("matvec_q4k", "matvec_nbits"):
         return q4k_case(a)
     g = torch.Generator(device=dev)
     g.manual_seed(0)
@@ -113,33 +117,48 @@ def main():
 def q4k_case(a):
     """Back-to-back mlq_matvec_q4k launches over rotating weight copies."""
     from . import inputs as I
+    import numpy as np
     rows, cols = a.rows, a.cols
-    q, s, d, dmin = I.q4k_weights(rows, cols, seed=0)
-    wbytes = q.nbytes + s.nbytes + d.nbytes + dmin.nbytes
+    dev = torch.device("cuda:0")
+    tt = lambda t: torch.from_numpy(np.ascontiguousarray(t)).to(dev)
+    x = torch.from_numpy(I.activations(1, cols, seed=1)[0]).to(dev)
+    if a.op == "matvec_q4k":
+        host = I.q4k_weights(rows, cols, seed=0)
+        make = lambda: B.Q4KTensor(*(tt(t) for t in host), rows, cols)
+        act = B.Q8KAct(torch.empty(cols, dtype=torch.int8, device=dev),
+                       torch.empty(cols // 256, dtype=torch.float32, device=dev),
+                       torch.empty(cols // 32, dtype=torch.int32, device=dev), cols)
+        B.mlq_quantize_q8k(act, x, cols)
+        mv = B.mlq_matvec_q4k
+    else:
+        q, sc, zp = I.nbits_weights(rows, cols, a.bits, a.blk, a.f16, a.zp, seed=0)
+        host = (q, sc) + (() if zp is None else (zp,))
+        scp, zpp = I.pad_rows(sc), (None if zp is None else I.pad_rows(zp))
+        make = lambda: B.NBitsTensor(tt(q), tt(scp.view(np.uint16) if a.f16 else scp),
+                                     None if zpp is None else tt(zpp), rows, cols, a.bits, a.blk,
+                                     1 if a.f16 else 0, scp.shape[1], 0 if zpp is None else zpp.shape[1])
+        act = B.BlkAct(torch.empty(cols, dtype=torch.int8, device=dev),
+                       torch.empty(cols // a.blk, dtype=torch.float32, device=dev),
+                       torch.empty(cols // a.blk, dtype=torch.int32, device=dev), cols, a.blk)
+        B.mlq_quantize_blk(act, x, cols)
+        mv = B.mlq_matvec_nbits
+    wbytes = sum(t.nbytes for t in host)
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     copies = a.copies or max(1, math.ceil(3 * l2 / wbytes))
     copies = min(copies, a.iters)
-    dev = torch.device("cuda:0")
-    Ws = []
-    for c in range(copies):
-        Ws.append(B.Q4KTensor(*(torch.from_numpy(t).to(dev) for t in (q, s, d, dmin)), rows, cols))
-    x = torch.from_numpy(I.activations(1, cols, seed=1)[0]).to(dev)
-    act = B.Q8KAct(torch.empty(cols, dtype=torch.int8, device=dev),
-                   torch.empty(cols // 256, dtype=torch.float32, device=dev),
-                   torch.empty(cols // 32, dtype=torch.int32, device=dev), cols)
-    B.mlq_quantize_q8k(act, x, cols)
+    Ws = [make() for _ in range(copies)]
     y = torch.empty(rows, dtype=torch.float32, device=dev)
     s_ = torch.cuda.Stream()
     with torch.cuda.stream(s_):
         for i in range(copies):
-            B.mlq_matvec_q4k(y, Ws[i], act, 0, rows)
+            mv(y, Ws[i], act, 0, rows)
     s_.synchronize()
     graph = None
     if not a.no_graph:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=s_):
             for i in range(a.iters):
-                B.mlq_matvec_q4k(y, Ws[i % copies], act, 0, rows)
+                mv(y, Ws[i % copies], act, 0, rows)
     times = []
     for _ in range(a.reps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -149,7 +168,7 @@ def q4k_case(a):
                 graph.replay()
             else:
                 for i in range(a.iters):
-                    B.mlq_matvec_q4k(y, Ws[i % copies], act, 0, rows)
+                    mv(y, Ws[i % copies], act, 0, rows)
             e1.record(s_)
         s_.synchronize()
         times.append(e0.elapsed_time(e1) / a.iters * 1e3)

@@ -320,3 +320,61 @@ class Q4KRunner:
 
     def ops(self) -> int:
         return sum(2 * rows * cols for _, rows, cols, _ in self.wl.mats)
+
+
+class NBitsRunner:
+    """Device buffers and one pass of an NBitsWorkload through the C ABI:
+    per input mlq_quantize_blk, then every mlq_matvec_nbits that reads it.
+    Scale and zero-point rows are padded to 16 bytes (the tensor's strides)."""
+
+    def __init__(self, wl: I.NBitsWorkload, copies: int = 1, device: str = "cuda:0"):
+        self.wl = wl
+        self.copies = copies
+        self.dev = torch.device(device)
+        self.host = {}
+        self.W = [dict() for _ in range(copies)]
+        self.y = {}
+        self.src = {}
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(self.dev)
+        for i, (name, rows, cols, inp) in enumerate(wl.mats):
+            q, sc, zp = I.nbits_weights(rows, cols, wl.bits, wl.blk, wl.f16, wl.with_zp, seed=wl.seed + i)
+            self.host[name] = (q, sc, zp)
+            scp = I.pad_rows(sc)
+            zpp = None if zp is None else I.pad_rows(zp)
+            for c in range(copies):
+                self.W[c][name] = B.NBitsTensor(
+                    t(q), t(scp.view(np.uint16) if wl.f16 else scp), None if zpp is None else t(zpp),
+                    rows, cols, wl.bits, wl.blk, 1 if wl.f16 else 0, scp.shape[1],
+                    0 if zpp is None else zpp.shape[1])
+            self.y[name] = torch.zeros(rows, dtype=torch.float32, device=self.dev)
+            self.src.setdefault(inp, cols)
+        self.x_host = I.activations(1, self.src["x"], seed=wl.seed + 1000)[0]
+        self.x = torch.from_numpy(self.x_host).to(self.dev)
+        self.x_pinned = torch.from_numpy(self.x_host).pin_memory()
+        self.act = {}
+        for name, k in self.src.items():
+            self.act[name] = B.BlkAct(torch.empty(k, dtype=torch.int8, device=self.dev),
+                                      torch.empty(k // wl.blk, dtype=torch.float32, device=self.dev),
+                                      torch.empty(k // wl.blk, dtype=torch.int32, device=self.dev), k, wl.blk)
+        self.launches_per_step = len(self.src) + len(wl.mats)
+
+    def vec(self, name):
+        return self.x if name == "x" else self.y[name]
+
+    def step(self, copy: int = 0, stream=None) -> None:
+        done = set()
+        for name, rows, cols, inp in self.wl.mats:
+            if inp not in done:
+                B.mlq_quantize_blk(self.act[inp], self.vec(inp), cols, stream)
+                done.add(inp)
+            B.mlq_matvec_nbits(self.y[name], self.W[copy][name], self.act[inp], 0, rows, stream)
+
+    def product(self, name: str, copy: int = 0, stream=None) -> None:
+        rows, inp = [(m[1], m[3]) for m in self.wl.mats if m[0] == name][0]
+        B.mlq_matvec_nbits(self.y[name], self.W[copy][name], self.act[inp], 0, rows, stream)
+
+    def weight_bytes(self) -> int:
+        return sum(q.nbytes + sc.nbytes + (0 if zp is None else zp.nbytes) for q, sc, zp in self.host.values())
+
+    def ops(self) -> int:
+        return sum(2 * rows * cols for _, rows, cols, _ in self.wl.mats)

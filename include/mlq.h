@@ -210,6 +210,64 @@ mlq_status mlq_matvec_q4k(float *y, const mlq_q4k_tensor *W, const mlq_q8k_act *
 mlq_status mlq_block_sums_q4k(int32_t *isum, int32_t *msum, const mlq_q4k_tensor *W,
                               const mlq_q8k_act *x, int r0, int r1, void *stream);
 
+/* ---- block length 32 / 128, float16 scales, signed-offset 8-bit -------- */
+/* Page "ONNX Runtime" (SpaceMiT X60), "How we got there": item 3 (AMD's
+ * Qwen2.5-0.5B export uses block_size 128; int8 activations), item 4
+ * (8-bit weights packed as B' = B - 128 with flat scales and a per-block
+ * zero-point correction that vanishes for zp = 128), item 5 (float16
+ * scales).  Per block b of `blk` weights of row r:
+ *   sumi = sum_i w_i * a_i,  w = nibble - 8 (bits 4) or B' + 128 - zp_b (bits 8),
+ *   y[r] += ((float)sumi * scale_b) * x->d[b]   (float32, in this order);
+ * the kernel forms sumi as sum B' a + (128 - zp) * sum a (or sum n a -
+ * 8 * sum a) in int32, exactly.  Layout (the page gives none; rows
+ * row-major, device pointers, all 16-byte aligned):
+ *   q:      bits 4: rows x cols/2 bytes, block b's byte j holding element j
+ *           (low nibble) and element j + blk/2 (high nibble);
+ *           bits 8: rows x cols int8 B' = B - 128;
+ *   scales: rows x scale_ld, float32 (scale_f16 = 0) or IEEE binary16
+ *           (scale_f16 = 1); scale_ld >= cols/blk with scale_ld * (4 or 2)
+ *           a multiple of 16 bytes;
+ *   zp:     bits 8 only (NULL for bits 4): rows x zp_ld uint8 zero points
+ *           of B, zp_ld >= cols/blk a multiple of 16; NULL means 128.
+ * blk is 32 or 128; cols a positive multiple of blk, at most MLQ_MAX_COLS. */
+typedef struct {
+    const void *q;
+    const void *scales;
+    const uint8_t *zp;
+    int rows, cols;
+    int bits, blk;
+    int scale_f16;
+    int scale_ld, zp_ld;
+} mlq_nbits_tensor;
+
+/* Activations quantised per block of blk (32 or 128) elements: n int8
+ * quants q (16-byte aligned), n/blk float32 scales d and n/blk int32 quant
+ * sums bsums (4-byte aligned). */
+typedef struct {
+    int8_t *q;
+    float *d;
+    int32_t *bsums;
+    int n;
+    int blk;
+} mlq_blk_act;
+
+/* Quantise k float32 (x, device, 16-byte aligned) per out->blk elements
+ * with the rule of mlq_quantize_q8 (bit-identical), and write each block's
+ * quant sum.  out->n == k, k a positive multiple of out->blk, at most
+ * MLQ_MAX_COLS; out->blk is 32 or 128. */
+mlq_status mlq_quantize_blk(mlq_blk_act *out, const float *x, int k, void *stream);
+
+/* y[r] for r in [r0, r1) as above; the sum over blocks is taken in another
+ * order than b = 0, 1, ... and agrees with the in-order sum within
+ * 1e-5 * sum_b |term_b| per row.  x->n == W->cols, x->blk == W->blk. */
+mlq_status mlq_matvec_nbits(float *y, const mlq_nbits_tensor *W, const mlq_blk_act *x, int r0,
+                            int r1, void *stream);
+
+/* Test hook: sumi[(r - r0)*(cols/blk) + b] for r in [r0, r1), by the same
+ * code as mlq_matvec_nbits. */
+mlq_status mlq_block_sumi_nbits(int32_t *sumi, const mlq_nbits_tensor *W, const mlq_blk_act *x,
+                                int r0, int r1, void *stream);
+
 /* ---- the floating-point steps of a decode layer ------------------------ */
 /* Page "Legacy-ISA ML Inference Runtime -- Design Spec", Sec. 5 (ml_k_rmsnorm,
  * ml_k_softmax, ml_k_rope, ml_k_silu_mul, ml_k_add, ml_k_dot_f32,

@@ -335,3 +335,42 @@ def test_validation_q4k(M):
     assert qk(ka(n=512), k=256) == M.MLQ_E_SHAPE
     assert qk(ka(), x=6 * A + 4) == M.MLQ_E_ALIGN
     assert qk(ka(d=4 * A + 4)) == M.MLQ_E_ALIGN
+
+
+def test_validation_nbits(M):
+    from block_quantized_decode_gb300.binding import _BlkAct, _NBitsTensor
+
+    def nt(q=A, sc=2 * A, zp=0, rows=64, cols=896, bits=4, blk=128, f16=0, sld=8, zld=0):
+        return _NBitsTensor(q, sc, zp or None, rows, cols, bits, blk, f16, sld, zld)
+
+    def ba(q=3 * A, d=4 * A, bs=9 * A, n=896, blk=128):
+        return _BlkAct(q, d, bs, n, blk)
+
+    def mvn(y=5 * A, W=None, x=None, r0=0, r1=64):
+        W = nt() if W is None else W
+        x = ba() if x is None else x
+        return call(M, "mlq_matvec_nbits", y, ctypes.byref(W), ctypes.byref(x), r0, r1, None)
+
+    assert mvn(y=None) == M.MLQ_E_NULL
+    assert mvn(W=nt(sc=0)) == M.MLQ_E_NULL
+    assert mvn(x=ba(bs=0)) == M.MLQ_E_NULL
+    assert mvn(W=nt(bits=2)) == M.MLQ_E_TYPE
+    assert mvn(W=nt(f16=2)) == M.MLQ_E_TYPE
+    assert mvn(W=nt(zp=6 * A, zld=16)) == M.MLQ_E_TYPE                # zero points on 4-bit
+    assert mvn(W=nt(blk=64), x=ba(blk=64)) == M.MLQ_E_SHAPE
+    assert mvn(W=nt(cols=960), x=ba(n=960)) == M.MLQ_E_SHAPE          # not whole blocks of 128
+    assert mvn(x=ba(blk=32)) == M.MLQ_E_SHAPE                         # block lengths differ
+    assert mvn(W=nt(sld=6)) == M.MLQ_E_SHAPE                          # stride < 7 blocks
+    assert mvn(W=nt(sld=7)) == M.MLQ_E_SHAPE                          # 28-byte rows
+    assert mvn(W=nt(bits=8, zp=6 * A, zld=8)) == M.MLQ_E_SHAPE        # zero-point rows not 16 B
+    assert mvn(r1=65) == M.MLQ_E_SHAPE
+    assert mvn(W=nt(q=A + 8)) == M.MLQ_E_ALIGN
+    assert mvn(W=nt(bits=8, zp=6 * A + 4, zld=16)) == M.MLQ_E_ALIGN
+    assert mvn(x=ba(d=4 * A + 2)) == M.MLQ_E_ALIGN
+    assert call(M, "mlq_block_sumi_nbits", None, ctypes.byref(nt()), ctypes.byref(ba()), 0, 64,
+                None) == M.MLQ_E_NULL
+    qb = lambda out, x=6 * A, k=896: call(M, "mlq_quantize_blk", ctypes.byref(out), x, k, None)
+    assert qb(ba(), x=None) == M.MLQ_E_NULL
+    assert qb(ba(blk=64)) == M.MLQ_E_SHAPE
+    assert qb(ba(n=960), k=960) == M.MLQ_E_SHAPE
+    assert qb(ba(), x=6 * A + 8) == M.MLQ_E_ALIGN
