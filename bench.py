@@ -957,6 +957,10 @@ def run_q4k(args, wl, world, rank, local, pg):
     nbits = isinstance(wl, I.NBitsWorkload)
     Q4KRunner = NBitsRunner if nbits else Q4KRunner
 
+    # The runner writes its weights once, before any product: declare them
+    # static, so that under programmatic dependent launch each product
+    # streams its weights before the previous launch has finished.
+    os.environ.setdefault("MLQ_STATIC_WEIGHTS", "1")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     M.mlq_init()
@@ -1114,7 +1118,8 @@ def run_q4k(args, wl, world, rank, local, pg):
                        "l2": f"inputs larger than L2: {copies} rotating weight copies "
                              f"({copies * wbytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
                        "graphs": ("one graph per cycle of %d steps" % copies) if cycle is not None else False,
-                       "path": "calls", "parallelism": f"replicas x{world} (independent decode streams)"},
+                       "path": "calls", "static_weights": os.environ.get("MLQ_STATIC_WEIGHTS") == "1",
+                       "parallelism": f"replicas x{world} (independent decode streams)"},
             "gops": world * r.ops() * steps / (ms_max / 1e3) / 1e9, "hbm_frac": value / world / hbm,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": r.launches_per_step * steps,

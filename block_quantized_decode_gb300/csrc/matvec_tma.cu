@@ -343,7 +343,11 @@ cudaError_t launch_matvec_m1_tma(const LaunchCtx &ctx, int qtype, const void *wq
     part = align_up(static_cast<size_t>(rows_cta) * S * 4, 128);
   }
   static const size_t stage_target = env_size("MLQ_TMA_STAGE_KB", kStageTarget / 1024) * 1024;
-  static const int max_slots = static_cast<int>(env_size("MLQ_TMA_SLOTS", 4));
+  // ring slots: at most kMaxSlots (the barrier arrays' size), at least 2
+  static const int max_slots = [] {
+    const size_t v = env_size("MLQ_TMA_SLOTS", 4);
+    return static_cast<int>(v < 2 ? 2 : (v > static_cast<size_t>(kMaxSlots) ? kMaxSlots : v));
+  }();
   static const int pre_stages = static_cast<int>(env_size("MLQ_TMA_PREFETCH_STAGES", 8));
   int rs = static_cast<int>(stage_target / rowbytes);
   if (rs < 1) rs = 1;

@@ -214,7 +214,10 @@ __global__ void __launch_bounds__(kKThreads, 2) matvec_q4k_kernel(const __grid_c
   // ------------------------------ consumers ------------------------------
   griddep_wait();  // x may come from the previous kernel
   if (rb <= ra) return;
-  {  // the activation vector into shared memory, all loads before any store
+  // The activation quants in shared memory: sub-block u at u*32, its two
+  // 16-byte halves swapped when bit 2 of u is set, so that the 8 lanes of a
+  // quarter warp (sub-blocks u .. u+7) read distinct banks.
+  {  // all loads before any store
     const int uq = K / 16, ub = nsub / 4;
     for (int base = 0; base < uq + ub; base += 2 * kKWarps * 32) {
       int4 v[2];
@@ -227,7 +230,7 @@ __global__ void __launch_bounds__(kKThreads, 2) matvec_q4k_kernel(const __grid_c
 #pragma unroll
       for (int p = 0; p < 2; ++p) {
         const int u = base + p * kKWarps * 32 + tid;
-        if (u < uq) reinterpret_cast<int4 *>(xq_s)[u] = v[p];
+        if (u < uq) reinterpret_cast<int4 *>(xq_s)[u ^ ((u >> 3) & 1)] = v[p];  // 16-byte unit u: sub-block u/2
         else if (u < uq + ub) reinterpret_cast<int4 *>(xbs_s)[u - uq] = v[p];
       }
     }
@@ -261,8 +264,9 @@ __global__ void __launch_bounds__(kKThreads, 2) matvec_q4k_kernel(const __grid_c
           ms[h] = 0;
           if (u < nsub) {  // whole groups of 8 lanes (nsub is a multiple of 8)
             const uint4 w = *reinterpret_cast<const uint4 *>(wrow + static_cast<size_t>(u) * 16);
-            const int4 xa = *reinterpret_cast<const int4 *>(xq_s + static_cast<size_t>(u) * kQK);
-            const int4 xb = *reinterpret_cast<const int4 *>(xq_s + static_cast<size_t>(u) * kQK + 16);
+            const int hs = (u >> 2) & 1;  // the swapped halves (see the staging above)
+            const int4 xa = *reinterpret_cast<const int4 *>(xq_s + static_cast<size_t>(u) * kQK + 16 * hs);
+            const int4 xb = *reinterpret_cast<const int4 *>(xq_s + static_cast<size_t>(u) * kQK + 16 * (hs ^ 1));
             const int B = u >> 3, j = u & 7;
             constexpr uint32_t kLo = 0x0F0F0F0Fu;
             int dot = 0;
