@@ -7,8 +7,9 @@
 // blocks, block dot), Sec. 5 (quantize_q8 rounding, matvec), Sec. 6
 // "Forward pass".
 //
-// Per CTA (one per SM; two fit on an SM, so the next phase's CTA is already
-// resident while this one runs):
+// Per CTA (one per SM; for slices up to 256 KB two fit on an SM, so the
+// next phase's CTA is already resident while this one runs; larger slices
+// take a 200 KB ring with the SM to themselves):
 //  * a producer warp copies the CTA's rows, stage by stage, with 1-D bulk
 //    copies (rows of one product per stage, quants then scales), completion
 //    on a full mbarrier per ring slot; with static weights it starts before
@@ -34,7 +35,8 @@ constexpr int kRingWarps = 8;                        // consumer warps
 constexpr int kRingThreads = (kRingWarps + 1) * 32;  // + the producer warp
 constexpr int kRingMaxSlots = 8;
 constexpr size_t kRingBudget = 110 * 1024;      // two CTAs per SM
-constexpr size_t kRingBudgetWide = 200 * 1024;  // one CTA per SM (very long rows)
+constexpr size_t kRingBudgetWide = 216 * 1024;  // one CTA per SM (very long rows, large slices)
+constexpr size_t kRingWideSlice = 256 * 1024;    // CTA slices from this size take the 200 KB ring
 
 __device__ __forceinline__ void consumers_sync() {
   asm volatile("bar.sync 1, %0;" ::"r"(kRingWarps * 32) : "memory");
@@ -257,7 +259,22 @@ static cudaError_t launch_ring_t(const LaunchCtx &ctx, const FusedArgs &args) {
   // Geometry: the fewest K-chunks (a power of two, at most 64 blocks each,
   // at most one per consumer warp) whose ring of >= 2 stages of R = 4 * G
   // rows fits the budget; two CTAs per SM if possible, else one.
-  for (size_t budget : {kRingBudget, kRingBudgetWide}) {
+  // Ring size.  Two CTAs per SM (110 KB each) let the next phase's CTA
+  // stream its first stages while this one finishes; a CTA alone on its SM
+  // keeps twice the bytes in flight (200 KB).  For slices well beyond the
+  // small ring (the 7B Q8_0 products: 330 KB per CTA) the deeper ring wins
+  // (measured: the Q8_0 stack with the lm_head 228 -> 199 us); for the
+  // TinyLlama and 7B Q4_0 phases (<= 185 KB) both measure the same.
+  // MLQ_RING_WIDE=1 / 0 forces one order (A/B timing).
+  static const int wide_env = [] {
+    const char *e = std::getenv("MLQ_RING_WIDE");
+    return e == nullptr ? -1 : (e[0] == '1' ? 1 : 0);
+  }();
+  const size_t slice = static_cast<size_t>(rows_max) * (rowq + static_cast<size_t>(nb) * 4);
+  const bool wide_first = wide_env >= 0 ? wide_env == 1 : slice >= kRingWideSlice;
+  const size_t budgets[2] = {wide_first ? kRingBudgetWide : kRingBudget,
+                             wide_first ? kRingBudget : kRingBudgetWide};
+  for (size_t budget : budgets) {
     for (int C = 1; C <= kRingWarps; C *= 2) {
       if (C * kPhChunk < nb) continue;
       const int R = 4 * (kRingWarps / C);
