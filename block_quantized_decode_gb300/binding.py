@@ -32,6 +32,7 @@ EXPORTS = (
     "mlq_rope_tables", "mlq_rope", "mlq_attention",
     "mlq_quantize_q8k", "mlq_matvec_q4k", "mlq_block_sums_q4k",
     "mlq_quantize_blk", "mlq_matvec_nbits", "mlq_block_sumi_nbits",
+    "mlq_debug_chain_plan",
 )
 MLQ_QKK = 256
 MLQ_MAX_SEQ = 32768
@@ -148,6 +149,8 @@ def lib() -> ctypes.CDLL:
         L.mlq_quantize_blk.argtypes = [BA, P, I, P]
         L.mlq_matvec_nbits.argtypes = [P, NT, BA, I, I, P]
         L.mlq_block_sumi_nbits.argtypes = [P, NT, BA, I, I, P]
+        L.mlq_debug_chain_plan.argtypes = [ctypes.POINTER(_ChainPhase), I, ctypes.POINTER(_ChainProduct),
+                                           I, I, P, I]
         L.mlq_status_str.argtypes = [S]
         L.mlq_status_str.restype = ctypes.c_char_p
         for name in EXPORTS:

@@ -407,6 +407,18 @@ mlq_status mlq_decode_chain_static(const mlq_chain_phase *phases, int nphases,
   return from_cuda(mlq::launch_decode_chain_static(ctx, dev, products[0].W.type, a));
 }
 
+mlq_status mlq_debug_chain_plan(const mlq_chain_phase *phases, int nphases,
+                                const mlq_chain_product *products, int nproducts, int num_sms,
+                                int32_t *info, int info_len) {
+  mlq::ChainArgs a;
+  mlq_status s = build_chain_args(phases, nphases, products, nproducts, &a);
+  if (s != MLQ_OK) return s;
+  if (info == nullptr) return MLQ_E_NULL;
+  if (num_sms < 1 || info_len < 0) return MLQ_E_SHAPE;
+  return mlq::describe_decode_stream(num_sms, products[0].W.type, a, info, info_len) < 0 ? MLQ_E_SHAPE
+                                                                                          : MLQ_OK;
+}
+
 mlq_status mlq_prefetch_l2(const void *const *ptrs, const size_t *bytes, int n, void *stream) {
   if (n < 0 || n > MLQ_MAX_PREFETCH_RANGES) return MLQ_E_SHAPE;
   if (n > 0 && (ptrs == nullptr || bytes == nullptr)) return MLQ_E_NULL;

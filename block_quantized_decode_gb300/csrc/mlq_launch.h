@@ -105,6 +105,10 @@ cudaError_t launch_decode_chain(const LaunchCtx &ctx, int qtype, const ChainArgs
 // phases and in-chain Q8_0 hand-offs; cudaErrorNotSupported (nothing
 // launched) when a phase is wider than its consumer warps can hold.
 cudaError_t launch_decode_stream(const LaunchCtx &ctx, int qtype, const ChainArgs &a);
+// The streaming kernel's plan for `a` on `num_sms` CTAs, as integers (the
+// layout of mlq_debug_chain_plan); host only.  Returns -1 when info_len is
+// too small, 0 when the chain does not suit the kernel, 1 otherwise.
+int describe_decode_stream(int num_sms, int qtype, const ChainArgs &a, int32_t *info, int info_len);
 // Same chain with its barrier counters in a fixed device array of chain.cu
 // (no workspace, no allocation); at most kStaticChainWords - 1 phases.
 constexpr int kStaticChainWords = 64;

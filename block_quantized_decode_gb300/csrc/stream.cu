@@ -613,6 +613,44 @@ cudaError_t plan_decode_stream(int num_sms, int qtype, const ChainArgs &args, St
   return cudaSuccess;
 }
 
+int describe_decode_stream(int num_sms, int qtype, const ChainArgs &args, int32_t *info, int info_len) {
+  StreamArgs *sap = new StreamArgs();
+  struct Free {
+    StreamArgs *p;
+    ~Free() { delete p; }
+  } guard{sap};
+  StreamArgs &sa = *sap;
+  size_t smem = 0;
+  int grid = 0;
+  const cudaError_t e = plan_decode_stream(num_sms, qtype, args, sa, &smem, &grid);
+  const int np = args.nphases;
+  const int need = 4 + 8 * np + (e == cudaSuccess ? np * (grid + 1) : 0);
+  if (info_len < need) return -1;
+  for (int i = 0; i < need; ++i) info[i] = 0;
+  if (e != cudaSuccess) return 0;  // info[0] = 0: the chain takes the other kernel
+  info[0] = 1;
+  info[1] = grid;
+  info[2] = static_cast<int32_t>(sa.ring_bytes);
+  info[3] = static_cast<int32_t>(smem);
+  for (int p = 0; p < np; ++p) {
+    const StreamPhaseDev &sp = sa.ph[p];
+    int32_t *o = info + 4 + 8 * p;
+    o[0] = sp.C;
+    o[1] = sp.cblk;
+    o[2] = sp.G;
+    o[3] = sp.RW;
+    o[4] = sp.R;
+    o[5] = sp.qin;
+    o[6] = sp.any_out;
+    int out = 0;
+    for (int j = args.phase[p].first; j < args.phase[p].first + args.phase[p].count; ++j)
+      out |= sa.out[j].yq != nullptr ? 1 << (j - args.phase[p].first) : 0;
+    o[7] = out;  // bit i: product first + i writes an in-chain Q8_0 output
+    for (int b = 0; b <= grid; ++b) info[4 + 8 * np + p * (grid + 1) + b] = sa.bounds[p][b];
+  }
+  return 1;
+}
+
 cudaError_t launch_decode_stream(const LaunchCtx &ctx, int qtype, const ChainArgs &args) {
   StreamArgs *sap = new StreamArgs();  // ~19 KB: keep it off the host stack
   struct Free {

@@ -503,6 +503,25 @@ mlq_status mlq_last_device_error(void *stream);
  * and returns.  Affects launches made after the call. */
 mlq_status mlq_debug_set_wait_limit_ns(uint64_t limit_ns);
 
+/* Test hook, host only (no device work, pointers not dereferenced): the
+ * plan mlq_decode_chain's streaming kernel would use for these arguments
+ * on num_sms CTAs, written to info (int32):
+ *   info[0] 1 if the streaming kernel takes the chain, 0 if the legacy
+ *           kernel would (then only info[0..3 + 8*nphases] are written, 0);
+ *   info[1] CTAs; info[2] ring bytes; info[3] dynamic shared memory bytes;
+ *   info[4 + 8p ..]: phase p's K-chunks C, blocks per chunk, warps per
+ *           chunk G, rows per warp RW, rows per stage R, input read as
+ *           Q8_0 from an earlier phase (0/1), some output written as Q8_0
+ *           in-chain (0/1), bit mask of the phase's products that do;
+ *   info[4 + 8*nphases + p*(CTAs + 1) + b]: the first row (phase
+ *           numbering) of CTA b in phase p, b = 0..CTAs.
+ * Arguments are validated as by mlq_decode_chain.  MLQ_E_SHAPE when
+ * info_len is too small or num_sms < 1.  Nothing on the pages corresponds
+ * to this entry point. */
+mlq_status mlq_debug_chain_plan(const mlq_chain_phase *phases, int nphases,
+                                const mlq_chain_product *products, int nproducts, int num_sms,
+                                int32_t *info, int info_len);
+
 /* Human-readable name of a status. Never NULL. */
 const char *mlq_status_str(mlq_status s);
 
