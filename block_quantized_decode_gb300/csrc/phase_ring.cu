@@ -7,15 +7,15 @@
 // blocks, block dot), Sec. 5 (quantize_q8 rounding, matvec), Sec. 6
 // "Forward pass".
 //
-// Per CTA (one per SM; for slices up to 256 KB two fit on an SM, so the
+// Per CTA (one per SM; for slices below 128 KB two fit on an SM, so the
 // next phase's CTA is already resident while this one runs; larger slices
-// take a 200 KB ring with the SM to themselves):
+// take a 216 KB ring and 16 consumer warps with the SM to themselves):
 //  * a producer warp copies the CTA's rows, stage by stage, with 1-D bulk
 //    copies (rows of one product per stage, quants then scales), completion
 //    on a full mbarrier per ring slot; with static weights it starts before
 //    the dependency wait, so the ring is full when the phase begins and the
 //    HBM stream continues across the launch boundary;
-//  * 8 consumer warps read the input (as phase.cu: the Q8_0 input loaded
+//  * 8 (16) consumer warps read the input (as phase.cu: the Q8_0 input loaded
 //    once per CTA, or float x quantised in the CTA), keep their K-chunk of it
 //    in registers, reduce each stage -- warp (chunk c, group g) takes one
 //    four-row group per stage -- and free the slot on an empty mbarrier;
@@ -31,15 +31,18 @@
 
 namespace mlq {
 
-constexpr int kRingWarps = 8;                        // consumer warps
-constexpr int kRingThreads = (kRingWarps + 1) * 32;  // + the producer warp
+// consumer warps: 8 with two CTAs per SM, 16 with the SM to itself (both
+// at 96 registers: an SM sub-partition holds at most 5 warps of either)
+constexpr int kRingWarps = 8;
+constexpr int kRingWarpsWide = 16;
 constexpr int kRingMaxSlots = 8;
 constexpr size_t kRingBudget = 110 * 1024;      // two CTAs per SM
 constexpr size_t kRingBudgetWide = 216 * 1024;  // one CTA per SM (very long rows, large slices)
-constexpr size_t kRingWideSlice = 256 * 1024;    // CTA slices from this size take the 200 KB ring
+constexpr size_t kRingWideSlice = 128 * 1024;    // CTA slices from this size take the wide ring
 
+template <int NW>
 __device__ __forceinline__ void consumers_sync() {
-  asm volatile("bar.sync 1, %0;" ::"r"(kRingWarps * 32) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive1(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -78,8 +81,9 @@ __device__ __forceinline__ int stage_next(StageIter &it, const FusedArgs &a, int
   return n;
 }
 
-template <int QT>
-__global__ void __launch_bounds__(kRingThreads, 2) phase_ring_kernel(const __grid_constant__ PhaseArgs pa) {
+template <int QT, int NW>
+__global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
+    phase_ring_kernel(const __grid_constant__ PhaseArgs pa) {
   const FusedArgs &a = pa.a;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kRingMaxSlots];
@@ -94,7 +98,7 @@ __global__ void __launch_bounds__(kRingThreads, 2) phase_ring_kernel(const __gri
   const int nr = rb - ra;
   const size_t rowq = static_cast<size_t>(nb) * (QT == 1 ? 16 : 32);
   const int C = a.nchunks, cblk = a.chunk_blocks;
-  const int G = kRingWarps / C;  // warps per chunk; a stage has R = 4 * G rows
+  const int G = NW / C;  // warps per chunk; a stage has R = 4 * G rows
   const int R = a.ring_rows, ns = a.ring_slots;
   const size_t stage_bytes = a.ring_stage, dq = a.ring_dq;
   int8_t *xq_s = reinterpret_cast<int8_t *>(smem);
@@ -105,7 +109,7 @@ __global__ void __launch_bounds__(kRingThreads, 2) phase_ring_kernel(const __gri
   if (tid == 0) {
     for (int s = 0; s < ns; ++s) {
       mbar_init(smem_addr(&full_bar[s]), 1);
-      mbar_init(smem_addr(&empty_bar[s]), kRingWarps);  // one arrival per consumer warp
+      mbar_init(smem_addr(&empty_bar[s]), NW);  // one arrival per consumer warp
     }
     abort_flag = 0;
     fence_mbar_init();
@@ -115,7 +119,7 @@ __global__ void __launch_bounds__(kRingThreads, 2) phase_ring_kernel(const __gri
   // complete before it reads anything we write).
   griddep_launch_dependents();
 
-  if (warp == kRingWarps) {
+  if (warp == NW) {
     // ------------------------------ producer ------------------------------
     if (lane != 0 || nr == 0) return;
     if (!a.early) griddep_wait();  // weights written by earlier work: wait for it first
@@ -146,27 +150,27 @@ __global__ void __launch_bounds__(kRingThreads, 2) phase_ring_kernel(const __gri
   // ------------------------------ consumers ------------------------------
   griddep_wait();  // the input may come from the previous kernel
   if (IN == 0) {
-    if (nr > 0 || (blockIdx.x == 0 && a.xq_out != nullptr)) phase_quantize<kRingWarps>(a, xq_s, xd_s, tid);
+    if (nr > 0 || (blockIdx.x == 0 && a.xq_out != nullptr)) phase_quantize<NW>(a, xq_s, xd_s, tid);
   } else if (nr > 0) {
     const int uq = nb * 2, nu = nb * 2 + nb / 4;
-    for (int base = 0; base < nu; base += 4 * kRingWarps * 32) {  // all loads before any store
+    for (int base = 0; base < nu; base += 4 * NW * 32) {  // all loads before any store
       int4 v[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const int u = base + q * kRingWarps * 32 + tid;
+        const int u = base + q * NW * 32 + tid;
         if (u < nu)
           v[q] = u < uq ? __ldcg(reinterpret_cast<const int4 *>(a.xq_in) + u)
                         : __ldcg(reinterpret_cast<const int4 *>(a.xd_in) + (u - uq));
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const int u = base + q * kRingWarps * 32 + tid;
+        const int u = base + q * NW * 32 + tid;
         if (u < uq) reinterpret_cast<int4 *>(xq_s)[u] = v[q];
         else if (u < nu) reinterpret_cast<int4 *>(xd_s)[u - uq] = v[q];
       }
     }
   }
-  consumers_sync();
+  consumers_sync<NW>();
   if (nr == 0) return;
 
   const int c = warp & (C - 1), g = warp / C;
@@ -205,13 +209,13 @@ __global__ void __launch_bounds__(kRingThreads, 2) phase_ring_kernel(const __gri
     if (lane == 0) mbar_arrive1(smem_addr(&empty_bar[slot]));
     ++s;
   }
-  consumers_sync();
+  consumers_sync<NW>();
   if (*abort_v) return;
 
   // y: the K-chunks of each row added in a fixed order, product by product
   for (int jj = 0, off = 0; jj < a.nproducts; off += a.prod[jj].rows, ++jj) {
     const int lo = max(ra, off), hi = min(rb, off + a.prod[jj].rows);
-    for (int gr = lo + tid; gr < hi; gr += kRingWarps * 32) {
+    for (int gr = lo + tid; gr < hi; gr += NW * 32) {
       const int r = gr - ra;
       float v = part_s[r * C];
       for (int cc = 1; cc < C; ++cc) v += part_s[r * C + cc];
@@ -220,7 +224,7 @@ __global__ void __launch_bounds__(kRingThreads, 2) phase_ring_kernel(const __gri
     }
   }
   if (a.any_yq) {
-    consumers_sync();
+    consumers_sync<NW>();
     // each whole 32-row block of a product with a quantised output, from
     // exactly the stored floats; one warp per block
     int t = 0;
@@ -228,7 +232,7 @@ __global__ void __launch_bounds__(kRingThreads, 2) phase_ring_kernel(const __gri
       const int lo = max(ra, off), hi = min(rb, off + a.prod[jj].rows);
       if (a.prod[jj].yq == nullptr || hi <= lo) continue;
       for (int gr = lo; gr < hi; gr += kQK, ++t) {
-        if ((t & (kRingWarps - 1)) != warp) continue;
+        if ((t & (NW - 1)) != warp) continue;
         const float v = part_s[(gr - ra + lane) * C];
         uint32_t m = __float_as_uint(fabsf(v));
 #pragma unroll
@@ -259,13 +263,14 @@ static cudaError_t launch_ring_t(const LaunchCtx &ctx, const FusedArgs &args) {
   // Geometry: the fewest K-chunks (a power of two, at most 64 blocks each,
   // at most one per consumer warp) whose ring of >= 2 stages of R = 4 * G
   // rows fits the budget; two CTAs per SM if possible, else one.
-  // Ring size.  Two CTAs per SM (110 KB each) let the next phase's CTA
-  // stream its first stages while this one finishes; a CTA alone on its SM
-  // keeps twice the bytes in flight (200 KB).  For slices well beyond the
-  // small ring (the 7B Q8_0 products: 330 KB per CTA) the deeper ring wins
-  // (measured: the Q8_0 stack with the lm_head 228 -> 199 us); for the
-  // TinyLlama and 7B Q4_0 phases (<= 185 KB) both measure the same.
-  // MLQ_RING_WIDE=1 / 0 forces one order (A/B timing).
+  // Ring size.  Two CTAs per SM (110 KB each, 8 consumer warps) let the
+  // next phase's CTA stream its first stages while this one finishes; a CTA
+  // alone on its SM (216 KB, 16 consumer warps) keeps twice the bytes in
+  // flight and reduces a landed stage twice as fast.  For slices beyond
+  // the small ring the wide one wins (measured: the 7B Q4_0 stack, 185 KB
+  // per CTA, 129.5 -> 115.6 us; the Q8_0 stack with the lm_head, 330 KB and
+  // 1 MB per CTA, 228 -> 192 us).  MLQ_RING_WIDE=1 / 0 forces one order
+  // (A/B timing).
   static const int wide_env = [] {
     const char *e = std::getenv("MLQ_RING_WIDE");
     return e == nullptr ? -1 : (e[0] == '1' ? 1 : 0);
@@ -275,9 +280,10 @@ static cudaError_t launch_ring_t(const LaunchCtx &ctx, const FusedArgs &args) {
   const size_t budgets[2] = {wide_first ? kRingBudgetWide : kRingBudget,
                              wide_first ? kRingBudget : kRingBudgetWide};
   for (size_t budget : budgets) {
-    for (int C = 1; C <= kRingWarps; C *= 2) {
+    const int NW = budget == kRingBudgetWide ? kRingWarpsWide : kRingWarps;
+    for (int C = 1; C <= NW && C <= kRingWarps; C *= 2) {
       if (C * kPhChunk < nb) continue;
-      const int R = 4 * (kRingWarps / C);
+      const int R = 4 * (NW / C);
       const size_t dq = up128(static_cast<size_t>(R) * rowq);
       const size_t stage = up128(dq + static_cast<size_t>(R) * nb * 4);
       const size_t ps = up128(static_cast<size_t>(rows_max) * C * 4);
@@ -294,14 +300,14 @@ static cudaError_t launch_ring_t(const LaunchCtx &ctx, const FusedArgs &args) {
       a.smem_part = static_cast<unsigned>(xs);
       a.smem_w = static_cast<unsigned>(fixed);
       const size_t smem = fixed + static_cast<size_t>(ns) * stage;
-      auto kern = phase_ring_kernel<QT>;
+      auto kern = NW == kRingWarps ? phase_ring_kernel<QT, kRingWarps> : phase_ring_kernel<QT, kRingWarpsWide>;
       prefer_max_shared(kern);
       if (smem > 48 * 1024) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(smem));
         if (e != cudaSuccess) return e;
       }
-      return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kRingThreads), smem, ctx, pa);
+      return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3((NW + 1) * 32), smem, ctx, pa);
     }
   }
   return cudaErrorNotSupported;
