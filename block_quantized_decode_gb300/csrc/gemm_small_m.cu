@@ -193,7 +193,10 @@ static cudaError_t launch_gemm_mm(const LaunchCtx &ctx, GemmArgs a) {
 // small M (M = 2: 11 us vs 19-24 us).  Of the tensor-core kernels the
 // cluster kernel (gemm_mma_cluster.cu) is the default; the register-load
 // kernel (gemm_mma.cu) serves the shapes it does not take (K above 16384).
-// MLQ_GEMM_KERNEL=dp4a|mma|mma_ldg overrides (A/B timing, tests).
+// The tcgen05 kernel (gemm_umma.cu) is exact and tested but slower on these
+// shapes (28-34 us at M = 16): each of its N = 16 MMAs costs the full
+// instruction latency.
+// MLQ_GEMM_KERNEL=dp4a|mma|mma_ldg|umma overrides (A/B timing, tests).
 static int gemm_override() {
   static const int v = [] {
     const char *e = std::getenv("MLQ_GEMM_KERNEL");
@@ -201,6 +204,7 @@ static int gemm_override() {
     if (std::strcmp(e, "dp4a") == 0) return 1;
     if (std::strcmp(e, "mma") == 0) return 2;
     if (std::strcmp(e, "mma_ldg") == 0) return 3;
+    if (std::strcmp(e, "umma") == 0) return 4;
     return 0;
   }();
   return v;
@@ -213,6 +217,11 @@ cudaError_t launch_gemm_q4_small_m(const LaunchCtx &ctx, const void *wq, const f
   if (r1 <= r0 || M <= 0) return cudaSuccess;
   const int o = gemm_override();
   if (o == 3) return launch_gemm_q4_mma(ctx, wq, wd, nb, xq, xd, M, Y, ldy, r0, r1);
+  if (o == 4) {
+    const cudaError_t e = launch_gemm_q4_umma(ctx, wq, wd, nb, xq, xd, M, Y, ldy, r0, r1, rows);
+    if (e != cudaErrorNotSupported) return e;
+    return launch_gemm_q4_mma(ctx, wq, wd, nb, xq, xd, M, Y, ldy, r0, r1);
+  }
   if (o == 2 || (o == 0 && M >= 8)) {
     const cudaError_t e = launch_gemm_q4_mma_cluster(ctx, wq, wd, nb, xq, xd, M, Y, ldy, r0, r1, rows);
     if (e != cudaErrorNotSupported) return e;

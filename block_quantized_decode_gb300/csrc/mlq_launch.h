@@ -176,6 +176,14 @@ cudaError_t launch_gemm_q4_mma_cluster(const LaunchCtx &ctx, const void *wq, con
                                        int nb, const int8_t *xq, const float *xd, int M, float *Y,
                                        int ldy, int r0, int r1, int rows);
 
+// gemm_umma.cu: the same product on the tcgen05 tensor cores, the weights
+// and the block sums in tensor memory, K split over a thread-block cluster.
+// cudaErrorNotSupported when K is above 16384, nb is not a multiple of 4,
+// or the device cannot hold one cluster.
+cudaError_t launch_gemm_q4_umma(const LaunchCtx &ctx, const void *wq, const float *wd, int nb,
+                                const int8_t *xq, const float *xd, int M, float *Y, int ldy, int r0,
+                                int r1, int rows);
+
 // q4k.cu: Q4_K-style super-blocks (per-256 activation quantiser; M = 1
 // product with the sub-block scales folded in int32; isum/msum non-null
 // selects the integer-sums test hook instead of y).

@@ -275,3 +275,33 @@ def test_gemm_small_m_unit_scales_exact(lib, Mr):
                           M.QAct(PT.to_dev(Xq), PT.to_dev(Xd), cols, Mr), Mr, 0, rows)
     want = P.decode_q4_elements(wq, cols) @ Xq.astype(np.int64).T   # [rows, Mr]
     assert np.array_equal(Y.cpu().numpy().astype(np.int64), want.T)
+
+
+@pytest.mark.skipif(os.environ.get("MLQ_GEMM_KERNEL") != "umma",
+                    reason="the tcgen05 small-M kernel's abort path; run by the forced-kernel test")
+def test_gemm_small_m_umma_timeout_path(lib):
+    """A wait limit of 0 makes the tcgen05 kernel's first wait give up: every
+    role leaves its loop, the producer drains its copies, the cluster meets
+    once more, the tensor memory is freed, and MLQ_E_TIMEOUT is recorded.
+    The next launch with the normal limit is clean and correct."""
+    M = lib
+    rng = np.random.default_rng(11)
+    Mr, rows, cols = 16, 512, 4096
+    wq, wd = rand_q4(rng, rows, cols)
+    Xq, Xd = oracle.quantize_q8(rand_x(rng, Mr, cols))
+    W = PT.weights_dev(oracle.Q4_0, wq, wd, rows, cols)
+    X = M.QAct(PT.to_dev(Xq), PT.to_dev(Xd), cols, Mr)
+    Y = torch.zeros((Mr, rows), dtype=torch.float32, device=PT.DEV)
+    assert M.mlq_last_device_error() == M.MLQ_OK
+    try:
+        M.mlq_debug_set_wait_limit_ns(0)
+        M.mlq_gemm_q4_small_m(Y, rows, W, X, Mr, 0, rows)
+        assert M.mlq_last_device_error() == M.MLQ_E_TIMEOUT
+        assert M.mlq_last_device_error() == M.MLQ_OK
+    finally:
+        M.mlq_debug_set_wait_limit_ns(10 ** 9)
+    M.mlq_gemm_q4_small_m(Y, rows, W, X, Mr, 0, rows)
+    Yg = Y.cpu().numpy()
+    for m in (0, 7, 15):
+        PT.check_matvec(oracle.Q4_0, wq, wd, rows, cols, Xq[m], Xd[m], 0, rows, y_gpu=Yg[m],
+                        what=f"after timeout m={m}")
