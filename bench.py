@@ -493,13 +493,16 @@ def run_ours(args, wl, world, rank, local, pg):
     dominant = "matvec_m1_kernel<Q4_0>" if r.m == 1 and any(
         m.spec.wtype == I.Q4_0 for m in r.mats) else (
         "matvec_m1_kernel<Q8_0>" if r.m == 1 else
-        "gemm_q4_mma_cluster_kernel" if r.m >= 8 else "gemm_q4_small_m_dp4a_kernel")
+        "gemm_q4_mma_cluster_kernel" if r.m >= 8 else
+        "gemm_q4_ring_kernel" if r.m <= 4 else "gemm_q4_small_m_dp4a_kernel")
     # the dominant kernel's sources and committed ncu summary (for the traffic figure)
     kernel_src = (("matvec.cu", "mlq_device.cuh") if r.m == 1 else
                   ("gemm_mma_cluster.cu", "mma_frag.cuh", "mlq_device.cuh") if r.m >= 8 else
+                  ("gemm_ring.cu", "phase_common.cuh", "mlq_device.cuh") if r.m <= 4 else
                   ("gemm_small_m.cu", "mlq_device.cuh"))
     kernel_profile = ("matvec_q4" if r.m == 1 else
-                      "gemm_mma_cluster" if r.m >= 8 else "gemm_small_m")
+                      "gemm_mma_cluster" if r.m >= 8 else
+                      "gemm_ring" if r.m <= 4 else "gemm_small_m")
     with torch.cuda.stream(stream):
         for c in range(copies):  # eager warm-up of every copy (kernel attributes, caches)
             one_pass(c)

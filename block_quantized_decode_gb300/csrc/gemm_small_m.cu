@@ -196,7 +196,10 @@ static cudaError_t launch_gemm_mm(const LaunchCtx &ctx, GemmArgs a) {
 // The tcgen05 kernel (gemm_umma.cu) is exact and tested but slower on these
 // shapes (28-34 us at M = 16): each of its N = 16 MMAs costs the full
 // instruction latency.
-// MLQ_GEMM_KERNEL=dp4a|mma|mma_ldg|umma overrides (A/B timing, tests).
+// Below M = 8 the ring kernel (gemm_ring.cu: activations in registers,
+// whole weight rows through a shared-memory ring) comes first for M <= 4;
+// this dp4a kernel takes the shapes it declines and M = 5..7.
+// MLQ_GEMM_KERNEL=dp4a|mma|mma_ldg|umma|ring overrides (A/B timing, tests).
 static int gemm_override() {
   static const int v = [] {
     const char *e = std::getenv("MLQ_GEMM_KERNEL");
@@ -205,6 +208,7 @@ static int gemm_override() {
     if (std::strcmp(e, "mma") == 0) return 2;
     if (std::strcmp(e, "mma_ldg") == 0) return 3;
     if (std::strcmp(e, "umma") == 0) return 4;
+    if (std::strcmp(e, "ring") == 0) return 5;
     return 0;
   }();
   return v;
@@ -226,6 +230,10 @@ cudaError_t launch_gemm_q4_small_m(const LaunchCtx &ctx, const void *wq, const f
     const cudaError_t e = launch_gemm_q4_mma_cluster(ctx, wq, wd, nb, xq, xd, M, Y, ldy, r0, r1, rows);
     if (e != cudaErrorNotSupported) return e;
     return launch_gemm_q4_mma(ctx, wq, wd, nb, xq, xd, M, Y, ldy, r0, r1);
+  }
+  if ((o == 0 || o == 5) && M <= 4) {
+    const cudaError_t e = launch_gemm_q4_ring(ctx, wq, wd, nb, xq, xd, M, Y, ldy, r0, r1);
+    if (e != cudaErrorNotSupported) return e;
   }
   GemmArgs a;
   a.wq = static_cast<const uint8_t *>(wq);

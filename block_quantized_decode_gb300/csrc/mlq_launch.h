@@ -176,6 +176,14 @@ cudaError_t launch_gemm_q4_mma_cluster(const LaunchCtx &ctx, const void *wq, con
                                        int nb, const int8_t *xq, const float *xd, int M, float *Y,
                                        int ldy, int r0, int r1, int rows);
 
+// gemm_ring.cu: M <= 4 activation rows against a Q4_0 matrix, the
+// activations in registers, whole weight rows streamed through a shared-
+// memory ring.  cudaErrorNotSupported when M > 4, nb is not a multiple of 4
+// or K needs more than 16 chunks of 32 (M > 2) or 64 (M <= 2) blocks.
+cudaError_t launch_gemm_q4_ring(const LaunchCtx &ctx, const void *wq, const float *wd, int nb,
+                                const int8_t *xq, const float *xd, int M, float *Y, int ldy, int r0,
+                                int r1);
+
 // gemm_umma.cu: the same product on the tcgen05 tensor cores, the weights
 // and the block sums in tensor memory, K split over a thread-block cluster.
 // cudaErrorNotSupported when K is above 16384, nb is not a multiple of 4,

@@ -28,7 +28,7 @@ def test_parity_with_forced_kernel(kernel):
 
 @pytest.mark.skipif(os.environ.get("MLQ_GEMM_KERNEL") is not None,
                     reason="already inside a forced-kernel run")
-@pytest.mark.parametrize("kernel", ["dp4a", "mma", "mma_ldg", "umma"])
+@pytest.mark.parametrize("kernel", ["dp4a", "mma", "mma_ldg", "umma", "ring"])
 def test_small_m_parity_with_forced_kernel(kernel):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
