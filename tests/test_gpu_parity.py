@@ -305,3 +305,33 @@ def test_gemm_small_m_umma_timeout_path(lib):
     for m in (0, 7, 15):
         PT.check_matvec(oracle.Q4_0, wq, wd, rows, cols, Xq[m], Xd[m], 0, rows, y_gpu=Yg[m],
                         what=f"after timeout m={m}")
+
+
+def test_gemm_small_m_ring_timeout_path(lib):
+    """M <= 4 runs the ring kernel: with a wait limit of 0 its consumers give
+    up on their first stage and its producer on its first refill; the
+    producer drains the copies it issued, MLQ_E_TIMEOUT is recorded, and the
+    next launch with the normal limit is clean and correct."""
+    if os.environ.get("MLQ_GEMM_KERNEL") not in (None, "ring"):
+        pytest.skip("another small-M kernel is forced")
+    M = lib
+    rng = np.random.default_rng(12)
+    Mr, rows, cols = 4, 2048, 4096
+    wq, wd = rand_q4(rng, rows, cols)
+    Xq, Xd = oracle.quantize_q8(rand_x(rng, Mr, cols))
+    W = PT.weights_dev(oracle.Q4_0, wq, wd, rows, cols)
+    X = M.QAct(PT.to_dev(Xq), PT.to_dev(Xd), cols, Mr)
+    Y = torch.zeros((Mr, rows), dtype=torch.float32, device=PT.DEV)
+    assert M.mlq_last_device_error() == M.MLQ_OK
+    try:
+        M.mlq_debug_set_wait_limit_ns(0)
+        M.mlq_gemm_q4_small_m(Y, rows, W, X, Mr, 0, rows)
+        assert M.mlq_last_device_error() == M.MLQ_E_TIMEOUT
+        assert M.mlq_last_device_error() == M.MLQ_OK
+    finally:
+        M.mlq_debug_set_wait_limit_ns(10 ** 9)
+    M.mlq_gemm_q4_small_m(Y, rows, W, X, Mr, 0, rows)
+    Yg = Y.cpu().numpy()
+    for m in range(Mr):
+        PT.check_matvec(oracle.Q4_0, wq, wd, rows, cols, Xq[m], Xd[m], 0, rows, y_gpu=Yg[m],
+                        what=f"after timeout m={m}")
