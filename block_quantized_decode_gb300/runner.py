@@ -44,6 +44,13 @@ class WorkloadRunner:
         self.x_pinned: dict[str, torch.Tensor] = {}
         self.fp32: dict[str, torch.Tensor] = {}   # float32 vectors feeding a quantize
         self.qbuf: dict[str, B.QAct] = {}
+        # every product's output is a view of one buffer (128-byte aligned
+        # offsets), so one copy brings all of them to the host
+        self.y_offs, tot = [], 0
+        for mv in wl.mats:
+            self.y_offs.append(tot)
+            tot += (self.m * mv.rows + 31) // 32 * 32
+        self.y_all = torch.zeros(tot, dtype=torch.float32, device=self.dev)
         for i, mv in enumerate(wl.mats):
             src = f"x{mv.cols}" if mv.input_of == "x" else mv.input_of
             if mv.input_of == "x" and src not in self.x_host:
@@ -57,7 +64,7 @@ class WorkloadRunner:
             for _ in range(copies):
                 qs.append(torch.from_numpy(hq.reshape(-1)).to(self.dev))
                 ds.append(torch.from_numpy(hd.reshape(-1)).to(self.dev))
-            y = torch.zeros((self.m, mv.rows), dtype=torch.float32, device=self.dev)
+            y = self.y_all[self.y_offs[i]: self.y_offs[i] + self.m * mv.rows].view(self.m, mv.rows)
             self.mats.append(_Mat(mv, src, qs, ds, y, hq, hd))
         for m in self.mats:
             self.fp32.setdefault(m.spec.name, m.y)
@@ -194,7 +201,7 @@ class WorkloadRunner:
         return sum(t.numel() * 4 for t in self.x_pinned.values())
 
     def d2h_bytes(self) -> int:
-        return sum(m.y.numel() * 4 for m in self.mats)
+        return self.y_all.numel() * 4
 
     # ---- one pass --------------------------------------------------------------
     def weight_ranges(self, i: int, copy: int = 0):
@@ -253,11 +260,14 @@ class WorkloadRunner:
                 self.fp32[src].copy_(t, non_blocking=True)
 
     def outputs_to_host(self, host: dict | None = None) -> dict:
-        host = {} if host is None else host
-        for m in self.mats:
-            if m.spec.name not in host:
-                host[m.spec.name] = torch.empty(m.y.shape, dtype=torch.float32).pin_memory()
-            host[m.spec.name].copy_(m.y, non_blocking=True)
+        """Every product's output to pinned host memory in one D2H copy (the
+        outputs are views of one device buffer); returns {name: host view}."""
+        if host is None:
+            flat = torch.empty(self.y_all.numel(), dtype=torch.float32).pin_memory()
+            host = {"_flat": flat}
+            for m, off in zip(self.mats, self.y_offs):
+                host[m.spec.name] = flat[off: off + m.y.numel()].view(m.y.shape)
+        host["_flat"].copy_(self.y_all, non_blocking=True)
         return host
 
 
