@@ -254,6 +254,52 @@ __device__ __forceinline__ void rows4_q4(float acc[4], const uint8_t *wq_s, cons
 
 // Four per-lane partial sums -> four warp sums.  Lane l returns the sum of
 // row (l >> 3) & 3; fixed order, so the result is deterministic.
+// rows4_q4 for Q8_0 weights: the same block arithmetic as row_part<0>,
+// with the shared-memory loads of the four rows issued before any dp4a.
+__device__ __forceinline__ void rows4_q8(float acc[4], const uint8_t *wq_s, const float *wd_s,
+                                         size_t rowq, int nb, int r0, int G, int nr,
+                                         const XChunk &c, int u0, int lane) {
+  const uint8_t *wr[4];
+  const float *dr[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int row = min(r0 + G * j, nr - 1);
+    wr[j] = wq_s + static_cast<size_t>(row) * rowq;
+    dr[j] = wd_s + static_cast<size_t>(row) * nb;
+    acc[j] = 0.0f;
+  }
+  const int h = (lane >> 2) & 1;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    if (!c.v[k]) continue;
+    const int u = u0 + 32 * k;
+    uint4 w0[4], w1[4];
+    float dw[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      w0[j] = *reinterpret_cast<const uint4 *>(wr[j] + u * 32 + 16 * h);
+      w1[j] = *reinterpret_cast<const uint4 *>(wr[j] + u * 32 + 16 * (h ^ 1));
+      dw[j] = dr[j][u];
+    }
+    const int4 xa = c.x[k][0], xb = c.x[k][1];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int s = __dp4a(static_cast<int>(w0[j].x), xa.x, c.adj[k]);
+      s = __dp4a(static_cast<int>(w0[j].y), xa.y, s);
+      s = __dp4a(static_cast<int>(w0[j].z), xa.z, s);
+      s = __dp4a(static_cast<int>(w0[j].w), xa.w, s);
+      s = __dp4a(static_cast<int>(w1[j].x), xb.x, s);
+      s = __dp4a(static_cast<int>(w1[j].y), xb.y, s);
+      s = __dp4a(static_cast<int>(w1[j].z), xb.z, s);
+      s = __dp4a(static_cast<int>(w1[j].w), xb.w, s);
+      const float sumi = __fsub_rn(__int_as_float(s), kMagic);
+      acc[j] = __fmaf_rn(__fmul_rn(sumi, dw[j]), c.d[k], acc[j]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = r0 + G * j < nr ? acc[j] : 0.0f;
+}
+
 __device__ __forceinline__ float reduce4(float a0, float a1, float a2, float a3, int lane) {
   const bool b4 = (lane & 16) != 0;
   float k0 = b4 ? a2 : a0, k1 = b4 ? a3 : a1;

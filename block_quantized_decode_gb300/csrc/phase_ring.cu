@@ -194,13 +194,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
     if (QT == 1) {
       rows4_q4(acc, wq_s, wd_s, rowq, nb, g, G, n, xc, u0);
     } else {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int row = g + G * q;
-        acc[q] = row < n ? row_part<QT>(wq_s + static_cast<size_t>(row) * rowq,
-                                        wd_s + static_cast<size_t>(row) * nb, xc, u0, lane)
-                         : 0.0f;
-      }
+      rows4_q8(acc, wq_s, wd_s, rowq, nb, g, G, n, xc, u0, lane);
     }
     const float v = reduce4(acc[0], acc[1], acc[2], acc[3], lane);
     const int row = g + G * (lane >> 3);
