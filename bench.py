@@ -1012,28 +1012,38 @@ def run_q4k(args, wl, world, rank, local, pg):
     del probe
     copies = args.copies or max(2, math.ceil(3 * l2 / wbytes))
     r = Q4KRunner(wl, copies=copies, device=f"cuda:{local}")
+    # Q4_K-style passes run as phases by default (mlq_q4k_phase: products
+    # sharing an input in one launch that quantises it); --path calls keeps
+    # one quantiser launch per input and one launch per product.
+    phase = not nbits and args.path in ("auto", "phase")
+
+    def one_pass(c):
+        if phase:
+            r.step_phase(copy=c, stream=stream)
+        else:
+            r.step(copy=c, stream=stream)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         for c in range(copies):
-            r.step(copy=c, stream=stream)
+            one_pass(c)
     stream.synchronize()
     graphs, cycle = [], None
     if not args.no_graph:
         for c in range(copies):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                r.step(copy=c, stream=stream)
+                one_pass(c)
             graphs.append(g)
         cycle = torch.cuda.CUDAGraph()
         with torch.cuda.graph(cycle, stream=stream):
             for c in range(copies):
-                r.step(copy=c, stream=stream)
+                one_pass(c)
 
     def do_step(i):
         if graphs:
             graphs[i % copies].replay()
         else:
-            r.step(copy=i % copies, stream=stream)
+            one_pass(i % copies)
 
     def do_steps(n):
         i = 0
@@ -1121,7 +1131,7 @@ def run_q4k(args, wl, world, rank, local, pg):
 
     def e2e_body(c):
         r.x.copy_(r.x_pinned, non_blocking=True)
-        r.step(copy=c, stream=stream)
+        one_pass(c)
         host_y.copy_(r.y[last], non_blocking=True)
     e2e_step = e2e_graph_steps(args, copies, stream, e2e_body)
     e2e_steps = min(steps, 500)
@@ -1164,11 +1174,11 @@ def run_q4k(args, wl, world, rank, local, pg):
                        "l2": f"inputs larger than L2: {copies} rotating weight copies "
                              f"({copies * wbytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
                        "graphs": ("one graph per cycle of %d steps" % copies) if cycle is not None else False,
-                       "path": "calls", "static_weights": os.environ.get("MLQ_STATIC_WEIGHTS") == "1",
+                       "path": "phase" if phase else "calls", "static_weights": os.environ.get("MLQ_STATIC_WEIGHTS") == "1",
                        "parallelism": f"replicas x{world} (independent decode streams)"},
             "gops": world * r.ops() * steps / (ms_max / 1e3) / 1e9, "hbm_frac": value / world / hbm,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": r.launches_per_step * steps,
+            "gpu_launches": (len(r.phases()) if phase else r.launches_per_step) * steps,
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)

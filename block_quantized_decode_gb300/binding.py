@@ -30,7 +30,7 @@ EXPORTS = (
     "mlq_decode_chain_static", "mlq_decode_phase",
     "mlq_rmsnorm", "mlq_add_rmsnorm", "mlq_add", "mlq_softmax", "mlq_silu_mul",
     "mlq_rope_tables", "mlq_rope", "mlq_attention",
-    "mlq_quantize_q8k", "mlq_matvec_q4k", "mlq_block_sums_q4k",
+    "mlq_quantize_q8k", "mlq_matvec_q4k", "mlq_block_sums_q4k", "mlq_q4k_phase",
     "mlq_quantize_blk", "mlq_matvec_nbits", "mlq_block_sumi_nbits",
     "mlq_debug_chain_plan",
 )
@@ -62,6 +62,10 @@ class _QAct(ctypes.Structure):
 class _Q4KTensor(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("s", ctypes.c_void_p), ("d", ctypes.c_void_p),
                 ("dmin", ctypes.c_void_p), ("rows", ctypes.c_int), ("cols", ctypes.c_int)]
+
+
+class _Q4KProduct(ctypes.Structure):
+    _fields_ = [("W", _Q4KTensor), ("y", ctypes.c_void_p)]
 
 
 class _Q8KAct(ctypes.Structure):
@@ -145,6 +149,7 @@ def lib() -> ctypes.CDLL:
         L.mlq_quantize_q8k.argtypes = [KA, P, I, P]
         L.mlq_matvec_q4k.argtypes = [P, KT, KA, I, I, P]
         L.mlq_block_sums_q4k.argtypes = [P, P, KT, KA, I, I, P]
+        L.mlq_q4k_phase.argtypes = [P, I, ctypes.POINTER(_Q4KProduct), I, P]
         NT, BA = ctypes.POINTER(_NBitsTensor), ctypes.POINTER(_BlkAct)
         L.mlq_quantize_blk.argtypes = [BA, P, I, P]
         L.mlq_matvec_nbits.argtypes = [P, NT, BA, I, I, P]
@@ -300,6 +305,12 @@ def mlq_block_sums_q4k(isum, msum, W: Q4KTensor, x: Q8KAct, r0: int, r1: int, st
     cw, cx = W.c(), x.c()
     _check(lib().mlq_block_sums_q4k(_addr(isum), _addr(msum), ctypes.byref(cw), ctypes.byref(cx), r0,
                                     r1, _stream(stream)), "mlq_block_sums_q4k")
+
+
+def mlq_q4k_phase(x, k: int, products, stream=None) -> None:
+    """products: [(Q4KTensor, y), ...] (1..4) sharing the float input x."""
+    arr = (_Q4KProduct * len(products))(*[_Q4KProduct(W.c(), _addr(y)) for W, y in products])
+    _check(lib().mlq_q4k_phase(_addr(x), k, arr, len(products), _stream(stream)), "mlq_q4k_phase")
 
 
 # ---- block length 32 / 128, float16 scales, signed-offset 8-bit ------------

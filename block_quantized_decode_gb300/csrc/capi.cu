@@ -488,6 +488,29 @@ mlq_status mlq_block_sums_q4k(int32_t *isum, int32_t *msum, const mlq_q4k_tensor
   return q4k_common(nullptr, isum, msum, W, x, r0, r1, stream);
 }
 
+mlq_status mlq_q4k_phase(const float *x, int k, const mlq_q4k_product *products, int nproducts,
+                         void *stream) {
+  if (x == nullptr || products == nullptr) return MLQ_E_NULL;
+  if (nproducts < 1 || nproducts > 4 || !q4k_cols_ok(k)) return MLQ_E_SHAPE;
+  if (!aligned(x, 16)) return MLQ_E_ALIGN;
+  mlq::Q4KProductDev p[4];
+  for (int j = 0; j < nproducts; ++j) {
+    const mlq_q4k_tensor &W = products[j].W;
+    if (products[j].y == nullptr || W.q == nullptr || W.s == nullptr || W.d == nullptr ||
+        W.dmin == nullptr)
+      return MLQ_E_NULL;
+    if (W.cols != k || W.rows < 0) return MLQ_E_SHAPE;
+    if (!aligned(W.q, 16) || !aligned(W.s, 16) || !aligned(W.d, 4) || !aligned(W.dmin, 4) ||
+        !aligned(products[j].y, 4))
+      return MLQ_E_ALIGN;
+    p[j] = mlq::Q4KProductDev{W.q, W.s, W.d, W.dmin, products[j].y, W.rows};
+  }
+  mlq::LaunchCtx ctx;
+  mlq_status s = make_ctx(&ctx, stream);
+  if (s != MLQ_OK) return s;
+  return from_cuda(mlq::launch_phase_q4k(ctx, x, k / 256, p, nproducts));
+}
+
 // ---- block length 32 / 128, float16 scales, signed-offset 8-bit ---------------
 namespace {
 mlq_status check_nbits(const mlq_nbits_tensor *W, const mlq_blk_act *x, int r0, int r1) {

@@ -201,6 +201,17 @@ cudaError_t launch_matvec_q4k(const LaunchCtx &ctx, const void *wq, const void *
                               const float *wdmin, int nsb, const int8_t *xq, const float *xd,
                               const int32_t *xbs, float *y, int32_t *isum, int32_t *msum, int r0,
                               int r1);
+// A Q4_K-style phase: up to 4 products sharing the float input x (nsb
+// super-blocks), every CTA quantising x itself; product j writes rows
+// 0 .. rows_j of y_j.
+struct Q4KProductDev {
+  const void *q, *s;
+  const float *d, *dmin;
+  float *y;
+  int rows;
+};
+cudaError_t launch_phase_q4k(const LaunchCtx &ctx, const float *x, int nsb, const Q4KProductDev *p,
+                             int np);
 
 // nbits.cu: blocks of 32 or 128, float32 / binary16 scales, 4-bit or
 // signed-offset 8-bit weights (sumi non-null: the integer test hook).

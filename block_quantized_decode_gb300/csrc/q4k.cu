@@ -54,13 +54,11 @@ constexpr size_t kKStageTarget = 32 * 1024;
 // ---- quantiser ------------------------------------------------------------
 // One warp per 256-element block; lane l holds elements 8l .. 8l + 7, and
 // the four lanes of each 32-element sub-block add their quants for bsums.
-__global__ void __launch_bounds__(256) quantize_q8k_kernel(const float *__restrict__ x, int8_t *q,
-                                                           float *d, int32_t *bsums, int nblocks) {
-  const int blk = static_cast<int>((blockIdx.x * static_cast<unsigned>(blockDim.x) + threadIdx.x) >> 5);
-  const int lane = threadIdx.x & 31;
-  griddep_wait();
-  if (blk >= nblocks) return;
-  const float4 *src = reinterpret_cast<const float4 *>(x + static_cast<size_t>(blk) * kQKK + lane * 8);
+// Returns the lane's 8 quants; *d = the block's scale; *sum = its sub-block's
+// quant sum (in every lane).  Used by the quantiser kernel and by the phase
+// kernel's in-CTA quantisation alike.
+__device__ __forceinline__ uint2 q8k_block(const float *xb, int lane, float *d, int *sum_out) {
+  const float4 *src = reinterpret_cast<const float4 *>(xb + lane * 8);
   const float4 a = src[0], b = src[1];
   const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
   uint32_t m = 0;
@@ -83,9 +81,23 @@ __global__ void __launch_bounds__(256) quantize_q8k_kernel(const float *__restri
              (static_cast<uint32_t>(qs[3] & 0xff) << 24);
   packed.y = (qs[4] & 0xff) | ((qs[5] & 0xff) << 8) | ((qs[6] & 0xff) << 16) |
              (static_cast<uint32_t>(qs[7] & 0xff) << 24);
-  *reinterpret_cast<uint2 *>(q + static_cast<size_t>(blk) * kQKK + lane * 8) = packed;
   sum += __shfl_xor_sync(0xffffffffu, sum, 1);
   sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+  *d = dd;
+  *sum_out = sum;
+  return packed;
+}
+
+__global__ void __launch_bounds__(256) quantize_q8k_kernel(const float *__restrict__ x, int8_t *q,
+                                                           float *d, int32_t *bsums, int nblocks) {
+  const int blk = static_cast<int>((blockIdx.x * static_cast<unsigned>(blockDim.x) + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  griddep_wait();
+  if (blk >= nblocks) return;
+  float dd;
+  int sum;
+  const uint2 packed = q8k_block(x + static_cast<size_t>(blk) * kQKK, lane, &dd, &sum);
+  *reinterpret_cast<uint2 *>(q + static_cast<size_t>(blk) * kQKK + lane * 8) = packed;
   if ((lane & 3) == 0) bsums[static_cast<size_t>(blk) * kKSubs + (lane >> 2)] = sum;
   if (lane == 0) d[blk] = dd;
 }
@@ -100,15 +112,22 @@ cudaError_t launch_quantize_q8k(const LaunchCtx &ctx, const float *x, int8_t *q,
 }
 
 // ---- product ----------------------------------------------------------------
+constexpr int kKMaxProducts = 4;
+// The launch's rows: products j = 0 .. nprod-1, rows rbase[j] .. rbase[j] +
+// rows[j] of each, one after another ([0, total) over all of them); every
+// product reads the same input.
 struct Q4KArgs {
-  const uint8_t *wq, *ws;
-  const float *wd, *wdmin;
-  const int8_t *xq;
+  const uint8_t *wq[kKMaxProducts], *ws[kKMaxProducts];
+  const float *wd[kKMaxProducts], *wdmin[kKMaxProducts];
+  float *y[kKMaxProducts];
+  int rbase[kKMaxProducts], rows[kKMaxProducts];
+  int nprod, total;
+  const float *xf;       // float input quantised in each CTA (a phase), or null:
+  const int8_t *xq;      // the quantised input (quants, scales, sub-block sums)
   const float *xd;
   const int32_t *xbs;
-  float *y;
-  int32_t *isum, *msum;  // test hook: per-super-block integer sums instead of y
-  int nsb, r0, r1;
+  int32_t *isum, *msum;  // test hook (one product): per-super-block integer sums instead of y
+  int nsb;
   int R, ns;                                    // rows per stage, ring slots
   int P;                                        // parts per row (P > 1: partial sums in smem_part)
   int early;                                    // weights not written by earlier work
@@ -142,6 +161,20 @@ __device__ __forceinline__ bool k_wait(uint32_t bar, uint32_t parity, const vola
   }
 }
 
+// The stage of at most R rows that starts at row r of [0, total) and ends
+// before rb and before the end of r's product: returns its row count, with
+// *j its product and *lrow its first row in that product.
+__device__ __forceinline__ int k_stage(const Q4KArgs &a, int r, int rb, int R, int *j, int *lrow) {
+  int jj = 0, off = 0;
+  while (jj + 1 < a.nprod && r >= off + a.rows[jj]) {
+    off += a.rows[jj];
+    ++jj;
+  }
+  *j = jj;
+  *lrow = a.rbase[jj] + (r - off);
+  return min(R, min(rb, off + a.rows[jj]) - r);
+}
+
 template <bool SUMS>
 __global__ void __launch_bounds__(kKThreads, 2) matvec_q4k_kernel(const __grid_constant__ Q4KArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -152,9 +185,9 @@ __global__ void __launch_bounds__(kKThreads, 2) matvec_q4k_kernel(const __grid_c
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nsb = a.nsb, nsub = nsb * kKSubs, K = nsb * kQKK;
   const size_t rowq = static_cast<size_t>(nsb) * (kQKK / 2), rows_s = static_cast<size_t>(nsb) * 16;
-  const int n_all = a.r1 - a.r0;
-  const int ra = a.r0 + static_cast<int>(static_cast<long long>(n_all) * blockIdx.x / gridDim.x);
-  const int rb = a.r0 + static_cast<int>(static_cast<long long>(n_all) * (blockIdx.x + 1) / gridDim.x);
+  const int n_all = a.total;
+  const int ra = static_cast<int>(static_cast<long long>(n_all) * blockIdx.x / gridDim.x);
+  const int rb = static_cast<int>(static_cast<long long>(n_all) * (blockIdx.x + 1) / gridDim.x);
   const int R = a.R, ns = a.ns;
   int8_t *xq_s = reinterpret_cast<int8_t *>(smem);
   int32_t *xbs_s = reinterpret_cast<int32_t *>(smem + K);
@@ -177,9 +210,10 @@ __global__ void __launch_bounds__(kKThreads, 2) matvec_q4k_kernel(const __grid_c
   if (warp == kKWarps) {
     // ------------------------------ producer ------------------------------
     if (!a.early) griddep_wait();  // weights written by earlier work: wait for it first
-    int s = 0;
-    for (int r = ra; r < rb; r += R, ++s) {
-      const int n = min(R, rb - r);
+    int s = 0, n = 0;
+    for (int r = ra; r < rb; r += n, ++s) {
+      int j, lrow;
+      n = k_stage(a, r, rb, R, &j, &lrow);
       const int slot = s % ns;
       if (s >= ns && !warp_wait([&] {
             return k_wait(smem_addr(&empty_bar[slot]), ((s / ns) - 1) & 1, abort_v, a.wait_ns);
@@ -193,14 +227,14 @@ __global__ void __launch_bounds__(kKThreads, 2) matvec_q4k_kernel(const __grid_c
       if (lane == 0) {
         const uint32_t qb = static_cast<uint32_t>(n * rowq), sb = static_cast<uint32_t>(n * rows_s);
         mbar_arrive_expect_tx(fb, qb + sb);
-        bulk_copy_g2s(smem_addr(dst), a.wq + static_cast<size_t>(r) * rowq, qb, fb);
-        bulk_copy_g2s(smem_addr(dst + a.stage_s), a.ws + static_cast<size_t>(r) * rows_s, sb, fb);
+        bulk_copy_g2s(smem_addr(dst), a.wq[j] + static_cast<size_t>(lrow) * rowq, qb, fb);
+        bulk_copy_g2s(smem_addr(dst + a.stage_s), a.ws[j] + static_cast<size_t>(lrow) * rows_s, sb, fb);
       }
       float *dd = reinterpret_cast<float *>(dst + a.stage_d);
       float *dm = dd + static_cast<size_t>(R) * nsb;
       for (int e = lane; e < n * nsb; e += 32) {
-        cp_async4(dd + e, a.wd + static_cast<size_t>(r) * nsb + e);
-        cp_async4(dm + e, a.wdmin + static_cast<size_t>(r) * nsb + e);
+        cp_async4(dd + e, a.wd[j] + static_cast<size_t>(lrow) * nsb + e);
+        cp_async4(dm + e, a.wdmin[j] + static_cast<size_t>(lrow) * nsb + e);
       }
       cp_async_arrive(fb);
     }
@@ -217,7 +251,19 @@ __global__ void __launch_bounds__(kKThreads, 2) matvec_q4k_kernel(const __grid_c
   // The activation quants in shared memory: sub-block u at u*32, its two
   // 16-byte halves swapped when bit 2 of u is set, so that the 8 lanes of a
   // quarter warp (sub-blocks u .. u+7) read distinct banks.
-  {  // all loads before any store
+  if (a.xf != nullptr) {
+    // a phase: every CTA quantises the float input itself, one warp per
+    // 256-element block, with the quantiser kernel's own arithmetic
+    for (int blk = warp; blk < nsb; blk += kKWarps) {
+      float dd;
+      int sum;
+      const uint2 packed = q8k_block(a.xf + static_cast<size_t>(blk) * kQKK, lane, &dd, &sum);
+      const int u = blk * 16 + (lane >> 1);  // the lane's 16-byte unit, placed as in the loads below
+      *reinterpret_cast<uint2 *>(xq_s + (u ^ ((u >> 3) & 1)) * 16 + (lane & 1) * 8) = packed;
+      if ((lane & 3) == 0) xbs_s[blk * kKSubs + (lane >> 2)] = sum;
+      if (lane == 0) xd_s[blk] = dd;
+    }
+  } else {  // all loads before any store
     const int uq = K / 16, ub = nsub / 4;
     for (int base = 0; base < uq + ub; base += 2 * kKWarps * 32) {
       int4 v[2];
@@ -238,9 +284,10 @@ __global__ void __launch_bounds__(kKThreads, 2) matvec_q4k_kernel(const __grid_c
   }
   k_consumers_sync();
 
-  int s = 0;
-  for (int r = ra; r < rb; r += R, ++s) {
-    const int n = min(R, rb - r);
+  int s = 0, n = 0;
+  for (int r = ra; r < rb; r += n, ++s) {
+    int j, lrow;
+    n = k_stage(a, r, rb, R, &j, &lrow);
     const int slot = s % ns;
     if (!warp_wait([&] { return k_wait(smem_addr(&full_bar[slot]), (s / ns) & 1, abort_v, a.wait_ns); })) {
       if (lane == 0 && atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
@@ -297,8 +344,8 @@ __global__ void __launch_bounds__(kKThreads, 2) matvec_q4k_kernel(const __grid_c
           if (u < nsub && (lane & 7) == 0) {
             const int B = u >> 3;
             if (SUMS) {
-              a.isum[static_cast<size_t>(r + i - a.r0) * nsb + B] = is[h];
-              a.msum[static_cast<size_t>(r + i - a.r0) * nsb + B] = ms[h];
+              a.isum[static_cast<size_t>(lrow + i - a.rbase[0]) * nsb + B] = is[h];
+              a.msum[static_cast<size_t>(lrow + i - a.rbase[0]) * nsb + B] = ms[h];
             } else {
               const float t = __fmul_rn(__int2float_rn(is[h]), std_[static_cast<size_t>(i) * nsb + B]);
               const float um = __fmul_rn(__int2float_rn(ms[h]), stm[static_cast<size_t>(i) * nsb + B]);
@@ -311,7 +358,7 @@ __global__ void __launch_bounds__(kKThreads, 2) matvec_q4k_kernel(const __grid_c
         acc += __shfl_xor_sync(0xffffffffu, acc, 8);
         acc += __shfl_xor_sync(0xffffffffu, acc, 16);
         if (lane == 0) {
-          if (P == 1) a.y[r + i] = acc;
+          if (P == 1) a.y[j][lrow + i] = acc;
           else part_s[static_cast<size_t>(r + i - ra) * P + part] = acc;
         }
       }
@@ -325,18 +372,20 @@ __global__ void __launch_bounds__(kKThreads, 2) matvec_q4k_kernel(const __grid_c
     for (int i = tid; i < rb - ra; i += kKWarps * 32) {
       float v = part_s[static_cast<size_t>(i) * P];
       for (int p = 1; p < P; ++p) v = __fadd_rn(v, part_s[static_cast<size_t>(i) * P + p]);
-      a.y[ra + i] = v;
+      int j, lrow;
+      k_stage(a, ra + i, rb, 1, &j, &lrow);
+      a.y[j][lrow] = v;
     }
   }
 }
 
-cudaError_t launch_matvec_q4k(const LaunchCtx &ctx, const void *wq, const void *ws, const float *wd,
-                              const float *wdmin, int nsb, const int8_t *xq, const float *xd,
-                              const int32_t *xbs, float *y, int32_t *isum, int32_t *msum, int r0,
-                              int r1) {
-  const int n = r1 - r0;
+// Geometry of a launch over a.total rows of a.nsb super-blocks (a's products
+// and input already filled), then the launch.
+static cudaError_t launch_q4k_common(const LaunchCtx &ctx, Q4KArgs &a, bool sums) {
+  const int n = a.total;
+  const int nsb = a.nsb;
   if (n <= 0) return cudaSuccess;
-  auto up = [](size_t v, size_t a) { return (v + a - 1) / a * a; };
+  auto up = [](size_t v, size_t al) { return (v + al - 1) / al * al; };
   const size_t K = static_cast<size_t>(nsb) * kQKK;
   const size_t rowq = static_cast<size_t>(nsb) * (kQKK / 2), rows_s = static_cast<size_t>(nsb) * 16;
   const size_t rowbytes = rowq + rows_s + 8 * static_cast<size_t>(nsb);
@@ -354,7 +403,7 @@ cudaError_t launch_matvec_q4k(const LaunchCtx &ctx, const void *wq, const void *
   int P = R >= kKWarps ? 1 : kKWarps / R;
   if (P > cols64) P = cols64;
   if (P < 1) P = 1;
-  size_t part = isum != nullptr || P == 1 ? 0 : up(static_cast<size_t>(rows_cta) * P * 4, 128);
+  size_t part = sums || P == 1 ? 0 : up(static_cast<size_t>(rows_cta) * P * 4, 128);
   if (part > 32 * 1024) {  // very many rows per CTA: whole rows per warp
     P = 1;
     part = 0;
@@ -366,22 +415,9 @@ cudaError_t launch_matvec_q4k(const LaunchCtx &ctx, const void *wq, const void *
   if (xs + part + 2 * stage > budget) return cudaErrorNotSupported;
   int ns = static_cast<int>((budget - xs - part) / stage);
   if (ns > kKSlots) ns = kKSlots;
-  const int stages_cta = (rows_cta + R - 1) / R;
+  // stages per CTA, counted with the breaks at product boundaries
+  const int stages_cta = (rows_cta + R - 1) / R + a.nprod - 1;
   if (ns > stages_cta) ns = stages_cta < 2 ? 2 : stages_cta;
-  Q4KArgs a;
-  a.wq = static_cast<const uint8_t *>(wq);
-  a.ws = static_cast<const uint8_t *>(ws);
-  a.wd = wd;
-  a.wdmin = wdmin;
-  a.xq = xq;
-  a.xd = xd;
-  a.xbs = xbs;
-  a.y = y;
-  a.isum = isum;
-  a.msum = msum;
-  a.nsb = nsb;
-  a.r0 = r0;
-  a.r1 = r1;
   a.R = R;
   a.ns = ns;
   a.stage_bytes = static_cast<unsigned>(stage);
@@ -394,12 +430,57 @@ cudaError_t launch_matvec_q4k(const LaunchCtx &ctx, const void *wq, const void *
   a.status = ctx.status;
   a.wait_ns = ctx.wait_ns;
   const size_t smem = xs + part + static_cast<size_t>(ns) * stage;
-  auto kern = isum != nullptr ? matvec_q4k_kernel<true> : matvec_q4k_kernel<false>;
+  auto kern = sums ? matvec_q4k_kernel<true> : matvec_q4k_kernel<false>;
   prefer_max_shared(kern);
   const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kKThreads), smem, ctx, a);
+}
+
+cudaError_t launch_matvec_q4k(const LaunchCtx &ctx, const void *wq, const void *ws, const float *wd,
+                              const float *wdmin, int nsb, const int8_t *xq, const float *xd,
+                              const int32_t *xbs, float *y, int32_t *isum, int32_t *msum, int r0,
+                              int r1) {
+  Q4KArgs a = {};
+  a.wq[0] = static_cast<const uint8_t *>(wq);
+  a.ws[0] = static_cast<const uint8_t *>(ws);
+  a.wd[0] = wd;
+  a.wdmin[0] = wdmin;
+  a.y[0] = y;
+  a.rbase[0] = r0;
+  a.rows[0] = r1 - r0;
+  a.nprod = 1;
+  a.total = r1 - r0;
+  a.xf = nullptr;
+  a.xq = xq;
+  a.xd = xd;
+  a.xbs = xbs;
+  a.isum = isum;
+  a.msum = msum;
+  a.nsb = nsb;
+  return launch_q4k_common(ctx, a, isum != nullptr);
+}
+
+cudaError_t launch_phase_q4k(const LaunchCtx &ctx, const float *x, int nsb, const Q4KProductDev *p,
+                             int np) {
+  if (np < 1 || np > kKMaxProducts) return cudaErrorInvalidValue;
+  Q4KArgs a = {};
+  a.total = 0;
+  for (int j = 0; j < np; ++j) {
+    a.wq[j] = static_cast<const uint8_t *>(p[j].q);
+    a.ws[j] = static_cast<const uint8_t *>(p[j].s);
+    a.wd[j] = p[j].d;
+    a.wdmin[j] = p[j].dmin;
+    a.y[j] = p[j].y;
+    a.rbase[j] = 0;
+    a.rows[j] = p[j].rows;
+    a.total += p[j].rows;
+  }
+  a.nprod = np;
+  a.xf = x;
+  a.nsb = nsb;
+  return launch_q4k_common(ctx, a, false);
 }
 
 }  // namespace mlq

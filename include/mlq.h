@@ -210,6 +210,22 @@ mlq_status mlq_matvec_q4k(float *y, const mlq_q4k_tensor *W, const mlq_q8k_act *
 mlq_status mlq_block_sums_q4k(int32_t *isum, int32_t *msum, const mlq_q4k_tensor *W,
                               const mlq_q8k_act *x, int r0, int r1, void *stream);
 
+/* A Q4_K-style decode phase (the phase of mlq_decode_phase, Design Spec
+ * Sec. 6 "Forward pass": products that read one activation): for each of
+ * the nproducts (1..4) products, y_j = W_j * Q8K(x), every row of W_j,
+ * where Q8K(x) is exactly what mlq_quantize_q8k writes for x and the
+ * product is computed as mlq_matvec_q4k computes it.  One launch: every
+ * CTA quantises x itself, so no quantiser launch precedes it.
+ * x: k float32, device, 16-byte aligned; every W_j->cols == k (a positive
+ * multiple of 256, at most MLQ_MAX_COLS); y_j: W_j->rows float32, 4-byte
+ * aligned, owned by the caller.  Tensors as for mlq_matvec_q4k. */
+typedef struct {
+    mlq_q4k_tensor W;
+    float *y;
+} mlq_q4k_product;
+mlq_status mlq_q4k_phase(const float *x, int k, const mlq_q4k_product *products, int nproducts,
+                         void *stream);
+
 /* ---- block length 32 / 128, float16 scales, signed-offset 8-bit -------- */
 /* Page "ONNX Runtime" (SpaceMiT X60), "How we got there": item 3 (AMD's
  * Qwen2.5-0.5B export uses block_size 128; int8 activations), item 4

@@ -335,6 +335,25 @@ def test_validation_q4k(M):
     assert qk(ka(n=512), k=256) == M.MLQ_E_SHAPE
     assert qk(ka(), x=6 * A + 4) == M.MLQ_E_ALIGN
     assert qk(ka(d=4 * A + 4)) == M.MLQ_E_ALIGN
+    # the Q4_K-style phase: products sharing one float input
+    from block_quantized_decode_gb300.binding import _Q4KProduct
+
+    def ph(x=6 * A, k=512, prods=None, n=None):
+        prods = [_Q4KProduct(kt(), 5 * A)] if prods is None else prods
+        arr = (_Q4KProduct * max(1, len(prods)))(*prods)
+        return call(M, "mlq_q4k_phase", x, k, arr, len(prods) if n is None else n, None)
+
+    assert ph(x=None) == M.MLQ_E_NULL
+    assert ph(prods=[_Q4KProduct(kt(), 0)]) == M.MLQ_E_NULL
+    assert ph(prods=[_Q4KProduct(kt(dmin=0), 5 * A)]) == M.MLQ_E_NULL
+    assert ph(n=0) == M.MLQ_E_SHAPE
+    assert ph(prods=[_Q4KProduct(kt(), 5 * A)] * 5) == M.MLQ_E_SHAPE  # at most 4 products
+    assert ph(k=480) == M.MLQ_E_SHAPE
+    assert ph(prods=[_Q4KProduct(kt(), 5 * A), _Q4KProduct(kt(cols=768), 12 * A)]) == M.MLQ_E_SHAPE
+    assert ph(prods=[_Q4KProduct(kt(rows=-1), 5 * A)]) == M.MLQ_E_SHAPE
+    assert ph(x=6 * A + 4) == M.MLQ_E_ALIGN
+    assert ph(prods=[_Q4KProduct(kt(q=A + 8), 5 * A)]) == M.MLQ_E_ALIGN
+    assert ph(prods=[_Q4KProduct(kt(), 5 * A + 2)]) == M.MLQ_E_ALIGN
 
 
 def test_validation_nbits(M):

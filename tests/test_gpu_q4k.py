@@ -207,3 +207,76 @@ def test_q4k_layer_pass_through_runner(M):
         bound = REL * np.abs(t.astype(np.float64)).sum(axis=1)
         yg = r.y[name].cpu().numpy()
         assert np.all(np.abs(yg.astype(np.float64) - yo) <= bound), name
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 256), (77, 2048), (2048, 2048), (300, 5632)])
+def test_q4k_phase_single_product_bitwise(M, rows, cols):
+    """One product through mlq_q4k_phase (x quantised inside the launch)
+    against mlq_quantize_q8k + mlq_matvec_q4k: the same launch geometry and
+    the same quantiser arithmetic, so y must be bit-identical; and within
+    the bound of the oracle."""
+    q, s, d, dmin = I.q4k_weights(rows, cols, seed=rows + cols)
+    x = I.activations(1, cols, seed=cols + 3)[0]
+    W = tensor(M, q, s, d, dmin, rows, cols)
+    xd_ = dev(x.astype(np.float32))
+    y1 = torch.full((rows,), float("nan"), dtype=torch.float32, device=DEV)
+    y2 = torch.full((rows,), float("nan"), dtype=torch.float32, device=DEV)
+    M.mlq_q4k_phase(xd_, cols, [(W, y1)])
+    act = gpu_q8k(M, x)
+    M.mlq_matvec_q4k(y2, W, act, 0, rows)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2), "the phase and the separate calls differ"
+    xq, xdq, xbs = oracle.quantize_q8k(x)
+    yo = oracle.matvec_q4k(q, s, d, dmin, rows, cols, xq, xdq, xbs)
+    oi, om = oracle.block_sums_q4k(q, s, rows, cols, xq, xbs)
+    t = (oi.astype(np.float32) * d - om.astype(np.float32) * dmin) * xdq[None, :]
+    bound = REL * np.abs(t.astype(np.float64)).sum(axis=1)
+    assert np.all(np.abs(y1.cpu().numpy().astype(np.float64) - yo) <= bound + 1e-30)
+
+
+@pytest.mark.parametrize("shapes,cols", [([(2048, 2048), (256, 2048), (256, 2048)], 2048),
+                                         ([(5632, 2048), (5632, 2048)], 2048),
+                                         ([(77, 512), (1, 512), (300, 512), (33, 512)], 512)])
+def test_q4k_phase_grouped_vs_oracle(M, shapes, cols):
+    """Products sharing one float input in one launch (rows of several
+    products in one CTA, stages that stop at product ends): every y within
+    the bound of the oracle on the oracle's quantisation of x."""
+    x = I.activations(1, cols, seed=len(shapes) + cols)[0]
+    xq, xdq, xbs = oracle.quantize_q8k(x)
+    prods, host = [], []
+    for i, (rows, c) in enumerate(shapes):
+        q, s, d, dmin = I.q4k_weights(rows, c, seed=100 + i)
+        y = torch.full((rows,), float("nan"), dtype=torch.float32, device=DEV)
+        prods.append((tensor(M, q, s, d, dmin, rows, c), y))
+        host.append((q, s, d, dmin, rows))
+    M.mlq_q4k_phase(dev(x.astype(np.float32)), cols, prods)
+    torch.cuda.synchronize()
+    for (q, s, d, dmin, rows), (_, y) in zip(host, prods):
+        yo = oracle.matvec_q4k(q, s, d, dmin, rows, cols, xq, xdq, xbs)
+        oi, om = oracle.block_sums_q4k(q, s, rows, cols, xq, xbs)
+        t = (oi.astype(np.float32) * d - om.astype(np.float32) * dmin) * xdq[None, :]
+        bound = REL * np.abs(t.astype(np.float64)).sum(axis=1)
+        yg = y.cpu().numpy()
+        assert np.all(np.isfinite(yg)), f"{rows} rows: not every row written"
+        assert np.all(np.abs(yg.astype(np.float64) - yo) <= bound + 1e-30), f"{rows}x{cols}"
+
+
+def test_q4k_layer_phase_pass_through_runner(M):
+    """The bench's Q4_K pass as four phase launches (q|k|v, o, gate|up,
+    down): every product's y within the bound of the oracle on the oracle's
+    quantisation of the GPU's own float input."""
+    from block_quantized_decode_gb300.runner import Q4KRunner
+    wl = I.tinyllama_layer_q4k()
+    r = Q4KRunner(wl, copies=1)
+    assert len(r.phases()) == 4
+    r.step_phase()
+    torch.cuda.synchronize()
+    for name, rows, cols, inp in wl.mats:
+        oq, od, obs = oracle.quantize_q8k(r.vec(inp).cpu().numpy())
+        q, s, d, dmin, _, _ = r.host[name]
+        yo = oracle.matvec_q4k(q, s, d, dmin, rows, cols, oq, od, obs)
+        oi, om = oracle.block_sums_q4k(q, s, rows, cols, oq, obs)
+        t = (oi.astype(np.float32) * d - om.astype(np.float32) * dmin) * od[None, :]
+        bound = REL * np.abs(t.astype(np.float64)).sum(axis=1)
+        yg = r.y[name].cpu().numpy()
+        assert np.all(np.abs(yg.astype(np.float64) - yo) <= bound), name
