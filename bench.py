@@ -1012,10 +1012,10 @@ def run_q4k(args, wl, world, rank, local, pg):
     del probe
     copies = args.copies or max(2, math.ceil(3 * l2 / wbytes))
     r = Q4KRunner(wl, copies=copies, device=f"cuda:{local}")
-    # Q4_K-style passes run as phases by default (mlq_q4k_phase: products
-    # sharing an input in one launch that quantises it); --path calls keeps
-    # one quantiser launch per input and one launch per product.
-    phase = not nbits and args.path in ("auto", "phase")
+    # Both formats run as phases by default (mlq_q4k_phase / mlq_nbits_phase:
+    # products sharing an input in one launch that quantises it); --path
+    # calls keeps one quantiser launch per input and one launch per product.
+    phase = args.path in ("auto", "phase")
 
     def one_pass(c):
         if phase:

@@ -18,5 +18,5 @@ from .binding import (  # noqa: F401
     MLQ_MAX_SEQ, MLQ_MAX_HEAD_DIM, mlq_rmsnorm, mlq_add_rmsnorm, mlq_add, mlq_softmax, mlq_silu_mul,
     mlq_rope_tables, mlq_rope, mlq_attention,
     MLQ_QKK, Q4KTensor, Q8KAct, mlq_quantize_q8k, mlq_matvec_q4k, mlq_block_sums_q4k, mlq_q4k_phase,
-    NBitsTensor, BlkAct, mlq_quantize_blk, mlq_matvec_nbits, mlq_block_sumi_nbits,
+    NBitsTensor, BlkAct, mlq_quantize_blk, mlq_matvec_nbits, mlq_block_sumi_nbits, mlq_nbits_phase,
 )

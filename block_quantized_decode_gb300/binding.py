@@ -30,7 +30,7 @@ EXPORTS = (
     "mlq_decode_chain_static", "mlq_decode_phase",
     "mlq_rmsnorm", "mlq_add_rmsnorm", "mlq_add", "mlq_softmax", "mlq_silu_mul",
     "mlq_rope_tables", "mlq_rope", "mlq_attention",
-    "mlq_quantize_q8k", "mlq_matvec_q4k", "mlq_block_sums_q4k", "mlq_q4k_phase",
+    "mlq_quantize_q8k", "mlq_matvec_q4k", "mlq_block_sums_q4k", "mlq_q4k_phase", "mlq_nbits_phase",
     "mlq_quantize_blk", "mlq_matvec_nbits", "mlq_block_sumi_nbits",
     "mlq_debug_chain_plan",
 )
@@ -78,6 +78,10 @@ class _NBitsTensor(ctypes.Structure):
                 ("rows", ctypes.c_int), ("cols", ctypes.c_int), ("bits", ctypes.c_int),
                 ("blk", ctypes.c_int), ("scale_f16", ctypes.c_int), ("scale_ld", ctypes.c_int),
                 ("zp_ld", ctypes.c_int)]
+
+
+class _NBitsProduct(ctypes.Structure):
+    _fields_ = [("W", _NBitsTensor), ("y", ctypes.c_void_p)]
 
 
 class _BlkAct(ctypes.Structure):
@@ -153,6 +157,7 @@ def lib() -> ctypes.CDLL:
         NT, BA = ctypes.POINTER(_NBitsTensor), ctypes.POINTER(_BlkAct)
         L.mlq_quantize_blk.argtypes = [BA, P, I, P]
         L.mlq_matvec_nbits.argtypes = [P, NT, BA, I, I, P]
+        L.mlq_nbits_phase.argtypes = [P, I, ctypes.POINTER(_NBitsProduct), I, P]
         L.mlq_block_sumi_nbits.argtypes = [P, NT, BA, I, I, P]
         L.mlq_debug_chain_plan.argtypes = [ctypes.POINTER(_ChainPhase), I, ctypes.POINTER(_ChainProduct),
                                            I, I, P, I]
@@ -351,6 +356,12 @@ class BlkAct:
 def mlq_quantize_blk(out: BlkAct, x, k: int, stream=None) -> None:
     co = out.c()
     _check(lib().mlq_quantize_blk(ctypes.byref(co), _addr(x), k, _stream(stream)), "mlq_quantize_blk")
+
+
+def mlq_nbits_phase(x, k: int, products, stream=None) -> None:
+    """products: [(NBitsTensor, y), ...] (1..4, one format) sharing the float input x."""
+    arr = (_NBitsProduct * len(products))(*[_NBitsProduct(W.c(), _addr(y)) for W, y in products])
+    _check(lib().mlq_nbits_phase(_addr(x), k, arr, len(products), _stream(stream)), "mlq_nbits_phase")
 
 
 def mlq_matvec_nbits(y, W: NBitsTensor, x: BlkAct, r0: int, r1: int, stream=None) -> None:

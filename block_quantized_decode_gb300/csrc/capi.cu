@@ -559,6 +559,40 @@ mlq_status mlq_quantize_blk(mlq_blk_act *out, const float *x, int k, void *strea
   return from_cuda(mlq::launch_quantize_blk(ctx, x, out->q, out->d, out->bsums, k, out->blk));
 }
 
+mlq_status mlq_nbits_phase(const float *x, int k, const mlq_nbits_product *products, int nproducts,
+                           void *stream) {
+  if (x == nullptr || products == nullptr) return MLQ_E_NULL;
+  if (nproducts < 1 || nproducts > 4) return MLQ_E_SHAPE;
+  if (!aligned(x, 16)) return MLQ_E_ALIGN;
+  const mlq_nbits_tensor &W0 = products[0].W;
+  mlq::NBitsProductDev p[4];
+  for (int j = 0; j < nproducts; ++j) {
+    const mlq_nbits_tensor &W = products[j].W;
+    if (products[j].y == nullptr || W.q == nullptr || W.scales == nullptr) return MLQ_E_NULL;
+    if (W.bits != 4 && W.bits != 8) return MLQ_E_TYPE;
+    if (W.scale_f16 != 0 && W.scale_f16 != 1) return MLQ_E_TYPE;
+    if (W.bits == 4 && W.zp != nullptr) return MLQ_E_TYPE;
+    // one format and one row layout of scales and zero points for all
+    if (W.bits != W0.bits || W.scale_f16 != W0.scale_f16 || (W.zp == nullptr) != (W0.zp == nullptr))
+      return MLQ_E_TYPE;
+    if (W.blk != W0.blk || W.scale_ld != W0.scale_ld || (W.zp != nullptr && W.zp_ld != W0.zp_ld))
+      return MLQ_E_SHAPE;
+    if (W.blk != 32 && W.blk != 128) return MLQ_E_SHAPE;
+    if (W.cols != k || k <= 0 || k % W.blk != 0 || k > MLQ_MAX_COLS || W.rows < 0) return MLQ_E_SHAPE;
+    const int nb = k / W.blk;
+    if (W.scale_ld < nb || (W.scale_ld * (W.scale_f16 ? 2 : 4)) % 16 != 0) return MLQ_E_SHAPE;
+    if (W.zp != nullptr && (W.zp_ld < nb || W.zp_ld % 16 != 0)) return MLQ_E_SHAPE;
+    if (!aligned(W.q, 16) || !aligned(W.scales, 16) || !aligned(W.zp, 16) || !aligned(products[j].y, 4))
+      return MLQ_E_ALIGN;
+    p[j] = mlq::NBitsProductDev{W.q, W.scales, W.zp, products[j].y, W.rows};
+  }
+  mlq::LaunchCtx ctx;
+  mlq_status s = make_ctx(&ctx, stream);
+  if (s != MLQ_OK) return s;
+  return from_cuda(mlq::launch_phase_nbits(ctx, W0.bits, W0.blk, W0.scale_f16, W0.scale_ld, W0.zp_ld, k,
+                                           x, p, nproducts));
+}
+
 mlq_status mlq_matvec_nbits(float *y, const mlq_nbits_tensor *W, const mlq_blk_act *x, int r0, int r1,
                             void *stream) {
   if (y == nullptr) return MLQ_E_NULL;

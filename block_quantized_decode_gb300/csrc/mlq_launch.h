@@ -221,6 +221,17 @@ cudaError_t launch_matvec_nbits(const LaunchCtx &ctx, int bits, int blk, const v
                                 int sc_f16, int sc_ld, const uint8_t *zp, int zp_ld, int cols,
                                 const int8_t *xq, const float *xd, const int32_t *xbs, float *y,
                                 int32_t *sumi, int r0, int r1);
+// A block-length phase: up to 4 products of one format sharing the float
+// input x (cols elements), every CTA quantising x itself; product j writes
+// rows 0 .. rows_j of y_j.
+struct NBitsProductDev {
+  const void *q, *scales;
+  const uint8_t *zp;
+  float *y;
+  int rows;
+};
+cudaError_t launch_phase_nbits(const LaunchCtx &ctx, int bits, int blk, int sc_f16, int sc_ld, int zp_ld,
+                               int cols, const float *x, const NBitsProductDev *p, int np);
 
 // layer.cu: the floating-point steps of a decode layer (each one launch).
 cudaError_t launch_rmsnorm_q8(const LaunchCtx &ctx, float *x, const float *y, const float *w,

@@ -42,15 +42,13 @@ constexpr size_t kNStageTarget = 32 * 1024;
 // ---- per-block activation quantiser ------------------------------------------
 // One warp per block of `blk` (32 or 128) elements; lane l holds elements
 // l*E .. l*E + E - 1 (E = blk / 32).
+// Returns the lane's E quants packed in bytes; *d = the block's scale;
+// *sum_out = the block's quant sum (every lane).  Used by the quantiser
+// kernel and by the phase kernel's in-CTA quantisation alike.
 template <int E>
-__global__ void __launch_bounds__(256) quantize_blk_kernel(const float *__restrict__ x, int8_t *q,
-                                                           float *d, int32_t *bsums, int nblocks) {
-  const int blk = static_cast<int>((blockIdx.x * static_cast<unsigned>(blockDim.x) + threadIdx.x) >> 5);
-  const int lane = threadIdx.x & 31;
-  griddep_wait();
-  if (blk >= nblocks) return;
+__device__ __forceinline__ uint32_t blk_quant(const float *xb, int lane, float *d, int *sum_out) {
   float v[E];
-  const float *src = x + static_cast<size_t>(blk) * (32 * E) + lane * E;
+  const float *src = xb + lane * E;
   if (E == 4) {
     const float4 t = *reinterpret_cast<const float4 *>(src);
     v[0] = t.x;
@@ -76,11 +74,26 @@ __global__ void __launch_bounds__(256) quantize_blk_kernel(const float *__restri
     sum += qq;
     packed |= static_cast<uint32_t>(qq & 0xff) << (8 * i);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  *d = dd;
+  *sum_out = sum;
+  return packed;
+}
+
+template <int E>
+__global__ void __launch_bounds__(256) quantize_blk_kernel(const float *__restrict__ x, int8_t *q,
+                                                           float *d, int32_t *bsums, int nblocks) {
+  const int blk = static_cast<int>((blockIdx.x * static_cast<unsigned>(blockDim.x) + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  griddep_wait();
+  if (blk >= nblocks) return;
+  float dd;
+  int sum;
+  const uint32_t packed = blk_quant<E>(x + static_cast<size_t>(blk) * (32 * E), lane, &dd, &sum);
   int8_t *dst = q + static_cast<size_t>(blk) * (32 * E) + lane * E;
   if (E == 4) *reinterpret_cast<uint32_t *>(dst) = packed;
   else *dst = static_cast<int8_t>(packed & 0xff);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   if (lane == 0) {
     d[blk] = dd;
     bsums[blk] = sum;
@@ -97,17 +110,24 @@ cudaError_t launch_quantize_blk(const LaunchCtx &ctx, const float *x, int8_t *q,
 }
 
 // ---- product ------------------------------------------------------------------
+constexpr int kNMaxProducts = 4;
+// The launch's rows: products j = 0 .. nprod-1 (one format, scale and zero-
+// point row strides), rows rbase[j] .. rbase[j] + rows[j] of each, one after
+// another ([0, total) over all of them); every product reads the same input.
 struct NBitsArgs {
-  const uint8_t *wq;
-  const void *sc;
-  const uint8_t *zp;  // 8-bit: zero points (nullptr: 128)
-  const int8_t *xq;
+  const uint8_t *wq[kNMaxProducts];
+  const void *sc[kNMaxProducts];
+  const uint8_t *zp[kNMaxProducts];  // 8-bit: zero points (nullptr: 128), all or none
+  float *y[kNMaxProducts];
+  int rbase[kNMaxProducts], rows[kNMaxProducts];
+  int nprod, total;
+  const float *xf;    // float input quantised in each CTA (a phase), or null:
+  const int8_t *xq;   // the quantised input (quants, scales, block sums)
   const float *xd;
   const int32_t *xbs;
-  float *y;
-  int32_t *sumi;      // test hook: per-block int32 sums instead of y
+  int32_t *sumi;      // test hook (one product): per-block int32 sums instead of y
   int cols, blk, nb, f16, sc_ld, zp_ld;
-  int r0, r1, R, ns, P, early;
+  int R, ns, P, early;
   unsigned rowq, row_sc, row_zp;          // bytes per row of each array
   unsigned stage_bytes, stage_sc, stage_zp, smem_part, smem_ring;
   int *status;
@@ -129,6 +149,20 @@ __device__ __forceinline__ bool n_wait(uint32_t bar, uint32_t parity, const vola
   }
 }
 
+// The stage of at most R rows that starts at row r of [0, total) and ends
+// before rb and before the end of r's product: returns its row count, with
+// *j its product and *lrow its first row in that product.
+__device__ __forceinline__ int n_stage(const NBitsArgs &a, int r, int rb, int R, int *j, int *lrow) {
+  int jj = 0, off = 0;
+  while (jj + 1 < a.nprod && r >= off + a.rows[jj]) {
+    off += a.rows[jj];
+    ++jj;
+  }
+  *j = jj;
+  *lrow = a.rbase[jj] + (r - off);
+  return min(R, min(rb, off + a.rows[jj]) - r);
+}
+
 template <int BITS, bool SUMS>
 __global__ void __launch_bounds__(kNThreads, 2) matvec_nbits_kernel(const __grid_constant__ NBitsArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -139,9 +173,9 @@ __global__ void __launch_bounds__(kNThreads, 2) matvec_nbits_kernel(const __grid
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = a.cols, blk = a.blk, nb = a.nb;
   const size_t rowq = a.rowq, row_sc = a.row_sc, row_zp = a.row_zp;
-  const int n_all = a.r1 - a.r0;
-  const int ra = a.r0 + static_cast<int>(static_cast<long long>(n_all) * blockIdx.x / gridDim.x);
-  const int rb = a.r0 + static_cast<int>(static_cast<long long>(n_all) * (blockIdx.x + 1) / gridDim.x);
+  const int n_all = a.total;
+  const int ra = static_cast<int>(static_cast<long long>(n_all) * blockIdx.x / gridDim.x);
+  const int rb = static_cast<int>(static_cast<long long>(n_all) * (blockIdx.x + 1) / gridDim.x);
   const int R = a.R, ns = a.ns, P = a.P;
   int8_t *xq_s = reinterpret_cast<int8_t *>(smem);
   float *xd_s = reinterpret_cast<float *>(smem + K);
@@ -164,9 +198,10 @@ __global__ void __launch_bounds__(kNThreads, 2) matvec_nbits_kernel(const __grid
     // ------------------------------ producer ------------------------------
     if (lane != 0) return;
     if (!a.early) griddep_wait();  // weights written by earlier work: wait for it first
-    int s = 0;
-    for (int r = ra; r < rb; r += R, ++s) {
-      const int n = min(R, rb - r);
+    int s = 0, n = 0;
+    for (int r = ra; r < rb; r += n, ++s) {
+      int j, lrow;
+      n = n_stage(a, r, rb, R, &j, &lrow);
       const int slot = s % ns;
       if (s >= ns && !n_wait(smem_addr(&empty_bar[slot]), ((s / ns) - 1) & 1, abort_v, a.wait_ns)) {
         if (atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
@@ -176,12 +211,12 @@ __global__ void __launch_bounds__(kNThreads, 2) matvec_nbits_kernel(const __grid
       uint8_t *dst = ring + static_cast<size_t>(slot) * a.stage_bytes;
       const uint32_t fb = smem_addr(&full_bar[slot]);
       const uint32_t qb = static_cast<uint32_t>(n * rowq), sb = static_cast<uint32_t>(n * row_sc);
-      const uint32_t zb = a.zp != nullptr ? static_cast<uint32_t>(n * row_zp) : 0u;
+      const uint32_t zb = a.zp[j] != nullptr ? static_cast<uint32_t>(n * row_zp) : 0u;
       mbar_arrive_expect_tx(fb, qb + sb + zb);
-      bulk_copy_g2s(smem_addr(dst), a.wq + static_cast<size_t>(r) * rowq, qb, fb);
-      bulk_copy_g2s(smem_addr(dst + a.stage_sc), static_cast<const uint8_t *>(a.sc) + static_cast<size_t>(r) * row_sc,
-                    sb, fb);
-      if (zb) bulk_copy_g2s(smem_addr(dst + a.stage_zp), a.zp + static_cast<size_t>(r) * row_zp, zb, fb);
+      bulk_copy_g2s(smem_addr(dst), a.wq[j] + static_cast<size_t>(lrow) * rowq, qb, fb);
+      bulk_copy_g2s(smem_addr(dst + a.stage_sc),
+                    static_cast<const uint8_t *>(a.sc[j]) + static_cast<size_t>(lrow) * row_sc, sb, fb);
+      if (zb) bulk_copy_g2s(smem_addr(dst + a.stage_zp), a.zp[j] + static_cast<size_t>(lrow) * row_zp, zb, fb);
     }
     if (*abort_v) {  // copies may still be landing: the last issued stages (bounded)
       for (int t = s > ns ? s - ns : 0; t < s; ++t)
@@ -193,7 +228,25 @@ __global__ void __launch_bounds__(kNThreads, 2) matvec_nbits_kernel(const __grid
   // ------------------------------ consumers ------------------------------
   griddep_wait();  // x may come from the previous kernel
   if (rb <= ra) return;
-  {  // the activations into shared memory, all loads before any store
+  if (a.xf != nullptr) {
+    // a phase: every CTA quantises the float input itself, one warp per
+    // block, with the quantiser kernel's own arithmetic
+    for (int b = warp; b < nb; b += kNWarps) {
+      float dd;
+      int sum;
+      if (blk == 128) {
+        const uint32_t packed = blk_quant<4>(a.xf + static_cast<size_t>(b) * 128, lane, &dd, &sum);
+        *reinterpret_cast<uint32_t *>(xq_s + b * 128 + lane * 4) = packed;
+      } else {
+        const uint32_t packed = blk_quant<1>(a.xf + static_cast<size_t>(b) * 32, lane, &dd, &sum);
+        xq_s[b * 32 + lane] = static_cast<int8_t>(packed & 0xff);
+      }
+      if (lane == 0) {
+        xd_s[b] = dd;
+        xbs_s[b] = sum;
+      }
+    }
+  } else {  // the activations into shared memory, all loads before any store
     const int uq = K / 16;
     for (int base = 0; base < uq; base += 2 * kNWarps * 32) {
       int4 v[2];
@@ -218,9 +271,10 @@ __global__ void __launch_bounds__(kNThreads, 2) matvec_nbits_kernel(const __grid
   // A row is U 16-byte units; UPB units per block (a power of two).
   const int U = static_cast<int>(rowq / 16);
   const int upb = BITS == 4 ? blk / 32 : blk / 16;
-  int s = 0;
-  for (int r = ra; r < rb; r += R, ++s) {
-    const int n = min(R, rb - r);
+  int s = 0, n = 0;
+  for (int r = ra; r < rb; r += n, ++s) {
+    int j, lrow;
+    n = n_stage(a, r, rb, R, &j, &lrow);
     const int slot = s % ns;
     if (!warp_wait([&] { return n_wait(smem_addr(&full_bar[slot]), (s / ns) & 1, abort_v, a.wait_ns); })) {
       if (lane == 0 && atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
@@ -267,11 +321,11 @@ __global__ void __launch_bounds__(kNThreads, 2) matvec_nbits_kernel(const __grid
           if (BITS == 4) {
             corr = -8;
           } else {
-            corr = 128 - (a.zp != nullptr ? static_cast<int>(stz[static_cast<size_t>(i) * row_zp + b]) : 128);
+            corr = 128 - (a.zp[j] != nullptr ? static_cast<int>(stz[static_cast<size_t>(i) * row_zp + b]) : 128);
           }
           const int sumi = sacc + corr * xbs_s[b];
           if (SUMS) {
-            a.sumi[static_cast<size_t>(r + i - a.r0) * nb + b] = sumi;
+            a.sumi[static_cast<size_t>(lrow + i - a.rbase[0]) * nb + b] = sumi;
           } else {
             const float sc = a.f16 ? __half2float(reinterpret_cast<const __half *>(sts + static_cast<size_t>(i) * row_sc)[b])
                                    : reinterpret_cast<const float *>(sts + static_cast<size_t>(i) * row_sc)[b];
@@ -283,7 +337,7 @@ __global__ void __launch_bounds__(kNThreads, 2) matvec_nbits_kernel(const __grid
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
         if (lane == 0) {
-          if (P == 1) a.y[r + i] = acc;
+          if (P == 1) a.y[j][lrow + i] = acc;
           else part_s[static_cast<size_t>(r + i - ra) * P + part] = acc;
         }
       }
@@ -297,22 +351,23 @@ __global__ void __launch_bounds__(kNThreads, 2) matvec_nbits_kernel(const __grid
     for (int i = tid; i < rb - ra; i += kNWarps * 32) {
       float v = part_s[static_cast<size_t>(i) * P];
       for (int p = 1; p < P; ++p) v = __fadd_rn(v, part_s[static_cast<size_t>(i) * P + p]);
-      a.y[ra + i] = v;
+      int j, lrow;
+      n_stage(a, ra + i, rb, 1, &j, &lrow);
+      a.y[j][lrow] = v;
     }
   }
 }
 
-cudaError_t launch_matvec_nbits(const LaunchCtx &ctx, int bits, int blk, const void *wq, const void *sc,
-                                int sc_f16, int sc_ld, const uint8_t *zp, int zp_ld, int cols,
-                                const int8_t *xq, const float *xd, const int32_t *xbs, float *y,
-                                int32_t *sumi, int r0, int r1) {
-  const int n = r1 - r0;
+// Geometry of a launch over a.total rows (a's format, products and input
+// already filled), then the launch.
+static cudaError_t launch_nbits_common(const LaunchCtx &ctx, NBitsArgs &a, int bits, bool sums) {
+  const int n = a.total;
   if (n <= 0) return cudaSuccess;
   auto up = [](size_t v, size_t al) { return (v + al - 1) / al * al; };
-  const int nb = cols / blk;
+  const int cols = a.cols, blk = a.blk, nb = cols / blk;
   const size_t rowq = static_cast<size_t>(cols) * bits / 8;
-  const size_t row_sc = static_cast<size_t>(sc_ld) * (sc_f16 ? 2 : 4);
-  const size_t row_zp = zp != nullptr ? static_cast<size_t>(zp_ld) : 0;
+  const size_t row_sc = static_cast<size_t>(a.sc_ld) * (a.f16 ? 2 : 4);
+  const size_t row_zp = a.zp[0] != nullptr ? static_cast<size_t>(a.zp_ld) : 0;
   const size_t rowbytes = rowq + row_sc + row_zp;
   const size_t xs = up(static_cast<size_t>(cols) + 8 * static_cast<size_t>(nb), 128);
   int R = static_cast<int>(kNStageTarget / rowbytes);
@@ -328,7 +383,7 @@ cudaError_t launch_matvec_nbits(const LaunchCtx &ctx, int bits, int blk, const v
   int P = R >= kNWarps ? 1 : kNWarps / R;
   if (P > cols32) P = cols32;
   if (P < 1) P = 1;
-  size_t part = sumi != nullptr || P == 1 ? 0 : up(static_cast<size_t>(rows_cta) * P * 4, 128);
+  size_t part = sums || P == 1 ? 0 : up(static_cast<size_t>(rows_cta) * P * 4, 128);
   if (part > 32 * 1024) {
     P = 1;
     part = 0;
@@ -340,25 +395,10 @@ cudaError_t launch_matvec_nbits(const LaunchCtx &ctx, int bits, int blk, const v
   if (xs + part + 2 * stage > budget) return cudaErrorNotSupported;
   int ns = static_cast<int>((budget - xs - part) / stage);
   if (ns > kNSlots) ns = kNSlots;
-  const int stages_cta = (rows_cta + R - 1) / R;
+  // stages per CTA, counted with the breaks at product boundaries
+  const int stages_cta = (rows_cta + R - 1) / R + a.nprod - 1;
   if (ns > stages_cta) ns = stages_cta < 2 ? 2 : stages_cta;
-  NBitsArgs a;
-  a.wq = static_cast<const uint8_t *>(wq);
-  a.sc = sc;
-  a.zp = zp;
-  a.xq = xq;
-  a.xd = xd;
-  a.xbs = xbs;
-  a.y = y;
-  a.sumi = sumi;
-  a.cols = cols;
-  a.blk = blk;
   a.nb = nb;
-  a.f16 = sc_f16;
-  a.sc_ld = sc_ld;
-  a.zp_ld = zp_ld;
-  a.r0 = r0;
-  a.r1 = r1;
   a.R = R;
   a.ns = ns;
   a.P = P;
@@ -374,13 +414,63 @@ cudaError_t launch_matvec_nbits(const LaunchCtx &ctx, int bits, int blk, const v
   a.status = ctx.status;
   a.wait_ns = ctx.wait_ns;
   const size_t smem = xs + part + static_cast<size_t>(ns) * stage;
-  auto kern = bits == 4 ? (sumi ? matvec_nbits_kernel<4, true> : matvec_nbits_kernel<4, false>)
-                        : (sumi ? matvec_nbits_kernel<8, true> : matvec_nbits_kernel<8, false>);
+  auto kern = bits == 4 ? (sums ? matvec_nbits_kernel<4, true> : matvec_nbits_kernel<4, false>)
+                        : (sums ? matvec_nbits_kernel<8, true> : matvec_nbits_kernel<8, false>);
   prefer_max_shared(kern);
   const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kNThreads), smem, ctx, a);
+}
+
+cudaError_t launch_matvec_nbits(const LaunchCtx &ctx, int bits, int blk, const void *wq, const void *sc,
+                                int sc_f16, int sc_ld, const uint8_t *zp, int zp_ld, int cols,
+                                const int8_t *xq, const float *xd, const int32_t *xbs, float *y,
+                                int32_t *sumi, int r0, int r1) {
+  NBitsArgs a = {};
+  a.wq[0] = static_cast<const uint8_t *>(wq);
+  a.sc[0] = sc;
+  a.zp[0] = zp;
+  a.y[0] = y;
+  a.rbase[0] = r0;
+  a.rows[0] = r1 - r0;
+  a.nprod = 1;
+  a.total = r1 - r0;
+  a.xf = nullptr;
+  a.xq = xq;
+  a.xd = xd;
+  a.xbs = xbs;
+  a.sumi = sumi;
+  a.cols = cols;
+  a.blk = blk;
+  a.f16 = sc_f16;
+  a.sc_ld = sc_ld;
+  a.zp_ld = zp_ld;
+  return launch_nbits_common(ctx, a, bits, sumi != nullptr);
+}
+
+cudaError_t launch_phase_nbits(const LaunchCtx &ctx, int bits, int blk, int sc_f16, int sc_ld, int zp_ld,
+                               int cols, const float *x, const NBitsProductDev *p, int np) {
+  if (np < 1 || np > kNMaxProducts) return cudaErrorInvalidValue;
+  NBitsArgs a = {};
+  a.total = 0;
+  for (int j = 0; j < np; ++j) {
+    a.wq[j] = static_cast<const uint8_t *>(p[j].q);
+    a.sc[j] = p[j].scales;
+    a.zp[j] = p[j].zp;
+    a.y[j] = p[j].y;
+    a.rbase[j] = 0;
+    a.rows[j] = p[j].rows;
+    a.total += p[j].rows;
+  }
+  a.nprod = np;
+  a.xf = x;
+  a.cols = cols;
+  a.blk = blk;
+  a.f16 = sc_f16;
+  a.sc_ld = sc_ld;
+  a.zp_ld = zp_ld;
+  return launch_nbits_common(ctx, a, bits, false);
 }
 
 }  // namespace mlq

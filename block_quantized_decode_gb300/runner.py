@@ -395,6 +395,22 @@ class NBitsRunner:
                 done.add(inp)
             B.mlq_matvec_nbits(self.y[name], self.W[copy][name], self.act[inp], 0, rows, stream)
 
+    def phases(self):
+        """Consecutive products that read one input, at most four: [(input,
+        [names], K)].  One mlq_nbits_phase launch each."""
+        out = []
+        for name, rows, cols, inp in self.wl.mats:
+            if out and out[-1][0] == inp and len(out[-1][1]) < 4:
+                out[-1][1].append(name)
+            else:
+                out.append((inp, [name], cols))
+        return out
+
+    def step_phase(self, copy: int = 0, stream=None) -> None:
+        """One pass as phases: each launch quantises its float input itself."""
+        for inp, names, cols in self.phases():
+            B.mlq_nbits_phase(self.vec(inp), cols, [(self.W[copy][n], self.y[n]) for n in names], stream)
+
     def product(self, name: str, copy: int = 0, stream=None) -> None:
         rows, inp = [(m[1], m[3]) for m in self.wl.mats if m[0] == name][0]
         B.mlq_matvec_nbits(self.y[name], self.W[copy][name], self.act[inp], 0, rows, stream)

@@ -273,6 +273,22 @@ typedef struct {
  * MLQ_MAX_COLS; out->blk is 32 or 128. */
 mlq_status mlq_quantize_blk(mlq_blk_act *out, const float *x, int k, void *stream);
 
+/* A block-length decode phase (the phase of mlq_decode_phase, Design Spec
+ * Sec. 6 "Forward pass"): for each of the nproducts (1..4) products,
+ * y_j = W_j * Qblk(x), every row of W_j, where Qblk(x) is exactly what
+ * mlq_quantize_blk writes for x with the products' block length, and the
+ * product is computed as mlq_matvec_nbits computes it.  One launch: every
+ * CTA quantises x itself.  All W_j share bits, blk, scale_f16, scale_ld,
+ * zp_ld and whether zp is NULL (else MLQ_E_TYPE / MLQ_E_SHAPE); every
+ * W_j->cols == k.  x: k float32, device, 16-byte aligned; y_j: W_j->rows
+ * float32, 4-byte aligned, owned by the caller. */
+typedef struct {
+    mlq_nbits_tensor W;
+    float *y;
+} mlq_nbits_product;
+mlq_status mlq_nbits_phase(const float *x, int k, const mlq_nbits_product *products, int nproducts,
+                           void *stream);
+
 /* y[r] for r in [r0, r1) as above; the sum over blocks is taken in another
  * order than b = 0, 1, ... and agrees with the in-order sum within
  * 1e-5 * sum_b |term_b| per row.  x->n == W->cols, x->blk == W->blk. */

@@ -393,3 +393,26 @@ def test_validation_nbits(M):
     assert qb(ba(blk=64)) == M.MLQ_E_SHAPE
     assert qb(ba(n=960), k=960) == M.MLQ_E_SHAPE
     assert qb(ba(), x=6 * A + 8) == M.MLQ_E_ALIGN
+    # the block-length phase: products of one format sharing one float input
+    from block_quantized_decode_gb300.binding import _NBitsProduct
+
+    def ph(x=6 * A, k=896, prods=None, n=None):
+        prods = [_NBitsProduct(nt(), 5 * A)] if prods is None else prods
+        arr = (_NBitsProduct * max(1, len(prods)))(*prods)
+        return call(M, "mlq_nbits_phase", x, k, arr, len(prods) if n is None else n, None)
+
+    assert ph(x=None) == M.MLQ_E_NULL
+    assert ph(prods=[_NBitsProduct(nt(), 0)]) == M.MLQ_E_NULL
+    assert ph(prods=[_NBitsProduct(nt(sc=0), 5 * A)]) == M.MLQ_E_NULL
+    assert ph(n=0) == M.MLQ_E_SHAPE
+    assert ph(prods=[_NBitsProduct(nt(), 5 * A)] * 5) == M.MLQ_E_SHAPE
+    assert ph(prods=[_NBitsProduct(nt(bits=2), 5 * A)]) == M.MLQ_E_TYPE
+    assert ph(prods=[_NBitsProduct(nt(), 5 * A), _NBitsProduct(nt(f16=1), 12 * A)]) == M.MLQ_E_TYPE
+    assert ph(prods=[_NBitsProduct(nt(bits=8), 5 * A),
+                     _NBitsProduct(nt(bits=8, zp=6 * A, zld=16), 12 * A)]) == M.MLQ_E_TYPE  # zp all or none
+    assert ph(prods=[_NBitsProduct(nt(), 5 * A), _NBitsProduct(nt(cols=1024), 12 * A)]) == M.MLQ_E_SHAPE
+    assert ph(k=960, prods=[_NBitsProduct(nt(cols=960), 5 * A)]) == M.MLQ_E_SHAPE
+    assert ph(prods=[_NBitsProduct(nt(sld=6), 5 * A)]) == M.MLQ_E_SHAPE
+    assert ph(x=6 * A + 4) == M.MLQ_E_ALIGN
+    assert ph(prods=[_NBitsProduct(nt(q=A + 8), 5 * A)]) == M.MLQ_E_ALIGN
+    assert ph(prods=[_NBitsProduct(nt(), 5 * A + 2)]) == M.MLQ_E_ALIGN

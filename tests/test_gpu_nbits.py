@@ -149,3 +149,67 @@ def test_qwen_layer_pass_through_runner(M):
             bound = REL * np.abs(t.astype(np.float64)).sum(axis=1)
             yg = r.y[name].cpu().numpy()
             assert np.all(np.abs(yg.astype(np.float64) - yo) <= bound), f"{wl.name}/{name}"
+
+
+@pytest.mark.parametrize("bits,blk,f16,with_zp", COMBOS,
+                         ids=[f"b{b}_blk{k}_{'f16' if f else 'f32'}{'_zp' if z else ''}" for b, k, f, z in COMBOS])
+def test_nbits_phase_single_product_bitwise(M, bits, blk, f16, with_zp):
+    """One product through mlq_nbits_phase (x quantised inside the launch)
+    against mlq_quantize_blk + mlq_matvec_nbits: the same geometry and the
+    same quantiser arithmetic, so y must be bit-identical."""
+    rows, cols = 333, 896
+    q, sc, zp = I.nbits_weights(rows, cols, bits, blk, f16, with_zp, seed=rows + bits + blk)
+    x = I.activations(1, cols, seed=cols + bits)[0]
+    W = tensor(M, q, sc, zp, rows, cols, bits, blk)
+    y1 = torch.full((rows,), float("nan"), dtype=torch.float32, device=DEV)
+    y2 = torch.full((rows,), float("nan"), dtype=torch.float32, device=DEV)
+    M.mlq_nbits_phase(dev(x.astype(np.float32)), cols, [(W, y1)])
+    M.mlq_matvec_nbits(y2, W, gpu_quantize_blk(M, x, blk), 0, rows)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2), "the phase and the separate calls differ"
+
+
+@pytest.mark.parametrize("bits,blk,f16,with_zp", [(4, 128, False, False), (8, 32, True, True)])
+def test_nbits_phase_grouped_vs_oracle(M, bits, blk, f16, with_zp):
+    """Products of one format sharing one float input in one launch: every y
+    within the bound of the oracle on the oracle's quantisation of x."""
+    cols = 896
+    x = I.activations(1, cols, seed=bits * blk)[0]
+    xq, xd, xbs = oracle.quantize_blk(x, blk)
+    prods, host = [], []
+    for i, rows in enumerate((896, 128, 77, 1)):
+        q, sc, zp = I.nbits_weights(rows, cols, bits, blk, f16, with_zp, seed=200 + i)
+        y = torch.full((rows,), float("nan"), dtype=torch.float32, device=DEV)
+        prods.append((tensor(M, q, sc, zp, rows, cols, bits, blk), y))
+        host.append((q, sc, zp, rows))
+    M.mlq_nbits_phase(dev(x.astype(np.float32)), cols, prods)
+    torch.cuda.synchronize()
+    for (q, sc, zp, rows), (_, y) in zip(host, prods):
+        yo = oracle.matvec_nbits(q, sc, zp, rows, cols, bits, blk, xq, xd)
+        s_ = oracle.block_sumi_nbits(q, zp, rows, cols, bits, blk, xq)
+        t = (s_.astype(np.float32) * sc.astype(np.float32)) * xd[None, :]
+        bound = REL * np.abs(t.astype(np.float64)).sum(axis=1)
+        yg = y.cpu().numpy()
+        assert np.all(np.isfinite(yg)), f"{rows} rows: not every row written"
+        assert np.all(np.abs(yg.astype(np.float64) - yo) <= bound + 1e-30), f"{rows}x{cols}"
+
+
+def test_qwen_layer_phase_pass_through_runner(M):
+    """The Qwen2.5-0.5B-shaped pass in both forms as phase launches (q|k|v,
+    o, gate|up, down): every product's y within the bound of the oracle on
+    the oracle's quantisation of the GPU's own float input."""
+    from block_quantized_decode_gb300.runner import NBitsRunner
+    for wl in (I.qwen_layer_int4_blk128(), I.qwen_layer_int8_sq8()):
+        r = NBitsRunner(wl, copies=1)
+        assert len(r.phases()) == 4
+        r.step_phase()
+        torch.cuda.synchronize()
+        for name, rows, cols, inp in wl.mats:
+            oq, od, obs = oracle.quantize_blk(r.vec(inp).cpu().numpy(), wl.blk)
+            q, sc, zp = r.host[name]
+            yo = oracle.matvec_nbits(q, sc, zp, rows, cols, wl.bits, wl.blk, oq, od)
+            s_ = oracle.block_sumi_nbits(q, zp, rows, cols, wl.bits, wl.blk, oq)
+            t = (s_.astype(np.float32) * sc.astype(np.float32)) * od[None, :]
+            bound = REL * np.abs(t.astype(np.float64)).sum(axis=1)
+            yg = r.y[name].cpu().numpy()
+            assert np.all(np.abs(yg.astype(np.float64) - yo) <= bound), f"{wl.name}/{name}"
