@@ -279,6 +279,20 @@ class _null:
         return False
 
 
+def phase_groups(mats, max_products: int = 4):
+    """Consecutive products (name, rows, cols, input) that read one input,
+    at most max_products per group, in pass order: [(input, [names], K)].
+    A product that reads another's output starts a new group after it, so
+    every group's input exists before the group runs."""
+    out = []
+    for name, rows, cols, inp in mats:
+        if out and out[-1][0] == inp and len(out[-1][1]) < max_products:
+            out[-1][1].append(name)
+        else:
+            out.append((inp, [name], cols))
+    return out
+
+
 class Q4KRunner:
     """Device buffers and one pass of a Q4KWorkload through the C ABI: per
     input, mlq_quantize_q8k, then every mlq_matvec_q4k that reads it."""
@@ -322,15 +336,8 @@ class Q4KRunner:
             B.mlq_matvec_q4k(self.y[name], self.W[copy][name], self.act[inp], 0, rows, stream)
 
     def phases(self):
-        """Consecutive products that read one input, at most four: [(input,
-        [names], K)].  One mlq_q4k_phase launch each."""
-        out = []
-        for name, rows, cols, inp in self.wl.mats:
-            if out and out[-1][0] == inp and len(out[-1][1]) < 4:
-                out[-1][1].append(name)
-            else:
-                out.append((inp, [name], cols))
-        return out
+        """The pass's phases (phase_groups); one mlq_q4k_phase launch each."""
+        return phase_groups(self.wl.mats)
 
     def step_phase(self, copy: int = 0, stream=None) -> None:
         """One pass as phases: each launch quantises its float input itself."""
@@ -396,15 +403,8 @@ class NBitsRunner:
             B.mlq_matvec_nbits(self.y[name], self.W[copy][name], self.act[inp], 0, rows, stream)
 
     def phases(self):
-        """Consecutive products that read one input, at most four: [(input,
-        [names], K)].  One mlq_nbits_phase launch each."""
-        out = []
-        for name, rows, cols, inp in self.wl.mats:
-            if out and out[-1][0] == inp and len(out[-1][1]) < 4:
-                out[-1][1].append(name)
-            else:
-                out.append((inp, [name], cols))
-        return out
+        """The pass's phases (phase_groups); one mlq_nbits_phase launch each."""
+        return phase_groups(self.wl.mats)
 
     def step_phase(self, copy: int = 0, stream=None) -> None:
         """One pass as phases: each launch quantises its float input itself."""
