@@ -28,8 +28,8 @@
 // then scaled in fp32 as (sumi * dw) * dx and accumulated with a fused
 // multiply-add, as in every other kernel.
 //
-// Weights.  Thread 0 streams the CTA's share through a ring of four stages
-// with TMA tensor copies, three of them in flight: a stage is the cluster's rows (up to 160)
+// Weights.  Thread 0 streams the CTA's share through a ring of 4-8 stages
+// with TMA tensor copies, all but one in flight: a stage is the cluster's rows (up to 160)
 // x 8 blocks, one weight box (128 bytes per row) and one scale box, both
 // completing on the stage's mbarrier.  Measured on GB300, the copy engine
 // spends about 150 ns per copy whatever its size below 8 KB, so stages are
@@ -74,7 +74,7 @@ namespace mlq {
 constexpr int kMcConsumers = 16;                 // warps
 constexpr int kMcThreads = kMcConsumers * 32;
 constexpr int kMcMaxSlots = 8;                   // stages in the ring, at most (at least 4)
-constexpr int kMcFirst = 3;                      // stages copied before the activations are staged
+constexpr int kMcFirst = 4;                      // stages copied before the activations are staged (<= 4 slots)
 constexpr int kMcChunk = 8;                      // blocks per stage (128 bytes of a Q4_0 row)
 constexpr int kMcMaxRows = 160;                  // rows per round (tensor box height)
 constexpr int kMcMaxTpw = kMcMaxRows / 32;       // tiles of one parity in a round
