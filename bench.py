@@ -2,14 +2,20 @@
 
 One step = one pass of the workload's hot path through the C ABI: Q8_0
 quantisation of each input vector, then every Q4_0 / Q8_0 product.  The
-default workload is one TinyLlama-1.1B-shaped decode layer (Q4_0, M = 1:
-q, k, v, o, gate, up, down; 27.5 MB of weights); --workload picks another.
+default workload is the largest single-GPU configuration: the 8-layer
+Llama-7B-shaped FFN stack in Q8_0 (16 chained products, 811.6 MB) plus the
+Qwen2.5-0.5B-shaped lm_head (151936 x 896 Q8_0, 153.2 MB), M = 1.  The same
+line carries, under "also", the Q4_0 stack and the batched M = 4 / M = 16
+Q4_0 products, each timed the same way; --workload picks another workload
+alone.
 
-Timing: W untimed warm-up steps, then K steps bracketed by a barrier and a
-device synchronize, timed with CUDA events on the launching stream; the
-steps replay one CUDA graph per weight copy, and consecutive steps read
-different copies (together more than 3x the L2 size), so every step streams
-its weights from HBM.  Rank 0 prints one JSON line.
+Timing: W untimed warm-up steps, then R back-to-back repeats of exactly K
+steps, each bracketed by CUDA events on the launching stream, with a barrier
+and a device synchronize on both sides; R is chosen so that the region lasts
+at least --min-region seconds and ms_per_step is the median over the
+repeats.  The steps replay CUDA graphs, and consecutive steps read
+different weight copies (together more than 3x the L2 size), so every step
+streams its weights from HBM.  Rank 0 prints one JSON line.
 
 Also measured in the same run: the dominant kernel's per-launch duration
 (CUDA events captured into an instrumented copy of the graphs), the same
@@ -46,9 +52,14 @@ def parse_args():
     p.add_argument("--steps", type=int, default=0,
                    help="timed steps (0 = as many as fill about --seconds of the timed region)")
     p.add_argument("--seconds", type=float, default=1.5)
+    p.add_argument("--min-region", type=float, default=1.0,
+                   help="the K timed steps are repeated back to back until the timed region "
+                        "lasts at least this many seconds (clock samples under load)")
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="tinyllama_layer")
+    p.add_argument("--workload", default="llama7b_ffn_q8_lm_head")
+    p.add_argument("--no-extras", action="store_true",
+                   help="headline workload only (skip the Q4_0 stack and M = 4 / 16 records)")
     p.add_argument("--copies", type=int, default=0, help="weight copies (0 = auto, > 3x L2)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -455,23 +466,25 @@ def run_reference(args, wl, world, rank):
     threads = host_cores()
     layer = isinstance(wl, (I.LayerShape, I.Q4KWorkload, I.NBitsWorkload))
     op = oracle_pass(wl, threads)
-    for _ in range(min(max(0, args.warmup), 3)):
+    warm = max(0, args.warmup)
+    for _ in range(warm):
         op.run()
-    t0 = time.perf_counter()
     steps = args.steps if args.steps > 0 else max(3, int(args.seconds / 0.1))
+    t0 = time.perf_counter()
     for _ in range(steps):
         op.run()
     el = time.perf_counter() - t0
     v = op.weight_bytes * steps / el / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
-        "steps": steps, "warmup": args.warmup, "ms_per_step": el / steps * 1e3,
+        "steps": steps, "warmup": warm, "ms_per_step": el / steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8 dot -> int32, f32 accumulate (CPU oracle)", "data": "synthetic",
         "config": {"workload": wl.name, "M": 1 if layer else wl.m, "weight_bytes_per_step": op.weight_bytes},
-        "gops": op.ops * args.steps / el / 1e9,
+        "gops": op.ops * steps / el / 1e9,
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"{steps} full passes of {wl.name} after {args.warmup} warm-up"},
+                         "sample": f"{steps} full passes of {wl.name} after {warm} warm-up passes, "
+                                   f"rows split over {threads} threads"},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -479,29 +492,106 @@ def run_reference(args, wl, world, rank):
 
 
 # ----------------------------------------------------------------------------
+# timing helpers shared by every workload kind
+# ----------------------------------------------------------------------------
+def timed_region(args, stream, do_steps, pg, dev, clocks):
+    """W warm-up steps (exactly args.warmup), then the timed region: R
+    back-to-back repeats of exactly K steps, each repeat bracketed by CUDA
+    events on `stream`, with a barrier and a device synchronize on both sides
+    of the region.  K = --steps (or, when 0, as many steps as fill about
+    --seconds); R = enough repeats that the region lasts at least
+    --min-region seconds, so that the clock sampler sees the GPU under load.
+    Returns (K, R, median ms per step over the repeats (max over ranks),
+    [ms per step of each repeat], region seconds, clocks)."""
+    import torch
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a0.record(stream)
+        do_steps(max(0, args.warmup))
+        a1.record(stream)
+    stream.synchronize()
+    per = a0.elapsed_time(a1) / 1e3 / max(1, args.warmup) if args.warmup > 0 else None
+    if per is None:  # no warm-up asked: one untimed probe step sizes the region
+        with torch.cuda.stream(stream):
+            a0.record(stream)
+            do_steps(1)
+            a1.record(stream)
+        stream.synchronize()
+        per = a0.elapsed_time(a1) / 1e3
+    steps = args.steps
+    if steps <= 0:
+        steps = max(10, int(args.seconds / max(per, 1e-7)))
+        steps = int(max_over_ranks(pg, float(steps), dev))
+    reps = max(1, math.ceil(args.min_region / max(steps * per, 1e-7)))
+    reps = int(max_over_ranks(pg, float(min(reps, 100000)), dev))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    barrier(pg, dev.index if dev is not None else None)
+    torch.cuda.synchronize()
+    t_host0 = time.time()
+    with torch.cuda.stream(stream):
+        for e0, e1 in evs:
+            e0.record(stream)
+            do_steps(steps)
+            e1.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    barrier(pg, dev.index if dev is not None else None)
+    clk = clocks.stop(t_host0, t_host1)
+    per_rep = [e0.elapsed_time(e1) / steps for e0, e1 in evs]
+    med = statistics.median(per_rep)
+    med = max_over_ranks(pg, med, dev)
+    return steps, reps, med, per_rep, t_host1 - t_host0, clk
+
+
+def back_to_back_us(stream, launch, launches: int) -> float:
+    """Mean duration of one launch: `launches` back-to-back calls of
+    launch(j) captured in one CUDA graph, best of 3 replays, CUDA events on
+    the launching stream."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for j in range(launches):
+            launch(j)
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    best = None
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        stream.synchronize()
+        t = a.elapsed_time(b) / 1e3 / launches
+        best = t if best is None else min(best, t)
+    del g
+    return best * 1e6
+
+
+# ----------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------
-def run_ours(args, wl, world, rank, local, pg):
+def measure_workload(args, wl, world, local, pg, *, path_arg="auto", with_e2e=True):
+    """Time one Workload (M = 1 products or a small-M GEMM pass) through the
+    C ABI: returns the fields of its bench record (value, step time,
+    roofline of the dominant kernel, end to end, launches)."""
     import torch
 
     import block_quantized_decode_gb300 as M
+    from block_quantized_decode_gb300 import inputs as I
     from block_quantized_decode_gb300.runner import WorkloadRunner
 
-    torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    M.mlq_init()
     props = torch.cuda.get_device_properties(local)
     l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
-    from block_quantized_decode_gb300 import inputs as I
     wbytes = sum((mv.rows * mv.cols // 2 if mv.wtype == I.Q4_0 else mv.rows * mv.cols)
                  + mv.rows * mv.cols // 32 * 4 for mv in wl.mats)
     copies = args.copies or max(2, math.ceil(3 * l2 / wbytes))
     r = WorkloadRunner(wl, copies=copies, device=f"cuda:{local}")
-    pf = args.prefetch
-    if pf == "none":
-        pf = None
-    path = args.path if args.path != "auto" else (
-        "phase" if r.m == 1 else "calls")
+    pf = None if args.prefetch == "none" else args.prefetch
+    path = path_arg if path_arg != "auto" else ("phase" if r.m == 1 else "calls")
 
     def one_pass(c):
         if path == "chain":
@@ -514,31 +604,20 @@ def run_ours(args, wl, world, rank, local, pg):
             r.step(copy=c, prefetch=pf)
     assert r.weight_bytes() == wbytes
     stream = torch.cuda.Stream(device=dev)
+    clocks = ClockSampler(local)
+    clocks.start()
 
-    # ---- graphs: one per weight copy (plain), one per copy instrumented
-    dominant = "matvec_m1_kernel<Q4_0>" if r.m == 1 and any(
-        m.spec.wtype == I.Q4_0 for m in r.mats) else (
-        "matvec_m1_kernel<Q8_0>" if r.m == 1 else
-        "gemm_q4_mma_cluster_kernel" if r.m >= 8 else
-        "gemm_q4_ring_kernel" if r.m <= 4 else "gemm_q4_small_m_dp4a_kernel")
-    # the dominant kernel's sources and committed ncu summary (for the traffic figure)
-    kernel_src = (("matvec.cu", "mlq_device.cuh") if r.m == 1 else
-                  ("gemm_mma_cluster.cu", "mma_frag.cuh", "mlq_device.cuh") if r.m >= 8 else
-                  ("gemm_ring.cu", "phase_common.cuh", "mlq_device.cuh") if r.m <= 4 else
-                  ("gemm_small_m.cu", "mlq_device.cuh"))
-    kernel_profile = ("matvec_q4" if r.m == 1 else
-                      "gemm_mma_cluster" if r.m >= 8 else
-                      "gemm_ring" if r.m <= 4 else "gemm_small_m")
+    # Initialisation (not counted as warm-up steps): one eager pass per weight
+    # copy (kernel attributes, first-touch of every buffer), then the graphs:
+    # one per weight copy (one step each) and one that runs a whole cycle of
+    # `copies` steps back to back -- as a decode loop captures a whole
+    # forward pass -- so consecutive steps chain through programmatic
+    # dependent launch instead of paying a graph launch each.
     with torch.cuda.stream(stream):
-        for c in range(copies):  # eager warm-up of every copy (kernel attributes, caches)
+        for c in range(copies):
             one_pass(c)
     stream.synchronize()
-    # One graph per weight copy (one step each), plus one graph that runs a
-    # whole cycle of `copies` steps back to back -- as a decode loop would
-    # capture a whole forward pass -- so consecutive steps chain through
-    # programmatic dependent launch instead of paying a graph launch each.
-    graphs = []
-    cycle = None
+    graphs, cycle = [], None
     if not args.no_graph:
         for c in range(copies):
             g = torch.cuda.CUDAGraph()
@@ -550,129 +629,59 @@ def run_ours(args, wl, world, rank, local, pg):
             for c in range(copies):
                 one_pass(c)
 
-    def do_step(i):
-        if graphs:
-            graphs[i % copies].replay()
-        else:
-            one_pass(i % copies)
-
-    def do_steps(n, start=0):
-        """Exactly n steps: whole cycles through the cycle graph, the rest
-        one graph per step."""
+    def do_steps(n):
+        """Exactly n steps from weight copy 0: whole cycles through the cycle
+        graph, the rest one graph (or one eager pass) per step."""
         i = 0
         if cycle is not None:
-            while start % copies == 0 and n - i >= copies:
+            while n - i >= copies:
                 cycle.replay()
                 i += copies
         while i < n:
-            do_step(start + i)
+            if graphs:
+                graphs[i % copies].replay()
+            else:
+                one_pass(i % copies)
             i += 1
 
-    # ---- headline timed region
-    clocks = ClockSampler(local)
-    clocks.start()
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    warm = max(args.warmup, copies if cycle is not None else 0)
-    with torch.cuda.stream(stream):
-        a0.record(stream)
-        do_steps(warm, 0)
-        a1.record(stream)
-    stream.synchronize()
-    steps = args.steps
-    if steps <= 0:  # fill about args.seconds, same count on every rank
-        per = a0.elapsed_time(a1) / 1e3 / max(1, warm)
-        steps = max(10, int(args.seconds / max(per, 1e-7)))
-        steps = int(max_over_ranks(pg, float(steps), dev))
-    barrier(pg, local)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    t_host0 = time.time()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        do_steps(steps, 0)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    t_host1 = time.time()
-    barrier(pg, local)
-    clk = clocks.stop(t_host0, t_host1)
-    ms = e0.elapsed_time(e1)
-    ms_max = max_over_ranks(pg, ms, dev)
-    value = world * wbytes * steps / (ms_max / 1e3) / 1e9
-    gops = world * r.ops() * steps / (ms_max / 1e3) / 1e9
+    steps, reps, ms, per_rep, region_s, clk = timed_region(args, stream, do_steps, pg, dev, clocks)
+    value = world * wbytes / (ms / 1e3) / 1e9
+    gops = world * r.ops() / (ms / 1e3) / 1e9
 
-    # ---- dominant-kernel launch durations: every distinct product shape of
-    # the step replayed back to back in its own graph (rotating weight
-    # copies, so every launch streams from HBM), CUDA events on the launching
-    # stream; achieved = algorithmic weight bytes per launch / mean duration,
-    # weighted by how often the shape occurs in the step.
+    # ---- the dominant kernel: every phase (or product shape) of the step
+    # replayed back to back in its own graph (rotating weight copies, so every
+    # launch streams from HBM); achieved = algorithmic weight bytes per launch
+    # / mean launch duration, summed over the step's launches.
     peaks, peak_src = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    launches = 2 * copies
+    qt = "Q4_0" if r.mats[0].spec.wtype == I.Q4_0 else "Q8_0"
     roofline = None
     if graphs and path == "chain":
-        launches = 2 * copies
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for j in range(launches):
-                r.step_chain(copy=j % copies)
-        with torch.cuda.stream(stream):
-            g.replay()
-        stream.synchronize()
-        best = None
-        for _ in range(3):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                a.record(stream)
-                g.replay()
-                b.record(stream)
-            stream.synchronize()
-            t = a.elapsed_time(b) / 1e3 / launches
-            best = t if best is None else min(best, t)
-        del g
-        ach = wbytes / best / 1e9
-        qt = "Q4_0" if r.mats[0].spec.wtype == I.Q4_0 else "Q8_0"
+        us = back_to_back_us(stream, lambda j: r.step_chain(copy=j % copies), launches)
+        ach = wbytes / (us * 1e-6) / 1e9
         roofline = {"kernel": f"decode_stream_kernel<{qt}>", "bound": "hbm", "achieved": ach,
                     "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_source": peak_src,
                     "traffic": ncu_traffic(f"chain_{wl.name}", ("stream.cu", "phase_common.cuh",
                                                                 "mlq_device.cuh"), wbytes),
-                    "bytes_per_launch": wbytes, "us_per_launch": best * 1e6,
+                    "bytes_per_launch": wbytes, "us_per_launch": us,
                     "method": f"{launches} back-to-back chain launches (one per step) in one CUDA "
                               "graph, best of 3 replays, CUDA events on the launching stream"}
     elif graphs and path in ("fused", "phase"):
-        # each phase's launch back to back in its own graph
         def calls_of(c):
             return r.fused_calls(c) if path == "fused" else r.phase_calls(
                 c, prefetch="self" if args.phase_prefetch != "none" else "none")
-        per_phase, tot_bytes, tot_s = [], 0.0, 0.0
-        launches = 2 * copies
+        per_phase, tot_bytes, tot_us = [], 0.0, 0.0
         for k, (src, first, count) in enumerate(r.chain_phases()):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for j in range(launches):
-                    calls_of(j % copies)[k]()
-            with torch.cuda.stream(stream):
-                g.replay()
-            stream.synchronize()
-            best = None
-            for _ in range(3):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                with torch.cuda.stream(stream):
-                    a.record(stream)
-                    g.replay()
-                    b.record(stream)
-                stream.synchronize()
-                t = a.elapsed_time(b) / 1e3 / launches
-                best = t if best is None else min(best, t)
-            del g
+            us = back_to_back_us(stream, lambda j, k=k: calls_of(j % copies)[k](), launches)
             mats = r.mats[first:first + count]
             nbytes = sum(m.host_q.nbytes + m.host_d.nbytes for m in mats)
             per_phase.append({"phase": "+".join(m.spec.name for m in mats),
                               "shape": f"{sum(m.spec.rows for m in mats)}x{mats[0].spec.cols}",
-                              "us_per_launch": best * 1e6, "GBps": nbytes / best / 1e9})
+                              "bytes": nbytes, "us_per_launch": us, "GBps": nbytes / us / 1e3})
             tot_bytes += nbytes
-            tot_s += best
-        ach = tot_bytes / tot_s / 1e9
-        qt = "Q4_0" if r.mats[0].spec.wtype == I.Q4_0 else "Q8_0"
+            tot_us += us
+        ach = tot_bytes / (tot_us * 1e-6) / 1e9
         nph = len(per_phase)
         kname, ksrc = phase_kernel_of(r, props.multi_processor_count)
         roofline = {"kernel": f"{kname}<{qt}>", "bound": "hbm", "achieved": ach,
@@ -680,50 +689,41 @@ def run_ours(args, wl, world, rank, local, pg):
                     "traffic": ncu_traffic(f"{ksrc[:-3]}_{wl.name}",
                                            (ksrc, "phase_common.cuh", "mlq_device.cuh"),
                                            tot_bytes / nph),
-                    "bytes_per_launch": tot_bytes / nph, "us_per_launch": tot_s / nph * 1e6,
+                    "bytes_per_launch": tot_bytes / nph, "us_per_launch": tot_us / nph,
                     "method": f"{launches} back-to-back launches of each phase in one CUDA graph, "
-                              "best of 3 replays, CUDA events on the launching stream",
+                              "best of 3 replays, CUDA events on the launching stream; achieved = "
+                              "sum of per_phase bytes / sum of per_phase us_per_launch",
                     "per_phase": per_phase}
     elif graphs:
+        dominant = (f"matvec_m1_kernel<{qt}>" if r.m == 1 else
+                    "gemm_q4_mma_cluster_kernel" if r.m >= 8 else
+                    "gemm_q4_ring_kernel" if r.m <= 4 else "gemm_q4_small_m_dp4a_kernel")
+        kernel_src = (("matvec.cu", "mlq_device.cuh") if r.m == 1 else
+                      ("gemm_mma_cluster.cu", "mma_frag.cuh", "mlq_device.cuh") if r.m >= 8 else
+                      ("gemm_ring.cu", "phase_common.cuh", "mlq_device.cuh") if r.m <= 4 else
+                      ("gemm_small_m.cu", "mlq_device.cuh"))
+        kernel_profile = ("matvec_q4" if r.m == 1 else "gemm_mma_cluster" if r.m >= 8 else
+                          "gemm_ring" if r.m <= 4 else "gemm_small_m")
         shapes = {}
         for i, m in enumerate(r.mats):
             shapes.setdefault((m.spec.wtype, m.spec.rows, m.spec.cols), []).append(i)
-        per_shape, tot_bytes, tot_s = [], 0.0, 0.0
-        launches = 2 * copies
+        per_shape, tot_bytes, tot_us, nl = [], 0.0, 0.0, 0
         for (wt, rows, cols), idx in shapes.items():
             i0 = idx[0]
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for j in range(launches):
-                    r.product(i0, copy=j % copies)
-            with torch.cuda.stream(stream):
-                g.replay()
-            stream.synchronize()
-            best = None
-            for _ in range(3):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                with torch.cuda.stream(stream):
-                    a.record(stream)
-                    g.replay()
-                    b.record(stream)
-                stream.synchronize()
-                t = a.elapsed_time(b) / 1e3 / launches
-                best = t if best is None else min(best, t)
+            us = back_to_back_us(stream, lambda j, i0=i0: r.product(i0, copy=j % copies), launches)
             m = r.mats[i0]
             nbytes = m.host_q.nbytes + m.host_d.nbytes
             per_shape.append({"shape": f"{rows}x{cols}:{'q4_0' if wt == I.Q4_0 else 'q8_0'}",
-                              "per_step": len(idx), "us_per_launch": best * 1e6,
-                              "GBps": nbytes / best / 1e9})
+                              "per_step": len(idx), "bytes": nbytes, "us_per_launch": us,
+                              "GBps": nbytes / us / 1e3})
             tot_bytes += nbytes * len(idx)
-            tot_s += best * len(idx)
-            del g
-        ach = tot_bytes / tot_s / 1e9
+            tot_us += us * len(idx)
+            nl += len(idx)
+        ach = tot_bytes / (tot_us * 1e-6) / 1e9
         roofline = {"kernel": dominant, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
                     "frac": ach / hbm, "peak_source": peak_src,
-                    "traffic": ncu_traffic(f"{kernel_profile}_{wl.name}", kernel_src,
-                                           tot_bytes / sum(p["per_step"] for p in per_shape)),
-                    "bytes_per_launch": tot_bytes / sum(p["per_step"] for p in per_shape),
-                    "us_per_launch": tot_s / sum(p["per_step"] for p in per_shape) * 1e6,
+                    "traffic": ncu_traffic(f"{kernel_profile}_{wl.name}", kernel_src, tot_bytes / nl),
+                    "bytes_per_launch": tot_bytes / nl, "us_per_launch": tot_us / nl,
                     "method": f"{launches} back-to-back launches per shape in one CUDA graph, "
                               "best of 3 replays, CUDA events on the launching stream",
                     "per_shape": per_shape}
@@ -731,37 +731,86 @@ def run_ours(args, wl, world, rank, local, pg):
             # the tensor-core side of the same launches: 2 M N K per product
             flops = sum(2.0 * r.m * r.mats[idx[0]].spec.rows * r.mats[idx[0]].spec.cols * len(idx)
                         for idx in shapes.values())
-            tf = flops / tot_s / 1e12
+            tf = flops / (tot_us * 1e-6) / 1e12
             bf16 = peaks.get("bf16_tflops")
             roofline["tensor"] = {"achieved": tf, "unit": "TFLOP/s", "operands": "fp16 mma.sync",
-                                  "peak_bf16_dense": bf16, "frac": tf / bf16 if bf16 else None}
+                                  "peak_bf16_dense": bf16, "frac": tf / bf16 if bf16 else None,
+                                  "peak_note": "fp16 dense = bf16 dense (same tensor rate); "
+                                               "burst peak, the kernel timed alone"}
 
     # ---- end to end: pinned host input -> step -> outputs to pinned host.
     # A decode loop replays one graph per step: the H2D copy of the inputs,
     # the C-ABI calls and the D2H copy of every output, then one sync.
-    host_out = r.outputs_to_host()
-    torch.cuda.synchronize()
+    e2e = None
+    if with_e2e:
+        host_out = r.outputs_to_host()
+        torch.cuda.synchronize()
 
-    def e2e_body(c):
-        r.upload_inputs(stream)
-        one_pass(c)
-        r.outputs_to_host(host_out)
-    e2e_step = e2e_graph_steps(args, copies, stream, e2e_body)
-    e2e_steps = min(steps, 500)
-    with torch.cuda.stream(stream):
-        t0 = time.perf_counter()
-        for i in range(e2e_steps):
-            e2e_step(i)
-            stream.synchronize()
-    e2e_s = time.perf_counter() - t0
-    e2e_s = max_over_ranks(pg, e2e_s, dev)
-    e2e = {"value": world * wbytes * e2e_steps / e2e_s / 1e9, "unit": UNIT,
-           "h2d_bytes_per_step": r.h2d_bytes(), "d2h_bytes_per_step": r.d2h_bytes(),
-           "steps": e2e_steps, "how": "wall clock; per step: one graph replay holding the pinned "
-                                      "H2D of the inputs, the C-ABI calls and the D2H of every "
-                                      "output, then a stream sync"}
-
+        def e2e_body(c):
+            r.upload_inputs(stream)
+            one_pass(c)
+            r.outputs_to_host(host_out)
+        e2e_step = e2e_graph_steps(args, copies, stream, e2e_body)
+        e2e_steps = max(steps, min(500, steps * reps))
+        with torch.cuda.stream(stream):
+            t0 = time.perf_counter()
+            for i in range(e2e_steps):
+                e2e_step(i)
+                stream.synchronize()
+        e2e_s = time.perf_counter() - t0
+        e2e_s = max_over_ranks(pg, e2e_s, dev)
+        e2e = {"value": world * wbytes * e2e_steps / e2e_s / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": r.h2d_bytes(), "d2h_bytes_per_step": r.d2h_bytes(),
+               "steps": e2e_steps, "how": "wall clock; per step: one graph replay holding the pinned "
+                                          "H2D of the inputs, the C-ABI calls and the D2H of every "
+                                          "output, then a stream sync"}
     assert M.mlq_last_device_error(stream) == M.MLQ_OK
+    per_step = (1 if path == "chain" else len(r.chain_phases()) if path in ("fused", "phase") else
+                r.kernels_per_step + {None: 0, "all": 1, "next": len(r.mats)}[pf])
+    out = {
+        "workload": wl.name, "M": r.m, "path": path, "value": value, "unit": UNIT,
+        "ms_per_step": ms, "steps": steps, "repeats": reps,
+        "ms_per_step_repeats": {"min": min(per_rep), "max": max(per_rep)},
+        "timed_region_s": region_s, "gops": gops, "hbm_frac": value / world / hbm,
+        "weight_bytes_per_step": wbytes, "roofline": roofline, "e2e": e2e,
+        "gpu_launches_per_step": per_step, "gpu_launches": per_step * steps * reps,
+        "clocks": clk,
+        "matrices": [f"{m.spec.name}:{m.spec.rows}x{m.spec.cols}:"
+                     f"{'q4_0' if m.spec.wtype == I.Q4_0 else 'q8_0'}" for m in r.mats],
+        "l2": f"inputs larger than L2: {copies} rotating weight copies "
+              f"({copies * wbytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
+        "graphs": ("one graph per cycle of %d steps" % copies) if cycle is not None else False,
+        "l2_prefetch": (args.phase_prefetch if path == "phase" else pf or "none"),
+    }
+    del graphs, cycle, r
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+# The headline line measures the largest single-GPU configuration (the
+# 8-layer Llama-7B FFN stack in Q8_0 plus the Qwen2.5-0.5B lm_head); the
+# same line carries the Q4_0 stack and the batched M = 4 / 16 products,
+# each timed the same way with its own roofline record.
+HEADLINE = "llama7b_ffn_q8_lm_head"
+EXTRAS = ("llama7b_ffn_q4", "small_m4", "small_m16")
+
+
+def run_ours(args, wl, world, rank, local, pg):
+    import torch
+
+    import block_quantized_decode_gb300 as M
+    from block_quantized_decode_gb300 import inputs as I
+
+    torch.cuda.set_device(local)
+    M.mlq_init()
+    head = measure_workload(args, wl, world, local, pg, path_arg=args.path, with_e2e=True)
+    extras = {}
+    if args.workload == HEADLINE and not args.no_extras:
+        for name in EXTRAS:
+            sub = measure_workload(args, I.WORKLOADS[name](), world, local, pg, with_e2e=False)
+            sub.pop("e2e", None)
+            extras[name] = sub
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -773,24 +822,30 @@ def run_ours(args, wl, world, rank, local, pg):
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
-            "warmup": warm, "ms_per_step": ms_max / steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None,
+            "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+            "steps": head["steps"], "warmup": max(0, args.warmup), "ms_per_step": head["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "q4_0/q8_0: int8 dot -> int32, f32 accumulate", "data": "synthetic",
-            "config": {"workload": wl.name, "M": r.m,
-                       "matrices": [f"{m.spec.name}:{m.spec.rows}x{m.spec.cols}:"
-                                    f"{'q4_0' if m.spec.wtype == I.Q4_0 else 'q8_0'}" for m in r.mats],
-                       "weight_bytes_per_step": wbytes,
-                       "l2": f"inputs larger than L2: {copies} rotating weight copies "
-                             f"({copies * wbytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
-                       "graphs": ("one graph per cycle of %d steps" % copies) if cycle is not None else False,
-                       "path": path, "l2_prefetch": (args.phase_prefetch if path == "phase" else pf or "none"), "parallelism": f"replicas x{world} (independent decode streams)"},
-            "gops": gops, "hbm_frac": value / world / hbm,
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": (1 if path == "chain" else len(r.chain_phases()) if path in ("fused", "phase") else
-                             r.kernels_per_step + {None: 0, "all": 1, "next": len(r.mats)}[pf]) * steps,
-            "clocks": clk,
+            "config": {"workload": head["workload"], "M": head["M"], "matrices": head["matrices"],
+                       "weight_bytes_per_step": head["weight_bytes_per_step"], "l2": head["l2"],
+                       "graphs": head["graphs"], "path": head["path"],
+                       "l2_prefetch": head["l2_prefetch"],
+                       "timing": (f"{head['repeats']} back-to-back repeats of exactly "
+                                  f"{head['steps']} steps, each bracketed by CUDA events; "
+                                  "ms_per_step is the median over the repeats"),
+                       "init": "one eager pass per weight copy and the graph captures, before "
+                               "the warm-up steps",
+                       "parallelism": f"replicas x{world} (independent decode streams)"},
+            "repeats": head["repeats"], "ms_per_step_repeats": head["ms_per_step_repeats"],
+            "timed_region_s": head["timed_region_s"],
+            "gops": head["gops"], "hbm_frac": head["hbm_frac"],
+            "roofline": head["roofline"], "cpu_baseline": cpu, "e2e": head["e2e"],
+            "gpu_launches": head["gpu_launches"],
+            "gpu_launches_per_step": head["gpu_launches_per_step"],
+            "clocks": head["clocks"],
         }
+        if extras:
+            line["also"] = extras
         print(json.dumps(line), flush=True)
     return 0
 
@@ -854,32 +909,9 @@ def run_layer(args, shape, world, rank, local, pg):
 
     clocks = ClockSampler(local)
     clocks.start()
-    warm = max(args.warmup, copies if cycle is not None else 0)
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        a0.record(stream)
-        do_steps(warm)
-        a1.record(stream)
-    stream.synchronize()
-    steps = args.steps
-    if steps <= 0:
-        per = a0.elapsed_time(a1) / 1e3 / max(1, warm)
-        steps = max(10, int(args.seconds / max(per, 1e-7)))
-        steps = int(max_over_ranks(pg, float(steps), dev))
-    barrier(pg, local)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_host0 = time.time()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        do_steps(steps)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    t_host1 = time.time()
-    barrier(pg, local)
-    clk = clocks.stop(t_host0, t_host1)
-    ms = e0.elapsed_time(e1)
-    ms_max = max_over_ranks(pg, ms, dev)
+    steps, reps, ms_step, per_rep, region_s, clk = timed_region(args, stream, do_steps, pg, dev, clocks)
+    warm = max(0, args.warmup)
+    ms_max = ms_step * steps  # median over the repeats, max over ranks
     value = world * wbytes * steps / (ms_max / 1e3) / 1e9
     peaks, peak_src = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
@@ -974,7 +1006,8 @@ def run_layer(args, shape, world, rank, local, pg):
                        "path": "layer", "parallelism": f"replicas x{world} (independent decode streams)"},
             "gops": world * ops * steps / (ms_max / 1e3) / 1e9, "hbm_frac": value / world / hbm,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": L.launches_per_step * steps,
+            "gpu_launches": L.launches_per_step * steps * reps, "repeats": reps,
+            "timed_region_s": region_s,
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)
@@ -1057,31 +1090,9 @@ def run_q4k(args, wl, world, rank, local, pg):
 
     clocks = ClockSampler(local)
     clocks.start()
-    warm = max(args.warmup, copies if cycle is not None else 0)
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        a0.record(stream)
-        do_steps(warm)
-        a1.record(stream)
-    stream.synchronize()
-    steps = args.steps
-    if steps <= 0:
-        per = a0.elapsed_time(a1) / 1e3 / max(1, warm)
-        steps = max(10, int(args.seconds / max(per, 1e-7)))
-        steps = int(max_over_ranks(pg, float(steps), dev))
-    barrier(pg, local)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_host0 = time.time()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        do_steps(steps)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    t_host1 = time.time()
-    barrier(pg, local)
-    clk = clocks.stop(t_host0, t_host1)
-    ms_max = max_over_ranks(pg, e0.elapsed_time(e1), dev)
+    steps, reps, ms_step, per_rep, region_s, clk = timed_region(args, stream, do_steps, pg, dev, clocks)
+    warm = max(0, args.warmup)
+    ms_max = ms_step * steps  # median over the repeats, max over ranks
     value = world * wbytes * steps / (ms_max / 1e3) / 1e9
     peaks, peak_src = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
@@ -1178,7 +1189,8 @@ def run_q4k(args, wl, world, rank, local, pg):
                        "parallelism": f"replicas x{world} (independent decode streams)"},
             "gops": world * r.ops() * steps / (ms_max / 1e3) / 1e9, "hbm_frac": value / world / hbm,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": (len(r.phases()) if phase else r.launches_per_step) * steps,
+            "gpu_launches": (len(r.phases()) if phase else r.launches_per_step) * steps * reps,
+            "repeats": reps, "timed_region_s": region_s,
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)
