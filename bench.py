@@ -74,6 +74,10 @@ def parse_args():
     p.add_argument("--phase-prefetch", choices=["none", "ahead1", "ahead2"], default="none",
                    help="phase path: each phase hints the weights of the phase one / two "
                         "later into L2 once it has read its input")
+    p.add_argument("--handoff", choices=["q8", "float"], default="q8",
+                   help="phase path: a phase's output reaches the next phase as Q8_0 written by "
+                        "the producing launch (q8), or as float32 quantised by every CTA of the "
+                        "reading launch (float)")
     p.add_argument("--prefetch", choices=["none", "all", "next"], default="none",
                    help="L2 prefetch of weights through mlq_prefetch_l2: all (whole pass "
                         "first) or next (one product ahead); measured slower in-chain, so off")
@@ -599,7 +603,7 @@ def measure_workload(args, wl, world, local, pg, *, path_arg="auto", with_e2e=Tr
         elif path == "fused":
             r.step_fused(copy=c)
         elif path == "phase":
-            r.step_phase(copy=c, prefetch=args.phase_prefetch)
+            r.step_phase(copy=c, prefetch=args.phase_prefetch, handoff=args.handoff)
         else:
             r.step(copy=c, prefetch=pf)
     assert r.weight_bytes() == wbytes
@@ -670,7 +674,8 @@ def measure_workload(args, wl, world, local, pg, *, path_arg="auto", with_e2e=Tr
     elif graphs and path in ("fused", "phase"):
         def calls_of(c):
             return r.fused_calls(c) if path == "fused" else r.phase_calls(
-                c, prefetch="self" if args.phase_prefetch != "none" else "none")
+                c, prefetch="self" if args.phase_prefetch != "none" else "none",
+                handoff=args.handoff)
         per_phase, tot_bytes, tot_us = [], 0.0, 0.0
         for k, (src, first, count) in enumerate(r.chain_phases()):
             us = back_to_back_us(stream, lambda j, k=k: calls_of(j % copies)[k](), launches)
@@ -781,6 +786,7 @@ def measure_workload(args, wl, world, local, pg, *, path_arg="auto", with_e2e=Tr
               f"({copies * wbytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
         "graphs": ("one graph per cycle of %d steps" % copies) if cycle is not None else False,
         "l2_prefetch": (args.phase_prefetch if path == "phase" else pf or "none"),
+        "handoff": args.handoff if path == "phase" else None,
     }
     del graphs, cycle, r
     torch.cuda.synchronize()

@@ -133,16 +133,22 @@ class WorkloadRunner:
             out += [(m.q[copy], m.host_q.nbytes), (m.d[copy], m.host_d.nbytes)]
         return out
 
-    def phase_calls(self, copy: int = 0, static_weights: bool = True, prefetch: str = "none"):
-        """One mlq_decode_phase call per phase.  A product whose output is
-        the input of a later phase also writes it in Q8_0 (into that input's
-        buffer), so the later phase starts from quantised bytes; the
-        workload's float inputs are quantised by the phase that reads them.
-        prefetch: "ahead1" / "ahead2" -- each phase hints the weights of the
-        phase one / two later into L2 (past the last phase: the next pass,
-        next weight copy); "self" -- the same phase's next copy (back-to-back
-        timing of one phase); "none"."""
-        key = ("phase", copy, static_weights, prefetch)
+    def phase_calls(self, copy: int = 0, static_weights: bool = True, prefetch: str = "none",
+                    handoff: str = "q8"):
+        """One mlq_decode_phase call per phase.  handoff "q8": a product whose
+        output is the input of a later phase also writes it in Q8_0 (into
+        that input's buffer), so the later phase starts from quantised bytes
+        (the producing phase then splits its rows in whole 32-row blocks);
+        "float": every phase reads its input as float32 and quantises it in
+        each CTA (rows split freely).  The workload's own float inputs are
+        quantised by the phase that reads them.  prefetch: "ahead1" /
+        "ahead2" -- each phase hints the weights of the phase one / two later
+        into L2 (past the last phase: the next pass, next weight copy);
+        "self" -- the same phase's next copy (back-to-back timing of one
+        phase); "none"."""
+        if handoff not in ("q8", "float"):
+            raise ValueError(f"handoff {handoff!r}")
+        key = ("phase", copy, static_weights, prefetch, handoff)
         if key not in self._chain_calls:
             if self.m != 1:
                 raise ValueError("decode phases are M = 1")
@@ -150,7 +156,7 @@ class WorkloadRunner:
             pre = set()   # sources whose producer quantises them
             for src, first, count in phases:
                 group = self.mats[first:first + count]
-                if all(m.spec.rows % I.QK == 0 for m in group):
+                if handoff == "q8" and all(m.spec.rows % I.QK == 0 for m in group):
                     pre.update(m.spec.name for m in group if m.spec.name in self.sources)
             flags = B.MLQ_F_STATIC_WEIGHTS if static_weights else 0
             calls = []
@@ -181,9 +187,9 @@ class WorkloadRunner:
         return self._chain_calls[key]
 
     def step_phase(self, copy: int = 0, stream=None, static_weights: bool = True,
-                   prefetch: str = "none") -> None:
+                   prefetch: str = "none", handoff: str = "q8") -> None:
         """One pass as one mlq_decode_phase launch per phase."""
-        for c in self.phase_calls(copy, static_weights, prefetch):
+        for c in self.phase_calls(copy, static_weights, prefetch, handoff):
             c(stream)
 
     def step_chain(self, copy: int = 0, stream=None) -> None:
