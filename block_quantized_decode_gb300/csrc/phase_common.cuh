@@ -342,7 +342,13 @@ inline int cut_up(const FusedArgs &a, int g) {  // smallest allowed cut >= g
 // balanced: each CTA takes its share of what is left (capped at L), so the
 // rows spread over all CTAs; otherwise each takes as much as it may
 // (greedy: uses the fewest CTAs, which decides whether L is feasible).
-inline bool split_rows(const FusedArgs &a, int total, int grid, int L, bool balanced, int *bounds) {
+// front_heavy (balanced only): a share that falls between two allowed cuts
+// is rounded up rather than down (within L), so the lower-numbered CTAs hold
+// the larger shares.  CTAs of a launch start in index order as SMs free up
+// (under programmatic dependent launch the last ones start several
+// microseconds after the first), so the larger shares should go first.
+inline bool split_rows(const FusedArgs &a, int total, int grid, int L, bool balanced, int *bounds,
+                       bool front_heavy = false) {
   int pos = 0;
   bounds[0] = 0;
   for (int b = 0; b < grid; ++b) {
@@ -352,7 +358,12 @@ inline bool split_rows(const FusedArgs &a, int total, int grid, int L, bool bala
       const int share = (rem + (grid - b) - 1) / (grid - b);
       take = share < L ? share : L;
     }
-    int end = cut_down(a, pos + take < total ? pos + take : total);
+    const int want = pos + take < total ? pos + take : total;
+    int end = cut_down(a, want);
+    if (front_heavy && end < want) {
+      const int up = cut_up(a, want);
+      if (up - pos <= L) end = up;
+    }
     if (end <= pos && pos < total) {
       end = cut_up(a, pos + 1);
       if (end - pos > L) return false;
@@ -363,14 +374,16 @@ inline bool split_rows(const FusedArgs &a, int total, int grid, int L, bool bala
   return pos == total;
 }
 // The split with the smallest largest run (the slowest CTA sets the time).
-inline int plan_rows(const FusedArgs &a, int total, int grid, int *bounds) {
+inline int plan_rows(const FusedArgs &a, int total, int grid, int *bounds, bool front_heavy = false) {
   int lo = 1, hi = total;
   while (lo < hi) {  // smallest L the greedy split achieves
     const int mid = lo + (hi - lo) / 2;
     if (split_rows(a, total, grid, mid, false, bounds)) hi = mid;
     else lo = mid + 1;
   }
-  if (!split_rows(a, total, grid, lo, true, bounds)) split_rows(a, total, grid, lo, false, bounds);
+  if (!(front_heavy && split_rows(a, total, grid, lo, true, bounds, true)) &&
+      !split_rows(a, total, grid, lo, true, bounds))
+    split_rows(a, total, grid, lo, false, bounds);
   int mx = 0;
   for (int b = 0; b < grid; ++b) mx = bounds[b + 1] - bounds[b] > mx ? bounds[b + 1] - bounds[b] : mx;
   return mx;

@@ -279,7 +279,15 @@ static cudaError_t launch_ring_t(const LaunchCtx &ctx, const FusedArgs &args) {
   if (a.total_rows <= 0 || nb % 4 != 0) return cudaErrorNotSupported;
   int grid = ctx.num_sms < a.total_rows ? ctx.num_sms : a.total_rows;
   grid = grid < kPhMaxGrid ? grid : kPhMaxGrid;
-  const int rows_max = plan_rows(a, a.total_rows, grid, pa.bounds);
+  // Front-heavy split: the CTAs that start first (lowest index) take the
+  // larger shares (the 11008-row product: the 40 CTAs with three 32-row
+  // blocks start first instead of last).  MLQ_RING_FRONT=0 turns it off
+  // (A/B timing).
+  static const bool front_env = [] {
+    const char *e = std::getenv("MLQ_RING_FRONT");
+    return e == nullptr || e[0] != '0';
+  }();
+  const int rows_max = plan_rows(a, a.total_rows, grid, pa.bounds, front_env);
   const size_t rowq = static_cast<size_t>(nb) * (QT == 1 ? 16 : 32);
   auto up128 = [](size_t v) { return (v + 127) / 128 * 128; };
   const size_t xs = up128(static_cast<size_t>(nb) * (kQK + 4));
