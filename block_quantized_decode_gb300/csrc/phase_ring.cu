@@ -235,35 +235,31 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
   consumers_sync<NW>();
   if (*abort_v) return;
 
-  // y: the K-chunks of each row added in a fixed order, product by product
+  // y and the quantised outputs in one pass.  Warp w takes every NW-th run
+  // of 32 of the CTA's rows (within a product with a quantised output these
+  // are its whole 32-row blocks), one row per lane: the K-chunk partial sums
+  // added in a fixed order, y stored, and a block quantised from exactly the
+  // floats stored -- its maximum by one warp reduction on the float bit
+  // patterns (non-negative floats order as unsigned integers).
+  int t = 0;
   for (int jj = 0, off = 0; jj < a.nproducts; off += a.prod[jj].rows, ++jj) {
     const int lo = max(ra, off), hi = min(rb, off + a.prod[jj].rows);
-    for (int gr = lo + tid; gr < hi; gr += NW * 32) {
-      const int r = gr - ra;
-      float v = part_s[r * C];
-      for (int cc = 1; cc < C; ++cc) v += part_s[r * C + cc];
-      a.prod[jj].y[gr - off] = v;
-      part_s[r * C] = v;
-    }
-  }
-  if (a.any_yq) {
-    consumers_sync<NW>();
-    // each whole 32-row block of a product with a quantised output, from
-    // exactly the stored floats; one warp per block
-    int t = 0;
-    for (int jj = 0, off = 0; jj < a.nproducts; off += a.prod[jj].rows, ++jj) {
-      const int lo = max(ra, off), hi = min(rb, off + a.prod[jj].rows);
-      if (a.prod[jj].yq == nullptr || hi <= lo) continue;
-      for (int gr = lo; gr < hi; gr += kQK, ++t) {
-        if ((t & (NW - 1)) != warp) continue;
-        const float v = part_s[(gr - ra + lane) * C];
-        uint32_t m = __float_as_uint(fabsf(v));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-        const float amax = __uint_as_float(m);
+    int8_t *yq = a.prod[jj].yq;
+    for (int g0 = lo; g0 < hi; g0 += kQK, ++t) {
+      if ((t & (NW - 1)) != warp) continue;
+      const int gr = g0 + lane;
+      float v = 0.0f;
+      if (gr < hi) {
+        const int r = gr - ra;
+        v = part_s[r * C];
+        for (int cc = 1; cc < C; ++cc) v += part_s[r * C + cc];
+        a.prod[jj].y[gr - off] = v;
+      }
+      if (yq != nullptr) {  // warp-uniform; gr < hi for every lane here
+        const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v))));
         const float dd = amax / 127.0f;
         const float id = amax != 0.0f ? 127.0f / amax : 0.0f;
-        a.prod[jj].yq[gr - off + lane] = static_cast<int8_t>(quant_one(v, id));
+        yq[gr - off] = static_cast<int8_t>(quant_one(v, id));
         if (lane == 0) a.prod[jj].yd[(gr - off) / kQK] = dd;
       }
     }
