@@ -389,6 +389,10 @@ mlq_status mlq_decode_chain(const mlq_chain_phase *phases, int nphases,
   return from_cuda(mlq::launch_decode_chain(ctx, products[0].W.type, a));
 }
 
+// The fixed counter array holds one word per phase plus the exit counter.
+static_assert(MLQ_CHAIN_STATIC_MAX_PHASES + 1 <= mlq::kStaticChainWords,
+              "the static chain's counter array is too small for its phase limit");
+
 mlq_status mlq_decode_chain_static(const mlq_chain_phase *phases, int nphases,
                                    const mlq_chain_product *products, int nproducts,
                                    void *stream) {

@@ -404,7 +404,11 @@ typedef struct {
  * work overlaps on the GPU (different streams, or different host threads)
  * race and give wrong results or MLQ_E_TIMEOUT: serialise them.  The first
  * call on each device looks up the array's device address (once, with that
- * device current); make that first call before any stream capture.
+ * device current); make that first call before any stream capture.  The
+ * address is kept for the life of the process: after cudaDeviceReset the
+ * library's device state (this array, like the per-device status word and
+ * properties that every entry point caches) is gone, so do not call into the
+ * library on that device again in the same process.
  * Nothing on the pages corresponds to this entry point. */
 mlq_status mlq_decode_chain_static(const mlq_chain_phase *phases, int nphases,
                                    const mlq_chain_product *products, int nproducts,

@@ -24,7 +24,7 @@
  *     rounds with q = trunc(x*id + copysign(0.5, x)), id = 127/amax; Q4
  *     kernels unpack nibbles (and 0x0F, shift 4, subtract 8) into int8 and
  *     then reuse the Q8 path.
- * Readings where the page is silent (each is listed in the design doc):
+ * Readings taken where the page is silent:
  *   - the rounding formula of Sec. 5 is normative over "round(x/d)" of Sec. 4;
  *     d is stored as amax/127, not as 1/id;
  *   - a NaN produced by 0 * inf (amax so small that 127/amax overflows) is
@@ -190,8 +190,8 @@ int mlqo_gemm_small_m(float *Y, int ldy, int type, const uint8_t *wq, const floa
  * softmax, sum of axpy over positions; GQA: the KV head of query head h is
  * h / (n_heads / n_kv_heads)).  The page fixes float32 interfaces but not
  * the internal precision of these steps, so they are computed here in
- * double and rounded to float once per output (readings listed in
- * the design doc):
+ * double and rounded to float once per output (readings taken where the
+ * page is silent):
  *   - rmsnorm: o_j = w_j * x_j / sqrt(sum_i x_i^2 / n + eps)
  *   - softmax: x_j = exp(x_j - max) / sum_i exp(x_i - max)
  *   - silu_mul: g_j = g_j / (1 + exp(-g_j)) * u_j
@@ -326,7 +326,7 @@ int mlqo_attention(float *o, const float *q, const float *kc, const float *vc, i
  * sum over the 8 sub-blocks of s_b * sum_i a_i w_i fits int32 with ~70x
  * headroom (8*63*32*127*15 = 3.07e7), so it is formed in integers and
  * converted to float once per block; the format keeps per-32 asymmetric
- * minima.  Readings where the page is silent (listed in the design doc):
+ * minima.  Readings taken where the page is silent:
  *   - a block ("super-block") is 256 elements = 8 sub-blocks of 32; per
  *     super-block a float32 scale d and a float32 scale of the minima dmin;
  *     per sub-block a 6-bit scale s_b and a 6-bit minimum m_b, one per byte;
@@ -434,8 +434,7 @@ int mlqo_matvec_q4k(float *y, const uint8_t *wq, const uint8_t *ws, const float 
  *   y[r] += ((float)sumi * scale_b) * dx_b   in float32, blocks in order.
  * The signed-offset correction reaches the same int32 sumi exactly:
  * sum (B' + 128 - zp) a = sum B' a + (128 - zp) sum a; the oracle forms
- * sumi from w_i directly.  Readings where the page is silent (listed in
- * the design doc):
+ * sumi from w_i directly.  Readings taken where the page is silent:
  *   - 4-bit blocks of `blk` elements pack element j in the low nibble and
  *     element j + blk/2 in the high nibble of byte j (the Q4_0 order, which
  *     it equals for blk = 32); 4-bit weights have no zero points;

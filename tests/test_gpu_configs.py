@@ -37,10 +37,19 @@ from block_quantized_decode_gb300.runner import WorkloadRunner  # noqa: E402
 
 
 def run_and_check(wl, full_rows_limit=300_000_000, graph=False, chain=False, fused=False,
-                  static_weights=True, phase=False):
+                  static_weights=True, phase=False, static_chain=False):
     r = WorkloadRunner(wl, copies=1)
     if chain:
         step = r.step_chain
+    elif static_chain:  # mlq_decode_chain_static: the chain without a caller workspace
+        import block_quantized_decode_gb300 as M
+        phases = [M.ChainPhase(r.fp32[src], r.sources[src], first, count, r.qbuf[src].q, r.qbuf[src].d)
+                  for src, first, count in r.chain_phases()]
+        products = [M.ChainProduct(M.QTensor(m.q[0], m.d[0], m.spec.rows, m.spec.cols, m.spec.wtype), m.y)
+                    for m in r.mats]
+
+        def step():
+            M.mlq_decode_chain_static(phases, products)
     elif phase:
         def step():
             r.step_phase(static_weights=static_weights)

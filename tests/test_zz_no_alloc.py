@@ -89,7 +89,22 @@ def test_static_chain_matches_workspace_chain(M, wl):
                               f"call {call}: {m.spec.name}")
 
 
+@pytest.mark.parametrize("wl", [I.tinyllama_layer(), I.llama7b_ffn(I.Q4_0)],
+                         ids=["tinyllama_layer_q4_0", "llama7b_ffn8_q4_0"])
+def test_static_chain_against_oracle(M, wl):
+    """The static chain checked against the oracle directly, per step on the
+    GPU's own inputs (quantised activations byte for byte, every product
+    within tolerance), on two calls in a row."""
+    from tests.test_gpu_configs import run_and_check
+    for _ in range(2):
+        run_and_check(wl, static_chain=True)
+        assert M.mlq_last_device_error() == M.MLQ_OK
+
+
 def test_static_chain_rejects_too_many_phases(M):
+    """25 phases: above MLQ_CHAIN_STATIC_MAX_PHASES, which equals the general
+    chain limit MLQ_CHAIN_MAX_PHASES, so this checks the limit the two entry
+    points share (the static array itself holds one word more than that)."""
     x = torch.zeros(128, device="cuda:0")
     q = torch.zeros(4 * 64, dtype=torch.uint8, device="cuda:0")
     d = torch.zeros(4 * 4, device="cuda:0")
