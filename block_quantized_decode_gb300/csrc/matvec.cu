@@ -322,18 +322,30 @@ static cudaError_t launch_qt(const LaunchCtx &ctx, MatvecArgs a, int upr) {
   return launch_variant<QT, 4, SUMI>(ctx, a);
 }
 
-// Kernel choice.  Measured on GB300 (graph replays, programmatic dependent
-// launch): the register-pipelined kernel above is faster for rows of 2048
-// or more elements (the Llama-7B FFN and TinyLlama shapes), the bulk-copy
-// ring kernel for very many short rows (a 151936 x 896 Q8_0 lm_head: 29.5 us
-// vs 54 us), where per-task overheads dominate the register kernel.
-// MLQ_MATVEC_KERNEL=ldg|tma overrides the choice (A/B timing).
+// Kernel choice.  A product y[r0, r1) of at least kPhaseMinBytes of
+// weights runs as a one-product decode phase (phase.cu: the CTA's rows whole
+// in shared memory; phase_ring.cu: streamed through a ring of bulk-copy
+// stages), the kernels the decode phases use, wherever they take the shape
+// (K a multiple of 128, at most 16384).  Measured on GB300, back-to-back
+// launches with static weights: 4096 x 11008 Q4_0 7.35 us (9.32 us on the
+// register kernel), Q8_0 9.73 us (14.11), 151936 x 896 Q8_0 24.3 us (34.1 on
+// the ring kernel of matvec_tma.cu).  Smaller products stay on the kernels
+// of this file: at 2.6 MB and below they are 0.2-0.4 us faster back to back,
+// and chained behind quantize launches the TinyLlama layer's 7.2 MB products
+// cost more as phases (the layer's calls step: 34.9 us with its gate, up and
+// down as phases, 25.9 us without).  The per-block sums of the test hook,
+// and the other shapes, take
+// the register-pipelined kernel above for rows of 2048 or more elements or
+// the bulk-copy ring kernel for very many short rows.
+// MLQ_MATVEC_KERNEL=phase|ldg|tma overrides the choice (A/B timing, tests).
+constexpr size_t kPhaseMinBytes = 16u << 20;
 static int kernel_override() {
   static const int v = [] {
     const char *e = std::getenv("MLQ_MATVEC_KERNEL");
     if (e == nullptr) return 0;
     if (e[0] == 'l') return 1;
     if (e[0] == 't') return 2;
+    if (e[0] == 'p') return 3;
     return 0;
   }();
   return v;
@@ -341,7 +353,7 @@ static int kernel_override() {
 
 static bool prefer_tma(int nb, int rows, int num_sms) {
   const int o = kernel_override();
-  if (o != 0) return o == 2;
+  if (o == 1 || o == 2) return o == 2;
   return nb <= 32 && rows >= 64 * num_sms;
 }
 
@@ -349,6 +361,28 @@ cudaError_t launch_matvec_m1(const LaunchCtx &ctx, int qtype, const void *wq, co
                              int nb, const int8_t *xq, const float *xd, float *y, int32_t *sumi,
                              int r0, int r1) {
   if (r1 <= r0) return cudaSuccess;
+  const int o = kernel_override();
+  const size_t rowq = static_cast<size_t>(nb) * (qtype == 1 ? 16 : 32);
+  const size_t wbytes = static_cast<size_t>(r1 - r0) * (rowq + static_cast<size_t>(nb) * 4);
+  if (y != nullptr && (o == 3 || (o == 0 && wbytes >= kPhaseMinBytes))) {
+    // rows [r0, r1) as a one-product phase on the Q8_0 input
+    FusedArgs f = {};
+    f.prod[0].wq = static_cast<const uint8_t *>(wq) + static_cast<size_t>(r0) * rowq;
+    f.prod[0].wd = wd + static_cast<size_t>(r0) * nb;
+    f.prod[0].y = y + r0;
+    f.prod[0].rows = r1 - r0;
+    f.nproducts = 1;
+    f.xq_in = xq;
+    f.xd_in = xd;
+    f.nb = nb;
+    f.total_rows = r1 - r0;
+    f.nchunks = 1;
+    f.early = ctx.early_weights ? 1 : 0;
+    f.status = ctx.status;
+    f.wait_ns = ctx.wait_ns;
+    const cudaError_t e = launch_phase(ctx, qtype, f);
+    if (e != cudaErrorNotSupported) return e;
+  }
   if (prefer_tma(nb, r1 - r0, ctx.num_sms)) {
     const cudaError_t e = launch_matvec_m1_tma(ctx, qtype, wq, wd, nb, xq, xd, y, sumi, r0, r1);
     if (e != cudaErrorNotSupported) return e;

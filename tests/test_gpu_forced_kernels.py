@@ -1,7 +1,10 @@
-"""The M = 1 products have two kernels (register-pipelined loads, and a
-bulk-copy ring); the dispatcher picks one per shape.  Re-run the per-block
-sum and product parity tests with each kernel forced, in child processes
-(the choice is read once per process from MLQ_MATVEC_KERNEL)."""
+"""The M = 1 products run as one-product decode phases (phase.cu /
+phase_ring.cu) where those kernels take the shape, else on one of two
+kernels of their own (register-pipelined loads, and a bulk-copy ring); the
+dispatcher picks per shape.  Re-run the per-block sum and product parity
+tests with each choice forced, in child processes (the choice is read once
+per process from MLQ_MATVEC_KERNEL); the small-M, fused and phase kernels
+likewise."""
 import os
 import subprocess
 import sys
@@ -14,7 +17,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.mark.skipif(os.environ.get("MLQ_MATVEC_KERNEL") is not None,
                     reason="already inside a forced-kernel run")
-@pytest.mark.parametrize("kernel", ["ldg", "tma"])
+@pytest.mark.parametrize("kernel", ["ldg", "tma", "phase"])
 def test_parity_with_forced_kernel(kernel):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
