@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmlq.so")
-SOURCES = ["capi.cu", "quantize.cu", "matvec.cu", "matvec_tma.cu", "gemm_small_m.cu", "prefetch.cu", "chain.cu", "fused.cu", "gemm_mma.cu", "gemm_mma_cluster.cu", "gemm_umma.cu", "gemm_ring.cu", "phase.cu", "phase_ring.cu", "layer.cu", "stream.cu", "q4k.cu", "nbits.cu"]
+SOURCES = ["capi.cu", "quantize.cu", "matvec.cu", "matvec_tma.cu", "gemm_small_m.cu", "prefetch.cu", "chain.cu", "fused.cu", "gemm_mma.cu", "gemm_mma_cluster.cu", "gemm_umma.cu", "gemm_ring.cu", "phase.cu", "phase_ring.cu", "layer.cu", "stream.cu", "q4k.cu", "nbits.cu", "diag.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

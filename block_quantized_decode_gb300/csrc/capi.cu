@@ -219,6 +219,7 @@ mlq_status mlq_init(void) {
 }
 
 mlq_status mlq_quantize_q8(mlq_qact *out, const float *x, int k, void *stream) {
+  mlq::diag_entry("mlq_quantize_q8", "k=%d m=%d", k, out ? out->m : -1);
   if (out == nullptr || x == nullptr || out->q == nullptr || out->d == nullptr) return MLQ_E_NULL;
   if (!cols_ok(k) || out->n != k || out->m < 1) return MLQ_E_SHAPE;
   if (!aligned(x, 16) || !aligned(out->q, 16) || !aligned(out->d, 16)) return MLQ_E_ALIGN;
@@ -230,24 +231,28 @@ mlq_status mlq_quantize_q8(mlq_qact *out, const float *x, int k, void *stream) {
 
 mlq_status mlq_matvec_q4(float *y, const mlq_qtensor *W, const mlq_qact *x, int r0, int r1,
                          void *stream) {
+  mlq::diag_entry("mlq_matvec_q4", "rows=%d cols=%d r=[%d,%d)", W ? W->rows : -1, W ? W->cols : -1, r0, r1);
   if (y == nullptr) return MLQ_E_NULL;
   return matvec_common(y, nullptr, W, x, r0, r1, stream, MLQ_Q4_0);
 }
 
 mlq_status mlq_matvec_q8(float *y, const mlq_qtensor *W, const mlq_qact *x, int r0, int r1,
                          void *stream) {
+  mlq::diag_entry("mlq_matvec_q8", "rows=%d cols=%d r=[%d,%d)", W ? W->rows : -1, W ? W->cols : -1, r0, r1);
   if (y == nullptr) return MLQ_E_NULL;
   return matvec_common(y, nullptr, W, x, r0, r1, stream, MLQ_Q8_0);
 }
 
 mlq_status mlq_block_sumi(int32_t *sumi, const mlq_qtensor *W, const mlq_qact *x, int r0, int r1,
                           void *stream) {
+  mlq::diag_entry("mlq_block_sumi", "rows=%d cols=%d r=[%d,%d)", W ? W->rows : -1, W ? W->cols : -1, r0, r1);
   if (sumi == nullptr) return MLQ_E_NULL;
   return matvec_common(nullptr, sumi, W, x, r0, r1, stream, -1);
 }
 
 mlq_status mlq_gemm_q4_small_m(float *Y, int ldy, const mlq_qtensor *W, const mlq_qact *X, int M,
                                int r0, int r1, void *stream) {
+  mlq::diag_entry("mlq_gemm_q4_small_m", "M=%d rows=%d cols=%d r=[%d,%d)", M, W ? W->rows : -1, W ? W->cols : -1, r0, r1);
   if (Y == nullptr) return MLQ_E_NULL;
   mlq_status s = check_weights(W, X, r0, r1);
   if (s != MLQ_OK) return s;
@@ -264,6 +269,7 @@ mlq_status mlq_gemm_q4_small_m(float *Y, int ldy, const mlq_qtensor *W, const ml
 mlq_status mlq_matvec_fused(const float *x, int n, const mlq_chain_product *products,
                             int nproducts, int8_t *xq_out, float *xd_out, unsigned flags,
                             void *stream) {
+  mlq::diag_entry("mlq_matvec_fused", "n=%d products=%d", n, nproducts);
   if (x == nullptr || products == nullptr) return MLQ_E_NULL;
   if ((xq_out == nullptr) != (xd_out == nullptr)) return MLQ_E_NULL;
   if (nproducts < 1 || nproducts > MLQ_FUSED_MAX_PRODUCTS || !cols_ok(n)) return MLQ_E_SHAPE;
@@ -305,6 +311,7 @@ mlq_status mlq_decode_phase(const mlq_phase_input *in, const mlq_phase_product *
                             int nproducts, const void *const *prefetch,
                             const size_t *prefetch_bytes, int nprefetch, unsigned flags,
                             void *stream) {
+  mlq::diag_entry("mlq_decode_phase", "n=%d products=%d input=%s", in ? in->n : -1, nproducts, in && in->x ? "f32" : "q8");
   if (in == nullptr || products == nullptr) return MLQ_E_NULL;
   if (nprefetch < 0 || nprefetch > MLQ_PHASE_MAX_PREFETCH) return MLQ_E_SHAPE;
   if (nprefetch > 0 && (prefetch == nullptr || prefetch_bytes == nullptr)) return MLQ_E_NULL;
@@ -376,6 +383,7 @@ size_t mlq_chain_workspace_bytes(int nphases) {
 mlq_status mlq_decode_chain(const mlq_chain_phase *phases, int nphases,
                             const mlq_chain_product *products, int nproducts, void *workspace,
                             size_t workspace_bytes, void *stream) {
+  mlq::diag_entry("mlq_decode_chain", "phases=%d products=%d", nphases, nproducts);
   mlq::ChainArgs a;
   mlq_status s = build_chain_args(phases, nphases, products, nproducts, &a);
   if (s != MLQ_OK) return s;
@@ -396,6 +404,7 @@ static_assert(MLQ_CHAIN_STATIC_MAX_PHASES + 1 <= mlq::kStaticChainWords,
 mlq_status mlq_decode_chain_static(const mlq_chain_phase *phases, int nphases,
                                    const mlq_chain_product *products, int nproducts,
                                    void *stream) {
+  mlq::diag_entry("mlq_decode_chain_static", "phases=%d products=%d", nphases, nproducts);
   mlq::ChainArgs a;
   mlq_status s = build_chain_args(phases, nphases, products, nproducts, &a);
   if (s != MLQ_OK) return s;
@@ -424,6 +433,7 @@ mlq_status mlq_debug_chain_plan(const mlq_chain_phase *phases, int nphases,
 }
 
 mlq_status mlq_prefetch_l2(const void *const *ptrs, const size_t *bytes, int n, void *stream) {
+  mlq::diag_entry("mlq_prefetch_l2", "");
   if (n < 0 || n > MLQ_MAX_PREFETCH_RANGES) return MLQ_E_SHAPE;
   if (n > 0 && (ptrs == nullptr || bytes == nullptr)) return MLQ_E_NULL;
   mlq::PrefetchList list;
@@ -469,6 +479,7 @@ mlq_status q4k_common(float *y, int32_t *isum, int32_t *msum, const mlq_q4k_tens
 }  // namespace
 
 mlq_status mlq_quantize_q8k(mlq_q8k_act *out, const float *x, int k, void *stream) {
+  mlq::diag_entry("mlq_quantize_q8k", "k=%d", k);
   if (out == nullptr || x == nullptr || out->q == nullptr || out->d == nullptr || out->bsums == nullptr)
     return MLQ_E_NULL;
   if (!q4k_cols_ok(k) || out->n != k) return MLQ_E_SHAPE;
@@ -482,6 +493,7 @@ mlq_status mlq_quantize_q8k(mlq_q8k_act *out, const float *x, int k, void *strea
 
 mlq_status mlq_matvec_q4k(float *y, const mlq_q4k_tensor *W, const mlq_q8k_act *x, int r0, int r1,
                           void *stream) {
+  mlq::diag_entry("mlq_matvec_q4k", "rows=%d cols=%d r=[%d,%d)", W ? W->rows : -1, W ? W->cols : -1, r0, r1);
   if (y == nullptr) return MLQ_E_NULL;
   return q4k_common(y, nullptr, nullptr, W, x, r0, r1, stream);
 }
@@ -494,6 +506,7 @@ mlq_status mlq_block_sums_q4k(int32_t *isum, int32_t *msum, const mlq_q4k_tensor
 
 mlq_status mlq_q4k_phase(const float *x, int k, const mlq_q4k_product *products, int nproducts,
                          void *stream) {
+  mlq::diag_entry("mlq_q4k_phase", "k=%d products=%d", k, nproducts);
   if (x == nullptr || products == nullptr) return MLQ_E_NULL;
   if (nproducts < 1 || nproducts > 4 || !q4k_cols_ok(k)) return MLQ_E_SHAPE;
   if (!aligned(x, 16)) return MLQ_E_ALIGN;
@@ -551,6 +564,7 @@ mlq_status nbits_common(float *y, int32_t *sumi, const mlq_nbits_tensor *W, cons
 }  // namespace
 
 mlq_status mlq_quantize_blk(mlq_blk_act *out, const float *x, int k, void *stream) {
+  mlq::diag_entry("mlq_quantize_blk", "k=%d blk=%d", k, out ? out->blk : -1);
   if (out == nullptr || x == nullptr || out->q == nullptr || out->d == nullptr || out->bsums == nullptr)
     return MLQ_E_NULL;
   if (out->blk != 32 && out->blk != 128) return MLQ_E_SHAPE;
@@ -565,6 +579,7 @@ mlq_status mlq_quantize_blk(mlq_blk_act *out, const float *x, int k, void *strea
 
 mlq_status mlq_nbits_phase(const float *x, int k, const mlq_nbits_product *products, int nproducts,
                            void *stream) {
+  mlq::diag_entry("mlq_nbits_phase", "k=%d products=%d", k, nproducts);
   if (x == nullptr || products == nullptr) return MLQ_E_NULL;
   if (nproducts < 1 || nproducts > 4) return MLQ_E_SHAPE;
   if (!aligned(x, 16)) return MLQ_E_ALIGN;
@@ -599,6 +614,7 @@ mlq_status mlq_nbits_phase(const float *x, int k, const mlq_nbits_product *produ
 
 mlq_status mlq_matvec_nbits(float *y, const mlq_nbits_tensor *W, const mlq_blk_act *x, int r0, int r1,
                             void *stream) {
+  mlq::diag_entry("mlq_matvec_nbits", "rows=%d cols=%d bits=%d blk=%d r=[%d,%d)", W ? W->rows : -1, W ? W->cols : -1, W ? W->bits : -1, W ? W->blk : -1, r0, r1);
   if (y == nullptr) return MLQ_E_NULL;
   return nbits_common(y, nullptr, W, x, r0, r1, stream);
 }
@@ -624,6 +640,7 @@ bool floats_ok(const void *p) { return aligned(p, 4); }
 
 mlq_status mlq_rmsnorm(float *o, const float *x, const float *w, int n, float eps, mlq_qact *oq,
                        void *stream) {
+  mlq::diag_entry("mlq_rmsnorm", "n=%d", n);
   if (x == nullptr || w == nullptr || (o == nullptr && oq == nullptr)) return MLQ_E_NULL;
   if (n < 1 || n > MLQ_MAX_COLS || !(eps >= 0.0f)) return MLQ_E_SHAPE;
   if (!floats_ok(x) || !floats_ok(w) || !floats_ok(o)) return MLQ_E_ALIGN;
@@ -637,6 +654,7 @@ mlq_status mlq_rmsnorm(float *o, const float *x, const float *w, int n, float ep
 
 mlq_status mlq_add_rmsnorm(float *x, const float *y, const float *w, int n, float eps, float *o,
                            mlq_qact *oq, void *stream) {
+  mlq::diag_entry("mlq_add_rmsnorm", "n=%d", n);
   if (x == nullptr || y == nullptr || w == nullptr || (o == nullptr && oq == nullptr)) return MLQ_E_NULL;
   if (n < 1 || n > MLQ_MAX_COLS || !(eps >= 0.0f)) return MLQ_E_SHAPE;
   if (!floats_ok(x) || !floats_ok(y) || !floats_ok(w) || !floats_ok(o)) return MLQ_E_ALIGN;
@@ -649,6 +667,7 @@ mlq_status mlq_add_rmsnorm(float *x, const float *y, const float *w, int n, floa
 }
 
 mlq_status mlq_add(float *y, const float *x, int n, void *stream) {
+  mlq::diag_entry("mlq_add", "n=%d", n);
   if (y == nullptr || x == nullptr) return MLQ_E_NULL;
   if (n < 1 || n > MLQ_MAX_COLS) return MLQ_E_SHAPE;
   if (!floats_ok(y) || !floats_ok(x)) return MLQ_E_ALIGN;
@@ -659,6 +678,7 @@ mlq_status mlq_add(float *y, const float *x, int n, void *stream) {
 }
 
 mlq_status mlq_softmax(float *x, int n, void *stream) {
+  mlq::diag_entry("mlq_softmax", "n=%d", n);
   if (x == nullptr) return MLQ_E_NULL;
   if (n < 1 || n > MLQ_MAX_COLS) return MLQ_E_SHAPE;
   if (!floats_ok(x)) return MLQ_E_ALIGN;
@@ -669,6 +689,7 @@ mlq_status mlq_softmax(float *x, int n, void *stream) {
 }
 
 mlq_status mlq_silu_mul(float *g, const float *u, int n, mlq_qact *gq, void *stream) {
+  mlq::diag_entry("mlq_silu_mul", "n=%d", n);
   if (g == nullptr || u == nullptr) return MLQ_E_NULL;
   if (n < 1 || n > MLQ_MAX_COLS) return MLQ_E_SHAPE;
   if (!floats_ok(g) || !floats_ok(u)) return MLQ_E_ALIGN;
@@ -681,6 +702,7 @@ mlq_status mlq_silu_mul(float *g, const float *u, int n, mlq_qact *gq, void *str
 
 mlq_status mlq_rope_tables(float *cos_t, float *sin_t, int max_seq, int head_dim, float theta,
                            void *stream) {
+  mlq::diag_entry("mlq_rope_tables", "");
   if (cos_t == nullptr || sin_t == nullptr) return MLQ_E_NULL;
   if (max_seq < 1 || max_seq > MLQ_MAX_SEQ || head_dim < 2 || head_dim > MLQ_MAX_HEAD_DIM ||
       head_dim % 2 != 0 || !(theta > 0.0f))
@@ -703,6 +725,7 @@ bool heads_ok(int head_dim, int n_heads, int n_kv_heads) {
 mlq_status mlq_rope(float *q, float *k, const float *cos_row, const float *sin_row, int head_dim,
                     int n_heads, int n_kv_heads, float *k_out, const float *v, float *v_out,
                     void *stream) {
+  mlq::diag_entry("mlq_rope", "");
   if (q == nullptr || k == nullptr || cos_row == nullptr || sin_row == nullptr) return MLQ_E_NULL;
   if ((v == nullptr) != (v_out == nullptr)) return MLQ_E_NULL;
   if (!heads_ok(head_dim, n_heads, n_kv_heads)) return MLQ_E_SHAPE;
@@ -719,6 +742,7 @@ mlq_status mlq_rope(float *q, float *k, const float *cos_row, const float *sin_r
 mlq_status mlq_attention(float *o, mlq_qact *oq, const float *q, const float *k_cache,
                          const float *v_cache, int n_pos, int head_dim, int n_heads, int n_kv_heads,
                          void *stream) {
+  mlq::diag_entry("mlq_attention", "");
   if (o == nullptr || q == nullptr || k_cache == nullptr || v_cache == nullptr) return MLQ_E_NULL;
   if (!heads_ok(head_dim, n_heads, n_kv_heads) || n_pos < 1 || n_pos > MLQ_MAX_SEQ) return MLQ_E_SHAPE;
   if (oq != nullptr && head_dim % MLQ_QK != 0) return MLQ_E_SHAPE;

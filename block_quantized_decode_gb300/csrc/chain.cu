@@ -374,6 +374,7 @@ cudaError_t launch_decode_chain(const LaunchCtx &ctx, int qtype, const ChainArgs
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  diag_launch_cfg(reinterpret_cast<const void *>(kern), cfg);
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 

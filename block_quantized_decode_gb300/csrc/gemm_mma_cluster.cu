@@ -700,6 +700,9 @@ cudaError_t launch_gemm_q4_mma_cluster(const LaunchCtx &ctx, const void *wq, con
   cfg.gridDim = dim3(static_cast<unsigned>(a.G * P));
   cfg.dynamicSmemBytes = L.bytes;
   cfg.numAttrs = ctx.pdl ? 2 : 1;
+  diag_note("mma_cluster: M=%d K-parts=%d clusters=%d rows/round=%d rounds=%d slots=%d", M, P, a.G, a.H, nrounds,
+            a.slots);
+  diag_launch_cfg(reinterpret_cast<const void *>(kern), cfg);
   return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 

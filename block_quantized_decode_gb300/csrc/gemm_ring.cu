@@ -284,6 +284,8 @@ static cudaError_t launch_ring_mm(const LaunchCtx &ctx, GrArgs a) {
   a.stage_bytes = static_cast<int>(stage);
   a.part = static_cast<int>(static_cast<size_t>(ns) * stage);
   const size_t smem = static_cast<size_t>(ns) * stage + part;
+  diag_note("ring: M=%d rows/CTA<=%d chunks=%d rows/stage=%d slots=%d stage=%zuB", a.M, rows_max, a.C, R, ns,
+            stage);
   auto kern = gemm_q4_ring_kernel<MM, NBL>;
   static const cudaError_t attr = [&] {
     prefer_max_shared(kern);

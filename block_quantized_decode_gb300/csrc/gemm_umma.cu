@@ -819,6 +819,7 @@ cudaError_t launch_gemm_q4_umma(const LaunchCtx &ctx, const void *wq, const floa
     return cudaErrorNotSupported;
   cfg.gridDim = dim3(static_cast<unsigned>(a.G * P));
   cfg.numAttrs = ctx.pdl ? 2 : 1;
+  diag_launch_cfg(reinterpret_cast<const void *>(kern), cfg);
   return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 

@@ -478,6 +478,7 @@ cudaError_t launch_attention(const LaunchCtx &ctx, AttnArgs a) {
   cfg.stream = ctx.stream;
   cfg.attrs = at;
   cfg.numAttrs = ctx.pdl ? 2 : 1;
+  diag_launch_cfg(reinterpret_cast<const void *>(kern), cfg);
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 

@@ -380,9 +380,11 @@ cudaError_t launch_matvec_m1(const LaunchCtx &ctx, int qtype, const void *wq, co
     f.early = ctx.early_weights ? 1 : 0;
     f.status = ctx.status;
     f.wait_ns = ctx.wait_ns;
+    diag_note("route=phase");
     const cudaError_t e = launch_phase(ctx, qtype, f);
     if (e != cudaErrorNotSupported) return e;
   }
+  diag_note("route=%s", prefer_tma(nb, r1 - r0, ctx.num_sms) ? "ring" : "ldg");
   if (prefer_tma(nb, r1 - r0, ctx.num_sms)) {
     const cudaError_t e = launch_matvec_m1_tma(ctx, qtype, wq, wd, nb, xq, xd, y, sumi, r0, r1);
     if (e != cudaErrorNotSupported) return e;

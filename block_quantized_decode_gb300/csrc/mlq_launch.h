@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "diag.h"
+
 namespace mlq {
 
 // Everything a launcher needs besides the operands.
@@ -46,6 +48,7 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = ctx.pdl ? 1 : 0;
+  if (diag_on()) diag_launch(reinterpret_cast<const void *>(kern), grid, block, smem, 1, ctx.pdl);
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 

@@ -302,6 +302,9 @@ static cudaError_t launch_phase_t(const LaunchCtx &ctx, const FusedArgs &args) {
   a.smem_wd = static_cast<unsigned>(xs + ps + rows_max * rowq);
   const size_t smem = a.smem_wd + static_cast<size_t>(rows_max) * nb * 4;
   if (smem > kPhBudget) return cudaErrorNotSupported;
+  diag_note("phase: products=%d rows=%d K=%d rows/CTA<=%d chunks=%d slice=%zuB input=%s q8_out=%d early=%d",
+            a.nproducts, a.total_rows, nb * kQK, rows_max, C, smem - a.smem_w, a.x != nullptr ? "f32" : "q8",
+            a.any_yq, a.early);
   auto kern = phase_kernel<QT, NW>;
   prefer_max_shared(kern);
   if (smem > 48 * 1024) {

@@ -327,6 +327,9 @@ static cudaError_t launch_ring_t(const LaunchCtx &ctx, const FusedArgs &args) {
       a.smem_part = static_cast<unsigned>(xs);
       a.smem_w = static_cast<unsigned>(fixed);
       const size_t smem = fixed + static_cast<size_t>(ns) * stage;
+      diag_note("ring: products=%d rows=%d K=%d rows/CTA<=%d chunks=%d rows/stage=%d slots=%d stage=%zuB "
+                "input=%s q8_out=%d early=%d", a.nproducts, a.total_rows, nb * kQK, rows_max, C, R, ns, stage,
+                a.x != nullptr ? "f32" : "q8", a.any_yq, a.early);
       auto kern = NW == kRingWarps ? phase_ring_kernel<QT, kRingWarps> : phase_ring_kernel<QT, kRingWarpsWide>;
       prefer_max_shared(kern);
       if (smem > 48 * 1024) {

@@ -677,6 +677,8 @@ cudaError_t launch_decode_stream(const LaunchCtx &ctx, int qtype, const ChainArg
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  diag_note("stream: phases=%d ring=%uB grid=%d", sa.c.nphases, sa.ring_bytes, grid);
+  diag_launch_cfg(reinterpret_cast<const void *>(kern), cfg);
   return cudaLaunchKernelEx(&cfg, kern, sa);
 }
 

@@ -53,6 +53,17 @@
  * per call through MLQ_F_STATIC_WEIGHTS).  MLQ_FUSED_L2_PREFETCH=1 makes
  * the register-pipelined mlq_matvec_fused kernel hint its whole weight
  * range into L2 first.  Both are off by default.
+ *
+ * Diagnostics: with MLQ_DIAG=1 every entry point reports on stderr, once per
+ * distinct line, which kernel it launched for the shape it was given and
+ * how (grid, threads, dynamic shared memory, cluster size, dependent launch,
+ * and the launcher's own geometry: rows per CTA, K-chunks, ring stages ...),
+ * e.g.
+ *   mlq diag: mlq_matvec_q4 rows=11008 cols=4096 r=[0,11008) ->
+ *     mlq::phase_ring_kernel<1, 16> grid=152 block=544 smem=... route=phase
+ *     ring: products=1 rows=11008 K=4096 rows/CTA<=96 chunks=2 ...
+ * (one line).  Off by default; when off it costs one predictable branch
+ * per call.
  */
 #ifndef MLQ_H
 #define MLQ_H
