@@ -12,14 +12,16 @@ import ctypes
 import os
 from dataclasses import dataclass
 
-MLQ_OK, MLQ_E_SHAPE, MLQ_E_ALIGN, MLQ_E_TYPE, MLQ_E_NULL, MLQ_E_ARCH, MLQ_E_CUDA, MLQ_E_TIMEOUT = range(8)
+MLQ_OK, MLQ_E_SHAPE, MLQ_E_ALIGN, MLQ_E_TYPE, MLQ_E_NULL, MLQ_E_ARCH, MLQ_E_CUDA, MLQ_E_TIMEOUT, MLQ_E_BOUNDS = range(9)
 MLQ_Q8_0 = 0
 MLQ_Q4_0 = 1
 MLQ_QK = 32
 MLQ_MAX_COLS = 65536
 MLQ_MAX_M = 16
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmlq.so")
+# MLQ_CHECK_BOUNDS=1 selects the bounds-checking build of the library
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                        "libmlq_checked.so" if os.environ.get("MLQ_CHECK_BOUNDS") == "1" else "libmlq.so")
 
 # every symbol include/mlq.h declares
 EXPORTS = (
@@ -175,7 +177,7 @@ def status_name(s: int) -> str:
         return lib().mlq_status_str(s).decode()
     except Exception:  # library not loadable: still name the code
         names = ["MLQ_OK", "MLQ_E_SHAPE", "MLQ_E_ALIGN", "MLQ_E_TYPE", "MLQ_E_NULL",
-                 "MLQ_E_ARCH", "MLQ_E_CUDA", "MLQ_E_TIMEOUT"]
+                 "MLQ_E_ARCH", "MLQ_E_CUDA", "MLQ_E_TIMEOUT", "MLQ_E_BOUNDS"]
         return names[s] if 0 <= s < len(names) else "MLQ_E_UNKNOWN"
 
 

@@ -795,6 +795,7 @@ const char *mlq_status_str(mlq_status s) {
     case MLQ_E_ARCH: return "MLQ_E_ARCH";
     case MLQ_E_CUDA: return "MLQ_E_CUDA";
     case MLQ_E_TIMEOUT: return "MLQ_E_TIMEOUT";
+    case MLQ_E_BOUNDS: return "MLQ_E_BOUNDS";
   }
   return "MLQ_E_UNKNOWN";
 }

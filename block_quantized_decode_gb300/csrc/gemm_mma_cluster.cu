@@ -538,7 +538,8 @@ __global__ void __launch_bounds__(kMcThreads, 1)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int m = gg + 8 * (e >> 1), rw = row + (e & 1);
-        if (m < a.M && rw < rhi) a.Y[static_cast<size_t>(m) * a.ldy + rw] = vals[e];
+        if (m < a.M && rw < rhi && in_bounds(rw >= a.r0 && rw < a.r1, a.status))
+          a.Y[static_cast<size_t>(m) * a.ldy + rw] = vals[e];
       }
     }
     cluster_sync_relaxed();  // no CTA reuses the area of its tile sums while others read them

@@ -254,7 +254,8 @@ __global__ void __launch_bounds__((kGrWarps + 1) * 32, 1) gemm_q4_ring_kernel(co
     const int row = i / a.M, m = i - row * a.M;
     float sum = 0.0f;
     for (int cc = 0; cc < C; ++cc) sum += part_s[(row * C + cc) * MM + m];
-    a.Y[static_cast<size_t>(m) * a.ldy + ra + row] = sum;
+    if (in_bounds(m < a.M && ra + row >= a.r0 && ra + row < a.r1, a.status))
+      a.Y[static_cast<size_t>(m) * a.ldy + ra + row] = sum;
   }
 }
 

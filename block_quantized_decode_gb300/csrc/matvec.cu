@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(kWarps * 32) matvec_m1_kernel(const MatvecArgs
       acc = warp_sum(acc);
       if (lane == 0) {
         if (nch == 1) {
-          a.y[row] = acc;
+          if (in_bounds(row >= a.r0 && row < a.r1, a.status)) a.y[row] = acc;
         } else {
           part_s[rl * nch + c] = acc;
         }
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(kWarps * 32) matvec_m1_kernel(const MatvecArgs
     for (int rl = tid; rl < nr; rl += kWarps * 32) {
       float s = 0.0f;
       for (int c = 0; c < nch; ++c) s += part_s[rl * nch + c];
-      a.y[ra + rl] = s;
+      if (in_bounds(ra + rl >= a.r0 && ra + rl < a.r1, a.status)) a.y[ra + rl] = s;
     }
   }
 }

@@ -11,6 +11,7 @@ namespace mlq {
 
 constexpr int kQK = 32;                 // block size (Design Spec Sec. 4)
 constexpr int kStatusTimeout = 7;       // == MLQ_E_TIMEOUT in mlq.h
+constexpr int kStatusBounds = 8;        // == MLQ_E_BOUNDS in mlq.h
 constexpr unsigned long long kDrainWaitNs = 1000000000ull;  // 1 s
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -169,5 +170,19 @@ __device__ __forceinline__ int quant_one(float x, float id) {
 __device__ __forceinline__ void set_status(int *status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
+
+// Index checks of the bounds-checking build (compiled with MLQ_CHECK_BOUNDS):
+//   if (in_bounds(i < n, status)) buf[i] = v;
+// records MLQ_E_BOUNDS and skips the access when the condition fails -- no
+// trap and no early return (a return could strand the CTA's barriers).  In
+// the normal build the check is the constant true and costs nothing.
+#ifdef MLQ_CHECK_BOUNDS
+__device__ __forceinline__ bool in_bounds(bool ok, int *status) {
+  if (!ok) set_status(status, kStatusBounds);
+  return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(bool, int *) { return true; }
+#endif
 
 }  // namespace mlq

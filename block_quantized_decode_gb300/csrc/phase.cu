@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(NW * 32, 32 / NW) phase_kernel(const __grid_co
   const size_t rowq = static_cast<size_t>(nb) * (QT == 1 ? 16 : 32);
   uint8_t *wq_s = smem + a.smem_w;
   float *wd_s = reinterpret_cast<float *>(smem + a.smem_wd);
+  const int part_cap = static_cast<int>((a.smem_w - a.smem_part) / 4);  // floats of part_s
 
   if (tid == 0) {
     // pieces of at most ceil(nr / 8) rows, never spanning two products
@@ -70,6 +71,7 @@ __global__ void __launch_bounds__(NW * 32, 32 / NW) phase_kernel(const __grid_co
     for (int j = 0; j < a.nproducts; ++j) {
       const int lo = max(ra, off) - off, hi = min(rb, off + a.prod[j].rows) - off;
       for (int r = lo; r < hi; r += rpp) {
+        if (!in_bounds(np < kPhPieces, a.status)) break;
         pt.start[np] = off + r - ra;
         pt.cnt[np] = min(rpp, hi - r);
         pt.prod[np] = j;
@@ -100,7 +102,9 @@ __global__ void __launch_bounds__(NW * 32, 32 / NW) phase_kernel(const __grid_co
       mbar_arrive_expect_tx(smem_addr(&bars[0]),
                             static_cast<uint32_t>(nr) * static_cast<uint32_t>(rowq + 4u * nb));
     __syncwarp();
-    if (lane < np) {
+    // the piece lies inside the slice area (rows_cap rows of quants, then scales)
+    const size_t rows_cap = rowq > 0 ? (a.smem_wd - a.smem_w) / rowq : 0;
+    if (lane < np && in_bounds(static_cast<size_t>(pt.start[lane]) + pt.cnt[lane] <= rows_cap, a.status)) {
       const int p = lane;
       const FusedProduct &pr = a.prod[pt.prod[p]];
       const uint32_t qb = static_cast<uint32_t>(pt.cnt[p] * rowq);
@@ -220,8 +224,8 @@ __global__ void __launch_bounds__(NW * 32, 32 / NW) phase_kernel(const __grid_co
         if (direct) {
           int lr;
           const int j = phase_product(a, ra + row, &lr);
-          a.prod[j].y[lr] = v;
-        } else {
+          if (in_bounds(lr >= 0 && lr < a.prod[j].rows, a.status)) a.prod[j].y[lr] = v;
+        } else if (in_bounds(row * C + c < part_cap, a.status)) {
           part_s[row * C + c] = v;
         }
       }
@@ -237,6 +241,7 @@ __global__ void __launch_bounds__(NW * 32, 32 / NW) phase_kernel(const __grid_co
       int lr;
       const int j = phase_product(a, ra + row, &lr);
       if (C == 1 && a.prod[j].yq != nullptr) continue;
+      if (!in_bounds((row + 1) * C <= part_cap && lr >= 0 && lr < a.prod[j].rows, a.status)) continue;
       float v = part_s[row * C];
       for (int cc = 1; cc < C; ++cc) v += part_s[row * C + cc];
       a.prod[j].y[lr] = v;
@@ -253,16 +258,18 @@ __global__ void __launch_bounds__(NW * 32, 32 / NW) phase_kernel(const __grid_co
         if (a.prod[j].yq == nullptr || hi <= lo) continue;
         for (int g = lo; g < hi; g += kQK, ++t) {
           if ((t & (kPhWarps - 1)) != warp) continue;
-          const float v = part_s[(g - ra + lane) * C];
-          if (C == 1) a.prod[j].y[g - off + lane] = v;
+          const bool ok = in_bounds((g - ra + lane + 1) * C <= part_cap && g - off + lane >= 0 &&
+                                        g - off + lane < a.prod[j].rows, a.status);
+          const float v = ok ? part_s[(g - ra + lane) * C] : 0.0f;
+          if (C == 1 && ok) a.prod[j].y[g - off + lane] = v;
           uint32_t m = __float_as_uint(fabsf(v));
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
           const float amax = __uint_as_float(m);
           const float dd = amax / 127.0f;
           const float id = amax != 0.0f ? 127.0f / amax : 0.0f;
-          a.prod[j].yq[g - off + lane] = static_cast<int8_t>(quant_one(v, id));
-          if (lane == 0) a.prod[j].yd[(g - off) / kQK] = dd;
+          if (ok) a.prod[j].yq[g - off + lane] = static_cast<int8_t>(quant_one(v, id));
+          if (lane == 0 && ok) a.prod[j].yd[(g - off) / kQK] = dd;
         }
       }
     }

@@ -121,6 +121,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
   int8_t *xq_s = reinterpret_cast<int8_t *>(smem);
   float *xd_s = reinterpret_cast<float *>(smem + static_cast<size_t>(nb) * kQK);
   float *part_s = reinterpret_cast<float *>(smem + a.smem_part);
+  const int part_cap = static_cast<int>((a.smem_w - a.smem_part) / 4);  // floats of part_s
   uint8_t *ring = smem + a.smem_w;
 
   if (tid == 0) {
@@ -163,6 +164,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
       const uint32_t qb = static_cast<uint32_t>(n * rowq), db = static_cast<uint32_t>(n) * nb * 4;
       uint8_t *dst = ring + static_cast<size_t>(slot) * stage_bytes;
       const uint32_t fb = smem_addr(&full_bar[slot]);
+      // the stage fits its slot, and its rows are rows of product j
+      if (!in_bounds(n <= R && qb <= dq && dq + db <= stage_bytes && lrow + n <= a.prod[j].rows, a.status)) {
+        mbar_arrive_expect_tx(fb, 0);  // complete the slot empty: the consumers do not wait
+        ++s;
+        continue;
+      }
       mbar_arrive_expect_tx(fb, qb + db);
       bulk_copy_g2s(smem_addr(dst), a.prod[j].wq + static_cast<size_t>(lrow) * rowq, qb, fb);
       bulk_copy_g2s(smem_addr(dst + dq), a.prod[j].wd + static_cast<size_t>(lrow) * nb, db, fb);
@@ -227,7 +234,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
     }
     const float v = reduce4(acc[0], acc[1], acc[2], acc[3], lane);
     const int row = g + G * (lane >> 3);
-    if ((lane & 7) == 0 && row < n) part_s[(srow + row) * C + c] = v;
+    const int pi = (srow + row) * C + c;
+    if ((lane & 7) == 0 && row < n && in_bounds(pi < part_cap, a.status)) part_s[pi] = v;
     __syncwarp();
     if (lane == 0) mbar_arrive1(smem_addr(&empty_bar[slot]));
     ++s;
@@ -249,18 +257,22 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
       if ((t & (NW - 1)) != warp) continue;
       const int gr = g0 + lane;
       float v = 0.0f;
+      // checked for the lanes that store (gr < hi) only
+      const bool ok = gr < hi && in_bounds(gr - off >= 0 && gr - off < a.prod[jj].rows, a.status);
       if (gr < hi) {
         const int r = gr - ra;
-        v = part_s[r * C];
-        for (int cc = 1; cc < C; ++cc) v += part_s[r * C + cc];
-        a.prod[jj].y[gr - off] = v;
+        if (in_bounds((r + 1) * C <= part_cap, a.status)) {
+          v = part_s[r * C];
+          for (int cc = 1; cc < C; ++cc) v += part_s[r * C + cc];
+        }
+        if (ok) a.prod[jj].y[gr - off] = v;
       }
       if (yq != nullptr) {  // warp-uniform; gr < hi for every lane here
         const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v))));
         const float dd = amax / 127.0f;
         const float id = amax != 0.0f ? 127.0f / amax : 0.0f;
-        yq[gr - off] = static_cast<int8_t>(quant_one(v, id));
-        if (lane == 0) a.prod[jj].yd[(gr - off) / kQK] = dd;
+        if (ok) yq[gr - off] = static_cast<int8_t>(quant_one(v, id));
+        if (lane == 0 && ok) a.prod[jj].yd[(gr - off) / kQK] = dd;
       }
     }
   }

@@ -31,10 +31,19 @@ class _Mat:
     host_d: np.ndarray
 
 
+# Guard bands (canary=True): every output buffer gets GUARD elements of a
+# sentinel before and after it; check_canaries() asserts them unchanged, so a
+# kernel that writes past the rows or blocks it owns is caught.
+GUARD = 64
+_SENTINEL_F32 = 0x7FA5A5A5   # a NaN bit pattern no kernel writes
+_SENTINEL_I8 = -91           # 0xA5
+
+
 class WorkloadRunner:
     def __init__(self, wl: I.Workload, copies: int = 1, device: str = "cuda:0",
-                 seed_base: int = 0, x_seed_base: int = 1000):
+                 seed_base: int = 0, x_seed_base: int = 1000, canary: bool = False):
         self.wl = wl
+        self.canary = canary
         self.m = wl.m
         self.copies = copies
         self.dev = torch.device(device)
@@ -46,11 +55,16 @@ class WorkloadRunner:
         self.qbuf: dict[str, B.QAct] = {}
         # every product's output is a view of one buffer (128-byte aligned
         # offsets), so one copy brings all of them to the host
+        g = GUARD if canary else 0
         self.y_offs, tot = [], 0
         for mv in wl.mats:
+            tot += g
             self.y_offs.append(tot)
             tot += (self.m * mv.rows + 31) // 32 * 32
+        tot += g
         self.y_all = torch.zeros(tot, dtype=torch.float32, device=self.dev)
+        if canary:
+            self.y_all.view(torch.int32).fill_(_SENTINEL_F32)
         for i, mv in enumerate(wl.mats):
             src = f"x{mv.cols}" if mv.input_of == "x" else mv.input_of
             if mv.input_of == "x" and src not in self.x_host:
@@ -68,13 +82,41 @@ class WorkloadRunner:
             self.mats.append(_Mat(mv, src, qs, ds, y, hq, hd))
         for m in self.mats:
             self.fp32.setdefault(m.spec.name, m.y)
+        self._qguard = {}
         for src, k in self.sources.items():
-            q = torch.empty((self.m, k), dtype=torch.int8, device=self.dev)
-            d = torch.empty((self.m, k // I.QK), dtype=torch.float32, device=self.dev)
+            if canary:
+                qb = torch.full((self.m * k + 2 * 128,), _SENTINEL_I8, dtype=torch.int8, device=self.dev)
+                db = torch.empty(self.m * (k // I.QK) + 2 * 32, dtype=torch.float32, device=self.dev)
+                db.view(torch.int32).fill_(_SENTINEL_F32)
+                q = qb[128:128 + self.m * k].view(self.m, k)
+                d = db[32:32 + self.m * (k // I.QK)].view(self.m, k // I.QK)
+                self._qguard[src] = (qb, db)
+            else:
+                q = torch.empty((self.m, k), dtype=torch.int8, device=self.dev)
+                d = torch.empty((self.m, k // I.QK), dtype=torch.float32, device=self.dev)
             self.qbuf[src] = B.QAct(q, d, k, self.m)
         self.kernels_per_step = len(self.sources) + len(self.mats)
         self._chain_calls = {}
         self.chain_ws = None
+
+    def check_canaries(self) -> None:
+        """With canary=True: every guard band around the outputs (the y
+        buffers, the quantised activations and their scales) still holds its
+        sentinel; raises AssertionError naming the buffer otherwise."""
+        if not self.canary:
+            return
+        yb = self.y_all.view(torch.int32).cpu().numpy()
+        inside = np.zeros(yb.size, dtype=bool)
+        for m, off in zip(self.mats, self.y_offs):
+            inside[off:off + m.y.numel()] = True
+        bad = np.nonzero(~inside & (yb != _SENTINEL_F32))[0]
+        assert bad.size == 0, f"y guard band overwritten at {bad[:8].tolist()} (buffer of {yb.size})"
+        for src, (qb, db) in self._qguard.items():
+            q = qb.cpu().numpy()
+            d = db.view(torch.int32).cpu().numpy()
+            for name, arr, n, sent in (("q", q, 128, _SENTINEL_I8), ("d", d, 32, _SENTINEL_F32)):
+                assert np.all(arr[:n] == sent), f"{src}.{name}: head guard band overwritten"
+                assert np.all(arr[arr.size - n:] == sent), f"{src}.{name}: tail guard band overwritten"
 
     # ---- the whole pass as one chain launch ------------------------------------
     def chain_phases(self):

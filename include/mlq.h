@@ -96,8 +96,12 @@ typedef enum {
     MLQ_E_ARCH = 5,    /* no CUDA device, or it is not compute capability
                           10.3 (the library is built for sm_103a only)     */
     MLQ_E_CUDA = 6,    /* a CUDA runtime call (launch, copy) failed        */
-    MLQ_E_TIMEOUT = 7  /* a bounded device-side wait gave up; results of
+    MLQ_E_TIMEOUT = 7, /* a bounded device-side wait gave up; results of
                           that work are undefined                          */
+    MLQ_E_BOUNDS = 8   /* bounds-checking build only (MLQ_CHECK_BOUNDS): a
+                          kernel found an index outside the buffer it was
+                          about to access and skipped that access; results
+                          of that work are undefined                       */
 } mlq_status;
 
 enum { MLQ_Q8_0 = 0, MLQ_Q4_0 = 1 };

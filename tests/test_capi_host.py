@@ -44,7 +44,7 @@ def test_exports_every_declared_symbol(M):
 
 def test_status_strings(M):
     names = ["MLQ_OK", "MLQ_E_SHAPE", "MLQ_E_ALIGN", "MLQ_E_TYPE", "MLQ_E_NULL", "MLQ_E_ARCH",
-             "MLQ_E_CUDA", "MLQ_E_TIMEOUT"]
+             "MLQ_E_CUDA", "MLQ_E_TIMEOUT", "MLQ_E_BOUNDS"]
     for i, n in enumerate(names):
         assert M.mlq_status_str(i) == n
     assert M.mlq_status_str(99) == "MLQ_E_UNKNOWN"

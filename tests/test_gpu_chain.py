@@ -121,12 +121,14 @@ def test_chain_wider_than_stream_falls_back():
 
 def test_chain_deterministic_and_matches_calls(lib):
     M = lib
-    r = WorkloadRunner(I.tinyllama_layer(), copies=1)
+    r = WorkloadRunner(I.tinyllama_layer(), copies=1, canary=True)
     r.step_chain()
     torch.cuda.synchronize()
+    r.check_canaries()
     first = [m.y.clone() for m in r.mats]
     r.step_chain()
     torch.cuda.synchronize()
+    r.check_canaries()
     for a, m in zip(first, r.mats):
         assert torch.equal(a, m.y), "chain results differ between two identical calls"
     assert M.mlq_last_device_error() == M.MLQ_OK

@@ -38,7 +38,7 @@ from block_quantized_decode_gb300.runner import WorkloadRunner  # noqa: E402
 
 def run_and_check(wl, full_rows_limit=300_000_000, graph=False, chain=False, fused=False,
                   static_weights=True, phase=False, static_chain=False):
-    r = WorkloadRunner(wl, copies=1)
+    r = WorkloadRunner(wl, copies=1, canary=True)
     if chain:
         step = r.step_chain
     elif static_chain:  # mlq_decode_chain_static: the chain without a caller workspace
@@ -74,6 +74,7 @@ def run_and_check(wl, full_rows_limit=300_000_000, graph=False, chain=False, fus
     else:
         step()
     torch.cuda.synchronize()
+    r.check_canaries()   # no write outside the outputs' own rows and blocks
     if chain:
         assert int(r.chain_ws.abs().sum()) == 0, "chain workspace not left zeroed"
     rng = np.random.default_rng(12345)

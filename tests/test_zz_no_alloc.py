@@ -56,7 +56,7 @@ def test_static_chain_matches_workspace_chain(M, wl):
     from block_quantized_decode_gb300.runner import WorkloadRunner
     from tests import parity as PT
 
-    r = WorkloadRunner(wl, copies=1)
+    r = WorkloadRunner(wl, copies=1, canary=True)
     phases, products = _args(M, r)
     ws = torch.zeros(M.mlq_chain_workspace_bytes(len(phases)) // 4, dtype=torch.int32,
                      device=PT.DEV)
@@ -80,6 +80,7 @@ def test_static_chain_matches_workspace_chain(M, wl):
             b.d.fill_(float("nan"))
         M.mlq_decode_chain_static(phases, products)
         assert M.mlq_last_device_error() == M.MLQ_OK, f"call {call}"
+        r.check_canaries()
         for src, (q, d) in ref_q.items():
             assert torch.equal(r.qbuf[src].q, q), f"call {call}: quantised {src} differs"
             assert torch.equal(r.qbuf[src].d.view(torch.int32), d.view(torch.int32)), \
