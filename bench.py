@@ -495,19 +495,27 @@ def run_reference(args, wl, world, rank):
     return 0
 
 
+MAX_GRAPH_LAUNCHES = 4096
+
 # ----------------------------------------------------------------------------
 # timing helpers shared by every workload kind
 # ----------------------------------------------------------------------------
-def timed_region(args, stream, do_steps, pg, dev, clocks):
+def timed_region(args, stream, do_steps, pg, dev, clocks, prepare=None):
     """W warm-up steps (exactly args.warmup), then the timed region: R
     back-to-back repeats of exactly K steps, each repeat bracketed by CUDA
     events on `stream`, with a barrier and a device synchronize on both sides
     of the region.  K = --steps (or, when 0, as many steps as fill about
     --seconds); R = enough repeats that the region lasts at least
     --min-region seconds, so that the clock sampler sees the GPU under load.
+    prepare(n), when given, is called before n steps are first run (outside
+    any timing), e.g. to capture them as one CUDA graph.
     Returns (K, R, median ms per step over the repeats (max over ranks),
     [ms per step of each repeat], region seconds, clocks)."""
     import torch
+    if prepare is not None:
+        prepare(max(0, args.warmup))
+        if args.steps > 0:
+            prepare(args.steps)
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         a0.record(stream)
@@ -526,6 +534,8 @@ def timed_region(args, stream, do_steps, pg, dev, clocks):
     if steps <= 0:
         steps = max(10, int(args.seconds / max(per, 1e-7)))
         steps = int(max_over_ranks(pg, float(steps), dev))
+    if prepare is not None:
+        prepare(steps)
     reps = max(1, math.ceil(args.min_region / max(steps * per, 1e-7)))
     reps = int(max_over_ranks(pg, float(min(reps, 100000)), dev))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -633,9 +643,31 @@ def measure_workload(args, wl, world, local, pg, *, path_arg="auto", with_e2e=Tr
             for c in range(copies):
                 one_pass(c)
 
+    # Each run of n steps (the warm-up, each timed repeat of K steps) as ONE
+    # CUDA graph of n consecutive steps cycling through the weight copies,
+    # captured before it is timed, so that every step of a repeat chains to
+    # the next through programmatic dependent launch; at most
+    # MAX_GRAPH_LAUNCHES kernel launches per graph, beyond that whole cycles.
+    per_step_launches = (1 if path == "chain" else len(r.chain_phases()) if path in ("fused", "phase")
+                         else r.kernels_per_step + {None: 0, "all": 1, "next": len(r.mats)}[pf])
+    run_graphs = {}
+
+    def prepare(n):
+        if not graphs or n <= 0 or n in run_graphs or n * per_step_launches > MAX_GRAPH_LAUNCHES:
+            return
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                one_pass(i % copies)
+        run_graphs[n] = g
+
     def do_steps(n):
-        """Exactly n steps from weight copy 0: whole cycles through the cycle
-        graph, the rest one graph (or one eager pass) per step."""
+        """Exactly n steps from weight copy 0: the graph of n steps if one was
+        captured, else whole cycles through the cycle graph and the rest one
+        graph (or one eager pass) per step."""
+        if n in run_graphs:
+            run_graphs[n].replay()
+            return
         i = 0
         if cycle is not None:
             while n - i >= copies:
@@ -648,7 +680,8 @@ def measure_workload(args, wl, world, local, pg, *, path_arg="auto", with_e2e=Tr
                 one_pass(i % copies)
             i += 1
 
-    steps, reps, ms, per_rep, region_s, clk = timed_region(args, stream, do_steps, pg, dev, clocks)
+    steps, reps, ms, per_rep, region_s, clk = timed_region(args, stream, do_steps, pg, dev, clocks,
+                                                           prepare=prepare)
     value = world * wbytes / (ms / 1e3) / 1e9
     gops = world * r.ops() / (ms / 1e3) / 1e9
 
@@ -784,7 +817,8 @@ def measure_workload(args, wl, world, local, pg, *, path_arg="auto", with_e2e=Tr
                      f"{'q4_0' if m.spec.wtype == I.Q4_0 else 'q8_0'}" for m in r.mats],
         "l2": f"inputs larger than L2: {copies} rotating weight copies "
               f"({copies * wbytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
-        "graphs": ("one graph per cycle of %d steps" % copies) if cycle is not None else False,
+        "graphs": (("one graph of the %d timed steps per repeat" % steps) if steps in run_graphs else
+                   ("one graph per cycle of %d steps" % copies) if cycle is not None else False),
         "l2_prefetch": (args.phase_prefetch if path == "phase" else pf or "none"),
         "handoff": args.handoff if path == "phase" else None,
     }
