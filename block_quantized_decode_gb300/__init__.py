@@ -12,7 +12,7 @@ from .binding import (  # noqa: F401
     EXPORTS, LIB_PATH, ChainCall, ChainPhase, ChainProduct, mlq_chain_workspace_bytes,
     mlq_decode_chain, mlq_decode_chain_static, FusedCall, mlq_matvec_fused, PhaseCall, PhaseProduct, mlq_decode_phase, MLQ_E_ALIGN, MLQ_E_ARCH, MLQ_E_CUDA, MLQ_E_NULL, MLQ_E_SHAPE,
     MLQ_E_TIMEOUT, MLQ_E_BOUNDS, MLQ_E_TYPE, MLQ_MAX_COLS, MLQ_MAX_M, MLQ_OK, MLQ_Q4_0, MLQ_Q8_0, MLQ_QK,
-    MLQ_F_STATIC_WEIGHTS, MlqError, QAct, QTensor, lib, mlq_block_sumi, mlq_debug_set_wait_limit_ns,
+    MLQ_F_STATIC_WEIGHTS, MLQ_F_STATIC_INPUT, MlqError, QAct, QTensor, lib, mlq_block_sumi, mlq_debug_set_wait_limit_ns,
     mlq_gemm_q4_small_m, mlq_init, mlq_last_device_error, mlq_matvec_q4, mlq_matvec_q8,
     mlq_prefetch_l2, mlq_quantize_q8, mlq_status_str,
     MLQ_MAX_SEQ, MLQ_MAX_HEAD_DIM, mlq_rmsnorm, mlq_add_rmsnorm, mlq_add, mlq_softmax, mlq_silu_mul,

@@ -41,6 +41,7 @@ MLQ_MAX_SEQ = 32768
 MLQ_MAX_HEAD_DIM = 256
 MLQ_FUSED_MAX_PRODUCTS = 8
 MLQ_F_STATIC_WEIGHTS = 1
+MLQ_F_STATIC_INPUT = 2
 MLQ_CHAIN_MAX_PRODUCTS = 32
 MLQ_CHAIN_MAX_PHASES = 24
 

@@ -327,7 +327,7 @@ mlq_status mlq_decode_phase(const mlq_phase_input *in, const mlq_phase_product *
   if (!aligned(in->x, 16) || !aligned(in->xq, 16) || !aligned(in->xd, 16) ||
       !aligned(in->xq_out, 16) || !aligned(in->xd_out, 16))
     return MLQ_E_ALIGN;
-  if ((flags & ~static_cast<unsigned>(MLQ_F_STATIC_WEIGHTS)) != 0) return MLQ_E_SHAPE;
+  if ((flags & ~static_cast<unsigned>(MLQ_F_STATIC_WEIGHTS | MLQ_F_STATIC_INPUT)) != 0) return MLQ_E_SHAPE;
   mlq::FusedArgs a = {};
   const uint8_t type = products[0].W.type;
   bool any_yq = false;
@@ -363,6 +363,7 @@ mlq_status mlq_decode_phase(const mlq_phase_input *in, const mlq_phase_product *
   a.any_yq = any_yq ? 1 : 0;
   a.nchunks = 1;
   a.early = (flags & MLQ_F_STATIC_WEIGHTS) ? 1 : 0;
+  a.early_input = (flags & MLQ_F_STATIC_INPUT) && in->x != nullptr ? 1 : 0;
   for (int i = 0; i < nprefetch; ++i) {
     if (prefetch_bytes[i] > 0 && prefetch[i] == nullptr) return MLQ_E_NULL;
     a.pf_ptr[a.npf] = prefetch[i];
@@ -372,7 +373,7 @@ mlq_status mlq_decode_phase(const mlq_phase_input *in, const mlq_phase_product *
   mlq::LaunchCtx ctx;
   mlq_status s = make_ctx(&ctx, stream);
   if (s != MLQ_OK) return s;
-  if (!ctx.pdl) a.early = 0;  // without dependent launch there is nothing to overlap
+  if (!ctx.pdl) a.early = a.early_input = 0;  // without dependent launch there is nothing to overlap
   return from_cuda(mlq::launch_matvec_fused(ctx, type, a));
 }
 

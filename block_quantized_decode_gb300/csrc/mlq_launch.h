@@ -146,6 +146,7 @@ struct FusedArgs {
   int ring_rows, ring_slots;            // set by the launcher (ring phase kernel: stage geometry)
   unsigned ring_stage, ring_dq;         //   stage bytes; offset of a stage's scales
   int early;        // first weight loads before the dependency wait (static weights)
+  int early_input;  // the float input x is read and quantised before the dependency wait (static input)
   int prefetch;     // set by the launcher: hint the CTA's weights into L2 first
   int *status;      // set by the launcher
   unsigned long long wait_ns;

@@ -127,13 +127,23 @@ __global__ void __launch_bounds__(NW * 32, 32 / NW) phase_kernel(const __grid_co
     // slice's bytes) for every warp, so no warp checks it again.
     if (!mbar_wait_warp(smem_addr(&bars[0]), 0, a.wait_ns) && lane == 0) slice_ok = 0;
   }
-  griddep_wait();  // the input (and, without static weights, W) may come from the previous kernel
-
   int8_t *xq_s = reinterpret_cast<int8_t *>(smem);
   float *xd_s = reinterpret_cast<float *>(smem + static_cast<size_t>(nb) * kQK);
+  // A static float input (no earlier work writes it) is read and quantised
+  // before the dependency wait; CTA 0 writes xq_out / xd_out after it.
+  const bool early_in = IN == 0 && a.early_input != 0;
+  const bool writer = blockIdx.x == 0 && a.xq_out != nullptr;
+  if (early_in && (nr > 0 || writer)) quantize_input<NW>(a.x, nb, nullptr, nullptr, false, xq_s, xd_s, tid);
+  griddep_wait();  // the input (and, without static weights, W) may come from the previous kernel
+
   bool ok = true;
   if (IN == 0) {
-    if (nr > 0 || (blockIdx.x == 0 && a.xq_out != nullptr)) phase_quantize<NW>(a, xq_s, xd_s, tid);
+    if (!early_in) {
+      if (nr > 0 || writer) phase_quantize<NW>(a, xq_s, xd_s, tid);
+    } else if (writer) {
+      __syncthreads();
+      store_input_copy(xq_s, xd_s, nb, a.xq_out, a.xd_out, tid, kPhThreads);
+    }
     __syncthreads();
   } else if (nr > 0) {
     // The Q8_0 input (n bytes + n/32 scales): one 16-byte load per thread

@@ -98,6 +98,17 @@ __device__ __forceinline__ void quantize_input(const float *x, int nb, int8_t *x
     }
   }
 }
+// The quantised input, already in shared memory, to xq_out / xd_out (16-byte
+// units; nb is a multiple of 4): for a CTA that quantised its input before
+// the dependency wait, when it may only write once that wait has returned.
+__device__ __forceinline__ void store_input_copy(const int8_t *xq_s, const float *xd_s, int nb, int8_t *xq_out,
+                                                 float *xd_out, int tid, int nthreads) {
+  const int uq = nb * 2, nu = nb * 2 + nb / 4;
+  for (int u = tid; u < nu; u += nthreads) {
+    if (u < uq) reinterpret_cast<int4 *>(xq_out)[u] = reinterpret_cast<const int4 *>(xq_s)[u];
+    else reinterpret_cast<int4 *>(xd_out)[u - uq] = reinterpret_cast<const int4 *>(xd_s)[u - uq];
+  }
+}
 template <int NW>
 __device__ __forceinline__ void phase_quantize(const FusedArgs &a, int8_t *xq_s, float *xd_s,
                                                int tid) {

@@ -183,9 +183,23 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
   }
 
   // ------------------------------ consumers ------------------------------
+  // A static float input (no earlier work writes it) is read and quantised
+  // before the dependency wait: off the critical path of a CTA that starts
+  // early, and ahead of the ring's copies for one that starts late.
+  const bool early_in = IN == 0 && a.early_input != 0;
+  const bool writer = blockIdx.x == 0 && a.xq_out != nullptr;
+  if (early_in) {
+    if (nr > 0 || writer) quantize_input<NW>(a.x, nb, nullptr, nullptr, false, xq_s, xd_s, tid);
+    consumers_sync<NW>();
+    if (tid == 0) *input_v = 1;  // the producer may fill the ring now
+  }
   griddep_wait();  // the input may come from the previous kernel
   if (IN == 0) {
-    if (nr > 0 || (blockIdx.x == 0 && a.xq_out != nullptr)) phase_quantize<NW>(a, xq_s, xd_s, tid);
+    if (!early_in) {
+      if (nr > 0 || writer) phase_quantize<NW>(a, xq_s, xd_s, tid);
+    } else if (writer) {
+      store_input_copy(xq_s, xd_s, nb, a.xq_out, a.xd_out, tid, NW * 32);
+    }
   } else if (nr > 0) {
     const int uq = nb * 2, nu = nb * 2 + nb / 4;
     for (int base = 0; base < nu; base += 4 * NW * 32) {  // all loads before any store

@@ -176,8 +176,10 @@ class WorkloadRunner:
         return out
 
     def phase_calls(self, copy: int = 0, static_weights: bool = True, prefetch: str = "none",
-                    handoff: str = "q8"):
-        """One mlq_decode_phase call per phase.  handoff "q8": a product whose
+                    handoff: str = "q8", static_input: bool = True):
+        """One mlq_decode_phase call per phase (static_input: the phases that
+        read the workload's own float inputs pass MLQ_F_STATIC_INPUT).  handoff
+        "q8": a product whose
         output is the input of a later phase also writes it in Q8_0 (into
         that input's buffer), so the later phase starts from quantised bytes
         (the producing phase then splits its rows in whole 32-row blocks);
@@ -190,7 +192,7 @@ class WorkloadRunner:
         phase); "none"."""
         if handoff not in ("q8", "float"):
             raise ValueError(f"handoff {handoff!r}")
-        key = ("phase", copy, static_weights, prefetch, handoff)
+        key = ("phase", copy, static_weights, prefetch, handoff, static_input)
         if key not in self._chain_calls:
             if self.m != 1:
                 raise ValueError("decode phases are M = 1")
@@ -223,8 +225,14 @@ class WorkloadRunner:
                     calls.append(B.PhaseCall(self.sources[src], pr, xq=qa.q, xd=qa.d, flags=flags,
                                              prefetch=pf))
                 else:
+                    # the workload's own inputs are written once (or by a copy
+                    # before the step's first launch): MLQ_F_STATIC_INPUT lets the
+                    # launch read them before the previous kernel has finished
+                    own = src in self.x_host and static_input
                     calls.append(B.PhaseCall(self.sources[src], pr, x=self.fp32[src],
-                                             xq_out=qa.q, xd_out=qa.d, flags=flags, prefetch=pf))
+                                             xq_out=qa.q, xd_out=qa.d,
+                                             flags=flags | (B.MLQ_F_STATIC_INPUT if own else 0),
+                                             prefetch=pf))
             self._chain_calls[key] = calls
         return self._chain_calls[key]
 

@@ -447,6 +447,11 @@ mlq_status mlq_decode_chain_static(const mlq_chain_phase *phases, int nphases,
  * while the previous kernel is still running.
  * No counterpart on the pages: a GPU fusion of quantize_q8 and matvec. */
 #define MLQ_F_STATIC_WEIGHTS 1u
+/* mlq_decode_phase: the float input x is not written by work queued earlier
+ * on the stream (a step's own input, copied in before its first launch): the
+ * launch may read and quantise x before that work has finished.  Its writes
+ * (xq_out / xd_out, the outputs) still wait.  Ignored for a Q8_0 input. */
+#define MLQ_F_STATIC_INPUT 2u
 mlq_status mlq_matvec_fused(const float *x, int n, const mlq_chain_product *products,
                             int nproducts, int8_t *xq_out, float *xd_out, unsigned flags,
                             void *stream);
@@ -485,8 +490,9 @@ typedef struct {
  * y[r] for every r < W.rows, within the tolerance of mlq_matvec_q4/_q8, and
  * each requested Q8_0 copy of y.  If any product has yq, every product's
  * W.rows must be a multiple of 32 (MLQ_E_SHAPE otherwise).  Outputs must
- * not overlap the input or each other.  flags: 0 or MLQ_F_STATIC_WEIGHTS
- * (as for mlq_matvec_fused).  A chain of such calls, each taking the
+ * not overlap the input or each other.  flags: 0, MLQ_F_STATIC_WEIGHTS (as
+ * for mlq_matvec_fused) and/or MLQ_F_STATIC_INPUT (anything else:
+ * MLQ_E_SHAPE).  A chain of such calls, each taking the
  * previous one's yq / yd, runs a decode step with no separate quantize
  * launches: each phase quantises its outputs while they are still on chip.
  * prefetch / prefetch_bytes (host arrays of nprefetch <= MLQ_PHASE_MAX_PREFETCH

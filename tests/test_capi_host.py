@@ -236,7 +236,8 @@ def test_validation_phase(M):
     assert run([R(qt(cols=256), 5 * A, 9 * A + 4, 10 * A)]) == M.MLQ_E_ALIGN
     assert run([quant, R(qt(cols=256, rows=40), 5 * A, None, None)]) == M.MLQ_E_SHAPE  # 40 % 32
     assert run([R(qt(cols=256, rows=33), 5 * A, 9 * A, 10 * A)]) == M.MLQ_E_SHAPE
-    assert run([good], flags=2) == M.MLQ_E_SHAPE
+    assert run([good], flags=4) == M.MLQ_E_SHAPE                      # unknown flag
+    assert run([good], flags=M.MLQ_F_STATIC_INPUT | M.MLQ_F_STATIC_WEIGHTS) == M.MLQ_E_ARCH  # valid
     ptrs = (ctypes.c_void_p * 17)(*([12 * A] * 17))
     sizes = (ctypes.c_size_t * 17)(*([4096] * 17))
     assert run([good], pf=ptrs, pfb=sizes, npf=17) == M.MLQ_E_SHAPE   # > MLQ_PHASE_MAX_PREFETCH
