@@ -257,37 +257,42 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
   consumers_sync<NW>();
   if (*abort_v) return;
 
-  // y and the quantised outputs in one pass.  Warp w takes every NW-th run
-  // of 32 of the CTA's rows (within a product with a quantised output these
-  // are its whole 32-row blocks), one row per lane: the K-chunk partial sums
-  // added in a fixed order, y stored, and a block quantised from exactly the
-  // floats stored -- its maximum by one warp reduction on the float bit
+  // y.  A product without a quantised output: one row per consumer thread,
+  // the K-chunk partial sums added in a fixed order.  A product with one: y
+  // and its Q8_0 blocks in one pass, warp w taking every NW-th of the CTA's
+  // 32-row blocks of it, one row per lane, the block quantised from exactly
+  // the floats stored -- its maximum by one warp reduction on the float bit
   // patterns (non-negative floats order as unsigned integers).
   int t = 0;
   for (int jj = 0, off = 0; jj < a.nproducts; off += a.prod[jj].rows, ++jj) {
     const int lo = max(ra, off), hi = min(rb, off + a.prod[jj].rows);
     int8_t *yq = a.prod[jj].yq;
-    for (int g0 = lo; g0 < hi; g0 += kQK, ++t) {
+    if (yq == nullptr) {
+      for (int gr = lo + tid; gr < hi; gr += NW * 32) {
+        const int r = gr - ra;
+        if (!in_bounds((r + 1) * C <= part_cap && gr - off < a.prod[jj].rows, a.status)) continue;
+        float v = part_s[r * C];
+        for (int cc = 1; cc < C; ++cc) v += part_s[r * C + cc];
+        a.prod[jj].y[gr - off] = v;
+      }
+      continue;
+    }
+    for (int g0 = lo; g0 < hi; g0 += kQK, ++t) {  // whole 32-row blocks here
       if ((t & (NW - 1)) != warp) continue;
       const int gr = g0 + lane;
+      const int r = gr - ra;
+      const bool ok = in_bounds((r + 1) * C <= part_cap && gr - off >= 0 && gr - off < a.prod[jj].rows, a.status);
       float v = 0.0f;
-      // checked for the lanes that store (gr < hi) only
-      const bool ok = gr < hi && in_bounds(gr - off >= 0 && gr - off < a.prod[jj].rows, a.status);
-      if (gr < hi) {
-        const int r = gr - ra;
-        if (in_bounds((r + 1) * C <= part_cap, a.status)) {
-          v = part_s[r * C];
-          for (int cc = 1; cc < C; ++cc) v += part_s[r * C + cc];
-        }
-        if (ok) a.prod[jj].y[gr - off] = v;
+      if (ok) {
+        v = part_s[r * C];
+        for (int cc = 1; cc < C; ++cc) v += part_s[r * C + cc];
+        a.prod[jj].y[gr - off] = v;
       }
-      if (yq != nullptr) {  // warp-uniform; gr < hi for every lane here
-        const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v))));
-        const float dd = amax / 127.0f;
-        const float id = amax != 0.0f ? 127.0f / amax : 0.0f;
-        if (ok) yq[gr - off] = static_cast<int8_t>(quant_one(v, id));
-        if (lane == 0 && ok) a.prod[jj].yd[(gr - off) / kQK] = dd;
-      }
+      const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v))));
+      const float dd = amax / 127.0f;
+      const float id = amax != 0.0f ? 127.0f / amax : 0.0f;
+      if (ok) yq[gr - off] = static_cast<int8_t>(quant_one(v, id));
+      if (lane == 0 && ok) a.prod[jj].yd[(gr - off) / kQK] = dd;
     }
   }
 }
