@@ -76,6 +76,19 @@ __device__ __forceinline__ bool ring_wait_either(uint32_t bar, uint32_t parity, 
   }
 }
 
+// Row r's K-chunk partial sums added in chunk order (C <= kRingWarps): all
+// loads issued before the additions.
+__device__ __forceinline__ float chunk_sum(const float *part_s, int prow, int r, int C) {
+  float p[kRingWarps];
+#pragma unroll
+  for (int cc = 0; cc < kRingWarps; ++cc) p[cc] = cc < C ? part_s[cc * prow + r] : 0.0f;
+  float v = p[0];
+#pragma unroll
+  for (int cc = 1; cc < kRingWarps; ++cc)
+    if (cc < C) v += p[cc];
+  return v;
+}
+
 // The CTA's stages: runs of at most R rows of [ra, rb), never spanning two
 // products.  Producer and consumers walk them in the same order.
 struct StageIter {
@@ -120,8 +133,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
   const size_t stage_bytes = a.ring_stage, dq = a.ring_dq;
   int8_t *xq_s = reinterpret_cast<int8_t *>(smem);
   float *xd_s = reinterpret_cast<float *>(smem + static_cast<size_t>(nb) * kQK);
+  // per-chunk partial sums: chunk c of the CTA's row r at part_s[c * prow + r]
+  // (the epilogue's lanes then read consecutive words)
   float *part_s = reinterpret_cast<float *>(smem + a.smem_part);
   const int part_cap = static_cast<int>((a.smem_w - a.smem_part) / 4);  // floats of part_s
+  const int prow = part_cap / C;  // >= the CTA's rows
   uint8_t *ring = smem + a.smem_w;
 
   if (tid == 0) {
@@ -248,8 +264,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
     }
     const float v = reduce4(acc[0], acc[1], acc[2], acc[3], lane);
     const int row = g + G * (lane >> 3);
-    const int pi = (srow + row) * C + c;
-    if ((lane & 7) == 0 && row < n && in_bounds(pi < part_cap, a.status)) part_s[pi] = v;
+    const int pi = c * prow + srow + row;
+    if ((lane & 7) == 0 && row < n && in_bounds(srow + row < prow, a.status)) part_s[pi] = v;
     __syncwarp();
     if (lane == 0) mbar_arrive1(smem_addr(&empty_bar[slot]));
     ++s;
@@ -270,10 +286,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
     if (yq == nullptr) {
       for (int gr = lo + tid; gr < hi; gr += NW * 32) {
         const int r = gr - ra;
-        if (!in_bounds((r + 1) * C <= part_cap && gr - off < a.prod[jj].rows, a.status)) continue;
-        float v = part_s[r * C];
-        for (int cc = 1; cc < C; ++cc) v += part_s[r * C + cc];
-        a.prod[jj].y[gr - off] = v;
+        if (!in_bounds(r < prow && gr - off < a.prod[jj].rows, a.status)) continue;
+        a.prod[jj].y[gr - off] = chunk_sum(part_s, prow, r, C);
       }
       continue;
     }
@@ -281,11 +295,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
       if ((t & (NW - 1)) != warp) continue;
       const int gr = g0 + lane;
       const int r = gr - ra;
-      const bool ok = in_bounds((r + 1) * C <= part_cap && gr - off >= 0 && gr - off < a.prod[jj].rows, a.status);
+      const bool ok = in_bounds(r < prow && gr - off >= 0 && gr - off < a.prod[jj].rows, a.status);
       float v = 0.0f;
       if (ok) {
-        v = part_s[r * C];
-        for (int cc = 1; cc < C; ++cc) v += part_s[r * C + cc];
+        v = chunk_sum(part_s, prow, r, C);
         a.prod[jj].y[gr - off] = v;
       }
       const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v))));
