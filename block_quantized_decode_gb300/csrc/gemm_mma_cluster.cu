@@ -9,11 +9,20 @@
 //
 // Operand roles.  The (up to 16) activation rows are the A operand of
 // mma.m16n8k16 and eight weight rows its B operand, so the activations of
-// a block are converted to fp16 once and serve every 8-row weight tile.
-// The CTA copies its K-part of the activations into shared memory with one
-// tensor copy and lays it out there as A fragments (1 KB per block of 32
-// columns), next to two 16-byte quads per block and row group: the scale
-// pairs (dx_g, dx_g, dx_g+8, dx_g+8) and the start values of the block sums.
+// a block serve every 8-row weight tile.  The CTA copies its K-part of the
+// activations into shared memory with one tensor copy and lays it out
+// there in fragment order, in one of two forms, next to two 16-byte quads
+// per block and row group: the scale pairs (dx_g, dx_g, dx_g+8, dx_g+8) and
+// the start values of the block sums.
+//  * fp16 A fragments, 1 KB per block of 32 columns, converted once;
+//  * int8 words, 512 bytes per block (lane (g, t) holds words t and t + 4
+//    of rows g and g + 8, biased to unsigned), which each warp turns into
+//    its fp16 A fragments when it takes the block of a stage (byte permutes
+//    and one fp16 subtract or multiply-add per pair, all exact).
+// The int8 form holds 96 blocks per CTA instead of 64, so a long row needs
+// fewer K-parts (4096 x 11008: clusters of 4 in one round of rows instead
+// of clusters of 6 in two); its conversion costs a stage about 8% more
+// issue, so it is taken only where it lowers the number of K-parts.
 //
 // Exact block sums without a per-weight subtraction.  A weight word turns
 // into B fragments with bit operations only: a low nibble n becomes the
@@ -73,20 +82,21 @@ namespace mlq {
 
 constexpr int kMcConsumers = 16;                 // warps
 constexpr int kMcThreads = kMcConsumers * 32;
-constexpr int kMcMaxSlots = 8;                   // stages in the ring, at most (at least 4)
+constexpr int kMcMaxSlots = 12;                  // stages in the ring, at most (at least 4)
 constexpr int kMcFirst = 4;                      // stages copied before the activations are staged (<= 4 slots)
 constexpr int kMcChunk = 8;                      // blocks per stage (128 bytes of a Q4_0 row)
 constexpr int kMcMaxRows = 160;                  // rows per round (tensor box height)
 constexpr int kMcMaxTpw = kMcMaxRows / 32;       // tiles of one parity in a round
-constexpr int kMcMaxPart = 64;                   // blocks of activations per CTA
-constexpr int kMcXfBlock = 1024;                 // A fragments of one block
+constexpr int kMcMaxPartF16 = 64;                // blocks of activations per CTA: fp16 fragments
+constexpr int kMcMaxPart = 96;                   //   int8 words
+template <bool I8> __host__ __device__ constexpr int mc_xblock() { return I8 ? 512 : 1024; }  // bytes of one block's activations
+template <bool I8> __host__ __device__ constexpr int mc_max_part() { return I8 ? kMcMaxPart : kMcMaxPartF16; }
 constexpr int kMcXdBlock = 128;                  // (dx_g, dx_g, dx_g+8, dx_g+8) for g < 8
 constexpr int kMcXcBlock = 128;                  // -(C_g, C_g, C_g+8, C_g+8) for g < 8
 constexpr int kMcXRaw = 16 * (kQK + 4);          // raw activation bytes and scale per block
 constexpr int kMcTileBytes = 1024;               // one warp's partial (or sum) of one tile
 constexpr int kMcMaxCluster = 8;
 constexpr int kMcSmemLimit = 227 * 1024 - 256;   // dynamic shared memory, leaving room for the barriers
-constexpr int kMcXTasks = kMcMaxPart * 32 / (kMcConsumers * 32);
 static_assert(kMcConsumers == 2 * kMcChunk, "two warps per block of a stage");
 
 struct McArgs {
@@ -114,7 +124,7 @@ struct McArgs {
 struct McParams {
   CUtensorMap wq;  // Q4_0 bytes: rows x (nb * 16), box H rows x 128 B, 128-byte swizzle
   CUtensorMap wd;  // scales: rows x nb floats, box H rows x 8
-  CUtensorMap xq;  // activations: M x K bytes as 8-byte elements, box 16 rows x one part
+  CUtensorMap xq;  // activations: M rows x nb blocks x 4 8-byte elements, box 16 x one part x 4
   CUtensorMap xd;  // their scales: M x nb floats, box 16 rows x one part
   McArgs a;
 };
@@ -164,6 +174,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// 3-D tensor copy global -> shared: coordinates (x innermost, y, z).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -204,6 +223,40 @@ __device__ __forceinline__ void mma_acc(float (&d)[4], const uint4 &a, uint32_t 
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
+}
+
+// The lane's A fragments of one block from its four biased int8 words
+// (row g: words t, t + 4; row g + 8: words t, t + 4): step 0 holds x, step 1
+// x / 16.  A biased byte u = x + 128 placed in the mantissa of 1024 is the
+// fp16 value 1024 + u; subtracting 1152 gives x, and (1024 + u) / 16 - 72 =
+// x / 16 in one fused multiply-add -- (1024 + u) / 16 has 1/16 steps below
+// 80, which fp16 holds, so both are exact.
+__device__ __forceinline__ void raw_to_frags(const uint4 &w, uint4 &f0, uint4 &f1) {
+  const __half2 sixteenth = __half2half2(__ushort_as_half(0x2C00));
+  const __half2 m72 = __half2half2(__ushort_as_half(0xD480));  // -72
+  auto place = [](uint32_t biased, uint32_t sel) {
+    uint32_t v;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(v) : "r"(biased), "r"(0x64646464u), "r"(sel));
+    return v;
+  };
+  auto lo = [&](uint32_t biased, uint32_t sel) {  // x
+    const uint32_t v = place(biased, sel);
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&v), __half2half2(__ushort_as_half(0x6480)));
+    return *reinterpret_cast<const uint32_t *>(&r);
+  };
+  auto hi = [&](uint32_t biased, uint32_t sel) {  // x / 16
+    const uint32_t v = place(biased, sel);
+    const __half2 r = __hfma2(*reinterpret_cast<const __half2 *>(&v), sixteenth, m72);
+    return *reinterpret_cast<const uint32_t *>(&r);
+  };
+  f0.x = lo(w.x, 0x4240u);  // row g,     elements 4t, 4t+2
+  f0.y = lo(w.z, 0x4240u);  // row g + 8
+  f0.z = lo(w.x, 0x4341u);  // row g,     elements 4t+1, 4t+3
+  f0.w = lo(w.z, 0x4341u);  // row g + 8
+  f1.x = hi(w.y, 0x4240u);  // the same, elements + 16, over 16
+  f1.y = hi(w.w, 0x4240u);
+  f1.z = hi(w.y, 0x4341u);
+  f1.w = hi(w.w, 0x4341u);
 }
 
 // The B fragments of one weight word (see the header comment): step 0,
@@ -254,8 +307,11 @@ __device__ __forceinline__ void stage_tiles(unsigned long long (&acc)[kMcMaxTpw]
   }
 }
 
+template <bool I8>
 __global__ void __launch_bounds__(kMcThreads, 1)
     gemm_q4_mma_cluster_kernel(const __grid_constant__ McParams prm) {
+  constexpr int kMcXfBlock = mc_xblock<I8>();
+  constexpr int kMcXTasks = mc_max_part<I8>() * 32 / (kMcConsumers * 32);
   const McArgs &a = prm.a;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kMcMaxSlots];
@@ -344,7 +400,7 @@ __global__ void __launch_bounds__(kMcThreads, 1)
     // the activations first: an SM serves its reads in order
     const uint32_t xb = smem_addr(&x_bar);
     mbar_arrive_expect_tx(xb, static_cast<uint32_t>(16 * a.xblocks * (kQK + 4)));
-    tma_load_2d(smem_addr(xraw), &prm.xq, kb0 * (kQK / 8), 0, xb);
+    tma_load_3d(smem_addr(xraw), &prm.xq, 0, kb0, 0, xb);  // lands as [16 rows][xblocks][32 bytes]
     tma_load_2d(smem_addr(xdraw), &prm.xd, kb0, 0, xb);
     while (static_cast<int>(issued) < min(total, kMcFirst) && issue_next()) {
     }
@@ -353,11 +409,12 @@ __global__ void __launch_bounds__(kMcThreads, 1)
     if (lane == 0 && atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
   }
   if (!*abort_v) {
-    // Activations -> A fragments.  Task (block j, lane (gg, tt)): words tt
-    // and tt + 4 of rows gg and gg + 8 become the lane's a0..a3 of both MMA
-    // steps (x, then x / 16); int8 -> fp16 by biasing to unsigned (exact).
-    // The four lanes of a row group add up the block halves for the start
-    // values.  Rows past M and blocks past the row end were copied as zeros.
+    // Activations -> fragment order.  Task (block j, lane (gg, tt)): words
+    // tt and tt + 4 of rows gg and gg + 8, biased to unsigned, are the
+    // lane's a0..a3 of both MMA steps: kept as int8 words (I8; raw_to_frags
+    // converts them per stage) or converted now.  The four lanes of a row
+    // group add up the block halves for the start values.  Rows past M and
+    // blocks past the row end were copied as zeros.
 #pragma unroll
     for (int q = 0; q < kMcXTasks; ++q) {
       const int i = tid + q * kMcThreads, j = i >> 5, ln = i & 31, gg = ln >> 2, tt = ln & 3;
@@ -378,25 +435,17 @@ __global__ void __launch_bounds__(kMcThreads, 1)
         sh1 += __shfl_xor_sync(0xffffffffu, sh1, o);
       }
       if (j < a.xblocks) {
-        const __half2 sixteenth = __half2half2(__ushort_as_half(0x2C00));
-        auto div16 = [&](uint32_t v) {
-          const __half2 r = __hmul2(*reinterpret_cast<const __half2 *>(&v), sixteenth);
-          return *reinterpret_cast<const uint32_t *>(&r);
-        };
-        uint4 f0, f1;
-        const uint32_t b0 = lo0 ^ 0x80808080u, b1 = lo1 ^ 0x80808080u;
-        const uint32_t c0h = hi0 ^ 0x80808080u, c1h = hi1 ^ 0x80808080u;
-        f0.x = s8_to_h2(b0, 0x4240u);  // row gg,     elements 4tt, 4tt+2
-        f0.y = s8_to_h2(b1, 0x4240u);  // row gg + 8
-        f0.z = s8_to_h2(b0, 0x4341u);  // row gg,     elements 4tt+1, 4tt+3
-        f0.w = s8_to_h2(b1, 0x4341u);  // row gg + 8
-        f1.x = div16(s8_to_h2(c0h, 0x4240u));  // the same, elements + 16, over 16
-        f1.y = div16(s8_to_h2(c1h, 0x4240u));
-        f1.z = div16(s8_to_h2(c0h, 0x4341u));
-        f1.w = div16(s8_to_h2(c1h, 0x4341u));
+        const uint4 words =
+            make_uint4(lo0 ^ 0x80808080u, hi0 ^ 0x80808080u, lo1 ^ 0x80808080u, hi1 ^ 0x80808080u);
         uint8_t *dst = xf + static_cast<size_t>(j) * kMcXfBlock + ln * 16;
-        *reinterpret_cast<uint4 *>(dst) = f0;
-        *reinterpret_cast<uint4 *>(dst + 512) = f1;
+        if (I8) {
+          *reinterpret_cast<uint4 *>(dst) = words;
+        } else {
+          uint4 f0, f1;
+          raw_to_frags(words, f0, f1);
+          *reinterpret_cast<uint4 *>(dst) = f0;
+          *reinterpret_cast<uint4 *>(dst + 512) = f1;
+        }
         if (tt == 0) {
           const float d0 = xdraw[gg * a.xblocks + j], d1 = xdraw[(gg + 8) * a.xblocks + j];
           *reinterpret_cast<float4 *>(xdx + static_cast<size_t>(j) * kMcXdBlock + gg * 16) =
@@ -445,9 +494,14 @@ __global__ void __launch_bounds__(kMcThreads, 1)
       if (tid == 0 && static_cast<int>(issued) < min(limit, static_cast<int>(used) + S) && !*abort_v)
         issue_next();
       const int jb = k * kMcChunk + jw;  // part-local block
-      const uint4 xa = *reinterpret_cast<const uint4 *>(xf + static_cast<size_t>(jb) * kMcXfBlock + lane * 16);
-      const uint4 xb =
-          *reinterpret_cast<const uint4 *>(xf + static_cast<size_t>(jb) * kMcXfBlock + 512 + lane * 16);
+      uint4 xa, xb;
+      if (I8) {
+        raw_to_frags(*reinterpret_cast<const uint4 *>(xf + static_cast<size_t>(jb) * kMcXfBlock + lane * 16), xa,
+                     xb);
+      } else {
+        xa = *reinterpret_cast<const uint4 *>(xf + static_cast<size_t>(jb) * kMcXfBlock + lane * 16);
+        xb = *reinterpret_cast<const uint4 *>(xf + static_cast<size_t>(jb) * kMcXfBlock + 512 + lane * 16);
+      }
       const ulonglong2 dx =
           *reinterpret_cast<const ulonglong2 *>(xdx + static_cast<size_t>(jb) * kMcXdBlock + g * 16);
       const float4 cc = *reinterpret_cast<const float4 *>(xcc + static_cast<size_t>(jb) * kMcXcBlock + g * 16);
@@ -576,20 +630,37 @@ static bool encode_2d(CUtensorMap *map, CUtensorMapDataType type, const void *pt
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The activations as M rows x nb blocks x 4 8-byte elements, box 16 rows x
+// xblocks x 4: the part lands densely as [16][xblocks][32 bytes], the
+// layout of a 2-D box of one row part, while every box dimension stays
+// within the 256-element limit of a tensor copy (a 2-D box of xblocks * 4
+// elements would exceed it beyond 64 blocks).  Rows past M read as zeros.
+static bool encode_act_3d(CUtensorMap *map, const void *xq, int nb, int M, int xblocks) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {kQK / 8, static_cast<cuuint64_t>(nb), static_cast<cuuint64_t>(M)};
+  const cuuint64_t strides[2] = {kQK, static_cast<cuuint64_t>(nb) * kQK};
+  const cuuint32_t box[3] = {kQK / 8, static_cast<cuuint32_t>(xblocks), 16};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void *>(xq), dims, strides, box, elem,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Clusters of P CTAs that fit on the device at once, by (P, activation chunks).
-static std::atomic<int> g_mc_clusters[kMcMaxCluster + 1][kMcMaxPart / kMcChunk + 1];
+static std::atomic<int> g_mc_clusters[2][kMcMaxCluster + 1][kMcMaxPart / kMcChunk + 1];
 
 // Shared-memory layout of a launch (byte offsets from the 1024-aligned base).
 struct McLayout {
   int slots, ring, xraw, parts;
   size_t bytes;  // dynamic shared memory, alignment slack included
 };
-static bool mc_layout(int H, int xblocks, bool multi_round, McLayout *L) {
+static bool mc_layout(int H, int xblocks, int xblock_bytes, bool multi_round, McLayout *L) {
   const int slot_q = (H * kMcChunk * 16 + 1023) / 1024 * 1024;
   const int slot_d = (H * kMcChunk * 4 + 127) / 128 * 128;
   const int tiles = (H + 15) / 16;
   const int parts = kMcConsumers * ((tiles + 1) / 2) * kMcTileBytes;
-  const int xfixed = xblocks * (kMcXfBlock + kMcXdBlock + kMcXcBlock);
+  const int xfixed = xblocks * (xblock_bytes + kMcXdBlock + kMcXcBlock);
   const int raw = xblocks * kMcXRaw;
   // most slots first; partials in their own area (several rounds) when it fits
   for (int own = multi_round ? 1 : 0; own >= 0; --own) {
@@ -621,7 +692,16 @@ cudaError_t launch_gemm_q4_mma_cluster(const LaunchCtx &ctx, const void *wq, con
     const char *e = std::getenv("MLQ_MMA_CLUSTER");
     return e != nullptr ? std::atoi(e) : 0;
   }();
-  const int p_min = (nchunks * kMcChunk + kMcMaxPart - 1) / kMcMaxPart;
+  // the int8 form only where it needs fewer K-parts than fp16 fragments
+  // (MLQ_MMA_I8=1 / 0 forces one form: A/B timing)
+  static const int i8_env = [] {
+    const char *e = std::getenv("MLQ_MMA_I8");
+    return e == nullptr ? -1 : (e[0] == '1' ? 1 : 0);
+  }();
+  const int p_f16 = (nchunks * kMcChunk + kMcMaxPartF16 - 1) / kMcMaxPartF16;
+  const int p_i8 = (nchunks * kMcChunk + kMcMaxPart - 1) / kMcMaxPart;
+  const bool i8 = i8_env >= 0 ? i8_env == 1 : p_i8 < p_f16;
+  const int p_min = i8 ? p_i8 : p_f16;
   const int P = p_env > p_min && p_env <= kMcMaxCluster && p_env <= nchunks ? p_env : p_min;
   // the scale map needs 16-byte row strides
   if (M > 16 || P > kMcMaxCluster || nb % 4 != 0) return cudaErrorNotSupported;
@@ -640,9 +720,14 @@ cudaError_t launch_gemm_q4_mma_cluster(const LaunchCtx &ctx, const void *wq, con
   const int part_chunks = (nchunks + P - 1) / P;
   a.xblocks = part_chunks * kMcChunk;
   a.units = (n + 7) / 8;
-  auto kern = gemm_q4_mma_cluster_kernel;
-  static const cudaError_t attr =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMcSmemLimit);
+  auto kern = i8 ? gemm_q4_mma_cluster_kernel<true> : gemm_q4_mma_cluster_kernel<false>;
+  static const cudaError_t attr = [] {
+    const cudaError_t e0 = cudaFuncSetAttribute(gemm_q4_mma_cluster_kernel<false>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize, kMcSmemLimit);
+    const cudaError_t e1 = cudaFuncSetAttribute(gemm_q4_mma_cluster_kernel<true>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize, kMcSmemLimit);
+    return e0 != cudaSuccess ? e0 : e1;
+  }();
   if (attr != cudaSuccess) return attr;
 
   cudaLaunchConfig_t cfg = {};
@@ -658,7 +743,7 @@ cudaError_t launch_gemm_q4_mma_cluster(const LaunchCtx &ctx, const void *wq, con
   cfg.attrs = at;
   cfg.numAttrs = 1;
 
-  int clusters = g_mc_clusters[P][part_chunks].load(std::memory_order_relaxed);
+  int clusters = g_mc_clusters[i8][P][part_chunks].load(std::memory_order_relaxed);
   if (clusters == 0) {
     // with the most shared memory a launch may take
     cfg.gridDim = dim3(static_cast<unsigned>(P * ctx.num_sms));
@@ -667,7 +752,7 @@ cudaError_t launch_gemm_q4_mma_cluster(const LaunchCtx &ctx, const void *wq, con
       cudaGetLastError();
       return cudaErrorNotSupported;
     }
-    g_mc_clusters[P][part_chunks].store(clusters, std::memory_order_relaxed);
+    g_mc_clusters[i8][P][part_chunks].store(clusters, std::memory_order_relaxed);
   }
   a.G = clusters < a.units ? clusters : a.units;
   // rows per round: a cluster's share in the fewest rounds of equal height
@@ -679,7 +764,8 @@ cudaError_t launch_gemm_q4_mma_cluster(const LaunchCtx &ctx, const void *wq, con
   // with several rounds, partials in their own area when it fits: the next
   // round's copies then overlap this round's reduction
   McLayout L;
-  if (!mc_layout(a.H, a.xblocks, nrounds > 1, &L)) return cudaErrorNotSupported;
+  if (!mc_layout(a.H, a.xblocks, i8 ? mc_xblock<true>() : mc_xblock<false>(), nrounds > 1, &L))
+    return cudaErrorNotSupported;
   a.slots = L.slots;
   a.ring = L.ring;
   a.xraw = L.xraw;
@@ -691,9 +777,7 @@ cudaError_t launch_gemm_q4_mma_cluster(const LaunchCtx &ctx, const void *wq, con
                  static_cast<uint64_t>(rows), static_cast<uint64_t>(nb) * 4, kMcChunk,
                  static_cast<uint32_t>(a.H), CU_TENSOR_MAP_SWIZZLE_NONE) ||
       // activations: a part of 16 rows (rows past M read as zeros), 8-byte elements
-      !encode_2d(&prm.xq, CU_TENSOR_MAP_DATA_TYPE_UINT64, xq, static_cast<uint64_t>(nb) * (kQK / 8),
-                 static_cast<uint64_t>(M), static_cast<uint64_t>(nb) * kQK,
-                 static_cast<uint32_t>(a.xblocks * (kQK / 8)), 16, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_act_3d(&prm.xq, xq, nb, M, a.xblocks) ||
       !encode_2d(&prm.xd, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xd, static_cast<uint64_t>(nb),
                  static_cast<uint64_t>(M), static_cast<uint64_t>(nb) * 4,
                  static_cast<uint32_t>(a.xblocks), 16, CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -701,8 +785,8 @@ cudaError_t launch_gemm_q4_mma_cluster(const LaunchCtx &ctx, const void *wq, con
   cfg.gridDim = dim3(static_cast<unsigned>(a.G * P));
   cfg.dynamicSmemBytes = L.bytes;
   cfg.numAttrs = ctx.pdl ? 2 : 1;
-  diag_note("mma_cluster: M=%d K-parts=%d clusters=%d rows/round=%d rounds=%d slots=%d", M, P, a.G, a.H, nrounds,
-            a.slots);
+  diag_note("mma_cluster: M=%d K-parts=%d clusters=%d rows/round=%d rounds=%d slots=%d activations=%s", M, P,
+            a.G, a.H, nrounds, a.slots, i8 ? "int8" : "fp16");
   diag_launch_cfg(reinterpret_cast<const void *>(kern), cfg);
   return cudaLaunchKernelEx(&cfg, kern, prm);
 }

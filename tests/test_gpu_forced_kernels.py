@@ -43,6 +43,23 @@ def test_small_m_parity_with_forced_kernel(kernel):
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
 
 
+@pytest.mark.skipif(os.environ.get("MLQ_MMA_I8") is not None,
+                    reason="already inside a forced-form run")
+@pytest.mark.parametrize("form", ["0", "1"])
+def test_small_m_parity_with_forced_activation_form(form):
+    """The cluster MMA kernel holds its activations as fp16 fragments or as
+    int8 words converted per stage (per shape); each form forced on every
+    small-M case (MLQ_MMA_I8, read once per process)."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    env = dict(os.environ, MLQ_MMA_I8=form, PYTHONPATH=ROOT)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        "tests/test_gpu_parity.py", "-k", "gemm"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=1200)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
+
 @pytest.mark.skipif(os.environ.get("MLQ_FUSED_KERNEL") is not None,
                     reason="already inside a forced-kernel run")
 @pytest.mark.parametrize("kernel", ["ldg", "phase"])
