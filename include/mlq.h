@@ -503,7 +503,9 @@ typedef struct {
  * critical-path read (an SM serves its reads in order: a prefetch issued
  * earlier would delay them).  Unaligned range ends are trimmed to 16 bytes.
  * A CTA's share of the weights is held whole in shared memory when it fits,
- * else streamed through a ring of shared-memory stages (K <= 16384); other
+ * else streamed through a ring of shared-memory stages (K <= 16384); the
+ * ring launch ignores the hint (its SMs' reads are its own stream: L2
+ * hints there measured slower on GB300).  Other
  * shapes (K not a multiple of 128, longer rows) get the same work as several
  * launches (products, then quantize, then the prefetch).
  * No counterpart on the pages: a GPU fusion of their quantize_q8 and
