@@ -147,6 +147,7 @@ struct FusedArgs {
   unsigned ring_stage, ring_dq;         //   stage bytes; offset of a stage's scales
   int early;        // first weight loads before the dependency wait (static weights)
   int early_input;  // the float input x is read and quantised before the dependency wait (static input)
+  int input_bulk;   // set by the launcher (ring phase kernel): the Q8_0 input lands by bulk copies
   int prefetch;     // set by the launcher: hint the CTA's weights into L2 first
   int *status;      // set by the launcher
   unsigned long long wait_ns;

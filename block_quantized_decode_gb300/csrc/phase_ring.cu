@@ -39,6 +39,7 @@ constexpr int kRingMaxSlots = 8;
 constexpr size_t kRingBudget = 110 * 1024;      // two CTAs per SM
 constexpr size_t kRingBudgetWide = 216 * 1024;  // one CTA per SM (very long rows, large slices)
 constexpr size_t kRingWideSlice = 128 * 1024;    // CTA slices from this size take the wide ring
+constexpr int kRingInputBulkDefault = 1;        // a Q8_0 input by bulk copies unless forced off
 
 template <int NW>
 __device__ __forceinline__ void consumers_sync() {
@@ -116,6 +117,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kRingMaxSlots];
   __shared__ __align__(8) uint64_t empty_bar[kRingMaxSlots];
+  __shared__ __align__(8) uint64_t in_bar;  // the Q8_0 input's bulk copies
   __shared__ int abort_flag;
   __shared__ int input_ready;
   volatile int *abort_v = &abort_flag;
@@ -145,6 +147,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
       mbar_init(smem_addr(&full_bar[s]), 1);
       mbar_init(smem_addr(&empty_bar[s]), NW);  // one arrival per consumer warp
     }
+    mbar_init(smem_addr(&in_bar), 1);
     abort_flag = 0;
     input_ready = 0;
     fence_mbar_init();
@@ -215,6 +218,18 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
       if (nr > 0 || writer) phase_quantize<NW>(a, xq_s, xd_s, tid);
     } else if (writer) {
       store_input_copy(xq_s, xd_s, nb, a.xq_out, a.xd_out, tid, NW * 32);
+    }
+  } else if (nr > 0 && a.input_bulk) {
+    // the Q8_0 input by two bulk copies (quants, scales) on one barrier
+    const uint32_t ib = smem_addr(&in_bar);
+    if (tid == 0) {
+      mbar_arrive_expect_tx(ib, static_cast<uint32_t>(nb) * (kQK + 4));
+      bulk_copy_g2s(smem_addr(xq_s), a.xq_in, static_cast<uint32_t>(nb) * kQK, ib);
+      bulk_copy_g2s(smem_addr(xd_s), a.xd_in, static_cast<uint32_t>(nb) * 4, ib);
+    }
+    if (!warp_wait([&] { return ring_wait(ib, 0, abort_v, a.wait_ns); })) {
+      if (lane == 0 && atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
+      if (tid == 0) mbar_wait_bounded(ib, 0, kDrainWaitNs);  // the copies may still be landing
     }
   } else if (nr > 0) {
     const int uq = nb * 2, nu = nb * 2 + nb / 4;
@@ -328,6 +343,15 @@ static cudaError_t launch_ring_t(const LaunchCtx &ctx, const FusedArgs &args) {
     return e == nullptr || e[0] != '0';
   }();
   const int rows_max = plan_rows(a, a.total_rows, grid, pa.bounds, front_env);
+  // A Q8_0 input by bulk copies (16-byte aligned source) or by the
+  // consumers' 16-byte loads; MLQ_RING_INPUT=ldg / bulk forces one (A/B timing).
+  static const int input_env = [] {
+    const char *e = std::getenv("MLQ_RING_INPUT");
+    return e == nullptr ? -1 : (e[0] == 'b' ? 1 : 0);
+  }();
+  const bool aligned = a.x == nullptr && (reinterpret_cast<uintptr_t>(a.xq_in) & 15) == 0 &&
+                       (reinterpret_cast<uintptr_t>(a.xd_in) & 15) == 0;
+  a.input_bulk = aligned && input_env != 0 ? (input_env == 1 ? 1 : kRingInputBulkDefault) : 0;
   const size_t rowq = static_cast<size_t>(nb) * (QT == 1 ? 16 : 32);
   auto up128 = [](size_t v) { return (v + 127) / 128 * 128; };
   const size_t xs = up128(static_cast<size_t>(nb) * (kQK + 4));
@@ -373,7 +397,7 @@ static cudaError_t launch_ring_t(const LaunchCtx &ctx, const FusedArgs &args) {
       const size_t smem = fixed + static_cast<size_t>(ns) * stage;
       diag_note("ring: products=%d rows=%d K=%d rows/CTA<=%d chunks=%d rows/stage=%d slots=%d stage=%zuB "
                 "input=%s q8_out=%d early=%d", a.nproducts, a.total_rows, nb * kQK, rows_max, C, R, ns, stage,
-                a.x != nullptr ? "f32" : "q8", a.any_yq, a.early);
+                a.x != nullptr ? "f32" : (a.input_bulk ? "q8 bulk" : "q8 ldg"), a.any_yq, a.early);
       auto kern = NW == kRingWarps ? phase_ring_kernel<QT, kRingWarps> : phase_ring_kernel<QT, kRingWarpsWide>;
       prefer_max_shared(kern);
       if (smem > 48 * 1024) {
