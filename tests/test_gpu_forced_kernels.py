@@ -101,3 +101,19 @@ def test_phase_parity_with_ring_kernel():
                         "tests/test_gpu_phase.py", "tests/test_gpu_fused.py"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=1200)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
+
+@pytest.mark.skipif(os.environ.get("MLQ_RING_INPUT") is not None,
+                    reason="already inside a forced-input run")
+def test_phase_parity_with_ring_input_loads():
+    """The ring kernel reads a Q8_0 input by bulk copies; the consumers'
+    16-byte loads (the path for an unaligned input) forced on every phase,
+    every phase through the ring kernel."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    env = dict(os.environ, MLQ_RING_INPUT="ldg", MLQ_PHASE_KERNEL="ring", PYTHONPATH=ROOT)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        "tests/test_gpu_phase.py", "tests/test_gpu_configs.py"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=1200)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
