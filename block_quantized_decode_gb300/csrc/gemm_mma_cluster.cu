@@ -21,8 +21,9 @@
 //    and one fp16 subtract or multiply-add per pair, all exact).
 // The int8 form holds 96 blocks per CTA instead of 64, so a long row needs
 // fewer K-parts (4096 x 11008: clusters of 4 in one round of rows instead
-// of clusters of 6 in two); its conversion costs a stage about 8% more
-// issue, so it is taken only where it lowers the number of K-parts.
+// of clusters of 6 in two; measured 26.1 -> 22.2 us).  Where the K-parts
+// stay the same its per-stage conversion only adds work (11008 x 4096:
+// 18.0-19.3 -> 19.1-20.2 us), so it is taken only where it needs fewer.
 //
 // Exact block sums without a per-weight subtraction.  A weight word turns
 // into B fragments with bit operations only: a low nibble n becomes the
@@ -89,7 +90,8 @@ constexpr int kMcMaxRows = 160;                  // rows per round (tensor box h
 constexpr int kMcMaxTpw = kMcMaxRows / 32;       // tiles of one parity in a round
 constexpr int kMcMaxPartF16 = 64;                // blocks of activations per CTA: fp16 fragments
 constexpr int kMcMaxPart = 96;                   //   int8 words
-template <bool I8> __host__ __device__ constexpr int mc_xblock() { return I8 ? 512 : 1024; }  // bytes of one block's activations
+// bytes of one block's activations, and blocks per CTA, of each form
+template <bool I8> __host__ __device__ constexpr int mc_xblock() { return I8 ? 512 : 1024; }
 template <bool I8> __host__ __device__ constexpr int mc_max_part() { return I8 ? kMcMaxPart : kMcMaxPartF16; }
 constexpr int kMcXdBlock = 128;                  // (dx_g, dx_g, dx_g+8, dx_g+8) for g < 8
 constexpr int kMcXcBlock = 128;                  // -(C_g, C_g, C_g+8, C_g+8) for g < 8
