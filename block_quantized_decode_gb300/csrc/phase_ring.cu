@@ -169,10 +169,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
         if (atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
         break;
       }
-      // Until the consumers hold the phase input, keep at most one stage in
-      // flight: an SM serves its reads in order, so the input read would
-      // otherwise wait behind the whole ring (measured: 4-6 us behind 216 KB
-      // under load).  Once stage s - 1 has landed, or the input is in, go on.
+      // Until the consumers hold the phase input (or, with bulk copies, have
+      // issued its copies), keep at most one stage in flight: an SM serves
+      // its reads in order, so the input read would otherwise wait behind
+      // the whole ring (measured: 4-6 us behind 216 KB under load).  Once
+      // stage s - 1 has landed, or the input is in, go on.
       if (s > 0 && !*input_v &&
           !ring_wait_either(smem_addr(&full_bar[(s - 1) % ns]), ((s - 1) / ns) & 1, input_v, abort_v,
                             a.wait_ns)) {
@@ -226,6 +227,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
       mbar_arrive_expect_tx(ib, static_cast<uint32_t>(nb) * (kQK + 4));
       bulk_copy_g2s(smem_addr(xq_s), a.xq_in, static_cast<uint32_t>(nb) * kQK, ib);
       bulk_copy_g2s(smem_addr(xd_s), a.xd_in, static_cast<uint32_t>(nb) * 4, ib);
+      // the producer may go on now: its copies queue behind the input's
+      if (a.input_issue_release) *input_v = 1;
     }
     if (!warp_wait([&] { return ring_wait(ib, 0, abort_v, a.wait_ns); })) {
       if (lane == 0 && atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
@@ -352,6 +355,14 @@ static cudaError_t launch_ring_t(const LaunchCtx &ctx, const FusedArgs &args) {
   const bool aligned = a.x == nullptr && (reinterpret_cast<uintptr_t>(a.xq_in) & 15) == 0 &&
                        (reinterpret_cast<uintptr_t>(a.xd_in) & 15) == 0;
   a.input_bulk = aligned && input_env != 0 ? (input_env == 1 ? 1 : kRingInputBulkDefault) : 0;
+  // With bulk copies, the producer may go on once the input's copies are
+  // issued instead of landed (Q4_0 stack 107.3 -> 106.3 us, Q8_0 + lm_head
+  // 175.9 -> 174.8 us); MLQ_RING_ISSUE_RELEASE=0 waits for the landing.
+  static const int release_env = [] {
+    const char *e = std::getenv("MLQ_RING_ISSUE_RELEASE");
+    return e != nullptr && e[0] == '0' ? 0 : 1;
+  }();
+  a.input_issue_release = release_env;
   const size_t rowq = static_cast<size_t>(nb) * (QT == 1 ? 16 : 32);
   auto up128 = [](size_t v) { return (v + 127) / 128 * 128; };
   const size_t xs = up128(static_cast<size_t>(nb) * (kQK + 4));
