@@ -163,6 +163,13 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
     if (!a.early) griddep_wait();  // weights written by earlier work: wait for it first
     StageIter it{0, 0, ra};
     int s = 0, j, lrow, n;
+    // CTAs start in index order as SMs free up, so the last ones meet a
+    // loaded memory system with their first stage.  With hint_partner = k,
+    // CTA b < grid / k hints into L2 the first stage of CTA b + grid -
+    // grid / k (static weights only), in the tail of the previous launch.
+    const int nh = a.hint_partner > 0 ? static_cast<int>(gridDim.x) / a.hint_partner : 0;  // CTAs hinted
+    const int partner = static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - nh;
+    const bool hint = a.early && nh > 0 && static_cast<int>(blockIdx.x) < nh && partner < static_cast<int>(gridDim.x);
     while ((n = stage_next(it, a, rb, R, &j, &lrow)) > 0) {
       const int slot = s % ns;
       if (s >= ns && !ring_wait(smem_addr(&empty_bar[slot]), ((s / ns) - 1) & 1, abort_v, a.wait_ns)) {
@@ -193,6 +200,17 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
       mbar_arrive_expect_tx(fb, qb + db);
       bulk_copy_g2s(smem_addr(dst), a.prod[j].wq + static_cast<size_t>(lrow) * rowq, qb, fb);
       bulk_copy_g2s(smem_addr(dst + dq), a.prod[j].wd + static_cast<size_t>(lrow) * nb, db, fb);
+      if (s == 0 && hint) {
+        StageIter pit{0, 0, pa.bounds[partner]};
+        int pj, plrow;
+        const int pn = stage_next(pit, a, pa.bounds[partner + 1], R, &pj, &plrow);
+        if (pn > 0) {
+          prefetch_range_l2(a.prod[pj].wq + static_cast<size_t>(plrow) * rowq, static_cast<size_t>(pn) * rowq,
+                            static_cast<size_t>(pn) * rowq);
+          prefetch_range_l2(a.prod[pj].wd + static_cast<size_t>(plrow) * nb, static_cast<size_t>(pn) * nb * 4,
+                            static_cast<size_t>(pn) * nb * 4);
+        }
+      }
       ++s;
     }
     if (*abort_v) {  // copies may still be landing: the last ns issued stages (bounded)
@@ -363,6 +381,16 @@ static cudaError_t launch_ring_t(const LaunchCtx &ctx, const FusedArgs &args) {
     return e != nullptr && e[0] == '0' ? 0 : 1;
   }();
   a.input_issue_release = release_env;
+  // Late CTAs' first stages hinted into L2 by early ones: the Q4_0 stack
+  // 106.6 -> 105.35 us with half the CTAs hinting (a quarter: 105.9), while
+  // every fraction slowed the Q8_0 stack with its larger stages (175.2 ->
+  // 176.2-179.9 us): on for Q4_0 only.  MLQ_RING_HINT_PARTNER=k (0: off)
+  // sets the fraction 1/k for both.
+  static const int hint_env = [] {
+    const char *e = std::getenv("MLQ_RING_HINT_PARTNER");
+    return e != nullptr ? std::atoi(e) : -1;
+  }();
+  a.hint_partner = hint_env >= 0 ? hint_env : (QT == 1 ? 2 : 0);
   const size_t rowq = static_cast<size_t>(nb) * (QT == 1 ? 16 : 32);
   auto up128 = [](size_t v) { return (v + 127) / 128 * 128; };
   const size_t xs = up128(static_cast<size_t>(nb) * (kQK + 4));
