@@ -497,6 +497,54 @@ def run_reference(args, wl, world, rank):
 
 MAX_GRAPH_LAUNCHES = 4096
 
+
+def step_graphs(stream, one_pass, copies, per_step_launches, use_graphs):
+    """Graphs for timed runs of whole steps: one graph per weight copy, one
+    cycle graph of every copy, and prepare(n), which captures n consecutive
+    steps (cycling through the copies from copy 0) as ONE graph, so that
+    every step of a timed repeat chains to the next through programmatic
+    dependent launch (at most MAX_GRAPH_LAUNCHES kernel launches per graph;
+    beyond that, do_steps runs whole cycles).  do_steps(n) runs exactly n
+    steps from copy 0.  Returns (prepare, do_steps)."""
+    import torch
+    graphs, cycle, run_graphs = [], None, {}
+    if use_graphs:
+        for c in range(copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                one_pass(c)
+            graphs.append(g)
+        cycle = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cycle, stream=stream):
+            for c in range(copies):
+                one_pass(c)
+
+    def prepare(n):
+        if not graphs or n <= 0 or n in run_graphs or n * per_step_launches > MAX_GRAPH_LAUNCHES:
+            return
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                one_pass(i % copies)
+        run_graphs[n] = g
+
+    def do_steps(n):
+        if n in run_graphs:
+            run_graphs[n].replay()
+            return
+        i = 0
+        if cycle is not None:
+            while n - i >= copies:
+                cycle.replay()
+                i += copies
+        while i < n:
+            if graphs:
+                graphs[i % copies].replay()
+            else:
+                one_pass(i % copies)
+            i += 1
+    return prepare, do_steps, run_graphs
+
 # ----------------------------------------------------------------------------
 # timing helpers shared by every workload kind
 # ----------------------------------------------------------------------------
@@ -622,63 +670,19 @@ def measure_workload(args, wl, world, local, pg, *, path_arg="auto", with_e2e=Tr
     clocks.start()
 
     # Initialisation (not counted as warm-up steps): one eager pass per weight
-    # copy (kernel attributes, first-touch of every buffer), then the graphs:
-    # one per weight copy (one step each) and one that runs a whole cycle of
-    # `copies` steps back to back -- as a decode loop captures a whole
-    # forward pass -- so consecutive steps chain through programmatic
+    # copy (kernel attributes, first-touch of every buffer), then the graphs
+    # of step_graphs, so that consecutive steps chain through programmatic
     # dependent launch instead of paying a graph launch each.
     with torch.cuda.stream(stream):
         for c in range(copies):
             one_pass(c)
     stream.synchronize()
-    graphs, cycle = [], None
-    if not args.no_graph:
-        for c in range(copies):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                one_pass(c)
-            graphs.append(g)
-        cycle = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(cycle, stream=stream):
-            for c in range(copies):
-                one_pass(c)
-
     # Each run of n steps (the warm-up, each timed repeat of K steps) as ONE
     # CUDA graph of n consecutive steps cycling through the weight copies,
-    # captured before it is timed, so that every step of a repeat chains to
-    # the next through programmatic dependent launch; at most
-    # MAX_GRAPH_LAUNCHES kernel launches per graph, beyond that whole cycles.
+    # captured before it is timed (step_graphs).
     per_step_launches = (1 if path == "chain" else len(r.chain_phases()) if path in ("fused", "phase")
                          else r.kernels_per_step + {None: 0, "all": 1, "next": len(r.mats)}[pf])
-    run_graphs = {}
-
-    def prepare(n):
-        if not graphs or n <= 0 or n in run_graphs or n * per_step_launches > MAX_GRAPH_LAUNCHES:
-            return
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(n):
-                one_pass(i % copies)
-        run_graphs[n] = g
-
-    def do_steps(n):
-        """Exactly n steps from weight copy 0: the graph of n steps if one was
-        captured, else whole cycles through the cycle graph and the rest one
-        graph (or one eager pass) per step."""
-        if n in run_graphs:
-            run_graphs[n].replay()
-            return
-        i = 0
-        if cycle is not None:
-            while n - i >= copies:
-                cycle.replay()
-                i += copies
-        while i < n:
-            if graphs:
-                graphs[i % copies].replay()
-            else:
-                one_pass(i % copies)
-            i += 1
+    prepare, do_steps, run_graphs = step_graphs(stream, one_pass, copies, per_step_launches, not args.no_graph)
 
     steps, reps, ms, per_rep, region_s, clk = timed_region(args, stream, do_steps, pg, dev, clocks,
                                                            prepare=prepare)
@@ -694,7 +698,8 @@ def measure_workload(args, wl, world, local, pg, *, path_arg="auto", with_e2e=Tr
     launches = 2 * copies
     qt = "Q4_0" if r.mats[0].spec.wtype == I.Q4_0 else "Q8_0"
     roofline = None
-    if graphs and path == "chain":
+    use_graphs = not args.no_graph
+    if use_graphs and path == "chain":
         us = back_to_back_us(stream, lambda j: r.step_chain(copy=j % copies), launches)
         ach = wbytes / (us * 1e-6) / 1e9
         roofline = {"kernel": f"decode_stream_kernel<{qt}>", "bound": "hbm", "achieved": ach,
@@ -704,7 +709,7 @@ def measure_workload(args, wl, world, local, pg, *, path_arg="auto", with_e2e=Tr
                     "bytes_per_launch": wbytes, "us_per_launch": us,
                     "method": f"{launches} back-to-back chain launches (one per step) in one CUDA "
                               "graph, best of 3 replays, CUDA events on the launching stream"}
-    elif graphs and path in ("fused", "phase"):
+    elif use_graphs and path in ("fused", "phase"):
         def calls_of(c):
             return r.fused_calls(c) if path == "fused" else r.phase_calls(
                 c, prefetch="self" if args.phase_prefetch != "none" else "none",
@@ -732,7 +737,7 @@ def measure_workload(args, wl, world, local, pg, *, path_arg="auto", with_e2e=Tr
                               "best of 3 replays, CUDA events on the launching stream; achieved = "
                               "sum of per_phase bytes / sum of per_phase us_per_launch",
                     "per_phase": per_phase}
-    elif graphs:
+    elif use_graphs:
         dominant = (f"matvec_m1_kernel<{qt}>" if r.m == 1 else
                     "gemm_q4_mma_cluster_kernel" if r.m >= 8 else
                     "gemm_q4_ring_kernel" if r.m <= 4 else "gemm_q4_small_m_dp4a_kernel")
@@ -817,12 +822,12 @@ def measure_workload(args, wl, world, local, pg, *, path_arg="auto", with_e2e=Tr
                      f"{'q4_0' if m.spec.wtype == I.Q4_0 else 'q8_0'}" for m in r.mats],
         "l2": f"inputs larger than L2: {copies} rotating weight copies "
               f"({copies * wbytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
-        "graphs": (("one graph of the %d timed steps per repeat" % steps) if steps in run_graphs else
-                   ("one graph per cycle of %d steps" % copies) if cycle is not None else False),
+        "graphs": (("one graph of the %d timed steps per repeat" % steps) if steps in run_graphs
+                   else False if args.no_graph else "one graph per step or per cycle of steps"),
         "l2_prefetch": (args.phase_prefetch if path == "phase" else pf or "none"),
         "handoff": args.handoff if path == "phase" else None,
     }
-    del graphs, cycle, r
+    del prepare, do_steps, run_graphs, r
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return out
@@ -918,38 +923,13 @@ def run_layer(args, shape, world, rank, local, pg):
         for c in range(copies):
             L.step(copy=c, stream=stream)
     stream.synchronize()
-    graphs = []
-    cycle = None
-    if not args.no_graph:
-        for c in range(copies):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                L.step(copy=c, stream=stream)
-            graphs.append(g)
-        cycle = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(cycle, stream=stream):
-            for c in range(copies):
-                L.step(copy=c, stream=stream)
-
-    def do_step(i):
-        if graphs:
-            graphs[i % copies].replay()
-        else:
-            L.step(copy=i % copies, stream=stream)
-
-    def do_steps(n):
-        i = 0
-        if cycle is not None:
-            while n - i >= copies:
-                cycle.replay()
-                i += copies
-        while i < n:
-            do_step(i)
-            i += 1
+    prepare, do_steps, run_graphs = step_graphs(stream, lambda c: L.step(copy=c, stream=stream), copies,
+                                                L.launches_per_step, not args.no_graph)
 
     clocks = ClockSampler(local)
     clocks.start()
-    steps, reps, ms_step, per_rep, region_s, clk = timed_region(args, stream, do_steps, pg, dev, clocks)
+    steps, reps, ms_step, per_rep, region_s, clk = timed_region(args, stream, do_steps, pg, dev, clocks,
+                                                                prepare=prepare)
     warm = max(0, args.warmup)
     ms_max = ms_step * steps  # median over the repeats, max over ranks
     value = world * wbytes * steps / (ms_max / 1e3) / 1e9
@@ -1042,7 +1022,8 @@ def run_layer(args, shape, world, rank, local, pg):
                        "hbm_frac_with_kv": (wbytes + kvb) * world * steps / (ms_max / 1e3) / 1e9 / hbm,
                        "l2": f"inputs larger than L2: {copies} rotating weight copies "
                              f"({copies * wbytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
-                       "graphs": ("one graph per cycle of %d steps" % copies) if cycle is not None else False,
+                       "graphs": (("one graph of the %d timed steps per repeat" % steps) if steps in run_graphs
+                                  else False if args.no_graph else "one graph per step or per cycle of steps"),
                        "path": "layer", "parallelism": f"replicas x{world} (independent decode streams)"},
             "gops": world * ops * steps / (ms_max / 1e3) / 1e9, "hbm_frac": value / world / hbm,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
@@ -1100,37 +1081,14 @@ def run_q4k(args, wl, world, rank, local, pg):
         for c in range(copies):
             one_pass(c)
     stream.synchronize()
-    graphs, cycle = [], None
-    if not args.no_graph:
-        for c in range(copies):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                one_pass(c)
-            graphs.append(g)
-        cycle = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(cycle, stream=stream):
-            for c in range(copies):
-                one_pass(c)
-
-    def do_step(i):
-        if graphs:
-            graphs[i % copies].replay()
-        else:
-            one_pass(i % copies)
-
-    def do_steps(n):
-        i = 0
-        if cycle is not None:
-            while n - i >= copies:
-                cycle.replay()
-                i += copies
-        while i < n:
-            do_step(i)
-            i += 1
+    prepare, do_steps, run_graphs = step_graphs(stream, one_pass, copies,
+                                                len(r.phases()) if phase else r.launches_per_step,
+                                                not args.no_graph)
 
     clocks = ClockSampler(local)
     clocks.start()
-    steps, reps, ms_step, per_rep, region_s, clk = timed_region(args, stream, do_steps, pg, dev, clocks)
+    steps, reps, ms_step, per_rep, region_s, clk = timed_region(args, stream, do_steps, pg, dev, clocks,
+                                                                prepare=prepare)
     warm = max(0, args.warmup)
     ms_max = ms_step * steps  # median over the repeats, max over ranks
     value = world * wbytes * steps / (ms_max / 1e3) / 1e9
@@ -1224,7 +1182,8 @@ def run_q4k(args, wl, world, rank, local, pg):
                        "weight_bytes_per_step": wbytes,
                        "l2": f"inputs larger than L2: {copies} rotating weight copies "
                              f"({copies * wbytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
-                       "graphs": ("one graph per cycle of %d steps" % copies) if cycle is not None else False,
+                       "graphs": (("one graph of the %d timed steps per repeat" % steps) if steps in run_graphs
+                                  else False if args.no_graph else "one graph per step or per cycle of steps"),
                        "path": "phase" if phase else "calls", "static_weights": os.environ.get("MLQ_STATIC_WEIGHTS") == "1",
                        "parallelism": f"replicas x{world} (independent decode streams)"},
             "gops": world * r.ops() * steps / (ms_max / 1e3) / 1e9, "hbm_frac": value / world / hbm,
