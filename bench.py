@@ -496,6 +496,9 @@ def run_reference(args, wl, world, rank):
 
 
 MAX_GRAPH_LAUNCHES = 4096
+# the size from which the library runs an M = 1 product call as a one-product
+# ring phase (matvec.cu)
+PHASE_ROUTE_BYTES = 16 << 20
 
 
 def step_graphs(stream, one_pass, copies, per_step_launches, use_graphs):
@@ -738,15 +741,21 @@ def measure_workload(args, wl, world, local, pg, *, path_arg="auto", with_e2e=Tr
                               "sum of per_phase bytes / sum of per_phase us_per_launch",
                     "per_phase": per_phase}
     elif use_graphs:
-        dominant = (f"matvec_m1_kernel<{qt}>" if r.m == 1 else
+        # M = 1 calls of PHASE_ROUTE_BYTES and more run as one-product ring
+        # phases inside the library (mlq_matvec_q4 / _q8), smaller ones on
+        # the M = 1 kernel
+        ring_route = r.m == 1 and all(m.host_q.nbytes + m.host_d.nbytes >= PHASE_ROUTE_BYTES for m in r.mats)
+        dominant = (f"phase_ring_kernel<{qt}> (one-product phases)" if ring_route else
+                    f"matvec_m1_kernel<{qt}>" if r.m == 1 else
                     "gemm_q4_mma_cluster_kernel" if r.m >= 8 else
                     "gemm_q4_ring_kernel" if r.m <= 4 else "gemm_q4_small_m_dp4a_kernel")
-        kernel_src = (("matvec.cu", "mlq_device.cuh") if r.m == 1 else
+        kernel_src = (("phase_ring.cu", "phase_common.cuh", "mlq_device.cuh") if ring_route else
+                      ("matvec.cu", "mlq_device.cuh") if r.m == 1 else
                       ("gemm_mma_cluster.cu", "mma_frag.cuh", "mlq_device.cuh") if r.m >= 8 else
                       ("gemm_ring.cu", "phase_common.cuh", "mlq_device.cuh") if r.m <= 4 else
                       ("gemm_small_m.cu", "mlq_device.cuh"))
-        kernel_profile = ("matvec_q4" if r.m == 1 else "gemm_mma_cluster" if r.m >= 8 else
-                          "gemm_ring" if r.m <= 4 else "gemm_small_m")
+        kernel_profile = ("phase_ring" if ring_route else "matvec_q4" if r.m == 1 else
+                          "gemm_mma_cluster" if r.m >= 8 else "gemm_ring" if r.m <= 4 else "gemm_small_m")
         shapes = {}
         for i, m in enumerate(r.mats):
             shapes.setdefault((m.spec.wtype, m.spec.rows, m.spec.cols), []).append(i)
