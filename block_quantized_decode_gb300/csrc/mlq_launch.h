@@ -150,6 +150,7 @@ struct FusedArgs {
   int input_bulk;   // set by the launcher (ring phase kernel): the Q8_0 input lands by bulk copies
   int input_issue_release;  // set by the launcher (ring): the producer goes on once the input's copies are issued
   int hint_partner;         // set by the launcher (ring): k > 0: CTAs b < grid / k hint a late CTA's first stage
+  int hint_stages;          // set by the launcher (ring): stages of the late CTA hinted
   int prefetch;     // set by the launcher: hint the CTA's weights into L2 first
   int *status;      // set by the launcher
   unsigned long long wait_ns;

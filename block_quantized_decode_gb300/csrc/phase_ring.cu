@@ -165,8 +165,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
     int s = 0, j, lrow, n;
     // CTAs start in index order as SMs free up, so the last ones meet a
     // loaded memory system with their first stage.  With hint_partner = k,
-    // CTA b < grid / k hints into L2 the first stage of CTA b + grid -
-    // grid / k (static weights only), in the tail of the previous launch.
+    // CTA b < grid / k hints into L2 the first hint_stages stages of CTA
+    // b + grid - grid / k (static weights only), in the tail of the previous
+    // launch.
     const int nh = a.hint_partner > 0 ? static_cast<int>(gridDim.x) / a.hint_partner : 0;  // CTAs hinted
     const int partner = static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - nh;
     const bool hint = a.early && nh > 0 && static_cast<int>(blockIdx.x) < nh && partner < static_cast<int>(gridDim.x);
@@ -202,9 +203,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, NW == kRingWarps ? 2 : 1)
       bulk_copy_g2s(smem_addr(dst + dq), a.prod[j].wd + static_cast<size_t>(lrow) * nb, db, fb);
       if (s == 0 && hint) {
         StageIter pit{0, 0, pa.bounds[partner]};
-        int pj, plrow;
-        const int pn = stage_next(pit, a, pa.bounds[partner + 1], R, &pj, &plrow);
-        if (pn > 0) {
+        int pj, plrow, pn;
+        for (int ps = 0; ps < a.hint_stages && (pn = stage_next(pit, a, pa.bounds[partner + 1], R, &pj, &plrow)) > 0;
+             ++ps) {
           prefetch_range_l2(a.prod[pj].wq + static_cast<size_t>(plrow) * rowq, static_cast<size_t>(pn) * rowq,
                             static_cast<size_t>(pn) * rowq);
           prefetch_range_l2(a.prod[pj].wd + static_cast<size_t>(plrow) * nb, static_cast<size_t>(pn) * nb * 4,
@@ -391,6 +392,11 @@ static cudaError_t launch_ring_t(const LaunchCtx &ctx, const FusedArgs &args) {
     return e != nullptr ? std::atoi(e) : -1;
   }();
   a.hint_partner = hint_env >= 0 ? hint_env : (QT == 1 ? 2 : 0);
+  static const int hint_stages_env = [] {
+    const char *e = std::getenv("MLQ_RING_HINT_STAGES");
+    return e != nullptr ? std::atoi(e) : 2;
+  }();
+  a.hint_stages = hint_stages_env > 0 ? hint_stages_env : 2;  // two: 103.5 -> 103.2 us (Q4_0 stack)
   const size_t rowq = static_cast<size_t>(nb) * (QT == 1 ? 16 : 32);
   auto up128 = [](size_t v) { return (v + 127) / 128 * 128; };
   const size_t xs = up128(static_cast<size_t>(nb) * (kQK + 4));
