@@ -121,6 +121,7 @@ struct McArgs {
   int xraw;      // offset of the raw activations: in ring slots kMcFirst.. or after the fragments
   int parts;     // offset of the partials and tile sums: 0 (they reuse the ring) or their own area
   int early;     // weights are not written by earlier queued work: copy before the wait
+  int refill_lag;  // 0: refill the previous stage's slot before computing a stage; 1: the one before
 };
 
 struct McParams {
@@ -491,9 +492,11 @@ __global__ void __launch_bounds__(kMcThreads, 1)
         if (lane == 0 && atomicExch(&abort_flag, 1) == 0) set_status(a.status, kStatusTimeout);
         continue;
       }
-      // refill the slot of the previous stage (all warps have most likely
-      // released it) before this one is computed: S - 1 stages stay in flight
-      if (tid == 0 && static_cast<int>(issued) < min(limit, static_cast<int>(used) + S) && !*abort_v)
+      // refill the slot of the stage before the previous one (all warps
+      // have released it) before this one is computed: S - 2 stages stay in
+      // flight (S - 1 with refill_lag = 0: the previous stage's slot)
+      if (tid == 0 && static_cast<int>(issued) < min(limit, static_cast<int>(used) + S - a.refill_lag) &&
+          !*abort_v)
         issue_next();
       const int jb = k * kMcChunk + jw;  // part-local block
       uint4 xa, xb;
@@ -719,6 +722,15 @@ cudaError_t launch_gemm_q4_mma_cluster(const LaunchCtx &ctx, const void *wq, con
   a.r1 = r1;
   a.P = P;
   a.early = ctx.early_weights ? 1 : 0;
+  // Thread 0 computes too: refilling the slot of the stage before the
+  // previous one, rather than of the previous one, spares it a wait for the
+  // slowest warp (11008 x 4096 M = 16: 19.6 -> 19.3 us); MLQ_MMA_REFILL_LAG=0
+  // refills the previous stage's slot.
+  static const int lag_env = [] {
+    const char *e = std::getenv("MLQ_MMA_REFILL_LAG");
+    return e != nullptr && e[0] == '0' ? 0 : 1;
+  }();
+  a.refill_lag = lag_env;
   const int part_chunks = (nchunks + P - 1) / P;
   a.xblocks = part_chunks * kMcChunk;
   a.units = (n + 7) / 8;
