@@ -356,6 +356,21 @@ static cudaError_t launch_ring_t(const LaunchCtx &ctx, const FusedArgs &args) {
   if (a.total_rows <= 0 || nb % 4 != 0) return cudaErrorNotSupported;
   int grid = ctx.num_sms < a.total_rows ? ctx.num_sms : a.total_rows;
   grid = grid < kPhMaxGrid ? grid : kPhMaxGrid;
+  // Q4_0 phases leave a few SMs free, on which the next launch's first CTAs
+  // start (and stream) before this one ends: the Q4_0 stack 103.5 -> 102.9 /
+  // 102.55 / 102.65 / 103.9 us with 148 / 144 / 140 / 128 of 152 SMs.  Q8_0
+  // phases, twice as long, lose more streaming than they gain (174.9 ->
+  // 177.7 us with 144).  MLQ_RING_GRID=n sets the grid (A/B timing).
+  constexpr int kRingSpareSmsQ4 = 8;
+  static const int grid_env = [] {
+    const char *e = std::getenv("MLQ_RING_GRID");
+    return e != nullptr ? std::atoi(e) : 0;
+  }();
+  if (grid_env > 0) {
+    grid = grid_env < grid ? grid_env : grid;
+  } else if (QT == 1 && grid == ctx.num_sms && grid > 2 * kRingSpareSmsQ4) {
+    grid -= kRingSpareSmsQ4;
+  }
   // Front-heavy split: the CTAs that start first (lowest index) take the
   // larger shares (the 11008-row product: the 40 CTAs with three 32-row
   // blocks start first instead of last).  MLQ_RING_FRONT=0 turns it off
