@@ -117,3 +117,21 @@ def test_phase_parity_with_ring_input_loads():
                         "tests/test_gpu_phase.py", "tests/test_gpu_configs.py"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=1200)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
+
+@pytest.mark.skipif(os.environ.get("MLQ_RING_GRID") is not None,
+                    reason="already inside a forced-variant run")
+def test_phase_parity_with_ring_variants():
+    """The ring kernel's measured choices changed together: another grid (and
+    so another row split), another L2-hint fraction and stage count (also for
+    Q8_0), and the producer waiting for the input to land.  Every phase
+    through the ring kernel."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    env = dict(os.environ, MLQ_PHASE_KERNEL="ring", MLQ_RING_GRID="100", MLQ_RING_HINT_PARTNER="3",
+               MLQ_RING_HINT_STAGES="3", MLQ_RING_ISSUE_RELEASE="0", PYTHONPATH=ROOT)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        "tests/test_gpu_phase.py", "tests/test_gpu_configs.py"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=1200)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
