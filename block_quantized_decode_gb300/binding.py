@@ -156,11 +156,11 @@ def lib() -> ctypes.CDLL:
         L.mlq_quantize_q8k.argtypes = [KA, P, I, P]
         L.mlq_matvec_q4k.argtypes = [P, KT, KA, I, I, P]
         L.mlq_block_sums_q4k.argtypes = [P, P, KT, KA, I, I, P]
-        L.mlq_q4k_phase.argtypes = [P, I, ctypes.POINTER(_Q4KProduct), I, P]
+        L.mlq_q4k_phase.argtypes = [P, I, ctypes.POINTER(_Q4KProduct), I, ctypes.c_uint, P]
         NT, BA = ctypes.POINTER(_NBitsTensor), ctypes.POINTER(_BlkAct)
         L.mlq_quantize_blk.argtypes = [BA, P, I, P]
         L.mlq_matvec_nbits.argtypes = [P, NT, BA, I, I, P]
-        L.mlq_nbits_phase.argtypes = [P, I, ctypes.POINTER(_NBitsProduct), I, P]
+        L.mlq_nbits_phase.argtypes = [P, I, ctypes.POINTER(_NBitsProduct), I, ctypes.c_uint, P]
         L.mlq_block_sumi_nbits.argtypes = [P, NT, BA, I, I, P]
         L.mlq_debug_chain_plan.argtypes = [ctypes.POINTER(_ChainPhase), I, ctypes.POINTER(_ChainProduct),
                                            I, I, P, I]
@@ -315,10 +315,11 @@ def mlq_block_sums_q4k(isum, msum, W: Q4KTensor, x: Q8KAct, r0: int, r1: int, st
                                     r1, _stream(stream)), "mlq_block_sums_q4k")
 
 
-def mlq_q4k_phase(x, k: int, products, stream=None) -> None:
-    """products: [(Q4KTensor, y), ...] (1..4) sharing the float input x."""
+def mlq_q4k_phase(x, k: int, products, stream=None, flags: int = 0) -> None:
+    """products: [(Q4KTensor, y), ...] (1..4) sharing the float input x;
+    flags: 0 or MLQ_F_STATIC_INPUT."""
     arr = (_Q4KProduct * len(products))(*[_Q4KProduct(W.c(), _addr(y)) for W, y in products])
-    _check(lib().mlq_q4k_phase(_addr(x), k, arr, len(products), _stream(stream)), "mlq_q4k_phase")
+    _check(lib().mlq_q4k_phase(_addr(x), k, arr, len(products), flags, _stream(stream)), "mlq_q4k_phase")
 
 
 # ---- block length 32 / 128, float16 scales, signed-offset 8-bit ------------
@@ -361,10 +362,11 @@ def mlq_quantize_blk(out: BlkAct, x, k: int, stream=None) -> None:
     _check(lib().mlq_quantize_blk(ctypes.byref(co), _addr(x), k, _stream(stream)), "mlq_quantize_blk")
 
 
-def mlq_nbits_phase(x, k: int, products, stream=None) -> None:
-    """products: [(NBitsTensor, y), ...] (1..4, one format) sharing the float input x."""
+def mlq_nbits_phase(x, k: int, products, stream=None, flags: int = 0) -> None:
+    """products: [(NBitsTensor, y), ...] (1..4, one format) sharing the float
+    input x; flags: 0 or MLQ_F_STATIC_INPUT."""
     arr = (_NBitsProduct * len(products))(*[_NBitsProduct(W.c(), _addr(y)) for W, y in products])
-    _check(lib().mlq_nbits_phase(_addr(x), k, arr, len(products), _stream(stream)), "mlq_nbits_phase")
+    _check(lib().mlq_nbits_phase(_addr(x), k, arr, len(products), flags, _stream(stream)), "mlq_nbits_phase")
 
 
 def mlq_matvec_nbits(y, W: NBitsTensor, x: BlkAct, r0: int, r1: int, stream=None) -> None:

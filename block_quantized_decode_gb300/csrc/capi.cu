@@ -506,10 +506,11 @@ mlq_status mlq_block_sums_q4k(int32_t *isum, int32_t *msum, const mlq_q4k_tensor
 }
 
 mlq_status mlq_q4k_phase(const float *x, int k, const mlq_q4k_product *products, int nproducts,
-                         void *stream) {
-  mlq::diag_entry("mlq_q4k_phase", "k=%d products=%d", k, nproducts);
+                         unsigned flags, void *stream) {
+  mlq::diag_entry("mlq_q4k_phase", "k=%d products=%d flags=%u", k, nproducts, flags);
   if (x == nullptr || products == nullptr) return MLQ_E_NULL;
   if (nproducts < 1 || nproducts > 4 || !q4k_cols_ok(k)) return MLQ_E_SHAPE;
+  if ((flags & ~MLQ_F_STATIC_INPUT) != 0) return MLQ_E_SHAPE;
   if (!aligned(x, 16)) return MLQ_E_ALIGN;
   mlq::Q4KProductDev p[4];
   for (int j = 0; j < nproducts; ++j) {
@@ -526,7 +527,8 @@ mlq_status mlq_q4k_phase(const float *x, int k, const mlq_q4k_product *products,
   mlq::LaunchCtx ctx;
   mlq_status s = make_ctx(&ctx, stream);
   if (s != MLQ_OK) return s;
-  return from_cuda(mlq::launch_phase_q4k(ctx, x, k / 256, p, nproducts));
+  return from_cuda(mlq::launch_phase_q4k(ctx, x, k / 256, p, nproducts,
+                                         ctx.pdl && (flags & MLQ_F_STATIC_INPUT) != 0));
 }
 
 // ---- block length 32 / 128, float16 scales, signed-offset 8-bit ---------------
@@ -579,10 +581,11 @@ mlq_status mlq_quantize_blk(mlq_blk_act *out, const float *x, int k, void *strea
 }
 
 mlq_status mlq_nbits_phase(const float *x, int k, const mlq_nbits_product *products, int nproducts,
-                           void *stream) {
-  mlq::diag_entry("mlq_nbits_phase", "k=%d products=%d", k, nproducts);
+                           unsigned flags, void *stream) {
+  mlq::diag_entry("mlq_nbits_phase", "k=%d products=%d flags=%u", k, nproducts, flags);
   if (x == nullptr || products == nullptr) return MLQ_E_NULL;
   if (nproducts < 1 || nproducts > 4) return MLQ_E_SHAPE;
+  if ((flags & ~MLQ_F_STATIC_INPUT) != 0) return MLQ_E_SHAPE;
   if (!aligned(x, 16)) return MLQ_E_ALIGN;
   const mlq_nbits_tensor &W0 = products[0].W;
   mlq::NBitsProductDev p[4];
@@ -610,7 +613,7 @@ mlq_status mlq_nbits_phase(const float *x, int k, const mlq_nbits_product *produ
   mlq_status s = make_ctx(&ctx, stream);
   if (s != MLQ_OK) return s;
   return from_cuda(mlq::launch_phase_nbits(ctx, W0.bits, W0.blk, W0.scale_f16, W0.scale_ld, W0.zp_ld, k,
-                                           x, p, nproducts));
+                                           x, p, nproducts, ctx.pdl && (flags & MLQ_F_STATIC_INPUT) != 0));
 }
 
 mlq_status mlq_matvec_nbits(float *y, const mlq_nbits_tensor *W, const mlq_blk_act *x, int r0, int r1,

@@ -218,8 +218,10 @@ struct Q4KProductDev {
   float *y;
   int rows;
 };
+// early_input: x is not written by earlier work (read and quantised before
+// the dependency wait).
 cudaError_t launch_phase_q4k(const LaunchCtx &ctx, const float *x, int nsb, const Q4KProductDev *p,
-                             int np);
+                             int np, bool early_input);
 
 // nbits.cu: blocks of 32 or 128, float32 / binary16 scales, 4-bit or
 // signed-offset 8-bit weights (sumi non-null: the integer test hook).
@@ -239,7 +241,7 @@ struct NBitsProductDev {
   int rows;
 };
 cudaError_t launch_phase_nbits(const LaunchCtx &ctx, int bits, int blk, int sc_f16, int sc_ld, int zp_ld,
-                               int cols, const float *x, const NBitsProductDev *p, int np);
+                               int cols, const float *x, const NBitsProductDev *p, int np, bool early_input);
 
 // layer.cu: the floating-point steps of a decode layer (each one launch).
 cudaError_t launch_rmsnorm_q8(const LaunchCtx &ctx, float *x, const float *y, const float *w,

@@ -128,6 +128,7 @@ struct NBitsArgs {
   int32_t *sumi;      // test hook (one product): per-block int32 sums instead of y
   int cols, blk, nb, f16, sc_ld, zp_ld;
   int R, ns, P, early;
+  int early_input;  // xf not written by earlier work: quantised before the dependency wait
   unsigned rowq, row_sc, row_zp;          // bytes per row of each array
   unsigned stage_bytes, stage_sc, stage_zp, smem_part, smem_ring;
   int *status;
@@ -226,7 +227,10 @@ __global__ void __launch_bounds__(kNThreads, 2) matvec_nbits_kernel(const __grid
   }
 
   // ------------------------------ consumers ------------------------------
-  griddep_wait();  // x may come from the previous kernel
+  // x may come from the previous kernel; a static float input is quantised
+  // before the wait (the outputs are written only after it)
+  const bool early_in = a.xf != nullptr && a.early_input != 0;
+  if (!early_in) griddep_wait();
   if (rb <= ra) return;
   if (a.xf != nullptr) {
     // a phase: every CTA quantises the float input itself, one warp per
@@ -267,6 +271,7 @@ __global__ void __launch_bounds__(kNThreads, 2) matvec_nbits_kernel(const __grid
     }
   }
   n_consumers_sync();
+  if (early_in) griddep_wait();
 
   // A row is U 16-byte units; UPB units per block (a power of two).
   const int U = static_cast<int>(rowq / 16);
@@ -450,7 +455,7 @@ cudaError_t launch_matvec_nbits(const LaunchCtx &ctx, int bits, int blk, const v
 }
 
 cudaError_t launch_phase_nbits(const LaunchCtx &ctx, int bits, int blk, int sc_f16, int sc_ld, int zp_ld,
-                               int cols, const float *x, const NBitsProductDev *p, int np) {
+                               int cols, const float *x, const NBitsProductDev *p, int np, bool early_input) {
   if (np < 1 || np > kNMaxProducts) return cudaErrorInvalidValue;
   NBitsArgs a = {};
   a.total = 0;
@@ -470,6 +475,7 @@ cudaError_t launch_phase_nbits(const LaunchCtx &ctx, int bits, int blk, int sc_f
   a.f16 = sc_f16;
   a.sc_ld = sc_ld;
   a.zp_ld = zp_ld;
+  a.early_input = early_input ? 1 : 0;
   return launch_nbits_common(ctx, a, bits, false);
 }
 

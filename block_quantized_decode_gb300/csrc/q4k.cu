@@ -131,6 +131,7 @@ struct Q4KArgs {
   int R, ns;                                    // rows per stage, ring slots
   int P;                                        // parts per row (P > 1: partial sums in smem_part)
   int early;                                    // weights not written by earlier work
+  int early_input;                              // xf not written by earlier work: quantised before the wait
   unsigned smem_part;
   unsigned stage_bytes, stage_s, stage_d;       // stage size; offsets of s and of d, dmin
   unsigned smem_ring;
@@ -246,7 +247,10 @@ __global__ void __launch_bounds__(kKThreads, 2) matvec_q4k_kernel(const __grid_c
   }
 
   // ------------------------------ consumers ------------------------------
-  griddep_wait();  // x may come from the previous kernel
+  // x may come from the previous kernel; a static float input is quantised
+  // before the wait (the outputs are written only after it)
+  const bool early_in = a.xf != nullptr && a.early_input != 0;
+  if (!early_in) griddep_wait();
   if (rb <= ra) return;
   // The activation quants in shared memory: sub-block u at u*32, its two
   // 16-byte halves swapped when bit 2 of u is set, so that the 8 lanes of a
@@ -283,6 +287,7 @@ __global__ void __launch_bounds__(kKThreads, 2) matvec_q4k_kernel(const __grid_c
     for (int u = tid; u < nsb; u += kKWarps * 32) xd_s[u] = __ldg(a.xd + u);
   }
   k_consumers_sync();
+  if (early_in) griddep_wait();
 
   int s = 0, n = 0;
   for (int r = ra; r < rb; r += n, ++s) {
@@ -463,7 +468,7 @@ cudaError_t launch_matvec_q4k(const LaunchCtx &ctx, const void *wq, const void *
 }
 
 cudaError_t launch_phase_q4k(const LaunchCtx &ctx, const float *x, int nsb, const Q4KProductDev *p,
-                             int np) {
+                             int np, bool early_input) {
   if (np < 1 || np > kKMaxProducts) return cudaErrorInvalidValue;
   Q4KArgs a = {};
   a.total = 0;
@@ -480,6 +485,7 @@ cudaError_t launch_phase_q4k(const LaunchCtx &ctx, const float *x, int nsb, cons
   a.nprod = np;
   a.xf = x;
   a.nsb = nsb;
+  a.early_input = early_input ? 1 : 0;
   return launch_q4k_common(ctx, a, false);
 }
 

@@ -396,9 +396,11 @@ class Q4KRunner:
         return phase_groups(self.wl.mats)
 
     def step_phase(self, copy: int = 0, stream=None) -> None:
-        """One pass as phases: each launch quantises its float input itself."""
+        """One pass as phases: each launch quantises its float input itself
+        (the pass's own input x, written once, as MLQ_F_STATIC_INPUT)."""
         for inp, names, cols in self.phases():
-            B.mlq_q4k_phase(self.vec(inp), cols, [(self.W[copy][n], self.y[n]) for n in names], stream)
+            B.mlq_q4k_phase(self.vec(inp), cols, [(self.W[copy][n], self.y[n]) for n in names], stream,
+                            flags=B.MLQ_F_STATIC_INPUT if inp == "x" else 0)
 
     def product(self, name: str, copy: int = 0, stream=None) -> None:
         rows, inp = self.host[name][4], [m[3] for m in self.wl.mats if m[0] == name][0]
@@ -463,9 +465,11 @@ class NBitsRunner:
         return phase_groups(self.wl.mats)
 
     def step_phase(self, copy: int = 0, stream=None) -> None:
-        """One pass as phases: each launch quantises its float input itself."""
+        """One pass as phases: each launch quantises its float input itself
+        (the pass's own input x, written once, as MLQ_F_STATIC_INPUT)."""
         for inp, names, cols in self.phases():
-            B.mlq_nbits_phase(self.vec(inp), cols, [(self.W[copy][n], self.y[n]) for n in names], stream)
+            B.mlq_nbits_phase(self.vec(inp), cols, [(self.W[copy][n], self.y[n]) for n in names], stream,
+                              flags=B.MLQ_F_STATIC_INPUT if inp == "x" else 0)
 
     def product(self, name: str, copy: int = 0, stream=None) -> None:
         rows, inp = [(m[1], m[3]) for m in self.wl.mats if m[0] == name][0]

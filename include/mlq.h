@@ -233,13 +233,16 @@ mlq_status mlq_block_sums_q4k(int32_t *isum, int32_t *msum, const mlq_q4k_tensor
  * CTA quantises x itself, so no quantiser launch precedes it.
  * x: k float32, device, 16-byte aligned; every W_j->cols == k (a positive
  * multiple of 256, at most MLQ_MAX_COLS); y_j: W_j->rows float32, 4-byte
- * aligned, owned by the caller.  Tensors as for mlq_matvec_q4k. */
+ * aligned, owned by the caller.  Tensors as for mlq_matvec_q4k.  flags: 0
+ * or MLQ_F_STATIC_INPUT (x is not written by work queued earlier on the
+ * stream: the launch reads and quantises it before that work has
+ * finished; its outputs still wait); anything else: MLQ_E_SHAPE. */
 typedef struct {
     mlq_q4k_tensor W;
     float *y;
 } mlq_q4k_product;
 mlq_status mlq_q4k_phase(const float *x, int k, const mlq_q4k_product *products, int nproducts,
-                         void *stream);
+                         unsigned flags, void *stream);
 
 /* ---- block length 32 / 128, float16 scales, signed-offset 8-bit -------- */
 /* Page "ONNX Runtime" (SpaceMiT X60), "How we got there": item 3 (AMD's
@@ -296,13 +299,14 @@ mlq_status mlq_quantize_blk(mlq_blk_act *out, const float *x, int k, void *strea
  * CTA quantises x itself.  All W_j share bits, blk, scale_f16, scale_ld,
  * zp_ld and whether zp is NULL (else MLQ_E_TYPE / MLQ_E_SHAPE); every
  * W_j->cols == k.  x: k float32, device, 16-byte aligned; y_j: W_j->rows
- * float32, 4-byte aligned, owned by the caller. */
+ * float32, 4-byte aligned, owned by the caller.  flags: 0 or
+ * MLQ_F_STATIC_INPUT, as for mlq_q4k_phase. */
 typedef struct {
     mlq_nbits_tensor W;
     float *y;
 } mlq_nbits_product;
 mlq_status mlq_nbits_phase(const float *x, int k, const mlq_nbits_product *products, int nproducts,
-                           void *stream);
+                           unsigned flags, void *stream);
 
 /* y[r] for r in [r0, r1) as above; the sum over blocks is taken in another
  * order than b = 0, 1, ... and agrees with the in-order sum within

@@ -339,12 +339,14 @@ def test_validation_q4k(M):
     # the Q4_K-style phase: products sharing one float input
     from block_quantized_decode_gb300.binding import _Q4KProduct
 
-    def ph(x=6 * A, k=512, prods=None, n=None):
+    def ph(x=6 * A, k=512, prods=None, n=None, flags=0):
         prods = [_Q4KProduct(kt(), 5 * A)] if prods is None else prods
         arr = (_Q4KProduct * max(1, len(prods)))(*prods)
-        return call(M, "mlq_q4k_phase", x, k, arr, len(prods) if n is None else n, None)
+        return call(M, "mlq_q4k_phase", x, k, arr, len(prods) if n is None else n, flags, None)
 
     assert ph(x=None) == M.MLQ_E_NULL
+    assert ph(flags=M.MLQ_F_STATIC_WEIGHTS) == M.MLQ_E_SHAPE  # only MLQ_F_STATIC_INPUT
+    assert ph(flags=4) == M.MLQ_E_SHAPE
     assert ph(prods=[_Q4KProduct(kt(), 0)]) == M.MLQ_E_NULL
     assert ph(prods=[_Q4KProduct(kt(dmin=0), 5 * A)]) == M.MLQ_E_NULL
     assert ph(n=0) == M.MLQ_E_SHAPE
@@ -397,12 +399,14 @@ def test_validation_nbits(M):
     # the block-length phase: products of one format sharing one float input
     from block_quantized_decode_gb300.binding import _NBitsProduct
 
-    def ph(x=6 * A, k=896, prods=None, n=None):
+    def ph(x=6 * A, k=896, prods=None, n=None, flags=0):
         prods = [_NBitsProduct(nt(), 5 * A)] if prods is None else prods
         arr = (_NBitsProduct * max(1, len(prods)))(*prods)
-        return call(M, "mlq_nbits_phase", x, k, arr, len(prods) if n is None else n, None)
+        return call(M, "mlq_nbits_phase", x, k, arr, len(prods) if n is None else n, flags, None)
 
     assert ph(x=None) == M.MLQ_E_NULL
+    assert ph(flags=M.MLQ_F_STATIC_WEIGHTS) == M.MLQ_E_SHAPE  # only MLQ_F_STATIC_INPUT
+    assert ph(flags=4) == M.MLQ_E_SHAPE
     assert ph(prods=[_NBitsProduct(nt(), 0)]) == M.MLQ_E_NULL
     assert ph(prods=[_NBitsProduct(nt(sc=0), 5 * A)]) == M.MLQ_E_NULL
     assert ph(n=0) == M.MLQ_E_SHAPE
