@@ -60,7 +60,8 @@ def test_phase_llama7b_ffn_q8_lm_head():
 
 
 def test_phase_chunks_q4():
-    # K = 128 .. 16384: 1, 2, 4 and 8 chunks per warp, chunk tails of 43/44 blocks
+    # K = 128 .. 16384: 1, 2, 4 and 8 chunks per warp, chunk tails of 38, 43
+    # and 44 blocks
     wl = I.Workload("chunks_q4", 1, [
         I.Matvec("a", I.Q4_0, 320, 4096, "x"),
         I.Matvec("b", I.Q4_0, 1024, 320, "a"),
@@ -69,6 +70,7 @@ def test_phase_chunks_q4():
         I.Matvec("e", I.Q4_0, 160, 5632, "d"),
         I.Matvec("f", I.Q4_0, 96, 11008, "x"),
         I.Matvec("g", I.Q4_0, 1000, 16384, "x"),
+        I.Matvec("h", I.Q4_0, 608, 9600, "x"),
     ])
     run_and_check(wl, phase=True)
 
