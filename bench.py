@@ -747,15 +747,15 @@ def measure_workload(args, wl, world, local, pg, *, path_arg="auto", with_e2e=Tr
         ring_route = r.m == 1 and all(m.host_q.nbytes + m.host_d.nbytes >= PHASE_ROUTE_BYTES for m in r.mats)
         dominant = (f"phase_ring_kernel<{qt}> (one-product phases)" if ring_route else
                     f"matvec_m1_kernel<{qt}>" if r.m == 1 else
-                    "gemm_q4_mma_cluster_kernel" if r.m >= 8 else
+                    "gemm_q4_mma_cluster_kernel" if r.m >= 6 else
                     "gemm_q4_ring_kernel" if r.m <= 4 else "gemm_q4_small_m_dp4a_kernel")
         kernel_src = (("phase_ring.cu", "phase_common.cuh", "mlq_device.cuh") if ring_route else
                       ("matvec.cu", "mlq_device.cuh") if r.m == 1 else
-                      ("gemm_mma_cluster.cu", "mma_frag.cuh", "mlq_device.cuh") if r.m >= 8 else
+                      ("gemm_mma_cluster.cu", "mma_frag.cuh", "mlq_device.cuh") if r.m >= 6 else
                       ("gemm_ring.cu", "phase_common.cuh", "mlq_device.cuh") if r.m <= 4 else
                       ("gemm_small_m.cu", "mlq_device.cuh"))
         kernel_profile = ("phase_ring" if ring_route else "matvec_q4" if r.m == 1 else
-                          "gemm_mma_cluster" if r.m >= 8 else "gemm_ring" if r.m <= 4 else "gemm_small_m")
+                          "gemm_mma_cluster" if r.m >= 6 else "gemm_ring" if r.m <= 4 else "gemm_small_m")
         shapes = {}
         for i, m in enumerate(r.mats):
             shapes.setdefault((m.spec.wtype, m.spec.rows, m.spec.cols), []).append(i)
@@ -779,7 +779,7 @@ def measure_workload(args, wl, world, local, pg, *, path_arg="auto", with_e2e=Tr
                     "method": f"{launches} back-to-back launches per shape in one CUDA graph, "
                               "best of 3 replays, CUDA events on the launching stream",
                     "per_shape": per_shape}
-        if r.m >= 8:
+        if r.m >= 6:
             # the tensor-core side of the same launches: 2 M N K per product
             flops = sum(2.0 * r.m * r.mats[idx[0]].spec.rows * r.mats[idx[0]].spec.cols * len(idx)
                         for idx in shapes.values())

@@ -197,8 +197,13 @@ static cudaError_t launch_gemm_mm(const LaunchCtx &ctx, GemmArgs a) {
 // shapes (28-34 us at M = 16): each of its N = 16 MMAs costs the full
 // instruction latency.
 // Below M = 8 the ring kernel (gemm_ring.cu: activations in registers,
-// whole weight rows through a shared-memory ring) comes first for M <= 4;
-// this dp4a kernel takes the shapes it declines and M = 5..7.
+// whole weight rows through a shared-memory ring) comes first for M <= 4.
+// At M = 6 and 7 the cluster kernel comes first too: its time stays flat in
+// M while this kernel's grows by about 3 us a row (per product, back to
+// back: 11008 x 4096 / 4096 x 11008 at M = 7 20.3 / 22.1 us against
+// 26.8 / 26.0, at M = 6 20.1 / 22.2 against 24.0 / 22.9; at M = 5 20.3 /
+// 22.4 against 20.8 / 20.1, where this kernel stays).  This dp4a kernel
+// takes M = 5 and the shapes the others decline.
 // MLQ_GEMM_KERNEL=dp4a|mma|mma_ldg|umma|ring overrides (A/B timing, tests).
 static int gemm_override() {
   static const int v = [] {
@@ -226,10 +231,11 @@ cudaError_t launch_gemm_q4_small_m(const LaunchCtx &ctx, const void *wq, const f
     if (e != cudaErrorNotSupported) return e;
     return launch_gemm_q4_mma(ctx, wq, wd, nb, xq, xd, M, Y, ldy, r0, r1);
   }
-  if (o == 2 || (o == 0 && M >= 8)) {
+  constexpr int kClusterMinM = 6;  // the cluster kernel from this M on (above)
+  if (o == 2 || (o == 0 && M >= kClusterMinM)) {
     const cudaError_t e = launch_gemm_q4_mma_cluster(ctx, wq, wd, nb, xq, xd, M, Y, ldy, r0, r1, rows);
     if (e != cudaErrorNotSupported) return e;
-    return launch_gemm_q4_mma(ctx, wq, wd, nb, xq, xd, M, Y, ldy, r0, r1);
+    if (o == 2 || M >= 8) return launch_gemm_q4_mma(ctx, wq, wd, nb, xq, xd, M, Y, ldy, r0, r1);
   }
   if ((o == 0 || o == 5) && M <= 4) {
     const cudaError_t e = launch_gemm_q4_ring(ctx, wq, wd, nb, xq, xd, M, Y, ldy, r0, r1);

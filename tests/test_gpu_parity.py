@@ -184,7 +184,7 @@ def test_matvec_all_zero_activation(lib):
 # ---------------------------------------------------------------------------
 # small-M product
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("Mr", [1, 2, 3, 4, 5, 8, 11, 16])
+@pytest.mark.parametrize("Mr", [1, 2, 3, 4, 5, 6, 7, 8, 11, 16])
 @pytest.mark.parametrize("rows,cols", [(1, 32), (70, 512), (37, 4128), (64, 11008)])
 def test_gemm_small_m_parity(lib, Mr, rows, cols):
     M = lib
