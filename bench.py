@@ -508,7 +508,8 @@ def step_graphs(stream, one_pass, copies, per_step_launches, use_graphs):
     every step of a timed repeat chains to the next through programmatic
     dependent launch (at most MAX_GRAPH_LAUNCHES kernel launches per graph;
     beyond that, do_steps runs whole cycles).  do_steps(n) runs exactly n
-    steps from copy 0.  Returns (prepare, do_steps)."""
+    steps from copy 0.  Returns (prepare, do_steps, run_graphs), the last
+    the graphs prepare() captured, by step count."""
     import torch
     graphs, cycle, run_graphs = [], None, {}
     if use_graphs:
